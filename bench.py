@@ -1,0 +1,326 @@
+"""Benchmark of the MoE layer step on GB300.
+
+Workload (one step = one pass of the whole layer step over one batch):
+  decode1: one decode token through one full-shape layer -- hidden 7168, expert
+  intermediate 1536, 896 routed MXFP4 experts resident in HBM (15.7 GB), top-16, one bf16
+  shared expert 7168x1536.  Synthetic seeded inputs (synth/), distinct tokens per step so
+  every step routes to its own experts; L2 is flushed (a 256 MB write) between timed steps.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the reference
+arm of this comparison), on the same workload, metric and unit.
+
+N > 1 (torchrun): the layer step does not shard without an exchange step, so every rank
+runs an independent replica; value = tokens processed by all ranks / max rank time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tokens/s & HBM GB/s vs ~8 TB/s; prefill tcgen05 % peak"
+WORKLOAD = ("decode1: 1 token/step through one full-shape MoE layer (hidden 7168, inter 1536, "
+            "896 MXFP4 experts top-16, 1 bf16 shared expert 7168x1536)")
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return None
+
+
+def step_bytes(cfg, U):
+    """Algorithmic bytes of one decode step with U distinct routed experts."""
+    H, I, E, SI = cfg.hidden, cfg.inter, cfg.n_experts, cfg.shared_inter
+    op = I * H // 2 + I * H // 32            # one MXFP4 operand (packed + scales)
+    return {
+        "k_router_shared": E * H * 2 + 2 * SI * H * 2 + H * 2,
+        "k_expert_gateup": U * 2 * op,
+        "k_down_combine": U * op + H * SI * 2 + H * 4,
+    }
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) during the timed region."""
+
+    def __init__(self, path):
+        self.path = path
+        self.p = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", "--query-gpu=" + q, "--format=csv,noheader",
+                                       "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            self.p.wait()
+            self.f.close()
+
+    def summary(self, dev_index=0):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        try:
+            rows = [l.split(",") for l in open(self.path).read().strip().splitlines()]
+        except OSError:
+            return out
+        mhz, reasons = [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9 or r[0] != str(dev_index):
+                continue
+            try:
+                mhz.append(float(r[1].split()[0]))
+                out["sm_max_mhz"] = float(r[2].split()[0])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if mhz:
+            out["sm_mhz"] = statistics.median(mhz)
+            out["samples"] = len(mhz)
+        out["reasons"] = sorted(reasons)
+        return out
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def cpu_baseline(cfg, seed, n_tokens=2):
+    """The oracle, as it stands, on a bounded sample of the same workload."""
+    import oracle
+    import synth
+    w = synth.layer_weights(cfg, seed)
+    x = synth.activations(cfg, seed + 1, n_tokens)
+    cache = {}
+
+    def rec(e):
+        if e not in cache:
+            cache[e] = synth.expert_record(cfg, seed, 0, e)
+        return cache[e]
+    # expert bytes are regenerated outside the timed region
+    oi, _, _, _ = oracle.router(x, w["wr"], w["bias"], cfg.topk)
+    for e in set(oi.ravel().tolist()):
+        rec(int(e))
+    nt = oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle.moe_layer(x, w["wr"], w["bias"], rec, cfg.topk, cfg.hidden, cfg.inter,
+                     w["sh_gate"], w["sh_up"], w["sh_down"], nthreads=nt)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+            "sample": "%d decode tokens through the full decode1 layer (router + 16 experts + "
+                      "shared expert, fp64 accumulation)" % n_tokens}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    cfg = synth.config("decode1")
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, 0, 1)
+    vals = []
+    t_all = 0.0
+    for s in range(args.steps):
+        r = cpu_baseline(cfg, 100 + s, 1)
+        vals.append(r["value"])
+        t_all += 1.0 / r["value"]
+    value = args.steps / t_all
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": r["cores"],
+                         "kind": "oracle", "sample": "1 decode token per step, %d steps"
+                                                     % args.steps},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import synth
+    import synth.device as sd
+    import mxfp4_routed_expert_02_gb300 as k3
+
+    cfg = synth.config("decode1")
+    seed = 0
+    dev = torch.device("cuda", local)
+    H, I, E, K = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
+    dims = k3.LayerDims(H, I, E, K, cfg.shared_inter)
+    stride = (cfg.record_bytes + 4095) // 4096 * 4096
+    experts = torch.empty(E * stride, dtype=torch.uint8, device=dev)
+    sd.fill_experts(experts, cfg, seed, 0, stride=stride)
+    w = synth.layer_weights(cfg, seed)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    wr, bias = t(w["wr"].view(np.int16)), t(w["bias"])
+    sg, su, sdn = (t(w[k].view(np.int16)) for k in ("sh_gate", "sh_up", "sh_down"))
+    NX = 256
+    xs_host = synth.activations(cfg, seed + 1 + rank, NX)
+    xs = t(xs_host.view(np.int16))
+    y = torch.empty((1, H), dtype=torch.float32, device=dev)
+    idx = torch.empty((NX, K), dtype=torch.int32, device=dev)
+    wt = torch.empty((NX, K), dtype=torch.float32, device=dev)
+    ws = k3.new_workspace(dims, 1, dev)
+    status = k3.new_status(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        j = s % NX
+        k3.k3moe_layer(dims, xs[j:j + 1], wr, bias, experts, stride, sg, su, sdn, y, ws, status,
+                       idx_out=idx[j:j + 1], w_out=wt[j:j + 1])
+
+    for s in range(args.warmup):
+        flush.fill_(s & 255)
+        step(s)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = Clocks("/tmp/k3moe_bench_clocks_%d_%d.csv" % (os.getpid(), rank))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    k3.k3moe_trace_enable(True)
+    with clocks:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            flush.fill_((s + 7) & 255)
+            ev[s][0].record(stream)
+            step(args.warmup + s)
+            ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    trace = k3.k3moe_trace_read()
+    k3.k3moe_trace_enable(False)
+    assert status.item() == 0, k3.status_str(status.item())
+    ms = [a.elapsed_time(b) for a, b in ev]
+    t_dev = sum(ms) / 1e3
+    if dist:
+        tt = torch.tensor([t_dev], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_dev = float(tt.item())
+
+    # distinct experts actually used per step (for the algorithmic bytes)
+    steps_idx = idx.cpu().numpy()
+    used = [len(set(steps_idx[(args.warmup + s) % NX].tolist())) for s in range(args.steps)]
+    U = statistics.mean(used)
+    nb = step_bytes(cfg, U)
+    bytes_step = sum(nb.values())
+    launches = sum(v[1] for v in trace.values())
+    kernels = {k: {"ms_avg": v[0] / v[1], "launches": v[1]} for k, v in trace.items() if v[1]}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_avg"] * kernels[k]["launches"])
+    pk = peaks()
+    peak_hbm = pk["hbm_gbs"] if pk else 6800.0
+    dom_ms = kernels[dom]["ms_avg"]
+    achieved = nb[dom] / (dom_ms * 1e-3) / 1e9
+    for k in kernels:
+        if k in nb:
+            kernels[k]["gbs"] = nb[k] / (kernels[k]["ms_avg"] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
+                "frac": achieved / peak_hbm, "traffic": None, "kernel": dom,
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else
+                               "fallback 6.8 TB/s (of fallback)"}
+
+    # end to end through the C ABI with host buffers: x in from pinned host memory,
+    # y back to pinned host memory, every step
+    xh = torch.from_numpy(xs_host.view(np.int16).copy()).pin_memory()
+    yh = torch.empty((1, H), dtype=torch.float32).pin_memory()
+    xd = torch.empty((1, H), dtype=torch.int16, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for s in range(args.steps):
+        j = s % NX
+        xd.copy_(xh[j:j + 1], non_blocking=True)
+        k3.k3moe_layer(dims, xd, wr, bias, experts, stride, sg, su, sdn, y, ws, status)
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    if dist:
+        tt = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, seed, 2)
+    if rank == 0:
+        tokens = args.steps * world
+        line = {
+            "metric": METRIC, "value": tokens / t_dev, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_dev / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "seed": seed,
+                       "l2": "flushed between timed steps (256 MB write, outside the step "
+                             "events)", "distinct_experts_per_step": U,
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "hbm_gbs_step": bytes_step / (t_dev / args.steps) / 1e9,
+            "algorithmic_bytes_per_step": bytes_step,
+            "roofline": roofline,
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(local),
+            "e2e": {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": H * 2,
+                    "d2h_bytes_per_step": H * 4},
+            "cpu_baseline": cpu,
+            "wall_s": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

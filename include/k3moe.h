@@ -1,0 +1,177 @@
+/*
+ * k3moe.h -- C ABI of the GB300 (sm_103a) MoE layer step of Kimi K3.
+ *
+ * The operation (what each call computes) is defined by the README of
+ * FareedKhan-dev/kimi-k3-in-c ("kimi-k3-in-c" below):
+ *   - the router: section 9 "Picking 16 experts of 896" (router listing) and
+ *     "Three invariants", item 3 (the bias steers selection only);
+ *   - the MXFP4 format and the nibble-direct product: section 4 "Reduction one: the
+ *     experts already ship at half a byte";
+ *   - the expert FFN with the SiTU-GLU activation, the routed sum and the shared
+ *     expert: section 9 (LatentMoE listing, steps 3 and 6; activation listing);
+ *   - RMSNorm: section 5 "Kernels with a floating point contract";
+ * and the README of Maknee/Kimi-K3.cpp ("The consumer-memory idea", item 7: results are
+ * reduced in router order).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated
+ *     otherwise.  The library allocates no device memory on these paths and frees
+ *     nothing; scratch space is the caller's `workspace`.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).  Argument
+ *     errors found on the host are returned at once and nothing is launched.
+ *   - Errors found on the device are written to `*status_dev` (an int32 the caller
+ *     allocates and zeroes; the first error wins, later ones do not overwrite it) and
+ *     are read by the caller after synchronising.  A failing work item still writes
+ *     defined output (zeros for its part), so results are never undefined memory.
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Row-major throughout.
+ *   - Pointers must be 16-byte aligned (K3MOE_ERR_ALIGN otherwise).
+ *   - Thread safety: calls are independent; two calls may run concurrently only if
+ *     they use different workspaces.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *k3moe_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    K3MOE_OK = 0,
+    K3MOE_ERR_ARG = 1,        /* NULL pointer, negative count, bad enum */
+    K3MOE_ERR_SHAPE = 2,      /* a dimension the kernels do not support */
+    K3MOE_ERR_ALIGN = 3,      /* a pointer or stride not 16-byte aligned */
+    K3MOE_ERR_WORKSPACE = 4,  /* ws_bytes below k3moe_workspace_size() */
+    K3MOE_ERR_CUDA = 5,       /* a CUDA launch failed (see cudaGetLastError) */
+    K3MOE_ERR_TIMEOUT = 6,    /* a bounded device-side wait gave up */
+    K3MOE_ERR_BAD_EXPERT = 7, /* an expert index outside [0, n_experts) */
+    K3MOE_ERR_NONFINITE = 8   /* a router score that is NaN or infinite */
+} k3moe_status;
+
+typedef enum { K3MOE_F32 = 0, K3MOE_BF16 = 1 } k3moe_dtype;
+
+/* Shapes and constants of one MoE layer (the model config fields of kimi-k3-in-c,
+ * section 2, K3Cfg: n_experts, topk, moe_inter, routed_scale, moe_renorm, situ_b1,
+ * situ_b2).
+ *   hidden        H, the layer width (x and y are [T][H]); multiple of 32
+ *   inter         I, the routed expert's intermediate width; multiple of 32
+ *   n_experts     E, 1..4096
+ *   topk          K, 1..32 and <= E
+ *   group         MXFP4 block size; must be 32
+ *   shared_inter  SI, the shared expert's intermediate width (multiple of 32), or 0 for
+ *                 no shared expert
+ *   situ_b1/b2    SiTU caps (4 and 25 in the model)
+ *   routed_scale  factor applied to every routed weight after renormalisation
+ *   renorm        1: divide the K selected scores by their sum when it is > 0          */
+typedef struct {
+    int32_t hidden, inter, n_experts, topk, group, shared_inter;
+    float situ_b1, situ_b2, routed_scale;
+    int32_t renorm;
+} k3moe_dims;
+
+/* Routed expert weights.  Expert e is the record at experts + e * expert_stride bytes.
+ * One record holds six operands, in this order (byte offsets from
+ * k3moe_record_layout):
+ *   w1 (gate) packed [I][H/2]   w1 scales [I][H/32]
+ *   w2 (down) packed [H][I/2]   w2 scales [H][I/32]
+ *   w3 (up)   packed [I][H/2]   w3 scales [I][H/32]
+ * Packed byte = two E2M1 codes, the low nibble the EVEN column (kimi-k3-in-c,
+ * section 4); scale byte = E8M0, value 2^(s-127), with 255 read as 0 (the group then
+ * contributes nothing).  For H = 7168, I = 1536 a record is 17,547,264 bytes
+ * (kimi-k3-in-c, "The problem: a model that does not fit", shard census).
+ * expert_stride must be >= the record size and a multiple of 16.                   */
+typedef struct {
+    const uint8_t *experts;
+    int64_t expert_stride;
+} k3moe_experts;
+
+/* Byte offsets of the six operands and the record size:
+ * offsets[0..5] = w1p, w1s, w2p, w2s, w3p, w3s; offsets[6] = total.  Host only. */
+k3moe_status k3moe_record_layout(const k3moe_dims *dims, int64_t offsets[7]);
+
+/* Bytes of workspace k3moe_route / k3moe_expert_ffn_mxfp4 / k3moe_layer need for T
+ * tokens.  Host only; 0 for invalid dims. */
+size_t k3moe_workspace_size(const k3moe_dims *dims, int32_t T);
+
+/* Router (kimi-k3-in-c, section 9).  For each token t:
+ *   logit[e] = sum_i x[t,i] Wr[e,i]  rounded to float; every bf16 product is exact in
+ *              float and the sum is carried as a float-float pair (about 48
+ *              significant bits), so the rounded logit agrees with a double sum
+ *              except for a vanishing fraction of inputs;
+ *   sc[e]    = 1 / (1 + exp(-logit[e])) evaluated in double, rounded to float;
+ *   ch[e]    = sc[e] + bias[e] (one float add; bias may be NULL = 0);
+ *   idx[t,:] = the K experts of largest ch, in descending ch, an equal ch going to the
+ *              lower expert index (the page's repeated strict maximum);
+ *   w[t,j]   = sc[idx[t,j]]; if renorm and s = sum_j w[t,j] (float, j order) > 0 then
+ *              w[t,j] /= s; then w[t,j] *= routed_scale.
+ * x_bf16 [T][H], wr_bf16 [E][H], bias [E] float, idx [T][K] int32, w [T][K] float.
+ * A non-finite ch sets K3MOE_ERR_NONFINITE (idx/w of that token are then undefined
+ * but written).  Needs k3moe_workspace_size(dims, T) bytes of workspace.          */
+k3moe_status k3moe_route(const k3moe_dims *dims, const uint16_t *x_bf16,
+                         const uint16_t *wr_bf16, const float *bias, int32_t T, int32_t *idx,
+                         float *w, void *workspace, size_t ws_bytes, int32_t *status_dev,
+                         k3moe_stream_t stream);
+
+/* Routed expert FFN straight from MXFP4 (kimi-k3-in-c, sections 4 and 9):
+ *   for each token t and slot j, e = idx[t,j]:
+ *     g = W1_e x_t, u = W3_e x_t                         (MXFP4, fp32 accumulate)
+ *     a = b1 tanh(g/b1) sigmoid(g) * b2 tanh(u/b2)      (SiTU-GLU, uncapped sigmoid)
+ *     d_j = W2_e a
+ *   y_t (=|+=) sum_{j=0}^{K-1} w[t,j] d_j               (float, in router order j)
+ * x_bf16 [T][H]; idx/w [T][K]; y [T][H] of dtype ydt.  accumulate = 1 adds to the
+ * existing y (for bf16: y = bf16(float(y) + sum)).  An idx outside [0, E) sets
+ * K3MOE_ERR_BAD_EXPERT and that slot contributes zero.                                */
+k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                                    const k3moe_experts *experts, const int32_t *idx,
+                                    const float *w, void *y, k3moe_dtype ydt,
+                                    int32_t accumulate, void *workspace, size_t ws_bytes,
+                                    int32_t *status_dev, k3moe_stream_t stream);
+
+/* The whole layer step: route, routed expert FFN, router-order combine, then the shared
+ * expert added unweighted (kimi-k3-in-c, section 9, LatentMoE listing step 6):
+ *   y_t (=|+=) sum_j w[t,j] d_j  +  W2s SiTU(W1s x_t, W3s x_t)
+ * sh_gate/sh_up bf16 [SI][H], sh_down bf16 [H][SI] (all NULL when SI = 0).
+ * idx_out [T][K] / w_out [T][K] receive the route when not NULL.                     */
+k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                         const uint16_t *wr_bf16, const float *bias,
+                         const k3moe_experts *experts, const uint16_t *sh_gate,
+                         const uint16_t *sh_up, const uint16_t *sh_down, int32_t *idx_out,
+                         float *w_out, void *y, k3moe_dtype ydt, int32_t accumulate,
+                         void *workspace, size_t ws_bytes, int32_t *status_dev,
+                         k3moe_stream_t stream);
+
+/* RMSNorm then bf16 (kimi-k3-in-c, section 5): for each of T rows of width n,
+ *   inv = 1 / sqrt(mean(h^2) + eps) (sum of squares in double), out = bf16(h * inv),
+ * round to nearest even.  h float [T][n], out bf16 [T][n].  The step between stacked
+ * MoE layers (the decoder's residual stream feeds the next layer's input).            */
+k3moe_status k3moe_rmsnorm_bf16(const float *h, int32_t T, int32_t n, float eps,
+                                uint16_t *out, k3moe_stream_t stream);
+
+/* Test hook, not on the hot path: dequantise an MXFP4 matrix to float through the same
+ * device decode the FFN kernels use (E2M1 pair -> f16x2 in registers, then the E8M0
+ * scale).  packed [rows][cols/2], scales [rows][cols/32], out [rows][cols] float;
+ * cols a multiple of 32.  Exact: every E2M1 * 2^(s-127) is a float.                  */
+k3moe_status k3moe_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int32_t rows,
+                                 int32_t cols, float *out, k3moe_stream_t stream);
+
+/* Tracing (no counterpart in the pages, which time whole tokens on the host).  When on,
+ * every kernel the library launches is bracketed by two CUDA events on its stream and
+ * its device duration is summed per kernel.  k3moe_trace_enable(1) clears the sums and
+ * starts; (0) stops.  k3moe_trace_read(k, ...) synchronises on the recorded events and
+ * returns kernel k's name (static string), total milliseconds and launch count; it
+ * returns the number of kernels (k < 0 only queries that), or -1 for an invalid k.
+ * Host only; not for use inside CUDA graph capture.                                  */
+k3moe_status k3moe_trace_enable(int32_t on);
+int32_t k3moe_trace_read(int32_t kernel, const char **name, double *total_ms, int64_t *launches);
+
+/* Static string for a status code. */
+const char *k3moe_status_str(k3moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3MOE_H */

@@ -1,0 +1,457 @@
+// k3moe_api.cu -- the C ABI of libk3moe: argument checks, workspace layout, launches.
+//
+// Operation definitions and the error contract are in include/k3moe.h.  Every step of
+// the path runs in this library's kernels; nothing here computes on the host.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "k3moe_kernels.cuh"
+
+using namespace k3;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int sms = 0;
+  bool attrs_set = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t up16(size_t n) { return (n + 15) & ~size_t(15); }
+
+// Per-device one-time set-up: SM count and the dynamic shared-memory limits.
+const DeviceInfo *device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.attrs_set) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    const int big = 200 * 1024;
+    if (cudaFuncSetAttribute(k_router_shared, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_down_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_dispatch, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+            cudaSuccess)
+      return nullptr;
+    d.attrs_set = true;
+  }
+  return &d;
+}
+
+// Lanes per pair in the down kernel: the largest power of two <= 32 dividing I/32 with
+// at most 8 groups per lane; 0 if none.
+int down_lanes(int I) {
+  const int G2 = I / kGroup;
+  for (int lr = 32; lr >= 1; lr >>= 1)
+    if (G2 % lr == 0 && G2 / lr <= 8) return lr;
+  return 0;
+}
+
+k3moe_status check_dims(const k3moe_dims *d) {
+  if (!d) return K3MOE_ERR_ARG;
+  if (d->group != kGroup) return K3MOE_ERR_SHAPE;
+  if (d->hidden < 32 || d->hidden > 8192 || d->hidden % 32) return K3MOE_ERR_SHAPE;
+  if (d->inter < 32 || d->inter > 16384 || d->inter % 32) return K3MOE_ERR_SHAPE;
+  if (d->n_experts < 1 || d->n_experts > 4096) return K3MOE_ERR_SHAPE;
+  if (d->topk < 1 || d->topk > 32 || d->topk > d->n_experts) return K3MOE_ERR_SHAPE;
+  if (d->shared_inter < 0 || d->shared_inter > 65536 || d->shared_inter % 32) return K3MOE_ERR_SHAPE;
+  if (!(d->situ_b1 > 0.f) || !(d->situ_b2 > 0.f)) return K3MOE_ERR_ARG;
+  if (!(d->routed_scale == d->routed_scale)) return K3MOE_ERR_ARG;
+  if (down_lanes(d->inter) == 0) return K3MOE_ERR_SHAPE;
+  return K3MOE_OK;
+}
+
+void record_offsets(const k3moe_dims *d, int64_t off[7]) {
+  const int64_t H = d->hidden, I = d->inter;
+  const int64_t gp = I * (H / 2), gs = I * (H / 32), dp = H * (I / 2), ds = H * (I / 32);
+  off[0] = 0;
+  off[1] = gp;
+  off[2] = off[1] + gs;
+  off[3] = off[2] + dp;
+  off[4] = off[3] + ds;
+  off[5] = off[4] + gp;
+  off[6] = off[5] + gs;
+}
+
+// Workspace carve-up for one pass of up to kDecodeTokens tokens.
+struct Ws {
+  float *logits;
+  int32_t *idx;
+  float *w;
+  int32_t *disp;
+  uint16_t *act_hi, *act_lo;
+  int32_t *act_ex;
+  float *act_s;
+  size_t total;
+};
+
+Ws ws_layout(const k3moe_dims *d, int T, void *base) {
+  const int Tc = T < kDecodeTokens ? T : kDecodeTokens;
+  const size_t P = (size_t)Tc * d->topk;
+  size_t o = 0;
+  Ws w{};
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += up16(bytes);
+    return reinterpret_cast<uint8_t *>(b + at);
+  };
+  w.logits = reinterpret_cast<float *>(take((size_t)Tc * d->n_experts * 4));
+  w.idx = reinterpret_cast<int32_t *>(take(P * 4));
+  w.w = reinterpret_cast<float *>(take(P * 4));
+  w.disp = reinterpret_cast<int32_t *>(take((size_t)disp_words((int)P) * 4));
+  w.act_hi = reinterpret_cast<uint16_t *>(take(P * d->inter * 2));
+  w.act_lo = reinterpret_cast<uint16_t *>(take(P * d->inter * 2));
+  w.act_ex = reinterpret_cast<int32_t *>(take(P * (d->inter / kGroup) * 4));
+  w.act_s = reinterpret_cast<float *>(take((size_t)Tc * (d->shared_inter > 0 ? d->shared_inter : 1) * 4));
+  w.total = o;
+  return w;
+}
+
+k3moe_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+// ---- tracing: CUDA events around every launch, durations summed per kernel ---------
+enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KID_RMSNORM,
+                KID_DEQUANT, KID_COUNT };
+const char *const kKernelNames[KID_COUNT] = {"k_router_shared", "k_topk", "k_dispatch",
+                                             "k_expert_gateup", "k_down_combine",
+                                             "k_rmsnorm_bf16", "k_dequant"};
+struct TraceRec {
+  int kid;
+  cudaEvent_t a, b;
+};
+struct Trace {
+  bool on = false;
+  std::vector<TraceRec> pending;
+  std::vector<cudaEvent_t> pool;
+  double total_ms[KID_COUNT] = {};
+  long long launches[KID_COUNT] = {};
+} g_trace;
+
+cudaEvent_t trace_event() {
+  if (!g_trace.pool.empty()) {
+    cudaEvent_t e = g_trace.pool.back();
+    g_trace.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one launch: call with the kernel id before (returns a token) and after.
+struct TraceScope {
+  int kid;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  TraceScope(int k, cudaStream_t s) : kid(k), st(s) {
+    if (g_trace.on) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      a = trace_event();
+      cudaEventRecord(a, st);
+    }
+  }
+  ~TraceScope() {
+    if (a) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      cudaEvent_t b = trace_event();
+      cudaEventRecord(b, st);
+      g_trace.pending.push_back({kid, a, b});
+    }
+  }
+};
+
+void trace_drain() {
+  for (auto &r : g_trace.pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      g_trace.total_ms[r.kid] += ms;
+      g_trace.launches[r.kid] += 1;
+    }
+    g_trace.pool.push_back(r.a);
+    g_trace.pool.push_back(r.b);
+  }
+  g_trace.pending.clear();
+}
+
+int tok_chunk_router(int H) {
+  int tc = (160 * 1024) / (2 * H);
+  if (tc > kTokChunk) tc = kTokChunk;
+  return tc < 1 ? 1 : tc;
+}
+
+// Router logits (+ shared gate/up when sh_gate != NULL) then top-k for Tc tokens.
+k3moe_status run_route(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+                       const uint16_t *wr, const float *bias, const uint16_t *sh_gate,
+                       const uint16_t *sh_up, Ws &ws, int32_t *idx, float *w, int32_t *status,
+                       cudaStream_t st) {
+  const int H = d->hidden, E = d->n_experts, SI = sh_gate ? d->shared_inter : 0;
+  const int tc = tok_chunk_router(H);
+  const int rows = E + SI;
+  int grid = (rows + 7) / 8;
+  if (grid > 8 * di->sms) grid = 8 * di->sms;
+  {
+  TraceScope ts(KID_ROUTER, st);
+  k_router_shared<<<grid, 256, (size_t)tc * H * 2, st>>>(x, Tc, H, wr, E, sh_gate, sh_up, SI,
+                                                        d->situ_b1, d->situ_b2, ws.logits,
+                                                        ws.act_s, tc);
+  }
+  const size_t tk_smem = (size_t)E * 8 + 8 * d->topk * 4;
+  {
+    TraceScope ts(KID_TOPK, st);
+    k_topk<<<Tc, 256, tk_smem, st>>>(ws.logits, bias, Tc, E, d->topk, d->renorm, d->routed_scale,
+                                     idx, w, status);
+  }
+  return launch_status();
+}
+
+// Dispatch + gate/up + down/combine for Tc tokens.
+k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+                     const k3moe_experts *ex, const int32_t *idx, const float *w,
+                     const uint16_t *sh_down, Ws &ws, void *y, k3moe_dtype ydt, int accumulate,
+                     int32_t *status, cudaStream_t st) {
+  const int H = d->hidden, I = d->inter, K = d->topk, E = d->n_experts;
+  const int P = Tc * K;
+  int Pp = 1;
+  while (Pp < P) Pp <<= 1;
+  int nt = Pp < 32 ? 32 : (Pp > 1024 ? 1024 : Pp);
+  {
+    TraceScope ts(KID_DISPATCH, st);
+    k_dispatch<<<1, nt, (size_t)2 * Pp * 4, st>>>(idx, P, E, ws.disp, status);
+  }
+
+  ExpertArgs ea;
+  ea.base = ex->experts;
+  ea.stride = ex->expert_stride;
+  int64_t off[7];
+  record_offsets(d, off);
+  for (int i = 0; i < 6; i++) ea.off[i] = off[i];
+
+  const int G = H / kGroup;
+  const bool pathB = (G <= 16) && ((G & (G - 1)) == 0);
+  const int maxU = P < E ? P : E;
+  const int tiles = I / kTileRows;
+  int grid = maxU * tiles;
+  if (grid > 16 * di->sms) grid = 16 * di->sms;
+  const int mb = Tc == 1 ? 1 : 2;
+  int bd = pathB ? 256 : ((G + 31) / 32) * 32;
+  if (bd < 32 * mb) bd = 32 * mb;
+  {
+    TraceScope ts(KID_GATEUP, st);
+    if (launch_expert_gateup(mb, grid, bd, st, x, H, I, K, ea, ws.disp, P, d->situ_b1,
+                             d->situ_b2, ws.act_hi, ws.act_lo, ws.act_ex) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+  }
+  const int LR = down_lanes(I);
+  const size_t dsmem = ((size_t)P * kDownRows + 256 * kDownRows + (size_t)Tc * kDownRows) * 4;
+  int dgrid = H / kDownRows;
+  TraceScope ts(KID_DOWN, st);
+  k_down_combine<<<dgrid, 256, dsmem, st>>>(Tc, H, I, K, ea, idx, w, ws.disp, P, ws.act_hi,
+                                            ws.act_lo, ws.act_ex, sh_down,
+                                            sh_down ? d->shared_inter : 0, ws.act_s, y, (int)ydt,
+                                            accumulate, LR);
+  return launch_status();
+}
+
+size_t dtype_size(k3moe_dtype t) { return t == K3MOE_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+const char *k3moe_status_str(k3moe_status s) {
+  switch (s) {
+    case K3MOE_OK: return "ok";
+    case K3MOE_ERR_ARG: return "invalid argument";
+    case K3MOE_ERR_SHAPE: return "unsupported shape";
+    case K3MOE_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case K3MOE_ERR_WORKSPACE: return "workspace too small";
+    case K3MOE_ERR_CUDA: return "CUDA launch failed";
+    case K3MOE_ERR_TIMEOUT: return "device wait timed out";
+    case K3MOE_ERR_BAD_EXPERT: return "expert index out of range";
+    case K3MOE_ERR_NONFINITE: return "non-finite router score";
+  }
+  return "unknown status";
+}
+
+k3moe_status k3moe_record_layout(const k3moe_dims *dims, int64_t offsets[7]) {
+  const k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (!offsets) return K3MOE_ERR_ARG;
+  record_offsets(dims, offsets);
+  return K3MOE_OK;
+}
+
+size_t k3moe_workspace_size(const k3moe_dims *dims, int32_t T) {
+  if (check_dims(dims) != K3MOE_OK || T < 0) return 0;
+  if (T == 0) return 16;
+  return ws_layout(dims, T, nullptr).total;
+}
+
+k3moe_status k3moe_route(const k3moe_dims *dims, const uint16_t *x_bf16, const uint16_t *wr_bf16,
+                         const float *bias, int32_t T, int32_t *idx, float *w, void *workspace,
+                         size_t ws_bytes, int32_t *status_dev, k3moe_stream_t stream) {
+  k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (T < 0) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!x_bf16 || !wr_bf16 || !idx || !w || !workspace || !status_dev) return K3MOE_ERR_ARG;
+  if (!aligned16(x_bf16) || !aligned16(wr_bf16) || !aligned16(workspace) ||
+      (bias && !aligned16(bias)) || !aligned16(idx) || !aligned16(w))
+    return K3MOE_ERR_ALIGN;
+  if (ws_bytes < k3moe_workspace_size(dims, T)) return K3MOE_ERR_WORKSPACE;
+  const DeviceInfo *di = device_info();
+  if (!di) return K3MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Ws ws = ws_layout(dims, T, workspace);
+  const int H = dims->hidden, K = dims->topk;
+  for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
+    const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
+    s = run_route(di, dims, x_bf16 + (size_t)t0 * H, Tc, wr_bf16, bias, nullptr, nullptr, ws,
+                  idx + (size_t)t0 * K, w + (size_t)t0 * K, status_dev, st);
+    if (s != K3MOE_OK) return s;
+  }
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                                    const k3moe_experts *experts, const int32_t *idx,
+                                    const float *w, void *y, k3moe_dtype ydt, int32_t accumulate,
+                                    void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                    k3moe_stream_t stream) {
+  k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (T < 0 || (ydt != K3MOE_F32 && ydt != K3MOE_BF16)) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!x_bf16 || !experts || !experts->experts || !idx || !w || !y || !workspace || !status_dev)
+    return K3MOE_ERR_ARG;
+  int64_t off[7];
+  record_offsets(dims, off);
+  if (experts->expert_stride < off[6] || experts->expert_stride % 16) return K3MOE_ERR_ALIGN;
+  if (!aligned16(x_bf16) || !aligned16(experts->experts) || !aligned16(idx) || !aligned16(w) ||
+      !aligned16(y) || !aligned16(workspace))
+    return K3MOE_ERR_ALIGN;
+  if (ws_bytes < k3moe_workspace_size(dims, T)) return K3MOE_ERR_WORKSPACE;
+  const DeviceInfo *di = device_info();
+  if (!di) return K3MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Ws ws = ws_layout(dims, T, workspace);
+  const int H = dims->hidden, K = dims->topk;
+  for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
+    const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
+    s = run_ffn(di, dims, x_bf16 + (size_t)t0 * H, Tc, experts, idx + (size_t)t0 * K,
+                w + (size_t)t0 * K, nullptr, ws,
+                static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt, accumulate,
+                status_dev, st);
+    if (s != K3MOE_OK) return s;
+  }
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                         const uint16_t *wr_bf16, const float *bias, const k3moe_experts *experts,
+                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
+                         int32_t *idx_out, float *w_out, void *y, k3moe_dtype ydt,
+                         int32_t accumulate, void *workspace, size_t ws_bytes,
+                         int32_t *status_dev, k3moe_stream_t stream) {
+  k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (T < 0 || (ydt != K3MOE_F32 && ydt != K3MOE_BF16)) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!x_bf16 || !wr_bf16 || !experts || !experts->experts || !y || !workspace || !status_dev)
+    return K3MOE_ERR_ARG;
+  const bool shared = dims->shared_inter > 0;
+  if (shared && (!sh_gate || !sh_up || !sh_down)) return K3MOE_ERR_ARG;
+  if ((idx_out == nullptr) != (w_out == nullptr)) return K3MOE_ERR_ARG;
+  int64_t off[7];
+  record_offsets(dims, off);
+  if (experts->expert_stride < off[6] || experts->expert_stride % 16) return K3MOE_ERR_ALIGN;
+  if (!aligned16(x_bf16) || !aligned16(wr_bf16) || !aligned16(experts->experts) ||
+      !aligned16(y) || !aligned16(workspace) || (bias && !aligned16(bias)) ||
+      (idx_out && (!aligned16(idx_out) || !aligned16(w_out))) ||
+      (shared && (!aligned16(sh_gate) || !aligned16(sh_up) || !aligned16(sh_down))))
+    return K3MOE_ERR_ALIGN;
+  if (ws_bytes < k3moe_workspace_size(dims, T)) return K3MOE_ERR_WORKSPACE;
+  const DeviceInfo *di = device_info();
+  if (!di) return K3MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Ws ws = ws_layout(dims, T, workspace);
+  const int H = dims->hidden, K = dims->topk;
+  for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
+    const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
+    int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : ws.idx;
+    float *w_c = w_out ? w_out + (size_t)t0 * K : ws.w;
+    const uint16_t *xc = x_bf16 + (size_t)t0 * H;
+    s = run_route(di, dims, xc, Tc, wr_bf16, bias, shared ? sh_gate : nullptr,
+                  shared ? sh_up : nullptr, ws, idx_c, w_c, status_dev, st);
+    if (s != K3MOE_OK) return s;
+    s = run_ffn(di, dims, xc, Tc, experts, idx_c, w_c, shared ? sh_down : nullptr, ws,
+                static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt, accumulate,
+                status_dev, st);
+    if (s != K3MOE_OK) return s;
+  }
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_rmsnorm_bf16(const float *h, int32_t T, int32_t n, float eps, uint16_t *out,
+                                k3moe_stream_t stream) {
+  if (T < 0 || n < 1 || !(eps >= 0.f)) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!h || !out) return K3MOE_ERR_ARG;
+  if (!aligned16(h) || !aligned16(out)) return K3MOE_ERR_ALIGN;
+  TraceScope ts(KID_RMSNORM, reinterpret_cast<cudaStream_t>(stream));
+  k_rmsnorm_bf16<<<T, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(h, T, n, eps, out);
+  return launch_status();
+}
+
+k3moe_status k3moe_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int32_t rows,
+                                 int32_t cols, float *out, k3moe_stream_t stream) {
+  if (rows < 0 || cols < 0 || cols % kGroup) return cols % kGroup ? K3MOE_ERR_SHAPE : K3MOE_ERR_ARG;
+  if (rows == 0 || cols == 0) return K3MOE_OK;
+  if (!packed || !scales || !out) return K3MOE_ERR_ARG;
+  if (!aligned16(packed) || !aligned16(out)) return K3MOE_ERR_ALIGN;
+  const long long n = (long long)rows * (cols / kGroup);
+  int grid = (int)((n + 255) / 256);
+  if (grid > 4096) grid = 4096;
+  TraceScope ts(KID_DEQUANT, reinterpret_cast<cudaStream_t>(stream));
+  k_dequant<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(packed, scales, rows, cols,
+                                                                    out);
+  return launch_status();
+}
+
+k3moe_status k3moe_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  trace_drain();
+  for (int k = 0; k < KID_COUNT; k++) {
+    g_trace.total_ms[k] = 0.0;
+    g_trace.launches[k] = 0;
+  }
+  g_trace.on = on != 0;
+  return K3MOE_OK;
+}
+
+int32_t k3moe_trace_read(int32_t kernel, const char **name, double *total_ms, int64_t *launches) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (kernel < 0) return KID_COUNT;
+  if (kernel >= KID_COUNT) return -1;
+  trace_drain();
+  if (name) *name = kKernelNames[kernel];
+  if (total_ms) *total_ms = g_trace.total_ms[kernel];
+  if (launches) *launches = g_trace.launches[kernel];
+  return KID_COUNT;
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// k3moe_device.cuh -- device helpers shared by the k3moe kernels (sm_103a).
+//
+// Number formats follow the README of FareedKhan-dev/kimi-k3-in-c, section 4
+// "Reduction one: the experts already ship at half a byte": a weight is an E2M1 code
+// (sign, two exponent bits, one mantissa bit) times an E8M0 scale 2^(s-127) shared by
+// 32 consecutive weights of a row; scale byte 255 reads as 0; in a packed byte the low
+// nibble is the even column.  bf16 widening is a 16-bit shift (section 5).
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "k3moe.h"
+
+namespace k3 {
+
+constexpr int kGroup = 32;  // MXFP4 block size
+
+// First error wins; later errors leave the word alone.
+__device__ __forceinline__ void set_status(int32_t *st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// float -> bf16 bits, round to nearest even (NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+// 2^e as a float: exact for -149 <= e <= 127, 0 below, +inf above.
+__device__ __forceinline__ float pow2i(int e) {
+  if (e >= -126 && e <= 127) return __int_as_float((e + 127) << 23);
+  if (e > 127) return __int_as_float(0x7f800000);
+  if (e >= -149) return __int_as_float(1 << (e + 149));
+  return 0.f;
+}
+
+// Unbiased exponent of a finite nonzero float's magnitude (floor(log2|v|)); the
+// subnormal range reports -127 (callers clamp).
+__device__ __forceinline__ int exponent_of(float v) {
+  return (int)((__float_as_uint(v) >> 23) & 0xff) - 127;
+}
+
+// One packed MXFP4 byte (two E2M1 codes) -> f16x2 with the low nibble (even column)
+// in the low half.  Hardware conversion, exact (every E2M1 value is an f16).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
+  uint32_t h;
+  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }"
+      : "=r"(h)
+      : "r"(byte_in_low_bits));
+  return h;
+}
+
+// Four packed bytes (eight E2M1 codes, columns 0..7 of the word) -> four f16x2.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t q, uint32_t &h0, uint32_t &h1,
+                                                  uint32_t &h2, uint32_t &h3) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(q));
+}
+
+// c + x.lo * w.lo + x.hi * w.hi with f16 operands and an f32 accumulator: each product
+// is exact (f16 x f16 fits in f32) and each add rounds once to f32.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t x2, uint32_t w2, float c) {
+  float d;
+  asm("{ .reg .b16 xl, xh, wl, wh; mov.b32 {xl, xh}, %1; mov.b32 {wl, wh}, %2;\n"
+      "  fma.rn.f32.f16 %0, xl, wl, %3; fma.rn.f32.f16 %0, xh, wh, %0; }"
+      : "=f"(d)
+      : "r"(x2), "r"(w2), "f"(c));
+  return d;
+}
+
+// Sum over the 32 columns of one MXFP4 group: sum_k x'[k] * e2m1[k] (unscaled), with
+// x' given as 16 f16x2 registers (pair p = columns 2p, 2p+1) and the weights as the 16
+// packed bytes of the group (4 words).  Two accumulators for latency.
+__device__ __forceinline__ float group_dot(const uint32_t (&x)[16], uint4 w) {
+  float a = 0.f, b = 0.f;
+  uint32_t h0, h1, h2, h3;
+  e2m1x8_to_f16x2x4(w.x, h0, h1, h2, h3);
+  a = fma2_f16_f32(x[0], h0, a); b = fma2_f16_f32(x[1], h1, b);
+  a = fma2_f16_f32(x[2], h2, a); b = fma2_f16_f32(x[3], h3, b);
+  e2m1x8_to_f16x2x4(w.y, h0, h1, h2, h3);
+  a = fma2_f16_f32(x[4], h0, a); b = fma2_f16_f32(x[5], h1, b);
+  a = fma2_f16_f32(x[6], h2, a); b = fma2_f16_f32(x[7], h3, b);
+  e2m1x8_to_f16x2x4(w.z, h0, h1, h2, h3);
+  a = fma2_f16_f32(x[8], h0, a); b = fma2_f16_f32(x[9], h1, b);
+  a = fma2_f16_f32(x[10], h2, a); b = fma2_f16_f32(x[11], h3, b);
+  e2m1x8_to_f16x2x4(w.w, h0, h1, h2, h3);
+  a = fma2_f16_f32(x[12], h0, a); b = fma2_f16_f32(x[13], h1, b);
+  a = fma2_f16_f32(x[14], h2, a); b = fma2_f16_f32(x[15], h3, b);
+  return a + b;
+}
+
+// Same with x' = hi + lo (two f16 terms per column): sum_k (hi[k] + lo[k]) * e2m1[k].
+__device__ __forceinline__ float group_dot2(const uint32_t (&xh)[16], const uint32_t (&xl)[16],
+                                            uint4 w) {
+  float a = 0.f, b = 0.f;
+  uint32_t h[4];
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; q++) {
+    e2m1x8_to_f16x2x4(ww[q], h[0], h[1], h[2], h[3]);
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+      a = fma2_f16_f32(xh[4 * q + p], h[p], a);
+      b = fma2_f16_f32(xl[4 * q + p], h[p], b);
+    }
+  }
+  return a + b;
+}
+
+// Factor turning an unscaled group sum into its contribution: 2^(s - 127 + ex) where s
+// is the E8M0 scale byte and ex the exponent the activation group was scaled by; a
+// scale byte of 255 contributes nothing.
+__device__ __forceinline__ float group_factor(uint32_t s, int ex) {
+  return (s == 255u) ? 0.f : pow2i((int)s - 127 + ex);
+}
+
+// Prescale a group of 32 activations to f16: x' = x * 2^-ex with ex chosen so that
+// max|x'| lies in [2^14, 2^15) (every bf16 value then converts to f16 exactly, bar
+// values more than 2^28 below the group maximum).  Returns ex.
+__device__ __forceinline__ int prescale_group_f16(const float (&v)[32], uint32_t (&out)[16]) {
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; k++) m = fmaxf(m, fabsf(v[k]));
+  int ex = 0;
+  if (m > 0.f) {
+    ex = exponent_of(m) - 14;
+    ex = ex < -110 ? -110 : ex;
+  }
+  const float s = pow2i(-ex);
+#pragma unroll
+  for (int p = 0; p < 16; p++) {
+    __half2 h = __floats2half2_rn(v[2 * p] * s, v[2 * p + 1] * s);
+    out[p] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  return ex;
+}
+
+// SiTU-GLU (kimi-k3-in-c, section 9): the sigmoid takes the uncapped gate.
+__device__ __forceinline__ float situ(float g, float u, float b1, float b2) {
+  const float a = b1 * tanhf(g / b1) * (1.f / (1.f + expf(-g)));
+  const float v = b2 * tanhf(u / b2);
+  return a * v;
+}
+
+// Error-free sum (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// (hi, lo) += (bh, bl) for float-float pairs, renormalised.
+__device__ __forceinline__ void ff_add(float &hi, float &lo, float bh, float bl) {
+  float s, e;
+  two_sum(hi, bh, s, e);
+  e = __fadd_rn(e, __fadd_rn(lo, bl));
+  hi = __fadd_rn(s, e);
+  lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
+}  // namespace k3

@@ -1,0 +1,62 @@
+// k3moe_kernels.cuh -- kernel declarations and launch-shape constants of libk3moe.
+#pragma once
+#include "k3moe_device.cuh"
+
+namespace k3 {
+
+constexpr int kTokChunk = 8;      // tokens of x staged in shared memory by k_router_shared
+constexpr int kDecodeTokens = 64; // tokens per pass of the decode expert path
+constexpr int kTileRows = 32;     // gate/up output rows per work item (one down-input group)
+constexpr int kDownRows = 16;     // down output rows per work item
+constexpr int kPairKeyShift = 12; // dispatch sort key = expert << 12 | pair id (pairs < 4096)
+
+// Dispatch buffer (int32), for P = T*K (token, slot) pairs:
+//   [0]            U, the number of distinct experts used
+//   [4 .. 4+P)     uexp[u], the distinct experts, ascending
+//   [4+P .. 5+2P)  uoff[u], start of expert u's pairs in plist (uoff[U] = valid pairs)
+//   [5+2P .. 5+3P) plist, pair ids t*K + j sorted by (expert, pair id)
+__host__ __device__ inline int disp_words(int P) { return 5 + 3 * P; }
+
+__global__ void k_router_shared(const uint16_t *__restrict__ x, int T, int H,
+                                const uint16_t *__restrict__ wr, int E,
+                                const uint16_t *__restrict__ sh_gate,
+                                const uint16_t *__restrict__ sh_up, int SI, float b1, float b2,
+                                float *__restrict__ logits, float *__restrict__ act_s,
+                                int tc_max);
+
+__global__ void k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T,
+                       int E, int K, int renorm, float routed_scale, int32_t *__restrict__ idx,
+                       float *__restrict__ w, int32_t *status);
+
+__global__ void k_dispatch(const int32_t *__restrict__ idx, int P, int E,
+                           int32_t *__restrict__ disp, int32_t *status);
+
+struct ExpertArgs {
+  const uint8_t *base;
+  long long stride;
+  long long off[6];  // w1p, w1s, w2p, w2s, w3p, w3s
+};
+
+// Launches k_expert_gateup<mb> (mb = tokens per register block: 1 or 2).
+cudaError_t launch_expert_gateup(int mb, int grid, int block, cudaStream_t st, const uint16_t *x,
+                                 int H, int I, int K, const ExpertArgs &ex, const int32_t *disp,
+                                 int P, float b1, float b2, uint16_t *act_hi, uint16_t *act_lo,
+                                 int32_t *act_ex);
+
+__global__ void k_down_combine(int T, int H, int I, int K, ExpertArgs ex,
+                               const int32_t *__restrict__ idx, const float *__restrict__ w,
+                               const int32_t *__restrict__ disp, int P,
+                               const uint16_t *__restrict__ act_hi,
+                               const uint16_t *__restrict__ act_lo,
+                               const int32_t *__restrict__ act_ex,
+                               const uint16_t *__restrict__ sh_down, int SI,
+                               const float *__restrict__ act_s, void *y, int ydt,
+                               int accumulate, int LR);
+
+__global__ void k_dequant(const uint8_t *__restrict__ packed, const uint8_t *__restrict__ scales,
+                          int rows, int cols, float *__restrict__ out);
+
+__global__ void k_rmsnorm_bf16(const float *__restrict__ h, int T, int n, float eps,
+                               uint16_t *__restrict__ out);
+
+}  // namespace k3

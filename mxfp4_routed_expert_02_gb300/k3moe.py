@@ -1,0 +1,238 @@
+"""Python binding of libk3moe (the C ABI declared in ``include/k3moe.h``).
+
+Argument marshalling only: each function takes torch CUDA tensors, checks their dtype,
+device and contiguity, and passes raw pointers to the library.  Every step of the MoE
+layer runs in the library's CUDA kernels; there is no CPU or PyTorch fallback: if the
+library cannot be loaded, every call raises.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+K3MOE_OK = 0
+STATUS_NAMES = {
+    0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_WORKSPACE", 5: "ERR_CUDA",
+    6: "ERR_TIMEOUT", 7: "ERR_BAD_EXPERT", 8: "ERR_NONFINITE",
+}
+F32, BF16 = 0, 1
+
+# Every symbol include/k3moe.h declares.
+EXPORTS = (
+    "k3moe_record_layout", "k3moe_workspace_size", "k3moe_route", "k3moe_expert_ffn_mxfp4",
+    "k3moe_layer", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4", "k3moe_trace_enable",
+    "k3moe_trace_read", "k3moe_status_str",
+)
+
+
+class K3MoeError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS_NAMES.get(code, "?"), code))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
+                ("situ_b1", ctypes.c_float), ("situ_b2", ctypes.c_float),
+                ("routed_scale", ctypes.c_float), ("renorm", ctypes.c_int32)]
+
+
+class Experts(ctypes.Structure):
+    _fields_ = [("experts", ctypes.c_void_p), ("expert_stride", ctypes.c_int64)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True):
+    """Load libk3moe.so (building it first if allowed).  Raises if it is unavailable."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libk3moe.so is not built (%s); run __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    dp = ctypes.POINTER(Dims)
+    ep = ctypes.POINTER(Experts)
+    L.k3moe_record_layout.restype = i32
+    L.k3moe_record_layout.argtypes = [dp, ctypes.POINTER(ctypes.c_int64)]
+    L.k3moe_workspace_size.restype = sz
+    L.k3moe_workspace_size.argtypes = [dp, i32]
+    L.k3moe_route.restype = i32
+    L.k3moe_route.argtypes = [dp, vp, vp, vp, i32, vp, vp, vp, sz, vp, vp]
+    L.k3moe_expert_ffn_mxfp4.restype = i32
+    L.k3moe_expert_ffn_mxfp4.argtypes = [dp, vp, i32, ep, vp, vp, vp, i32, i32, vp, sz, vp, vp]
+    L.k3moe_layer.restype = i32
+    L.k3moe_layer.argtypes = [dp, vp, i32, vp, vp, ep, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz,
+                              vp, vp]
+    L.k3moe_rmsnorm_bf16.restype = i32
+    L.k3moe_rmsnorm_bf16.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
+    L.k3moe_dequant_mxfp4.restype = i32
+    L.k3moe_dequant_mxfp4.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.k3moe_trace_enable.restype = i32
+    L.k3moe_trace_enable.argtypes = [i32]
+    L.k3moe_trace_read.restype = i32
+    L.k3moe_trace_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p),
+                                   ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+    L.k3moe_status_str.restype = ctypes.c_char_p
+    L.k3moe_status_str.argtypes = [i32]
+    _LIB = L
+    return L
+
+
+@dataclass
+class LayerDims:
+    hidden: int
+    inter: int
+    n_experts: int
+    topk: int
+    shared_inter: int = 0
+    situ_b1: float = 4.0
+    situ_b2: float = 25.0
+    routed_scale: float = 1.0
+    renorm: int = 1
+    group: int = 32
+
+    def c(self) -> Dims:
+        return Dims(self.hidden, self.inter, self.n_experts, self.topk, self.group,
+                    self.shared_inter, self.situ_b1, self.situ_b2, self.routed_scale, self.renorm)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, code):
+    if code != K3MOE_OK:
+        raise K3MoeError(fn, code)
+
+
+def _bits16(t, name):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16)
+    if t.dtype not in (torch.int16, torch.uint16):
+        raise TypeError("%s must be bf16 (or its 16-bit pattern)" % name)
+    return t
+
+
+def record_layout(dims: LayerDims):
+    off = (ctypes.c_int64 * 7)()
+    d = dims.c()
+    _check("k3moe_record_layout", lib().k3moe_record_layout(ctypes.byref(d), off))
+    return list(off)
+
+
+def workspace_size(dims: LayerDims, T: int) -> int:
+    d = dims.c()
+    return int(lib().k3moe_workspace_size(ctypes.byref(d), int(T)))
+
+
+def new_workspace(dims: LayerDims, T: int, device=None) -> torch.Tensor:
+    n = workspace_size(dims, T)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def k3moe_route(dims: LayerDims, x, wr, bias, idx, w, workspace, status, stream=None):
+    d = dims.c()
+    x, wr = _bits16(x, "x"), _bits16(wr, "wr")
+    T = x.shape[0]
+    _check("k3moe_route", lib().k3moe_route(
+        ctypes.byref(d), _ptr(x), _ptr(wr), _ptr(bias), T, _ptr(idx), _ptr(w), _ptr(workspace),
+        workspace.numel(), _ptr(status), _stream(stream)))
+
+
+def k3moe_expert_ffn_mxfp4(dims: LayerDims, x, experts, expert_stride: int, idx, w, y,
+                           workspace, status, accumulate: bool = False, stream=None):
+    d = dims.c()
+    x = _bits16(x, "x")
+    T = x.shape[0]
+    ydt = F32 if y.dtype == torch.float32 else BF16
+    if ydt == BF16:
+        y = _bits16(y, "y")
+    ex = Experts(ctypes.c_void_p(experts.data_ptr()), int(expert_stride))
+    _check("k3moe_expert_ffn_mxfp4", lib().k3moe_expert_ffn_mxfp4(
+        ctypes.byref(d), _ptr(x), T, ctypes.byref(ex), _ptr(idx), _ptr(w), _ptr(y), ydt,
+        int(bool(accumulate)), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)))
+
+
+def k3moe_layer(dims: LayerDims, x, wr, bias, experts, expert_stride: int, sh_gate, sh_up,
+                sh_down, y, workspace, status, idx_out=None, w_out=None,
+                accumulate: bool = False, stream=None):
+    d = dims.c()
+    x, wr = _bits16(x, "x"), _bits16(wr, "wr")
+    if sh_gate is not None:
+        sh_gate, sh_up, sh_down = (_bits16(sh_gate, "sh_gate"), _bits16(sh_up, "sh_up"),
+                                   _bits16(sh_down, "sh_down"))
+    T = x.shape[0]
+    ydt = F32 if y.dtype == torch.float32 else BF16
+    if ydt == BF16:
+        y = _bits16(y, "y")
+    ex = Experts(ctypes.c_void_p(experts.data_ptr()), int(expert_stride))
+    _check("k3moe_layer", lib().k3moe_layer(
+        ctypes.byref(d), _ptr(x), T, _ptr(wr), _ptr(bias), ctypes.byref(ex), _ptr(sh_gate),
+        _ptr(sh_up), _ptr(sh_down), _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
+        int(bool(accumulate)), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)))
+
+
+def k3moe_rmsnorm_bf16(h, out, eps: float = 1e-5, stream=None):
+    T, n = h.shape
+    out = _bits16(out, "out")
+    _check("k3moe_rmsnorm_bf16", lib().k3moe_rmsnorm_bf16(
+        _ptr(h), T, n, float(eps), _ptr(out), _stream(stream)))
+
+
+def k3moe_dequant_mxfp4(packed, scales, rows: int, cols: int, out, stream=None):
+    _check("k3moe_dequant_mxfp4", lib().k3moe_dequant_mxfp4(
+        _ptr(packed), _ptr(scales), int(rows), int(cols), _ptr(out), _stream(stream)))
+
+
+def status_str(code: int) -> str:
+    return lib().k3moe_status_str(int(code)).decode()
+
+
+def k3moe_trace_enable(on: bool = True):
+    _check("k3moe_trace_enable", lib().k3moe_trace_enable(int(bool(on))))
+
+
+def k3moe_trace_read() -> dict:
+    """{kernel name: (total ms, launches)} for every kernel the library launched."""
+    L = lib()
+    n = L.k3moe_trace_read(-1, None, None, None)
+    out = {}
+    for k in range(n):
+        name = ctypes.c_char_p()
+        ms = ctypes.c_double()
+        cnt = ctypes.c_int64()
+        L.k3moe_trace_read(k, ctypes.byref(name), ctypes.byref(ms), ctypes.byref(cnt))
+        out[name.value.decode()] = (ms.value, cnt.value)
+    return out
