@@ -35,14 +35,14 @@ const DeviceInfo *device_info() {
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return nullptr;
     const int big = 200 * 1024;
-    if (cudaFuncSetAttribute(k_router_shared, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
-            cudaSuccess ||
+    if (set_router_smem_limits(big) != cudaSuccess ||
         cudaFuncSetAttribute(k_down_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, big) !=
             cudaSuccess ||
         cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
             cudaSuccess ||
         cudaFuncSetAttribute(k_dispatch, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
-            cudaSuccess)
+            cudaSuccess ||
+        set_decode_smem_limits() != cudaSuccess)
       return nullptr;
     d.attrs_set = true;
   }
@@ -86,7 +86,7 @@ void record_offsets(const k3moe_dims *d, int64_t off[7]) {
 
 // Workspace carve-up for one pass of up to kDecodeTokens tokens.
 struct Ws {
-  float *logits;
+  float *sc, *ch;
   int32_t *idx;
   float *w;
   int32_t *disp;
@@ -107,7 +107,8 @@ Ws ws_layout(const k3moe_dims *d, int T, void *base) {
     o += up16(bytes);
     return reinterpret_cast<uint8_t *>(b + at);
   };
-  w.logits = reinterpret_cast<float *>(take((size_t)Tc * d->n_experts * 4));
+  w.sc = reinterpret_cast<float *>(take((size_t)Tc * d->n_experts * 4));
+  w.ch = reinterpret_cast<float *>(take((size_t)Tc * d->n_experts * 4));
   w.idx = reinterpret_cast<int32_t *>(take(P * 4));
   w.w = reinterpret_cast<float *>(take(P * 4));
   w.disp = reinterpret_cast<int32_t *>(take((size_t)disp_words((int)P) * 4));
@@ -125,10 +126,11 @@ k3moe_status launch_status() {
 
 // ---- tracing: CUDA events around every launch, durations summed per kernel ---------
 enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KID_RMSNORM,
-                KID_DEQUANT, KID_COUNT };
+                KID_DEQUANT, KID_GATEUP_T1, KID_DOWN_TMA, KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {"k_router_shared", "k_topk", "k_dispatch",
                                              "k_expert_gateup", "k_down_combine",
-                                             "k_rmsnorm_bf16", "k_dequant"};
+                                             "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1",
+                                             "k_down_tma"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -193,32 +195,109 @@ int tok_chunk_router(int H) {
   return tc < 1 ? 1 : tc;
 }
 
-// Router logits (+ shared gate/up when sh_gate != NULL) then top-k for Tc tokens.
+// Router scores (+ shared gate/up when sh_gate != NULL) for Tc tokens; then the top-k
+// kernel unless the caller fuses it into the next kernel (topk = false).
 k3moe_status run_route(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
                        const uint16_t *wr, const float *bias, const uint16_t *sh_gate,
                        const uint16_t *sh_up, Ws &ws, int32_t *idx, float *w, int32_t *status,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool topk) {
   const int H = d->hidden, E = d->n_experts, SI = sh_gate ? d->shared_inter : 0;
-  const int tc = tok_chunk_router(H);
+  int tc = tok_chunk_router(H);
+  if (tc > Tc) tc = Tc;
   const int rows = E + SI;
   int grid = (rows + 7) / 8;
   if (grid > 8 * di->sms) grid = 8 * di->sms;
   {
-  TraceScope ts(KID_ROUTER, st);
-  k_router_shared<<<grid, 256, (size_t)tc * H * 2, st>>>(x, Tc, H, wr, E, sh_gate, sh_up, SI,
-                                                        d->situ_b1, d->situ_b2, ws.logits,
-                                                        ws.act_s, tc);
+    TraceScope ts(KID_ROUTER, st);
+    if (launch_router_shared(tc, grid, (size_t)tc * H * 2, st, x, Tc, H, wr, E, bias, sh_gate,
+                             sh_up, SI, d->situ_b1, d->situ_b2, ws.sc, ws.ch, ws.act_s,
+                             status) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
   }
-  const size_t tk_smem = (size_t)E * 8 + 8 * d->topk * 4;
-  {
+  if (topk) {
     TraceScope ts(KID_TOPK, st);
-    k_topk<<<Tc, 256, tk_smem, st>>>(ws.logits, bias, Tc, E, d->topk, d->renorm, d->routed_scale,
-                                     idx, w, status);
+    k_topk<<<Tc, 256, (size_t)E * 8, st>>>(ws.sc, ws.ch, Tc, E, d->topk, d->renorm,
+                                           d->routed_scale, idx, w, status);
   }
   return launch_status();
 }
 
-// Dispatch + gate/up + down/combine for Tc tokens.
+// Row-block size of the single-token gate/up kernel: 4 rows if 4 rows of scale bytes are
+// 16-byte multiples, else 8 or 16; 0 if the kernel does not apply (fewer than 32 or more
+// than 224 groups per row, or a stage above 64 KB).
+int t1_row_block(int H) {
+  const int G = H / kGroup;
+  if (G < 32 || G > 224) return 0;
+  const int rb = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 8 : 16;
+  if ((size_t)2 * rb * (H / 2 + G) > 64 * 1024) return 0;
+  return rb;
+}
+
+// Ring slots of the bulk-copy down kernel for this shape (0: use the register kernel) and
+// whether the activations of all pairs are staged in its shared memory.
+int down_slots(int I, int Tc, int K, bool *act_smem) {
+  const int G2 = I / kGroup;
+  *act_smem = false;
+  if (G2 % 16 != 0 || G2 / 16 > 8) return 0;
+  const int P = Tc * K;
+  const size_t stage = (size_t)8 * (I / 2 + G2);  // 8-row half tiles
+  const size_t avail = 227 * 1024;
+  // one slot per consumer warp (16): all of them when they fit
+  const size_t fa = down_tma_smem(I, Tc, P, 0, true);
+  if (fa + 16 * stage <= avail) {
+    *act_smem = true;
+    return 16;
+  }
+  const size_t fg = down_tma_smem(I, Tc, P, 0, false);
+  if (fg + stage > avail) return 0;
+  const int ns = (int)((avail - fg) / stage);
+  return ns > 16 ? 16 : ns;
+}
+
+ExpertArgs expert_args(const k3moe_dims *d, const k3moe_experts *ex) {
+  ExpertArgs ea;
+  ea.base = ex->experts;
+  ea.stride = ex->expert_stride;
+  int64_t off[7];
+  record_offsets(d, off);
+  for (int i = 0; i < 6; i++) ea.off[i] = off[i];
+  return ea;
+}
+
+// Down projection + combine (+ shared expert) for Tc tokens: the bulk-copy ring kernel
+// when its slots fit in shared memory, else the register kernel.
+k3moe_status run_down(const DeviceInfo *di, const k3moe_dims *d, int Tc, const ExpertArgs &ea,
+                      const int32_t *idx, const float *w, const uint16_t *sh_down, Ws &ws,
+                      void *y, k3moe_dtype ydt, int accumulate, int32_t *status, cudaStream_t st,
+                      bool pdl) {
+  const int H = d->hidden, I = d->inter, K = d->topk;
+  const int P = Tc * K;
+  const int LR = down_lanes(I);
+  bool act_smem = false;
+  const int ns = down_slots(I, Tc, K, &act_smem);
+  TraceScope ts(ns >= 1 ? KID_DOWN_TMA : KID_DOWN, st);
+  if (ns >= 1) {
+    DownArgs a;
+    a.T = Tc; a.H = H; a.I = I; a.K = K; a.P = P;
+    a.ex = ea;
+    a.idx = idx; a.w = w; a.disp = ws.disp;
+    a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
+    a.sh_down = sh_down; a.SI = sh_down ? d->shared_inter : 0; a.act_s = ws.act_s;
+    a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate; a.LR = LR; a.NS = ns;
+    a.status = status;
+    int grid = H / kDownRows;
+    if (grid > di->sms) grid = di->sms;
+    return launch_down_tma(a, grid, st, pdl, act_smem) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+  }
+  const size_t dsmem = ((size_t)P * kDownRows + 256 * kDownRows + (size_t)Tc * kDownRows) * 4;
+  k_down_combine<<<H / kDownRows, 256, dsmem, st>>>(Tc, H, I, K, ea, idx, w, ws.disp, P,
+                                                    ws.act_hi, ws.act_lo, ws.act_ex, sh_down,
+                                                    sh_down ? d->shared_inter : 0, ws.act_s, y,
+                                                    (int)ydt, accumulate, LR);
+  return launch_status();
+}
+
+// Dispatch + gate/up + down/combine for Tc tokens with a given route.
 k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
                      const k3moe_experts *ex, const int32_t *idx, const float *w,
                      const uint16_t *sh_down, Ws &ws, void *y, k3moe_dtype ydt, int accumulate,
@@ -232,14 +311,7 @@ k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *
     TraceScope ts(KID_DISPATCH, st);
     k_dispatch<<<1, nt, (size_t)2 * Pp * 4, st>>>(idx, P, E, ws.disp, status);
   }
-
-  ExpertArgs ea;
-  ea.base = ex->experts;
-  ea.stride = ex->expert_stride;
-  int64_t off[7];
-  record_offsets(d, off);
-  for (int i = 0; i < 6; i++) ea.off[i] = off[i];
-
+  const ExpertArgs ea = expert_args(d, ex);
   const int G = H / kGroup;
   const bool pathB = (G <= 16) && ((G & (G - 1)) == 0);
   const int maxU = P < E ? P : E;
@@ -255,15 +327,48 @@ k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *
                              d->situ_b2, ws.act_hi, ws.act_lo, ws.act_ex) != cudaSuccess)
       return K3MOE_ERR_CUDA;
   }
-  const int LR = down_lanes(I);
-  const size_t dsmem = ((size_t)P * kDownRows + 256 * kDownRows + (size_t)Tc * kDownRows) * 4;
-  int dgrid = H / kDownRows;
-  TraceScope ts(KID_DOWN, st);
-  k_down_combine<<<dgrid, 256, dsmem, st>>>(Tc, H, I, K, ea, idx, w, ws.disp, P, ws.act_hi,
-                                            ws.act_lo, ws.act_ex, sh_down,
-                                            sh_down ? d->shared_inter : 0, ws.act_s, y, (int)ydt,
-                                            accumulate, LR);
-  return launch_status();
+  return run_down(di, d, Tc, ea, idx, w, sh_down, ws, y, ydt, accumulate, status, st, false);
+}
+
+// The whole layer for Tc tokens.  One token with a supported width: router kernel, then
+// the single-token gate/up kernel (top-k and dispatch fused), then the down kernel, the
+// last two launched as programmatic dependents so their prologues overlap the previous
+// kernel's tail.  Otherwise router, top-k, dispatch, gate/up and down kernels.
+k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+                       const uint16_t *wr, const float *bias, const k3moe_experts *ex,
+                       const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
+                       Ws &ws, int32_t *idx, float *w, void *y, k3moe_dtype ydt, int accumulate,
+                       int32_t *status, cudaStream_t st) {
+  const int rb = t1_row_block(d->hidden);
+  if (Tc == 1 && rb > 0) {
+    k3moe_status s = run_route(di, d, x, Tc, wr, bias, sh_gate, sh_up, ws, idx, w, status, st,
+                               false);
+    if (s != K3MOE_OK) return s;
+    const ExpertArgs ea = expert_args(d, ex);
+    const int H = d->hidden, G = H / kGroup;
+    const size_t stage = (size_t)2 * rb * (H / 2 + G);
+    int ns = (int)((227 * 1024 - gateup_t1_smem(H, d->n_experts, rb, 0)) / stage);
+    if (ns > 16) ns = 16;
+    GateUpT1Args a;
+    a.x = x; a.H = H; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
+    a.ex = ea; a.sc = ws.sc; a.ch = ws.ch; a.renorm = d->renorm;
+    a.routed_scale = d->routed_scale; a.idx_out = idx; a.w_out = w; a.disp = ws.disp;
+    a.b1 = d->situ_b1; a.b2 = d->situ_b2;
+    a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
+    a.status = status; a.RB = rb; a.NS = ns;
+    const bool pdl = !g_trace.on;
+    {
+      TraceScope ts(KID_GATEUP_T1, st);
+      int grid = d->topk * (d->inter / kTileRows);
+      if (grid > di->sms) grid = di->sms;
+      if (launch_gateup_t1(a, grid, st, pdl) != cudaSuccess) return K3MOE_ERR_CUDA;
+    }
+    return run_down(di, d, Tc, ea, idx, w, sh_down, ws, y, ydt, accumulate, status, st, pdl);
+  }
+  k3moe_status s = run_route(di, d, x, Tc, wr, bias, sh_gate, sh_up, ws, idx, w, status, st,
+                             true);
+  if (s != K3MOE_OK) return s;
+  return run_ffn(di, d, x, Tc, ex, idx, w, sh_down, ws, y, ydt, accumulate, status, st);
 }
 
 size_t dtype_size(k3moe_dtype t) { return t == K3MOE_F32 ? 4 : 2; }
@@ -321,7 +426,7 @@ k3moe_status k3moe_route(const k3moe_dims *dims, const uint16_t *x_bf16, const u
   for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
     const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
     s = run_route(di, dims, x_bf16 + (size_t)t0 * H, Tc, wr_bf16, bias, nullptr, nullptr, ws,
-                  idx + (size_t)t0 * K, w + (size_t)t0 * K, status_dev, st);
+                  idx + (size_t)t0 * K, w + (size_t)t0 * K, status_dev, st, true);
     if (s != K3MOE_OK) return s;
   }
   return K3MOE_OK;
@@ -395,12 +500,10 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
     int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : ws.idx;
     float *w_c = w_out ? w_out + (size_t)t0 * K : ws.w;
     const uint16_t *xc = x_bf16 + (size_t)t0 * H;
-    s = run_route(di, dims, xc, Tc, wr_bf16, bias, shared ? sh_gate : nullptr,
-                  shared ? sh_up : nullptr, ws, idx_c, w_c, status_dev, st);
-    if (s != K3MOE_OK) return s;
-    s = run_ffn(di, dims, xc, Tc, experts, idx_c, w_c, shared ? sh_down : nullptr, ws,
-                static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt, accumulate,
-                status_dev, st);
+    s = run_layer(di, dims, xc, Tc, wr_bf16, bias, experts, shared ? sh_gate : nullptr,
+                  shared ? sh_up : nullptr, shared ? sh_down : nullptr, ws, idx_c, w_c,
+                  static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt, accumulate,
+                  status_dev, st);
     if (s != K3MOE_OK) return s;
   }
   return K3MOE_OK;

@@ -1,0 +1,504 @@
+// k3moe_decode.cu -- decode-path kernels that stream expert tiles through shared memory
+// with bulk asynchronous copies (TMA, cp.async.bulk) into a ring of mbarrier-guarded
+// slots: one producer thread keeps up to ~200 KB per SM in flight while the consumer
+// warps decode MXFP4 in registers.
+//
+// Arithmetic is the same as k3moe_ffn.cu (README of FareedKhan-dev/kimi-k3-in-c,
+// section 4 for the MXFP4 product, section 9 for the expert FFN, SiTU and the router-order
+// sum; README of Maknee/Kimi-K3.cpp, "The consumer-memory idea" item 7).
+#include "k3moe_kernels.cuh"
+
+namespace k3 {
+
+// ------------------------------------------------------------------------------------
+// Gate/up + SiTU for ONE token, TMA ring.  Block = C consumer threads (one per 32-column
+// group of the H inputs, C = ceil(G/32)*32) + 1 producer warp.  Work items = (selected
+// expert j, 32-row tile), statically strided over the grid.  A stage holds RB rows of
+// gate and up (packed) and their scale bytes; the consumer keeps the 32x2 partial sums
+// of its group column in registers and reduces them once per tile.
+// Each CTA recomputes the top-k from the router's scores (a few microseconds, no extra
+// launch); CTA 0 publishes the route (idx, w) and the dispatch lists.
+// ------------------------------------------------------------------------------------
+// shared-memory map of k_gateup_t1 (bytes)
+constexpr int kGuBars = 0;       // full[16], empty[16]
+constexpr int kGuLst = 256;      // int [8][32]
+constexpr int kGuSel = 1280;     // int [32]
+constexpr int kGuWsel = 1408;    // float [32]
+constexpr int kGuAbort = 1536;   // int
+constexpr int kGuRed = 1664;     // float [2 parities][16 warps][32 rows][2]
+constexpr int kGuScores = kGuRed + 2 * 16 * 64 * 4;  // float [2][E]
+__host__ __device__ inline int gu_ring_offset(int E) { return (kGuScores + 8 * E + 127) & ~127; }
+
+// Two consumer threads per group column: thread (h, g), h = 0/1, takes the rows of a stage
+// with row parity h.  Every two stages a thread's 2*RB partial sums (RB/2 rows x gate/up
+// x 2 stages) are transpose-reduced inside its warp and parked in shared memory; at the end
+// of a 32-row tile warp 0 adds the warps' parts in a fixed order.
+template <int RB>
+__global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = a.H, I = a.I, K = a.K;
+  const int G = H / kGroup;
+  const int C = ((G + 31) / 32) * 32;   // threads per row parity
+  const int nwc = C / 32;               // warps per row parity
+  const int NS = a.NS;
+  const int rowb = H / 2;
+  const uint32_t stage_bytes = (uint32_t)(2 * RB * (rowb + G));
+  const int tiles = I / kTileRows;
+  constexpr int nblk = kTileRows / RB;  // stages per tile (even)
+  constexpr int V = RB * 2;             // values per two stages: RB/2 rows x 2 mats x 2
+
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kGuBars);
+  uint64_t *empty = full + 16;
+  int *lst = reinterpret_cast<int *>(smem + kGuLst);
+  int *sel = reinterpret_cast<int *>(smem + kGuSel);
+  float *wsel = reinterpret_cast<float *>(smem + kGuWsel);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kGuAbort);
+  float *red = reinterpret_cast<float *>(smem + kGuRed);
+  float *s_scores = reinterpret_cast<float *>(smem + kGuScores);
+  uint8_t *ring = smem + gu_ring_offset(a.E);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < NS; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 2 * nwc);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+
+  cta_topk(a.sc, a.ch, a.E, K, a.renorm, a.routed_scale, s_scores, s_scores + a.E, lst, sel,
+           wsel);
+  if (blockIdx.x == 0) {
+    if (tid < K) {
+      a.idx_out[tid] = sel[tid];
+      a.w_out[tid] = wsel[tid];
+      int *uexp = a.disp + 4;
+      int *uoff = uexp + K;
+      int *plist = uoff + K + 1;
+      uexp[tid] = sel[tid];
+      uoff[tid] = tid;
+      plist[tid] = tid;
+    }
+    if (tid == 0) {
+      a.disp[0] = K;
+      a.disp[4 + K + K] = K;  // uoff[U] = number of pairs
+    }
+  }
+  pdl_launch_dependents();
+
+  const int nitems = K * tiles;
+  if (warp == 2 * nwc) {
+    // ---------------- producer: one elected lane streams stages ----------------
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+        const int j = item / tiles, tile = item % tiles;
+        const uint8_t *rec = a.ex.base + (long long)sel[j] * a.ex.stride;
+        for (int b = 0; b < nblk; b++, it++) {
+          const int s = it % NS;
+          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const int r = tile * kTileRows + b * RB;
+          uint8_t *dst = ring + (size_t)s * stage_bytes;
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, RB * rowb, &full[s]);
+          bulk_g2s(dst + RB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, RB * rowb, &full[s]);
+          bulk_g2s(dst + 2 * RB * rowb, rec + a.ex.off[1] + (size_t)r * G, RB * G, &full[s]);
+          bulk_g2s(dst + 2 * RB * rowb + RB * G, rec + a.ex.off[5] + (size_t)r * G, RB * G,
+                   &full[s]);
+        }
+      }
+      if (!ok) {
+        // bounded wait for the copies already issued before leaving
+        for (int k = (it > NS ? it - NS : 0); k < it; k++)
+          mbar_wait(&full[k % NS], (k / NS) & 1, 400000000LL);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers: thread (h, g) ----------------
+  const int h = tid / C, g = tid % C;
+  const bool gact = g < G;
+  uint32_t xr[16];
+  int xe = 0;
+#pragma unroll
+  for (int p = 0; p < 16; p++) xr[p] = 0u;
+  if (gact) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + g * kGroup);
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const uint4 c = __ldg(src + q);
+      const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        v[8 * q + 2 * k] = bf16_lo(w4[k]);
+        v[8 * q + 2 * k + 1] = bf16_hi(w4[k]);
+      }
+    }
+    xe = prescale_group_f16(v, xr);
+  }
+
+  int it = 0, parity = 0;
+  bool aborted = false;
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x, parity ^= 1) {
+    const int j = item / tiles, tile = item % tiles;
+    float *rt = red + parity * (16 * 64);  // [warp][row 0..31][mat]
+#pragma unroll 1
+    for (int b = 0; b < nblk; b += 2) {
+      float vals[V];
+#pragma unroll
+      for (int v = 0; v < V; v++) vals[v] = 0.f;
+#pragma unroll
+      for (int b2 = 0; b2 < 2; b2++, it++) {
+        const int s = it % NS;
+        if (!aborted && !mbar_wait(&full[s], (it / NS) & 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          aborted = true;
+          *abort_flag = 1;
+        }
+        if (!aborted && gact) {
+          const uint8_t *st = ring + (size_t)s * stage_bytes;
+          const uint8_t *sgs = st + 2 * RB * rowb;
+          const uint8_t *sus = sgs + RB * G;
+#pragma unroll
+          for (int k = 0; k < RB / 2; k++) {
+            const int q = h + 2 * k;  // row within the stage
+            const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
+            const uint4 wu = reinterpret_cast<const uint4 *>(st + (RB + q) * rowb)[g];
+            const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
+            if (sg != 255u) vals[b2 * RB + 2 * k] = group_dot(xr, wg) * group_factor(sg, xe);
+            if (su != 255u) vals[b2 * RB + 2 * k + 1] = group_dot(xr, wu) * group_factor(su, xe);
+          }
+        }
+        __syncwarp();
+        if (lane == 0 && !aborted) mbar_arrive(&empty[s]);
+      }
+      // value v = b2*RB + 2k + m  ->  tile row b*RB + b2*RB + h + 2k, matrix m
+      const float tot = warp_transpose_reduce<V>(vals);
+      if (lane < V) {
+        const int b2 = lane / RB, k = (lane % RB) / 2, m = lane & 1;
+        rt[(warp * 32 + (b * RB + b2 * RB + h + 2 * k)) * 2 + m] = tot;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(2 * C) : "memory");
+    if (warp == 0) {
+      // row `lane` of the tile was computed by the warps of parity lane % 2
+      const int hp = lane & 1;
+      float gs = 0.f, us = 0.f;
+      for (int w = hp * nwc; w < (hp + 1) * nwc; w++) {
+        gs += rt[(w * 32 + lane) * 2];
+        us += rt[(w * 32 + lane) * 2 + 1];
+      }
+      float act = situ(gs, us, a.b1, a.b2);
+      if (*abort_flag) act = 0.f;
+      float mx = fabsf(act);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      int e2 = 0;
+      if (mx > 0.f) {
+        e2 = exponent_of(mx) - 14;
+        e2 = e2 < -110 ? -110 : e2;
+      }
+      const float sa = act * pow2i(-e2);
+      const __half hh = __float2half_rn(sa);
+      const __half hl = __float2half_rn(sa - __half2float(hh));
+      const size_t o = (size_t)j * I + tile * kTileRows + lane;
+      a.act_hi[o] = __half_as_ushort(hh);
+      a.act_lo[o] = __half_as_ushort(hl);
+      if (lane == 0) a.act_ex[(size_t)j * (I / kGroup) + tile] = e2;
+    }
+  }
+}
+
+size_t gateup_t1_smem(int H, int E, int RB, int NS) {
+  const int G = H / kGroup;
+  return gu_ring_offset(E) + (size_t)NS * 2 * RB * (H / 2 + G);
+}
+
+cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl) {
+  const int G = a.H / kGroup;
+  const int C = ((G + 31) / 32) * 32;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(2 * C + 32);
+  cfg.dynamicSmemBytes = gateup_t1_smem(a.H, a.E, a.RB, a.NS);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.RB == 4) return cudaLaunchKernelEx(&cfg, k_gateup_t1<4>, a);
+  if (a.RB == 8) return cudaLaunchKernelEx(&cfg, k_gateup_t1<8>, a);
+  return cudaLaunchKernelEx(&cfg, k_gateup_t1<16>, a);
+}
+
+// ------------------------------------------------------------------------------------
+// Down projection + router-order combine + shared expert, TMA ring.  Work item = 16
+// output rows.  A stage holds one distinct expert's 16 rows of W2 (packed + scales);
+// stages of an item go round-robin to NS "expert lanes" of LR threads (one slot per
+// lane); an expert lane computes d = W2_e act for every (token, slot) pair routed to e,
+// each thread covering NG = (I/32)/LR groups, and writes dbuf[pair][row].  After all
+// stages of the item: y[t] = sum_j w[t][j] dbuf[t*K+j] in router order (float), plus the
+// shared expert's rows (bf16 weights, fp32 activations), added last and unweighted.
+// ------------------------------------------------------------------------------------
+// A stage is one distinct expert's 8-row half of the 16-row tile (packed + scales).  Ring
+// slot p belongs to consumer warp p: a warp consumes the phases of its own slot in order,
+// so no two waiters ever wait on different phases of one barrier.  In a warp, lane =
+// (row quarter rq, group lane l): a thread covers 4 rows x NG = (I/32)/16 groups.
+// ACT_SMEM: the activations of all pairs are bulk-copied into shared memory once per CTA
+// (they are the same for every row tile); otherwise they are read from global memory (L2)
+// per pair and group.
+constexpr int kDnLanes = 16;   // group lanes per row quarter (a half warp)
+constexpr int kDnWarps = 16;   // consumer warps = ring slots
+constexpr int kDnStageRows = 8;
+
+template <bool ACT_SMEM>
+__global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = a.H, I = a.I, K = a.K, P = a.P, T = a.T;
+  const int G2 = I / kGroup;
+  const int NG = G2 / kDnLanes, NS = a.NS;
+  const int rowb = I / 2;
+  const uint32_t stage_bytes = (uint32_t)(kDnStageRows * (rowb + G2));
+  const int ntiles = H / kDownRows;
+  const int NC = kDnWarps * 32;  // consumer threads
+
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + 32;
+  uint64_t *actbar = empty + 32;
+  float *dbuf = reinterpret_cast<float *>(smem + 1024);   // [P][16]
+  float *ds = dbuf + (size_t)P * kDownRows;               // [T][16]
+  uint8_t *p8 = reinterpret_cast<uint8_t *>(ds + (size_t)T * kDownRows);
+  p8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p8) + 127) & ~uintptr_t(127));
+  uint16_t *s_hi = reinterpret_cast<uint16_t *>(p8);      // [P][I] (ACT_SMEM)
+  uint16_t *s_lo = s_hi + (ACT_SMEM ? (size_t)P * I : 0);
+  int32_t *s_ex = reinterpret_cast<int32_t *>(s_lo + (ACT_SMEM ? (size_t)P * I : 0));
+  uint8_t *ring = reinterpret_cast<uint8_t *>(s_ex + (ACT_SMEM ? (size_t)P * G2 : 0));
+  ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ring) + 127) & ~uintptr_t(127));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < NS; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(actbar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+
+  const int U = a.disp[0];
+  const int *uexp = a.disp + 4;
+  const int *uoff = uexp + P;
+  const int *plist = uoff + P + 1;
+
+  if (warp == kDnWarps) {
+    if (lane == 0) {
+      bool ok = true;
+      if (ACT_SMEM) {
+        const uint32_t nb = (uint32_t)((size_t)P * I * 2);
+        const uint32_t ne = (uint32_t)((size_t)P * G2 * 4);
+        mbar_arrive_expect_tx(actbar, 2 * nb + ne);
+        bulk_g2s(s_hi, a.act_hi, nb, actbar);
+        bulk_g2s(s_lo, a.act_lo, nb, actbar);
+        bulk_g2s(s_ex, a.act_ex, ne, actbar);
+      }
+      int it = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int r0 = tile * kDownRows;
+        for (int k = 0; k < 2 * U; k++, it++) {
+          const int s = it % NS;
+          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          if (k == 0 && a.sh_down != nullptr)  // this tile's shared-expert rows, into L2
+            bulk_prefetch_l2(a.sh_down + (size_t)r0 * a.SI, kDownRows * a.SI * 2);
+          const int u = k >> 1, rh = k & 1;
+          const int rs = r0 + rh * kDnStageRows;
+          const uint8_t *rec = a.ex.base + (long long)uexp[u] * a.ex.stride;
+          uint8_t *dst = ring + (size_t)s * stage_bytes;
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          bulk_g2s(dst, rec + a.ex.off[2] + (size_t)rs * rowb, kDnStageRows * rowb, &full[s]);
+          bulk_g2s(dst + kDnStageRows * rowb, rec + a.ex.off[3] + (size_t)rs * G2,
+                   kDnStageRows * G2, &full[s]);
+        }
+      }
+      if (!ok)
+        for (int k = (it > NS ? it - NS : 0); k < it; k++)
+          mbar_wait(&full[k % NS], (k / NS) & 1, 400000000LL);
+      if (ACT_SMEM) mbar_wait(actbar, 0, 400000000LL);
+    }
+    return;
+  }
+
+  const int rq = lane >> 4, l = lane & 15;  // row quarter (4 rows), group lane
+  bool aborted = false;
+  if (ACT_SMEM && !mbar_wait(actbar, 0)) {
+    set_status(a.status, K3MOE_ERR_TIMEOUT);
+    aborted = true;
+  }
+  const uint16_t *act_hi = ACT_SMEM ? s_hi : a.act_hi;
+  const uint16_t *act_lo = ACT_SMEM ? s_lo : a.act_lo;
+  const int32_t *act_ex = ACT_SMEM ? s_ex : a.act_ex;
+
+  int it0 = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int r0 = tile * kDownRows;
+    const int srow = tid >> 5, ls = lane;  // shared expert: one warp per row
+    const int nch = a.SI >> 3;
+    for (int i = tid; i < P * kDownRows; i += NC) dbuf[i] = 0.f;
+    asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
+    // this warp's stages of the tile: those in its own slot (it % NS == warp)
+    for (int k = (warp < NS) ? (((warp - it0) % NS) + NS) % NS : 2 * U; k < 2 * U; k += NS) {
+      const int it = it0 + k;
+      const int s = warp;
+      if (!aborted && !mbar_wait(&full[s], (it / NS) & 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        aborted = true;
+      }
+      const int u = k >> 1, rh = k & 1;
+      const uint8_t *st = ring + (size_t)s * stage_bytes;
+      const uint8_t *ss = st + kDnStageRows * rowb;
+      for (int pk = uoff[u]; pk < uoff[u + 1] && !aborted; pk++) {
+        const int i = plist[pk];
+        float acc[4];
+#pragma unroll
+        for (int r = 0; r < 4; r++) acc[r] = 0.f;
+        for (int q = 0; q < NG; q++) {
+          const int gg = l * NG + q;
+          uint32_t xh[16], xl[16];
+          const uint4 *ph = reinterpret_cast<const uint4 *>(act_hi + (size_t)i * I + gg * kGroup);
+          const uint4 *pl = reinterpret_cast<const uint4 *>(act_lo + (size_t)i * I + gg * kGroup);
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            const uint4 x0 = ph[c], x1 = pl[c];
+            xh[4 * c] = x0.x; xh[4 * c + 1] = x0.y; xh[4 * c + 2] = x0.z; xh[4 * c + 3] = x0.w;
+            xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
+          }
+          const int e2 = act_ex[(size_t)i * G2 + gg];
+#pragma unroll
+          for (int r = 0; r < 4; r++) {
+            const int row = rq * 4 + r;
+            const uint4 wv = reinterpret_cast<const uint4 *>(st + row * rowb)[gg];
+            const uint32_t sv = ss[row * G2 + gg];
+            if (sv != 255u) acc[r] += group_dot2(xh, xl, wv) * group_factor(sv, e2);
+          }
+        }
+        // reduce the 4 row partials over the 16 group lanes of this half warp
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+          for (int r = 0; r < 4; r++) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+        }
+        if (l == 0) {
+#pragma unroll
+          for (int r = 0; r < 4; r++)
+            dbuf[(size_t)i * kDownRows + rh * kDnStageRows + rq * 4 + r] = acc[r];
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(&empty[s]);
+    }
+    it0 += 2 * U;
+
+    // shared expert rows r0..r0+15: bf16 weights (prefetched into L2 by the producer at
+    // the start of the tile) x fp32 activations; one warp per row
+    if (a.sh_down != nullptr && srow < kDownRows) {
+      const uint4 *w4 = reinterpret_cast<const uint4 *>(a.sh_down + (size_t)(r0 + srow) * a.SI);
+      for (int t = 0; t < T; t++) {
+        const float4 *a4 = reinterpret_cast<const float4 *>(a.act_s + (size_t)t * a.SI);
+        float sacc = 0.f;
+        for (int c = ls; c < nch; c += 32) {
+          const uint4 wv = __ldg(w4 + c);
+          const float4 a0 = a4[2 * c], a1 = a4[2 * c + 1];
+          sacc = fmaf(bf16_lo(wv.x), a0.x, sacc);
+          sacc = fmaf(bf16_hi(wv.x), a0.y, sacc);
+          sacc = fmaf(bf16_lo(wv.y), a0.z, sacc);
+          sacc = fmaf(bf16_hi(wv.y), a0.w, sacc);
+          sacc = fmaf(bf16_lo(wv.z), a1.x, sacc);
+          sacc = fmaf(bf16_hi(wv.z), a1.y, sacc);
+          sacc = fmaf(bf16_lo(wv.w), a1.z, sacc);
+          sacc = fmaf(bf16_hi(wv.w), a1.w, sacc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+        if (ls == 0) ds[t * kDownRows + srow] = sacc;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
+
+    for (int q = tid; q < T * kDownRows; q += NC) {
+      const int t = q / kDownRows, row = q % kDownRows;
+      float sum = 0.f;
+      for (int j = 0; j < K; j++)
+        sum = __fadd_rn(sum, __fmul_rn(a.w[t * K + j], dbuf[(size_t)(t * K + j) * kDownRows + row]));
+      if (a.sh_down != nullptr) sum = __fadd_rn(sum, ds[t * kDownRows + row]);
+      const size_t o = (size_t)t * H + r0 + row;
+      if (aborted) sum = 0.f;
+      if (a.ydt == K3MOE_F32) {
+        float *yf = reinterpret_cast<float *>(a.y);
+        yf[o] = a.accumulate ? __fadd_rn(yf[o], sum) : sum;
+      } else {
+        uint16_t *yb = reinterpret_cast<uint16_t *>(a.y);
+        const float v = a.accumulate ? __fadd_rn(bf16_lo(yb[o]), sum) : sum;
+        yb[o] = f32_to_bf16(v);
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
+  }
+}
+
+// Shared memory of k_down_tma: barriers, dbuf, ds, [activations], NS ring slots.
+size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem) {
+  const int G2 = I / kGroup;
+  const size_t stage = (size_t)kDnStageRows * (I / 2 + G2);
+  size_t b = 1024 + ((size_t)P * kDownRows + (size_t)T * kDownRows) * 4 + 128;
+  if (act_smem) b += (size_t)P * I * 4 + (size_t)P * G2 * 4 + 128;
+  return b + NS * stage;
+}
+
+cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool pdl,
+                            bool act_smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDnWarps * 32 + 32);
+  cfg.dynamicSmemBytes = down_tma_smem(a.I, a.T, a.P, a.NS, act_smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (act_smem) return cudaLaunchKernelEx(&cfg, k_down_tma<true>, a);
+  return cudaLaunchKernelEx(&cfg, k_down_tma<false>, a);
+}
+
+cudaError_t set_decode_smem_limits() {
+  const int big = 227 * 1024;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_gateup_t1<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_gateup_t1<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_gateup_t1<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_down_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
+          cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_down_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+}
+
+}  // namespace k3

@@ -126,31 +126,6 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t *__restrict__ i
 }
 
 // ------------------------------------------------------------------------------------
-// Reductions
-// ------------------------------------------------------------------------------------
-// Transpose-reduce V values (V = 8, 16 or 32) over the 32 lanes of a warp: afterwards lane
-// l holds the warp total of value (l % V).  Fixed shuffle tree: deterministic.
-template <int V>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[V]) {
-  const int lane = threadIdx.x & 31;
-  // halving steps over lane bits log2(V)-1 .. 0
-#pragma unroll
-  for (int half = V / 2; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; i++) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int o = V; o < 32; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-  return r;
-}
-
-// ------------------------------------------------------------------------------------
 // Expert gate/up + SiTU.  Work item = (distinct expert u, 32-row tile of the I rows).
 // Path A (G = H/32 >= 32 or not a power of two): one thread per group column, the CTA
 // covers one row at a time, 4-row blocks software-pipelined; the 8 partial sums of a

@@ -1,6 +1,7 @@
 // k3moe_kernels.cuh -- kernel declarations and launch-shape constants of libk3moe.
 #pragma once
 #include "k3moe_device.cuh"
+#include "k3moe_topk.cuh"
 
 namespace k3 {
 
@@ -17,14 +18,15 @@ constexpr int kPairKeyShift = 12; // dispatch sort key = expert << 12 | pair id 
 //   [5+2P .. 5+3P) plist, pair ids t*K + j sorted by (expert, pair id)
 __host__ __device__ inline int disp_words(int P) { return 5 + 3 * P; }
 
-__global__ void k_router_shared(const uint16_t *__restrict__ x, int T, int H,
-                                const uint16_t *__restrict__ wr, int E,
-                                const uint16_t *__restrict__ sh_gate,
-                                const uint16_t *__restrict__ sh_up, int SI, float b1, float b2,
-                                float *__restrict__ logits, float *__restrict__ act_s,
-                                int tc_max);
+// Launches k_router_shared with tc tokens per chunk (1: a decode step; else up to
+// kTokChunk).
+cudaError_t launch_router_shared(int tc, int grid, size_t smem, cudaStream_t st, const uint16_t *x,
+                                 int T, int H, const uint16_t *wr, int E, const float *bias,
+                                 const uint16_t *sh_gate, const uint16_t *sh_up, int SI, float b1,
+                                 float b2, float *sc, float *ch, float *act_s, int32_t *status);
+cudaError_t set_router_smem_limits(int bytes);
 
-__global__ void k_topk(const float *__restrict__ logits, const float *__restrict__ bias, int T,
+__global__ void k_topk(const float *__restrict__ scores, const float *__restrict__ choice, int T,
                        int E, int K, int renorm, float routed_scale, int32_t *__restrict__ idx,
                        float *__restrict__ w, int32_t *status);
 
@@ -52,6 +54,47 @@ __global__ void k_down_combine(int T, int H, int I, int K, ExpertArgs ex,
                                const uint16_t *__restrict__ sh_down, int SI,
                                const float *__restrict__ act_s, void *y, int ydt,
                                int accumulate, int LR);
+
+// ---- decode kernels with bulk-copy rings (k3moe_decode.cu)
+struct GateUpT1Args {
+  const uint16_t *x;
+  int H, I, E, K;
+  ExpertArgs ex;
+  const float *sc, *ch;  // [E] router scores / selection scores
+  int renorm;
+  float routed_scale;
+  int32_t *idx_out;
+  float *w_out;
+  int32_t *disp;
+  float b1, b2;
+  uint16_t *act_hi, *act_lo;
+  int32_t *act_ex;
+  int32_t *status;
+  int RB, NS;
+};
+
+struct DownArgs {
+  int T, H, I, K, P;
+  ExpertArgs ex;
+  const int32_t *idx;
+  const float *w;
+  const int32_t *disp;
+  const uint16_t *act_hi, *act_lo;
+  const int32_t *act_ex;
+  const uint16_t *sh_down;
+  int SI;
+  const float *act_s;
+  void *y;
+  int ydt, accumulate, LR, NS;
+  int32_t *status;
+};
+
+size_t gateup_t1_smem(int H, int E, int RB, int NS);
+cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl);
+size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem);
+cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool pdl,
+                            bool act_smem);
+cudaError_t set_decode_smem_limits();
 
 __global__ void k_dequant(const uint8_t *__restrict__ packed, const uint8_t *__restrict__ scales,
                           int rows, int cols, float *__restrict__ out);

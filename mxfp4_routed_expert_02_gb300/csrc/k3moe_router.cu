@@ -16,13 +16,17 @@
 namespace k3 {
 
 // Rows [0, E) are router rows, rows [E, E + SI) shared-expert row pairs.
-// x: bf16 [T][H]; logits: float [T][E]; act_s: float [T][SI].
-// Dynamic shared memory: tc_max * H bf16 (one chunk of tokens).
+// x: bf16 [T][H]; sc/ch: float [T][E] (unbiased score, selection score); act_s: float
+// [T][SI].  Dynamic shared memory: TC * H bf16 (one chunk of tokens).  TC = tokens per
+// chunk held in registers (1 for a decode step, 8 for batches); tc_max <= TC.
+template <int TC>
 __global__ void __launch_bounds__(256) k_router_shared(
     const uint16_t *__restrict__ x, int T, int H, const uint16_t *__restrict__ wr, int E,
-    const uint16_t *__restrict__ sh_gate, const uint16_t *__restrict__ sh_up, int SI,
-    float b1, float b2, float *__restrict__ logits, float *__restrict__ act_s, int tc_max) {
+    const float *__restrict__ bias, const uint16_t *__restrict__ sh_gate,
+    const uint16_t *__restrict__ sh_up, int SI, float b1, float b2, float *__restrict__ sc,
+    float *__restrict__ ch, float *__restrict__ act_s, int tc_max, int32_t *status) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_wait();
   uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -43,15 +47,15 @@ __global__ void __launch_bounds__(256) k_router_shared(
     for (int row = blockIdx.x * nwarps + warp; row < nrows; row += gridDim.x * nwarps) {
       if (row < E) {
         const uint4 *w4 = reinterpret_cast<const uint4 *>(wr + (size_t)row * H);
-        float hi[kTokChunk], lo[kTokChunk];
+        float hi[TC], lo[TC];
 #pragma unroll
-        for (int t = 0; t < kTokChunk; t++) hi[t] = lo[t] = 0.f;
-#pragma unroll 4
+        for (int t = 0; t < TC; t++) hi[t] = lo[t] = 0.f;
+#pragma unroll 7
         for (int c = lane; c < nchunk; c += 32) {
           const uint4 wv = __ldg(w4 + c);
           const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-          for (int t = 0; t < kTokChunk; t++) {
+          for (int t = 0; t < TC; t++) {
             if (t < tc) {
               const uint4 xv = xs4[t * nchunk + c];
               const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -72,7 +76,7 @@ __global__ void __launch_bounds__(256) k_router_shared(
           }
         }
 #pragma unroll
-        for (int t = 0; t < kTokChunk; t++) {
+        for (int t = 0; t < TC; t++) {
           if (t < tc) {
             // normalise, then reduce the pairs across the warp in a fixed tree
             float h = hi[t], l = lo[t];
@@ -87,24 +91,32 @@ __global__ void __launch_bounds__(256) k_router_shared(
               const float ol = __shfl_xor_sync(0xffffffffu, l, o);
               ff_add(h, l, oh, ol);
             }
-            if (lane == 0) logits[(size_t)(t0 + t) * E + row] = h;
+            if (lane == 0) {
+              // unbiased score: logistic of the float logit, in double, rounded once;
+              // selection score: one float add of the correction bias
+              const float sv = (float)(1.0 / (1.0 + exp(-(double)h)));
+              const float cv = __fadd_rn(sv, bias ? bias[row] : 0.f);
+              sc[(size_t)(t0 + t) * E + row] = sv;
+              ch[(size_t)(t0 + t) * E + row] = cv;
+              if (!(fabsf(cv) <= 3.402823466e38f)) set_status(status, K3MOE_ERR_NONFINITE);
+            }
           }
         }
       } else {
         const int r = row - E;
         const uint4 *g4 = reinterpret_cast<const uint4 *>(sh_gate + (size_t)r * H);
         const uint4 *u4 = reinterpret_cast<const uint4 *>(sh_up + (size_t)r * H);
-        float ga[kTokChunk], ua[kTokChunk];
+        float ga[TC], ua[TC];
 #pragma unroll
-        for (int t = 0; t < kTokChunk; t++) ga[t] = ua[t] = 0.f;
-#pragma unroll 4
+        for (int t = 0; t < TC; t++) ga[t] = ua[t] = 0.f;
+#pragma unroll 7
         for (int c = lane; c < nchunk; c += 32) {
           const uint4 gv = __ldg(g4 + c);
           const uint4 uv = __ldg(u4 + c);
           const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
           const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
-          for (int t = 0; t < kTokChunk; t++) {
+          for (int t = 0; t < TC; t++) {
             if (t < tc) {
               const uint4 xv = xs4[t * nchunk + c];
               const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(256) k_router_shared(
           }
         }
 #pragma unroll
-        for (int t = 0; t < kTokChunk; t++) {
+        for (int t = 0; t < TC; t++) {
           if (t < tc) {
             float g = ga[t], u = ua[t];
 #pragma unroll
@@ -134,111 +146,50 @@ __global__ void __launch_bounds__(256) k_router_shared(
       }
     }
   }
+  pdl_launch_dependents();
 }
 
-// Larger selection score first; an equal score goes to the lower expert index.  A NaN
-// never wins against a number (the NaN itself is reported through the status word).
-__device__ __forceinline__ bool better(float ach, int ae, float bch, int be) {
-  if (ae < 0) return false;
-  if (be < 0) return true;
-  if (ach > bch) return true;
-  if (ach == bch) return ae < be;
-  return (bch != bch) && (ach == ach);
+cudaError_t launch_router_shared(int tc, int grid, size_t smem, cudaStream_t st, const uint16_t *x,
+                                 int T, int H, const uint16_t *wr, int E, const float *bias,
+                                 const uint16_t *sh_gate, const uint16_t *sh_up, int SI, float b1,
+                                 float b2, float *sc, float *ch, float *act_s, int32_t *status) {
+  if (tc == 1)
+    k_router_shared<1><<<grid, 256, smem, st>>>(x, T, H, wr, E, bias, sh_gate, sh_up, SI, b1, b2,
+                                                sc, ch, act_s, 1, status);
+  else
+    k_router_shared<kTokChunk><<<grid, 256, smem, st>>>(x, T, H, wr, E, bias, sh_gate, sh_up, SI,
+                                                        b1, b2, sc, ch, act_s, tc, status);
+  return cudaGetLastError();
 }
 
-__device__ __forceinline__ void warp_best(float &ch, int &e) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float och = __shfl_xor_sync(0xffffffffu, ch, o);
-    const int oe = __shfl_xor_sync(0xffffffffu, e, o);
-    if (better(och, oe, ch, e)) {
-      ch = och;
-      e = oe;
-    }
-  }
+cudaError_t set_router_smem_limits(int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(k_router_shared<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_router_shared<kTokChunk>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-// One CTA (256 threads = 8 warps) per token.  Scores and selection scores go to shared
-// memory; each warp takes the top K of its contiguous slice of experts by K rounds of a
-// warp-wide maximum, then warp 0 merges the eight sorted lists (same key), which equals
-// the page's repeated maximum over all experts.
-__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits,
-                                              const float *__restrict__ bias, int T, int E,
+// One CTA (256 threads) per token: the top-k of its selection scores (cta_topk).
+__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ scores,
+                                              const float *__restrict__ choice, int T, int E,
                                               int K, int renorm, float routed_scale,
                                               int32_t *__restrict__ idx, float *__restrict__ w,
                                               int32_t *status) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  float *sc = reinterpret_cast<float *>(smem_raw);  // [E]
-  float *ch = sc + E;                                // [E]
-  int *lst = reinterpret_cast<int *>(ch + E);        // [8][K]
+  __shared__ int lst[8 * 32];
+  __shared__ int sel[32];
+  __shared__ float wsel[32];
+  extern __shared__ __align__(16) float s_scores[];  // [2][E]
+  pdl_wait();
   const int t = blockIdx.x;
   if (t >= T) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const float lg = logits[(size_t)t * E + e];
-    const float s = (float)(1.0 / (1.0 + exp(-(double)lg)));
-    const float c = __fadd_rn(s, bias ? bias[e] : 0.f);
-    sc[e] = s;
-    ch[e] = c;
-    if (!(fabsf(c) <= 3.402823466e38f) || !(fabsf(s) <= 3.402823466e38f))
-      set_status(status, K3MOE_ERR_NONFINITE);
+  cta_topk(scores + (size_t)t * E, choice + (size_t)t * E, E, K, renorm, routed_scale, s_scores,
+           s_scores + E, lst, sel, wsel);
+  if (threadIdx.x < K) {
+    idx[(size_t)t * K + threadIdx.x] = sel[threadIdx.x];
+    w[(size_t)t * K + threadIdx.x] = wsel[threadIdx.x];
   }
-  __syncthreads();
-
-  // per-warp slice [lo, hi)
-  const int per = (E + 7) / 8;
-  const int lo = warp * per, hi = min(E, lo + per);
-  unsigned taken = 0u;  // bit i: expert lo + lane + 32 i already chosen (slice <= 32*32)
-  for (int k = 0; k < K; k++) {
-    float bc = 0.f;
-    int be = -1;
-    int i = 0;
-    for (int e = lo + lane; e < hi; e += 32, i++) {
-      if (taken & (1u << i)) continue;
-      const float c = ch[e];
-      if (better(c, e, bc, be)) {
-        bc = c;
-        be = e;
-      }
-    }
-    warp_best(bc, be);
-    if (be >= 0 && ((be - lo) & 31) == lane) taken |= 1u << ((be - lo) >> 5);
-    if (lane == 0) lst[warp * K + k] = be;
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    int head = 0;  // lanes 0..7 walk list `lane`
-    float wsum = 0.f;
-    float myw = 0.f;
-    int mye = -1;
-    for (int k = 0; k < K; k++) {
-      int e = -1;
-      float c = 0.f;
-      if (lane < 8 && head < K) {
-        e = lst[lane * K + head];
-        if (e >= 0) c = ch[e];
-      }
-      const int cand_e = e;
-      warp_best(c, e);
-      if (lane < 8 && e >= 0 && cand_e == e) head++;
-      // e is the k-th choice (every lane agrees)
-      const float s = (e >= 0) ? sc[e] : 0.f;
-      wsum = __fadd_rn(wsum, s);  // float sum in router order
-      if (lane == k) {
-        mye = e;
-        myw = s;
-      }
-    }
-    if (lane < K) {
-      float v = myw;
-      if (renorm && wsum > 0.f) v = __fdiv_rn(v, wsum);
-      v = __fmul_rn(v, routed_scale);
-      idx[(size_t)t * K + lane] = mye < 0 ? 0 : mye;
-      w[(size_t)t * K + lane] = v;
-    }
-  }
+  (void)status;
 }
 
 }  // namespace k3
