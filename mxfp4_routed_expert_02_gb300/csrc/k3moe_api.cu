@@ -209,15 +209,18 @@ k3moe_status run_route(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
   if (grid > 8 * di->sms) grid = 8 * di->sms;
   {
     TraceScope ts(KID_ROUTER, st);
-    if (launch_router_shared(tc, grid, (size_t)tc * H * 2, st, x, Tc, H, wr, E, bias, sh_gate,
-                             sh_up, SI, d->situ_b1, d->situ_b2, ws.sc, ws.ch, ws.act_s,
-                             status) != cudaSuccess)
-      return K3MOE_ERR_CUDA;
+    const cudaError_t e =
+        (Tc == 1) ? launch_router_t1(st, x, H, wr, E, bias, sh_gate, sh_up, SI, d->situ_b1,
+                                     d->situ_b2, ws.sc, ws.ch, ws.act_s, status)
+                  : launch_router_shared(tc, grid, (size_t)tc * H * 2, st, x, Tc, H, wr, E, bias,
+                                         sh_gate, sh_up, SI, d->situ_b1, d->situ_b2, ws.sc,
+                                         ws.ch, ws.act_s, status);
+    if (e != cudaSuccess) return K3MOE_ERR_CUDA;
   }
   if (topk) {
     TraceScope ts(KID_TOPK, st);
-    k_topk<<<Tc, 256, (size_t)E * 8, st>>>(ws.sc, ws.ch, Tc, E, d->topk, d->renorm,
-                                           d->routed_scale, idx, w, status);
+    k_topk<<<Tc, 512, (size_t)topk_scratch_keys(E, d->topk) * 8, st>>>(
+        ws.sc, ws.ch, Tc, E, d->topk, d->renorm, d->routed_scale, idx, w, status);
   }
   return launch_status();
 }
@@ -347,7 +350,7 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
     const ExpertArgs ea = expert_args(d, ex);
     const int H = d->hidden, G = H / kGroup;
     const size_t stage = (size_t)2 * rb * (H / 2 + G);
-    int ns = (int)((227 * 1024 - gateup_t1_smem(H, d->n_experts, rb, 0)) / stage);
+    int ns = (int)((227 * 1024 - gateup_t1_smem(H, d->n_experts, d->topk, rb, 0)) / stage);
     if (ns > 16) ns = 16;
     GateUpT1Args a;
     a.x = x; a.H = H; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;

@@ -21,20 +21,25 @@ namespace k3 {
 // ------------------------------------------------------------------------------------
 // shared-memory map of k_gateup_t1 (bytes)
 constexpr int kGuBars = 0;       // full[16], empty[16]
-constexpr int kGuLst = 256;      // int [8][32]
-constexpr int kGuSel = 1280;     // int [32]
-constexpr int kGuWsel = 1408;    // float [32]
-constexpr int kGuAbort = 1536;   // int
+constexpr int kGuRedBars = 256;  // redbar[2], redfree[2] (inside the 256..288 gap)
+constexpr int kGuLst = 320;      // int [8][32]
+constexpr int kGuSel = 1344;     // int [32]
+constexpr int kGuWsel = 1472;    // float [32]
+constexpr int kGuAbort = 1600;   // int
 constexpr int kGuRed = 1664;     // float [2 parities][16 warps][32 rows][2]
-constexpr int kGuScores = kGuRed + 2 * 16 * 64 * 4;  // float [2][E]
-__host__ __device__ inline int gu_ring_offset(int E) { return (kGuScores + 8 * E + 127) & ~127; }
+constexpr int kGuScores = kGuRed + 2 * 16 * 64 * 4;  // top-k scratch (uint64)
+__host__ __device__ inline int gu_ring_offset(int E, int K) {
+  return (kGuScores + 8 * topk_scratch_keys(E, K) + 127) & ~127;
+}
 
 // Two consumer threads per group column: thread (h, g), h = 0/1, takes the rows of a stage
 // with row parity h.  Every two stages a thread's 2*RB partial sums (RB/2 rows x gate/up
-// x 2 stages) are transpose-reduced inside its warp and parked in shared memory; at the end
-// of a 32-row tile warp 0 adds the warps' parts in a fixed order.
+// x 2 stages) are transpose-reduced inside its warp and parked in shared memory (one of two
+// buffers, by tile parity).  An epilogue warp adds the warps' parts of a 32-row tile in a
+// fixed order, applies SiTU and writes the activations; consumers hand tiles to it
+// through mbarriers and never wait for one another.
 template <int RB>
-__global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
+__global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = a.H, I = a.I, K = a.K;
   const int G = H / kGroup;
@@ -49,13 +54,14 @@ __global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
 
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kGuBars);
   uint64_t *empty = full + 16;
-  int *lst = reinterpret_cast<int *>(smem + kGuLst);
+  uint64_t *redbar = reinterpret_cast<uint64_t *>(smem + kGuRedBars);  // [2]
+  uint64_t *redfree = redbar + 2;                                       // [2]
   int *sel = reinterpret_cast<int *>(smem + kGuSel);
   float *wsel = reinterpret_cast<float *>(smem + kGuWsel);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kGuAbort);
   float *red = reinterpret_cast<float *>(smem + kGuRed);
-  float *s_scores = reinterpret_cast<float *>(smem + kGuScores);
-  uint8_t *ring = smem + gu_ring_offset(a.E);
+  float *s_scores = reinterpret_cast<float *>(smem + kGuScores);  // top-k key scratch
+  uint8_t *ring = smem + gu_ring_offset(a.E, a.K);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -63,14 +69,18 @@ __global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 2 * nwc);
     }
+    for (int p = 0; p < 2; p++) {
+      mbar_init(&redbar[p], 2 * nwc);
+      mbar_init(&redfree[p], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
   pdl_wait();
 
-  cta_topk(a.sc, a.ch, a.E, K, a.renorm, a.routed_scale, s_scores, s_scores + a.E, lst, sel,
-           wsel);
+  cta_topk(a.sc, a.ch, a.E, K, a.renorm, a.routed_scale,
+           reinterpret_cast<unsigned long long *>(s_scores), sel, wsel);
   if (blockIdx.x == 0) {
     if (tid < K) {
       a.idx_out[tid] = sel[tid];
@@ -91,35 +101,77 @@ __global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
 
   const int nitems = K * tiles;
   if (warp == 2 * nwc) {
-    // ---------------- producer: one elected lane streams stages ----------------
-    if (lane == 0) {
-      int it = 0;
+    // ---------------- producer: lane p < NS owns ring slot p ----------------
+    // A single thread issues only a few bulk copies per microsecond, so the stages are
+    // spread over NS lanes; each slot's fills are issued by one lane, in phase order.
+    if (lane < NS) {
+      const int p = lane;
+      const int nmine = (nitems - blockIdx.x + gridDim.x - 1) / gridDim.x;  // items of this CTA
+      const int nst = nmine > 0 ? nmine * nblk : 0;                            // stages
+      int it = p;
       bool ok = true;
-      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+      for (; it < nst; it += NS) {
+        const int item = blockIdx.x + (it / nblk) * gridDim.x;
+        const int b = it % nblk;
         const int j = item / tiles, tile = item % tiles;
         const uint8_t *rec = a.ex.base + (long long)sel[j] * a.ex.stride;
-        for (int b = 0; b < nblk; b++, it++) {
-          const int s = it % NS;
-          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
-            set_status(a.status, K3MOE_ERR_TIMEOUT);
-            ok = false;
-            break;
-          }
-          const int r = tile * kTileRows + b * RB;
-          uint8_t *dst = ring + (size_t)s * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
-          bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, RB * rowb, &full[s]);
-          bulk_g2s(dst + RB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, RB * rowb, &full[s]);
-          bulk_g2s(dst + 2 * RB * rowb, rec + a.ex.off[1] + (size_t)r * G, RB * G, &full[s]);
-          bulk_g2s(dst + 2 * RB * rowb + RB * G, rec + a.ex.off[5] + (size_t)r * G, RB * G,
-                   &full[s]);
+        if (!mbar_wait(&empty[p], ((it / NS) & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          ok = false;
+          break;
         }
+        const int r = tile * kTileRows + b * RB;
+        uint8_t *dst = ring + (size_t)p * stage_bytes;
+        mbar_arrive_expect_tx(&full[p], stage_bytes);
+        bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, RB * rowb, &full[p]);
+        bulk_g2s(dst + RB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, RB * rowb, &full[p]);
+        bulk_g2s(dst + 2 * RB * rowb, rec + a.ex.off[1] + (size_t)r * G, RB * G, &full[p]);
+        bulk_g2s(dst + 2 * RB * rowb + RB * G, rec + a.ex.off[5] + (size_t)r * G, RB * G,
+                 &full[p]);
       }
-      if (!ok) {
-        // bounded wait for the copies already issued before leaving
-        for (int k = (it > NS ? it - NS : 0); k < it; k++)
-          mbar_wait(&full[k % NS], (k / NS) & 1, 400000000LL);
+      if (!ok && it - NS >= 0)  // bounded wait for this slot's last issued fill
+        mbar_wait(&full[p], ((it - NS) / NS) & 1, 400000000LL);
+    }
+    return;
+  }
+
+  if (warp == 2 * nwc + 1) {
+    // ---------------- epilogue: SiTU and activation output per tile ----------------
+    int n = 0;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, n++) {
+      const int j = item / tiles, tile = item % tiles;
+      const int par = n & 1;
+      const float *rt = red + par * (16 * 64);
+      if (!mbar_wait(&redbar[par], (n >> 1) & 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
       }
+      // row `lane` of the tile was computed by the warps of row parity lane % 2
+      const int hp = lane & 1;
+      float gs = 0.f, us = 0.f;
+      for (int w = hp * nwc; w < (hp + 1) * nwc; w++) {
+        gs += rt[(w * 32 + lane) * 2];
+        us += rt[(w * 32 + lane) * 2 + 1];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&redfree[par]);
+      float act = situ(gs, us, a.b1, a.b2);
+      if (*abort_flag) act = 0.f;
+      float mx = fabsf(act);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      int e2 = 0;
+      if (mx > 0.f) {
+        e2 = exponent_of(mx) - 14;
+        e2 = e2 < -110 ? -110 : e2;
+      }
+      const float sa = act * pow2i(-e2);
+      const __half hh = __float2half_rn(sa);
+      const __half hl = __float2half_rn(sa - __half2float(hh));
+      const size_t o = act_index(j, I, tile, lane);
+      a.act_hi[o] = __half_as_ushort(hh);
+      a.act_lo[o] = __half_as_ushort(hl);
+      if (lane == 0) a.act_ex[(size_t)j * (I / kGroup) + tile] = e2;
     }
     return;
   }
@@ -147,11 +199,17 @@ __global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
     xe = prescale_group_f16(v, xr);
   }
 
-  int it = 0, parity = 0;
+  int it = 0, n = 0;
   bool aborted = false;
-  for (int item = blockIdx.x; item < nitems; item += gridDim.x, parity ^= 1) {
-    const int j = item / tiles, tile = item % tiles;
-    float *rt = red + parity * (16 * 64);  // [warp][row 0..31][mat]
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x, n++) {
+    const int par = n & 1;
+    float *rt = red + par * (16 * 64);  // [warp][row 0..31][mat]
+    // the epilogue must be done with this buffer's previous tile (two tiles back)
+    if (!aborted && !mbar_wait(&redfree[par], ((n >> 1) & 1) ^ 1)) {
+      set_status(a.status, K3MOE_ERR_TIMEOUT);
+      aborted = true;
+      *abort_flag = 1;
+    }
 #pragma unroll 1
     for (int b = 0; b < nblk; b += 2) {
       float vals[V];
@@ -189,39 +247,14 @@ __global__ void __launch_bounds__(480, 1) k_gateup_t1(GateUpT1Args a) {
         rt[(warp * 32 + (b * RB + b2 * RB + h + 2 * k)) * 2 + m] = tot;
       }
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(2 * C) : "memory");
-    if (warp == 0) {
-      // row `lane` of the tile was computed by the warps of parity lane % 2
-      const int hp = lane & 1;
-      float gs = 0.f, us = 0.f;
-      for (int w = hp * nwc; w < (hp + 1) * nwc; w++) {
-        gs += rt[(w * 32 + lane) * 2];
-        us += rt[(w * 32 + lane) * 2 + 1];
-      }
-      float act = situ(gs, us, a.b1, a.b2);
-      if (*abort_flag) act = 0.f;
-      float mx = fabsf(act);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      int e2 = 0;
-      if (mx > 0.f) {
-        e2 = exponent_of(mx) - 14;
-        e2 = e2 < -110 ? -110 : e2;
-      }
-      const float sa = act * pow2i(-e2);
-      const __half hh = __float2half_rn(sa);
-      const __half hl = __float2half_rn(sa - __half2float(hh));
-      const size_t o = (size_t)j * I + tile * kTileRows + lane;
-      a.act_hi[o] = __half_as_ushort(hh);
-      a.act_lo[o] = __half_as_ushort(hl);
-      if (lane == 0) a.act_ex[(size_t)j * (I / kGroup) + tile] = e2;
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&redbar[par]);  // also when aborted: the epilogue never hangs
   }
 }
 
-size_t gateup_t1_smem(int H, int E, int RB, int NS) {
+size_t gateup_t1_smem(int H, int E, int K, int RB, int NS) {
   const int G = H / kGroup;
-  return gu_ring_offset(E) + (size_t)NS * 2 * RB * (H / 2 + G);
+  return gu_ring_offset(E, K) + (size_t)NS * 2 * RB * (H / 2 + G);
 }
 
 cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl) {
@@ -229,8 +262,8 @@ cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, b
   const int C = ((G + 31) / 32) * 32;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(2 * C + 32);
-  cfg.dynamicSmemBytes = gateup_t1_smem(a.H, a.E, a.RB, a.NS);
+  cfg.blockDim = dim3(2 * C + 64);
+  cfg.dynamicSmemBytes = gateup_t1_smem(a.H, a.E, a.K, a.RB, a.NS);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -278,13 +311,15 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
   uint64_t *actbar = empty + 32;
   float *dbuf = reinterpret_cast<float *>(smem + 1024);   // [P][16]
   float *ds = dbuf + (size_t)P * kDownRows;               // [T][16]
-  uint8_t *p8 = reinterpret_cast<uint8_t *>(ds + (size_t)T * kDownRows);
-  p8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p8) + 127) & ~uintptr_t(127));
-  uint16_t *s_hi = reinterpret_cast<uint16_t *>(p8);      // [P][I] (ACT_SMEM)
-  uint16_t *s_lo = s_hi + (ACT_SMEM ? (size_t)P * I : 0);
-  int32_t *s_ex = reinterpret_cast<int32_t *>(s_lo + (ACT_SMEM ? (size_t)P * I : 0));
-  uint8_t *ring = reinterpret_cast<uint8_t *>(s_ex + (ACT_SMEM ? (size_t)P * G2 : 0));
-  ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ring) + 127) & ~uintptr_t(127));
+  // byte offsets inside the dynamic shared array (kept as smem + offset so the compiler
+  // sees shared-space accesses)
+  const size_t o_act = (1024 + ((size_t)P * kDownRows + (size_t)T * kDownRows) * 4 + 127) & ~size_t(127);
+  const size_t n_act = ACT_SMEM ? (size_t)P * I * 2 : 0;
+  uint16_t *s_hi = reinterpret_cast<uint16_t *>(smem + o_act);      // [P][I] (ACT_SMEM)
+  uint16_t *s_lo = reinterpret_cast<uint16_t *>(smem + o_act + n_act);
+  int32_t *s_ex = reinterpret_cast<int32_t *>(smem + o_act + 2 * n_act);
+  const size_t o_ring = (o_act + 2 * n_act + (ACT_SMEM ? (size_t)P * G2 * 4 : 0) + 127) & ~size_t(127);
+  uint8_t *ring = smem + o_ring;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -304,8 +339,9 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
   const int *plist = uoff + P + 1;
 
   if (warp == kDnWarps) {
-    if (lane == 0) {
-      bool ok = true;
+    // producer: lane p < NS owns ring slot p (stages it with it % NS == p), lane 31 stages
+    // the activations and prefetches the shared-expert rows
+    if (lane == 31) {
       if (ACT_SMEM) {
         const uint32_t nb = (uint32_t)((size_t)P * I * 2);
         const uint32_t ne = (uint32_t)((size_t)P * G2 * 4);
@@ -314,32 +350,36 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
         bulk_g2s(s_lo, a.act_lo, nb, actbar);
         bulk_g2s(s_ex, a.act_ex, ne, actbar);
       }
-      int it = 0;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const int r0 = tile * kDownRows;
-        for (int k = 0; k < 2 * U; k++, it++) {
-          const int s = it % NS;
-          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
-            set_status(a.status, K3MOE_ERR_TIMEOUT);
-            ok = false;
-            break;
-          }
-          if (k == 0 && a.sh_down != nullptr)  // this tile's shared-expert rows, into L2
-            bulk_prefetch_l2(a.sh_down + (size_t)r0 * a.SI, kDownRows * a.SI * 2);
-          const int u = k >> 1, rh = k & 1;
-          const int rs = r0 + rh * kDnStageRows;
-          const uint8_t *rec = a.ex.base + (long long)uexp[u] * a.ex.stride;
-          uint8_t *dst = ring + (size_t)s * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
-          bulk_g2s(dst, rec + a.ex.off[2] + (size_t)rs * rowb, kDnStageRows * rowb, &full[s]);
-          bulk_g2s(dst + kDnStageRows * rowb, rec + a.ex.off[3] + (size_t)rs * G2,
-                   kDnStageRows * G2, &full[s]);
-        }
-      }
-      if (!ok)
-        for (int k = (it > NS ? it - NS : 0); k < it; k++)
-          mbar_wait(&full[k % NS], (k / NS) & 1, 400000000LL);
+      if (a.sh_down != nullptr)
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+          bulk_prefetch_l2(a.sh_down + (size_t)tile * kDownRows * a.SI, kDownRows * a.SI * 2);
       if (ACT_SMEM) mbar_wait(actbar, 0, 400000000LL);
+    } else if (lane < NS) {
+      const int p = lane;
+      const int per_tile = 2 * U;
+      const int nmine = (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+      const int nst = nmine > 0 ? nmine * per_tile : 0;
+      int it = p;
+      bool ok = true;
+      for (; it < nst && per_tile > 0; it += NS) {
+        const int tile = blockIdx.x + (it / per_tile) * gridDim.x;
+        const int k = it % per_tile;
+        const int r0 = tile * kDownRows;
+        if (!mbar_wait(&empty[p], ((it / NS) & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const int u = k >> 1, rh = k & 1;
+        const int rs = r0 + rh * kDnStageRows;
+        const uint8_t *rec = a.ex.base + (long long)uexp[u] * a.ex.stride;
+        uint8_t *dst = ring + (size_t)p * stage_bytes;
+        mbar_arrive_expect_tx(&full[p], stage_bytes);
+        bulk_g2s(dst, rec + a.ex.off[2] + (size_t)rs * rowb, kDnStageRows * rowb, &full[p]);
+        bulk_g2s(dst + kDnStageRows * rowb, rec + a.ex.off[3] + (size_t)rs * G2,
+                 kDnStageRows * G2, &full[p]);
+      }
+      if (!ok && it - NS >= 0) mbar_wait(&full[p], ((it - NS) / NS) & 1, 400000000LL);
     }
     return;
   }
@@ -378,13 +418,15 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; r++) acc[r] = 0.f;
         for (int q = 0; q < NG; q++) {
-          const int gg = l * NG + q;
+          // group lanes interleave (gg = q*16 + l): the 16 lanes read 16 consecutive
+          // 16-byte weight chunks, and activation chunks 64 B apart
+          const int gg = q * kDnLanes + l;
           uint32_t xh[16], xl[16];
-          const uint4 *ph = reinterpret_cast<const uint4 *>(act_hi + (size_t)i * I + gg * kGroup);
-          const uint4 *pl = reinterpret_cast<const uint4 *>(act_lo + (size_t)i * I + gg * kGroup);
+          const uint4 *ph = reinterpret_cast<const uint4 *>(act_hi + act_index(i, I, gg, 0));
+          const uint4 *pl = reinterpret_cast<const uint4 *>(act_lo + act_index(i, I, gg, 0));
 #pragma unroll
           for (int c = 0; c < 4; c++) {
-            const uint4 x0 = ph[c], x1 = pl[c];
+            const uint4 x0 = ph[c * G2], x1 = pl[c * G2];
             xh[4 * c] = x0.x; xh[4 * c + 1] = x0.y; xh[4 * c + 2] = x0.z; xh[4 * c + 3] = x0.w;
             xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
           }
@@ -465,8 +507,9 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
 size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem) {
   const int G2 = I / kGroup;
   const size_t stage = (size_t)kDnStageRows * (I / 2 + G2);
-  size_t b = 1024 + ((size_t)P * kDownRows + (size_t)T * kDownRows) * 4 + 128;
-  if (act_smem) b += (size_t)P * I * 4 + (size_t)P * G2 * 4 + 128;
+  size_t b = (1024 + ((size_t)P * kDownRows + (size_t)T * kDownRows) * 4 + 127) & ~size_t(127);
+  if (act_smem) b += (size_t)P * I * 4 + (size_t)P * G2 * 4;
+  b = (b + 127) & ~size_t(127);
   return b + NS * stage;
 }
 

@@ -81,27 +81,32 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t x2, uint32_t w2, float c)
 // x' given as 16 f16x2 registers (pair p = columns 2p, 2p+1) and the weights as the 16
 // packed bytes of the group (4 words).  Two accumulators for latency.
 __device__ __forceinline__ float group_dot(const uint32_t (&x)[16], uint4 w) {
-  float a = 0.f, b = 0.f;
+  float a = 0.f, b = 0.f, c = 0.f, d = 0.f;  // four chains for latency
   uint32_t h0, h1, h2, h3;
   e2m1x8_to_f16x2x4(w.x, h0, h1, h2, h3);
   a = fma2_f16_f32(x[0], h0, a); b = fma2_f16_f32(x[1], h1, b);
-  a = fma2_f16_f32(x[2], h2, a); b = fma2_f16_f32(x[3], h3, b);
+  c = fma2_f16_f32(x[2], h2, c); d = fma2_f16_f32(x[3], h3, d);
   e2m1x8_to_f16x2x4(w.y, h0, h1, h2, h3);
   a = fma2_f16_f32(x[4], h0, a); b = fma2_f16_f32(x[5], h1, b);
-  a = fma2_f16_f32(x[6], h2, a); b = fma2_f16_f32(x[7], h3, b);
+  c = fma2_f16_f32(x[6], h2, c); d = fma2_f16_f32(x[7], h3, d);
   e2m1x8_to_f16x2x4(w.z, h0, h1, h2, h3);
   a = fma2_f16_f32(x[8], h0, a); b = fma2_f16_f32(x[9], h1, b);
-  a = fma2_f16_f32(x[10], h2, a); b = fma2_f16_f32(x[11], h3, b);
+  c = fma2_f16_f32(x[10], h2, c); d = fma2_f16_f32(x[11], h3, d);
   e2m1x8_to_f16x2x4(w.w, h0, h1, h2, h3);
   a = fma2_f16_f32(x[12], h0, a); b = fma2_f16_f32(x[13], h1, b);
-  a = fma2_f16_f32(x[14], h2, a); b = fma2_f16_f32(x[15], h3, b);
-  return a + b;
+  c = fma2_f16_f32(x[14], h2, c); d = fma2_f16_f32(x[15], h3, d);
+  return (a + b) + (c + d);
 }
 
 // Same with x' = hi + lo (two f16 terms per column): sum_k (hi[k] + lo[k]) * e2m1[k].
+// The hi products go through the exact f16 x f16 -> f32 path; the lo term (at most 2^-11
+// of hi) is accumulated in packed f16 (HFMA2), whose rounding is ~2^-11 of a term that is
+// itself ~2^-11 of the result, i.e. ~2^-22 relative -- far below f32 accumulation noise of
+// a 1536-term sum.  |lo| <= 2^4 after prescaling, so the f16 sums cannot overflow.
 __device__ __forceinline__ float group_dot2(const uint32_t (&xh)[16], const uint32_t (&xl)[16],
                                             uint4 w) {
   float a = 0.f, b = 0.f;
+  __half2 l2 = __float2half2_rn(0.f);
   uint32_t h[4];
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -109,11 +114,23 @@ __device__ __forceinline__ float group_dot2(const uint32_t (&xh)[16], const uint
     e2m1x8_to_f16x2x4(ww[q], h[0], h[1], h[2], h[3]);
 #pragma unroll
     for (int p = 0; p < 4; p++) {
-      a = fma2_f16_f32(xh[4 * q + p], h[p], a);
-      b = fma2_f16_f32(xl[4 * q + p], h[p], b);
+      if (p & 1)
+        b = fma2_f16_f32(xh[4 * q + p], h[p], b);
+      else
+        a = fma2_f16_f32(xh[4 * q + p], h[p], a);
+      l2 = __hfma2(*reinterpret_cast<const __half2 *>(&xl[4 * q + p]),
+                   *reinterpret_cast<const __half2 *>(&h[p]), l2);
     }
   }
-  return a + b;
+  return (a + b) + (__low2float(l2) + __high2float(l2));
+}
+
+// Layout of the routed activations handed from gate/up to down, per (token, slot) pair
+// i: element k of input group gg lives at  i*I + ((k / 8) * (I/32) + gg) * 8 + k % 8,
+// i.e. [pair][chunk of 8][group][8]: lanes that take consecutive groups read consecutive
+// 16-byte chunks.
+__host__ __device__ __forceinline__ size_t act_index(int i, int I, int gg, int k) {
+  return (size_t)i * I + ((size_t)(k >> 3) * (I / 32) + gg) * 8 + (k & 7);
 }
 
 // Factor turning an unscaled group sum into its contribution: 2^(s - 127 + ex) where s

@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(256) k_expert_gateup(
         const float sa = a * pow2i(-e2);
         const __half hh = __float2half_rn(sa);
         const __half hl = __float2half_rn(sa - __half2float(hh));
-        const size_t o = (size_t)i * I + r0 + lane;
+        const size_t o = act_index(i, I, tile, lane);
         act_hi[o] = __half_as_ushort(hh);
         act_lo[o] = __half_as_ushort(hl);
         if (lane == 0) act_ex[(size_t)i * (I / kGroup) + tile] = e2;
@@ -351,11 +351,11 @@ __global__ void __launch_bounds__(256) k_down_combine(
           const int gg = l * NG + q;
           uint32_t xh[16], xl[16];
           {
-            const uint4 *ph = reinterpret_cast<const uint4 *>(act_hi + (size_t)i * I + gg * kGroup);
-            const uint4 *pl = reinterpret_cast<const uint4 *>(act_lo + (size_t)i * I + gg * kGroup);
+            const uint4 *ph = reinterpret_cast<const uint4 *>(act_hi + act_index(i, I, gg, 0));
+            const uint4 *pl = reinterpret_cast<const uint4 *>(act_lo + act_index(i, I, gg, 0));
 #pragma unroll
             for (int c = 0; c < 4; c++) {
-              const uint4 a = ph[c], b = pl[c];
+              const uint4 a = ph[c * G2], b = pl[c * G2];
               xh[4 * c] = a.x; xh[4 * c + 1] = a.y; xh[4 * c + 2] = a.z; xh[4 * c + 3] = a.w;
               xl[4 * c] = b.x; xl[4 * c + 1] = b.y; xl[4 * c + 2] = b.z; xl[4 * c + 3] = b.w;
             }

@@ -25,6 +25,11 @@ cudaError_t launch_router_shared(int tc, int grid, size_t smem, cudaStream_t st,
                                  const uint16_t *sh_gate, const uint16_t *sh_up, int SI, float b1,
                                  float b2, float *sc, float *ch, float *act_s, int32_t *status);
 cudaError_t set_router_smem_limits(int bytes);
+// One decode token: router rows and shared gate/up rows, one warp each.
+cudaError_t launch_router_t1(cudaStream_t st, const uint16_t *x, int H, const uint16_t *wr,
+                             int E, const float *bias, const uint16_t *sh_gate,
+                             const uint16_t *sh_up, int SI, float b1, float b2, float *sc,
+                             float *ch, float *act_s, int32_t *status);
 
 __global__ void k_topk(const float *__restrict__ scores, const float *__restrict__ choice, int T,
                        int E, int K, int renorm, float routed_scale, int32_t *__restrict__ idx,
@@ -89,7 +94,7 @@ struct DownArgs {
   int32_t *status;
 };
 
-size_t gateup_t1_smem(int H, int E, int RB, int NS);
+size_t gateup_t1_smem(int H, int E, int K, int RB, int NS);
 cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl);
 size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem);
 cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool pdl,

@@ -149,6 +149,126 @@ __global__ void __launch_bounds__(256) k_router_shared(
   pdl_launch_dependents();
 }
 
+// One decode token.  Work units, one per warp, eight per CTA:
+//   [0, E)                router row e (float-float dot, then score and selection score)
+//   [Ep, Ep + 2 SI)       shared-expert rows: Ep + 2r = gate row r, Ep + 2r + 1 = up row r
+// with Ep = E rounded up to even, so the gate and up rows of r are two warps of one CTA;
+// the gate warp's lane 0 applies SiTU once both dots are in shared memory.  Each lane
+// keeps 14 16-byte loads in flight.
+__global__ void __launch_bounds__(256) k_router_t1(const uint16_t *__restrict__ x, int H,
+                                                   const uint16_t *__restrict__ wr, int E,
+                                                   const float *__restrict__ bias,
+                                                   const uint16_t *__restrict__ sh_gate,
+                                                   const uint16_t *__restrict__ sh_up, int SI,
+                                                   float b1, float b2, float *__restrict__ sc,
+                                                   float *__restrict__ ch,
+                                                   float *__restrict__ act_s, int32_t *status) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ float dots[8];
+  constexpr int kB = 14;  // loads in flight per lane
+  uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nchunk = H >> 3;
+  const int Ep = E + (E & 1);
+  pdl_wait();
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs);
+    for (int i = threadIdx.x; i < nchunk; i += blockDim.x) dst[i] = src[i];
+  }
+  __syncthreads();
+  const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
+  const int unit = blockIdx.x * 8 + warp;
+  const bool is_router = unit < E;
+  const bool is_shared = unit >= Ep && unit < Ep + 2 * SI;
+  if (is_router || is_shared) {
+    const int r = is_router ? unit : (unit - Ep) >> 1;
+    const bool up = is_shared && ((unit - Ep) & 1);
+    const uint16_t *row = is_router ? wr + (size_t)r * H
+                                    : (up ? sh_up : sh_gate) + (size_t)r * H;
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(row);
+    float hi = 0.f, lo = 0.f, acc = 0.f;
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * kB) {
+      uint4 wv[kB];
+#pragma unroll
+      for (int b = 0; b < kB; b++) {
+        const int c = c0 + 32 * b;
+        wv[b] = (c < nchunk) ? __ldg(w4 + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int b = 0; b < kB; b++) {
+        const int c = c0 + 32 * b;
+        if (c < nchunk) {
+          const uint4 xv = xs4[c];
+          const uint32_t wa[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
+          const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            if (is_router) {
+              // bf16 x bf16 is exact in float; carry the sum as a float-float pair
+              float p = __fmul_rn(bf16_lo(wa[q]), bf16_lo(xa[q]));
+              float s, e;
+              two_sum(hi, p, s, e);
+              hi = s;
+              lo = __fadd_rn(lo, e);
+              p = __fmul_rn(bf16_hi(wa[q]), bf16_hi(xa[q]));
+              two_sum(hi, p, s, e);
+              hi = s;
+              lo = __fadd_rn(lo, e);
+            } else {
+              acc = fmaf(bf16_lo(wa[q]), bf16_lo(xa[q]), acc);
+              acc = fmaf(bf16_hi(wa[q]), bf16_hi(xa[q]), acc);
+            }
+          }
+        }
+      }
+    }
+    if (is_router) {
+      {
+        const float s = __fadd_rn(hi, lo);
+        lo = __fsub_rn(lo, __fsub_rn(s, hi));
+        hi = s;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+        ff_add(hi, lo, oh, ol);
+      }
+      if (lane == 0) {
+        // unbiased score: logistic of the float logit, in double, rounded once;
+        // selection score: one float add of the correction bias
+        const float sv = (float)(1.0 / (1.0 + exp(-(double)hi)));
+        const float cv = __fadd_rn(sv, bias ? bias[r] : 0.f);
+        sc[r] = sv;
+        ch[r] = cv;
+        if (!(fabsf(cv) <= 3.402823466e38f)) set_status(status, K3MOE_ERR_NONFINITE);
+      }
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) dots[warp] = acc;
+    }
+  }
+  __syncthreads();
+  if (is_shared && !(((unit - Ep) & 1)) && lane == 0) {
+    const int r = (unit - Ep) >> 1;
+    act_s[r] = situ(dots[warp], dots[warp + 1], b1, b2);
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_router_t1(cudaStream_t st, const uint16_t *x, int H, const uint16_t *wr,
+                             int E, const float *bias, const uint16_t *sh_gate,
+                             const uint16_t *sh_up, int SI, float b1, float b2, float *sc,
+                             float *ch, float *act_s, int32_t *status) {
+  const int Ep = E + (E & 1);
+  const int units = Ep + 2 * SI;
+  k_router_t1<<<(units + 7) / 8, 256, (size_t)H * 2, st>>>(x, H, wr, E, bias, sh_gate, sh_up, SI,
+                                                          b1, b2, sc, ch, act_s, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_shared(int tc, int grid, size_t smem, cudaStream_t st, const uint16_t *x,
                                  int T, int H, const uint16_t *wr, int E, const float *bias,
                                  const uint16_t *sh_gate, const uint16_t *sh_up, int SI, float b1,
@@ -166,25 +286,26 @@ cudaError_t set_router_smem_limits(int bytes) {
   cudaError_t e = cudaFuncSetAttribute(k_router_shared<1>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_router_t1, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_router_shared<kTokChunk>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // One CTA (256 threads) per token: the top-k of its selection scores (cta_topk).
-__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ scores,
+__global__ void __launch_bounds__(512) k_topk(const float *__restrict__ scores,
                                               const float *__restrict__ choice, int T, int E,
                                               int K, int renorm, float routed_scale,
                                               int32_t *__restrict__ idx, float *__restrict__ w,
                                               int32_t *status) {
-  __shared__ int lst[8 * 32];
   __shared__ int sel[32];
   __shared__ float wsel[32];
-  extern __shared__ __align__(16) float s_scores[];  // [2][E]
+  extern __shared__ __align__(16) unsigned long long s_keys[];  // top-k scratch
   pdl_wait();
   const int t = blockIdx.x;
   if (t >= T) return;
-  cta_topk(scores + (size_t)t * E, choice + (size_t)t * E, E, K, renorm, routed_scale, s_scores,
-           s_scores + E, lst, sel, wsel);
+  cta_topk(scores + (size_t)t * E, choice + (size_t)t * E, E, K, renorm, routed_scale, s_keys,
+           sel, wsel);
   if (threadIdx.x < K) {
     idx[(size_t)t * K + threadIdx.x] = sel[threadIdx.x];
     w[(size_t)t * K + threadIdx.x] = wsel[threadIdx.x];
