@@ -49,7 +49,8 @@ typedef enum {
     K3MOE_ERR_CUDA = 5,       /* a CUDA launch failed (see cudaGetLastError) */
     K3MOE_ERR_TIMEOUT = 6,    /* a bounded device-side wait gave up */
     K3MOE_ERR_BAD_EXPERT = 7, /* an expert index outside [0, n_experts) */
-    K3MOE_ERR_NONFINITE = 8   /* a router score that is NaN or infinite */
+    K3MOE_ERR_NONFINITE = 8,  /* a router score that is NaN or infinite */
+    K3MOE_ERR_SCRATCH_LIMIT = 9 /* the call needs more than K3MOE_STATIC_SCRATCH_BYTES */
 } k3moe_status;
 
 typedef enum { K3MOE_F32 = 0, K3MOE_BF16 = 1 } k3moe_dtype;
@@ -143,6 +144,40 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
                          float *w_out, void *y, k3moe_dtype ydt, int32_t accumulate,
                          void *workspace, size_t ws_bytes, int32_t *status_dev,
                          k3moe_stream_t stream);
+
+/* Size of the library's static scratch array (8 MiB), the most scratch that
+ * k3moe_layer_static_scratch can use.  It holds the workspace of one pass of up to 64
+ * tokens at the model's shape (H 7168, I 1536, 896 experts, top 16, shared 1536:
+ * 7,360,544 bytes), so that shape runs at any T.                                     */
+#define K3MOE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* k3moe_layer without a workspace argument: the same kernels, arguments, results and
+ * error codes, with the scratch taken from an array of K3MOE_STATIC_SCRATCH_BYTES that
+ * the library declares as a static device variable (one copy per device).  The pages
+ * have no counterpart; it serves callers that must not allocate device memory while
+ * they run the layer: cudaMalloc and cudaFree can synchronise the whole device and
+ * stall a latency-bound decode loop, a host program may have handed all free memory to
+ * a cache pool already, and a plug-in may receive only the tensors of the step with no
+ * allocator to obtain a workspace from.  This call allocates and frees nothing.
+ *   - K3MOE_ERR_SCRATCH_LIMIT, with nothing launched, when k3moe_workspace_size(dims, T)
+ *     exceeds K3MOE_STATIC_SCRATCH_BYTES.
+ *   - The first call on a device, with that device current, does one-time set-up: it
+ *     looks up the device address of the array (which may load the library's device
+ *     code) and sets kernel attributes.  Make that first call before any stream capture
+ *     starts on the device.  K3MOE_ERR_CUDA if the lookup fails.
+ *   - Nothing in the array has to start at zero: each call writes every scratch word
+ *     before it reads it.
+ *   - Every call on a device shares the one array.  Calls ordered on one stream are
+ *     safe; two calls whose work can overlap on the device (different streams without
+ *     an ordering between them, or concurrent host threads) race on the array and
+ *     their results are undefined.  *status_dev stays the caller's.                  */
+k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *x_bf16,
+                                        int32_t T, const uint16_t *wr_bf16, const float *bias,
+                                        const k3moe_experts *experts, const uint16_t *sh_gate,
+                                        const uint16_t *sh_up, const uint16_t *sh_down,
+                                        int32_t *idx_out, float *w_out, void *y,
+                                        k3moe_dtype ydt, int32_t accumulate,
+                                        int32_t *status_dev, k3moe_stream_t stream);
 
 /* RMSNorm then bf16 (kimi-k3-in-c, section 5): for each of T rows of width n,
  *   inv = 1 / sqrt(mean(h^2) + eps) (sum of squares in double), out = bf16(h * inv),

@@ -378,6 +378,34 @@ size_t dtype_size(k3moe_dtype t) { return t == K3MOE_F32 ? 4 : 2; }
 
 }  // namespace
 
+// ---- scratch of k3moe_layer_static_scratch -------------------------------------------
+// A static device array: every device that loads this library's device code gets its own
+// copy, reserved when the code is loaded, so the call that uses it allocates nothing.
+static __device__ __align__(256) uint8_t g_static_scratch[K3MOE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+void *g_static_scratch_addr[kMaxDevices];
+
+// Device address of the current device's copy of g_static_scratch, looked up on the
+// first call made with that device current; nullptr if the lookup fails.
+void *static_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // leave no stale error for the next launch check
+      return nullptr;
+    }
+    g_static_scratch_addr[dev] = p;
+  }
+  return g_static_scratch_addr[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 const char *k3moe_status_str(k3moe_status s) {
@@ -391,6 +419,8 @@ const char *k3moe_status_str(k3moe_status s) {
     case K3MOE_ERR_TIMEOUT: return "device wait timed out";
     case K3MOE_ERR_BAD_EXPERT: return "expert index out of range";
     case K3MOE_ERR_NONFINITE: return "non-finite router score";
+    case K3MOE_ERR_SCRATCH_LIMIT:
+      return "call needs more scratch than the static array holds (K3MOE_STATIC_SCRATCH_BYTES)";
   }
   return "unknown status";
 }
@@ -510,6 +540,28 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
     if (s != K3MOE_OK) return s;
   }
   return K3MOE_OK;
+}
+
+// k3moe_layer with the static array as its workspace: size check first (nothing is
+// launched when the request does not fit), then the per-device address lookup.
+k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *x_bf16,
+                                        int32_t T, const uint16_t *wr_bf16, const float *bias,
+                                        const k3moe_experts *experts, const uint16_t *sh_gate,
+                                        const uint16_t *sh_up, const uint16_t *sh_down,
+                                        int32_t *idx_out, float *w_out, void *y,
+                                        k3moe_dtype ydt, int32_t accumulate,
+                                        int32_t *status_dev, k3moe_stream_t stream) {
+  const k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (T < 0) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (k3moe_workspace_size(dims, T) > (size_t)K3MOE_STATIC_SCRATCH_BYTES)
+    return K3MOE_ERR_SCRATCH_LIMIT;
+  void *scratch = static_scratch();
+  if (!scratch) return K3MOE_ERR_CUDA;
+  return k3moe_layer(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up, sh_down, idx_out,
+                     w_out, y, ydt, accumulate, scratch, K3MOE_STATIC_SCRATCH_BYTES, status_dev,
+                     stream);
 }
 
 k3moe_status k3moe_rmsnorm_bf16(const float *h, int32_t T, int32_t n, float eps, uint16_t *out,

@@ -16,14 +16,17 @@ from . import build as _build
 K3MOE_OK = 0
 STATUS_NAMES = {
     0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_WORKSPACE", 5: "ERR_CUDA",
-    6: "ERR_TIMEOUT", 7: "ERR_BAD_EXPERT", 8: "ERR_NONFINITE",
+    6: "ERR_TIMEOUT", 7: "ERR_BAD_EXPERT", 8: "ERR_NONFINITE", 9: "ERR_SCRATCH_LIMIT",
 }
+K3MOE_ERR_SCRATCH_LIMIT = 9
+# Bytes of the library's static scratch array (K3MOE_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 F32, BF16 = 0, 1
 
 # Every symbol include/k3moe.h declares.
 EXPORTS = (
     "k3moe_record_layout", "k3moe_workspace_size", "k3moe_route", "k3moe_expert_ffn_mxfp4",
-    "k3moe_layer", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4", "k3moe_trace_enable",
+    "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4", "k3moe_trace_enable",
     "k3moe_trace_read", "k3moe_status_str",
 )
 
@@ -78,6 +81,9 @@ def lib(build_if_missing: bool = True):
     L.k3moe_layer.restype = i32
     L.k3moe_layer.argtypes = [dp, vp, i32, vp, vp, ep, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz,
                               vp, vp]
+    L.k3moe_layer_static_scratch.restype = i32
+    L.k3moe_layer_static_scratch.argtypes = [dp, vp, i32, vp, vp, ep, vp, vp, vp, vp, vp, vp,
+                                             i32, i32, vp, vp]
     L.k3moe_rmsnorm_bf16.restype = i32
     L.k3moe_rmsnorm_bf16.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
     L.k3moe_dequant_mxfp4.restype = i32
@@ -202,6 +208,27 @@ def k3moe_layer(dims: LayerDims, x, wr, bias, experts, expert_stride: int, sh_ga
         _ptr(sh_up), _ptr(sh_down), _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
         int(bool(accumulate)), _ptr(workspace), workspace.numel(), _ptr(status),
         _stream(stream)))
+
+
+def k3moe_layer_static_scratch(dims: LayerDims, x, wr, bias, experts, expert_stride: int,
+                               sh_gate, sh_up, sh_down, y, status, idx_out=None, w_out=None,
+                               accumulate: bool = False, stream=None):
+    """k3moe_layer with the library's static scratch array in place of a workspace: for
+    callers that must not allocate device memory while they run the layer."""
+    d = dims.c()
+    x, wr = _bits16(x, "x"), _bits16(wr, "wr")
+    if sh_gate is not None:
+        sh_gate, sh_up, sh_down = (_bits16(sh_gate, "sh_gate"), _bits16(sh_up, "sh_up"),
+                                   _bits16(sh_down, "sh_down"))
+    T = x.shape[0]
+    ydt = F32 if y.dtype == torch.float32 else BF16
+    if ydt == BF16:
+        y = _bits16(y, "y")
+    ex = Experts(ctypes.c_void_p(experts.data_ptr()), int(expert_stride))
+    _check("k3moe_layer_static_scratch", lib().k3moe_layer_static_scratch(
+        ctypes.byref(d), _ptr(x), T, _ptr(wr), _ptr(bias), ctypes.byref(ex), _ptr(sh_gate),
+        _ptr(sh_up), _ptr(sh_down), _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
+        int(bool(accumulate)), _ptr(status), _stream(stream)))
 
 
 def k3moe_rmsnorm_bf16(h, out, eps: float = 1e-5, stream=None):
