@@ -146,9 +146,9 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
                          k3moe_stream_t stream);
 
 /* Size of the library's static scratch array (8 MiB), the most scratch that
- * k3moe_layer_static_scratch can use.  It holds the workspace of one pass of up to 64
- * tokens at the model's shape (H 7168, I 1536, 896 experts, top 16, shared 1536:
- * 7,360,544 bytes), so that shape runs at any T.                                     */
+ * k3moe_layer_static_scratch can use.  At the model's shape (H 7168, I 1536, 896
+ * experts, top 16, shared 1536) it holds the workspace of up to 9 tokens: 115,040 bytes
+ * for one token, 8,238,848 for nine.                                                  */
 #define K3MOE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 /* k3moe_layer without a workspace argument: the same kernels, arguments, results and

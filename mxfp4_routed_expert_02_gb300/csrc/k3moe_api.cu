@@ -126,11 +126,14 @@ k3moe_status launch_status() {
 
 // ---- tracing: CUDA events around every launch, durations summed per kernel ---------
 enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KID_RMSNORM,
-                KID_DEQUANT, KID_GATEUP_T1, KID_DOWN_TMA, KID_COUNT };
-const char *const kKernelNames[KID_COUNT] = {"k_router_shared", "k_topk", "k_dispatch",
-                                             "k_expert_gateup", "k_down_combine",
-                                             "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1",
-                                             "k_down_tma"};
+                KID_DEQUANT, KID_GATEUP_T1, KID_DOWN_TMA, KID_ROUTE_HIST, KID_ROUTE_SCATTER,
+                KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
+                KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_COUNT };
+const char *const kKernelNames[KID_COUNT] = {
+    "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
+    "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
+    "k_route_scatter", "k_quant_x", "k_tc_gemm_gateup", "k_quant_act", "k_tc_gemm_down",
+    "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -376,6 +379,236 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
 
 size_t dtype_size(k3moe_dtype t) { return t == K3MOE_F32 ? 4 : 2; }
 
+// ---- multi-token path on the tensor cores -------------------------------------------
+// Shapes it takes: H, I (and SI) multiples of 64 with rows of at least 128 bytes of
+// packed MXFP4 (H, I >= 256) and of bf16 (SI >= 64).
+bool tc_shape_ok(const k3moe_dims *d) {
+  const int H = d->hidden, I = d->inter, SI = d->shared_inter;
+  if (H % 64 || I % 64 || H < 256 || I < 256) return false;
+  if (SI > 0 && (SI % 64 || SI < 64)) return false;
+  return true;
+}
+
+// Workspace of one pass of up to kTcTokens tokens (P = Tc * K pairs).
+struct WsTc {
+  float *sc, *ch;                 // router scores of one 64-token sub-pass
+  int32_t *idx;
+  float *w;
+  int32_t *off, *tile_off, *inv, *perm, *off1, *tile_off1;
+  uint8_t *xq, *xs;               // [kTcTermsX][P][H/2], [kTcTermsX][P][H/32]
+  float *act;                     // [P][I]
+  uint8_t *aq, *as;               // [kTcTermsAct][P][I/2], [kTcTermsAct][P][I/32]
+  float *dpair;                   // [P][H]
+  float *act_s;                   // [Tc][SI]
+  uint16_t *hs;                   // [2][Tc][SI]
+  float *ds;                      // [Tc][H]
+  size_t total;
+};
+
+WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
+  const int Tc = T < kTcTokens ? T : kTcTokens;
+  const size_t H = d->hidden, I = d->inter, E = d->n_experts, SI = d->shared_inter;
+  const size_t P = (size_t)Tc * d->topk;
+  size_t o = 0;
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += (bytes + 255) & ~size_t(255);
+    return reinterpret_cast<uint8_t *>(b + at);
+  };
+  WsTc w{};
+  const size_t Tr = Tc < kDecodeTokens ? Tc : kDecodeTokens;
+  w.sc = reinterpret_cast<float *>(take(Tr * E * 4));
+  w.ch = reinterpret_cast<float *>(take(Tr * E * 4));
+  w.idx = reinterpret_cast<int32_t *>(take(P * 4));
+  w.w = reinterpret_cast<float *>(take(P * 4));
+  w.off = reinterpret_cast<int32_t *>(take((E + 1) * 4));
+  w.tile_off = reinterpret_cast<int32_t *>(take((E + 1) * 4));
+  w.inv = reinterpret_cast<int32_t *>(take(P * 4));
+  w.perm = reinterpret_cast<int32_t *>(take(P * 4));
+  w.off1 = reinterpret_cast<int32_t *>(take(8));
+  w.tile_off1 = reinterpret_cast<int32_t *>(take(8));
+  w.xq = take((size_t)kTcTermsX * P * (H / 2));
+  w.xs = take((size_t)kTcTermsX * P * (H / kGroup));
+  w.act = reinterpret_cast<float *>(take(P * I * 4));
+  w.aq = take((size_t)kTcTermsAct * P * (I / 2));
+  w.as = take((size_t)kTcTermsAct * P * (I / kGroup));
+  w.dpair = reinterpret_cast<float *>(take(P * H * 4));
+  if (SI > 0) {
+    w.act_s = reinterpret_cast<float *>(take((size_t)Tc * SI * 4));
+    w.hs = reinterpret_cast<uint16_t *>(take((size_t)2 * Tc * SI * 2));
+    w.ds = reinterpret_cast<float *>(take((size_t)Tc * H * 4));
+  }
+  w.total = o;
+  return w;
+}
+
+// Token/pair tables of a tensor-core GEMM over K_bytes of K per row.
+void tc_k_split(long long k_bytes, TcGemmArgs &a) {
+  a.kchunks = (int)((k_bytes + 127) / 128);
+  a.ksteps_last = (int)((k_bytes - 128LL * (a.kchunks - 1) + 31) / 32);
+}
+
+// Expert FFN of Tc tokens on the tensor cores, given the route (idx, w [Tc][K]):
+// dispatch, x encoding, gate/up + SiTU, activation encoding, down, then (with the shared
+// expert when sh_gate != NULL) the router-order combine into y.
+k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+                        const k3moe_experts *ex, const int32_t *idx, const float *w,
+                        const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
+                        WsTc &ws, void *y, k3moe_dtype ydt, int accumulate, int32_t *status,
+                        cudaStream_t st) {
+  const int H = d->hidden, I = d->inter, E = d->n_experts, K = d->topk;
+  const int SI = sh_gate ? d->shared_inter : 0;
+  const int P = Tc * K;
+  int64_t off[7];
+  record_offsets(d, off);
+  const uint8_t *rec = ex->experts;
+  const unsigned long long es = (unsigned long long)ex->expert_stride;
+  {
+    TraceScope ts(KID_ROUTE_HIST, st);
+    k_route_hist<<<1, 1024, (size_t)E * 4, st>>>(idx, P, E, ws.off, ws.tile_off, ws.inv, status);
+  }
+  {
+    TraceScope ts(KID_ROUTE_SCATTER, st);
+    k_route_scatter<<<E, 256, 0, st>>>(idx, P, ws.off, ws.perm, ws.inv);
+  }
+  {
+    TraceScope ts(KID_QUANT_X, st);
+    const long long n = (long long)Tc * (H / kGroup);
+    int grid = (int)((n + 255) / 256);
+    if (grid > 16 * di->sms) grid = 16 * di->sms;
+    k_quant_x<<<grid, 256, 0, st>>>(x, Tc, H, K, ws.inv, P, ws.xq, ws.xs);
+  }
+  if (launch_status() != K3MOE_OK) return K3MOE_ERR_CUDA;
+  CUtensorMap mg, mu, md, mx, ma;
+  if (!tc_map3d(&mg, rec + off[0], H / 2, I, E, H / 2, es) ||
+      !tc_map3d(&mu, rec + off[4], H / 2, I, E, H / 2, es) ||
+      !tc_map3d(&md, rec + off[2], I / 2, H, E, I / 2, es) ||
+      !tc_map3d(&mx, ws.xq, H / 2, P, kTcTermsX, H / 2, (unsigned long long)P * (H / 2)) ||
+      !tc_map3d(&ma, ws.aq, I / 2, P, kTcTermsAct, I / 2, (unsigned long long)P * (I / 2)))
+    return K3MOE_ERR_CUDA;
+  TcGemmArgs g{};
+  g.off = ws.off;
+  g.tile_off = ws.tile_off;
+  g.gid = nullptr;
+  g.ngroups = E;
+  g.b1 = d->situ_b1;
+  g.b2 = d->situ_b2;
+  g.status = status;
+  {
+    TcGemmArgs a = g;
+    a.mtiles = (I + kTcRows - 1) / kTcRows;
+    a.M_rows = I;
+    tc_k_split(H / 2, a);
+    a.sfa[0] = rec + off[1];
+    a.sfa[1] = rec + off[5];
+    a.sfa_gstride = ex->expert_stride;
+    a.sf_rowb = H / kGroup;
+    a.sfb = ws.xs;
+    a.sfb_tstride = (long long)P * (H / kGroup);
+    a.out = ws.act;
+    a.out_ld = I;
+    TraceScope ts(KID_TC_GATEUP, st);
+    if (launch_tc_gemm(TcKind::kMxf4GateUp, a, mg, mu, mx, di->sms, st) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+  }
+  {
+    TraceScope ts(KID_QUANT_ACT, st);
+    const long long n = (long long)P * (I / kGroup);
+    int grid = (int)((n + 255) / 256);
+    if (grid > 16 * di->sms) grid = 16 * di->sms;
+    k_quant_act<<<grid, 256, 0, st>>>(ws.act, P, I, ws.aq, ws.as);
+  }
+  {
+    TcGemmArgs a = g;
+    a.mtiles = (H + kTcRows - 1) / kTcRows;
+    a.M_rows = H;
+    tc_k_split(I / 2, a);
+    a.sfa[0] = rec + off[3];
+    a.sfa[1] = nullptr;
+    a.sfa_gstride = ex->expert_stride;
+    a.sf_rowb = I / kGroup;
+    a.sfb = ws.as;
+    a.sfb_tstride = (long long)P * (I / kGroup);
+    a.out = ws.dpair;
+    a.out_ld = H;
+    TraceScope ts(KID_TC_DOWN, st);
+    if (launch_tc_gemm(TcKind::kMxf4Down, a, md, md, ma, di->sms, st) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+  }
+  if (SI > 0) {
+    CUtensorMap msg, msu, msd, mxs, mhs;
+    if (!tc_map3d(&msg, sh_gate, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI) ||
+        !tc_map3d(&msu, sh_up, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI) ||
+        !tc_map3d(&msd, sh_down, 2ull * SI, H, 1, 2ull * SI, 2ull * SI * H) ||
+        !tc_map3d(&mxs, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc) ||
+        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc))
+      return K3MOE_ERR_CUDA;
+    k_group1<<<1, 32, 0, st>>>(Tc, ws.off1, ws.tile_off1);
+    TcGemmArgs s1 = g;
+    s1.off = ws.off1;
+    s1.tile_off = ws.tile_off1;
+    s1.ngroups = 1;
+    {
+      TcGemmArgs a = s1;
+      a.mtiles = (SI + kTcRows - 1) / kTcRows;
+      a.M_rows = SI;
+      tc_k_split(2LL * H, a);
+      a.out = ws.act_s;
+      a.out_ld = SI;
+      TraceScope ts(KID_TC_SH_GATEUP, st);
+      if (launch_tc_gemm(TcKind::kBf16GateUp, a, msg, msu, mxs, di->sms, st) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+    {
+      TraceScope ts(KID_SPLIT, st);
+      const long long n = (long long)Tc * SI;
+      int grid = (int)((n + 255) / 256);
+      if (grid > 16 * di->sms) grid = 16 * di->sms;
+      k_split_bf16<<<grid, 256, 0, st>>>(ws.act_s, n, ws.hs);
+    }
+    {
+      TcGemmArgs a = s1;
+      a.mtiles = (H + kTcRows - 1) / kTcRows;
+      a.M_rows = H;
+      tc_k_split(2LL * SI, a);
+      a.out = ws.ds;
+      a.out_ld = H;
+      TraceScope ts(KID_TC_SH_DOWN, st);
+      if (launch_tc_gemm(TcKind::kBf16Down, a, msd, msd, mhs, di->sms, st) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+  }
+  {
+    TraceScope ts(KID_COMBINE, st);
+    k_combine<<<Tc, 256, (size_t)2 * K * 4, st>>>(Tc, H, K, w, ws.inv, ws.dpair,
+                                                 SI > 0 ? ws.ds : nullptr, y, (int)ydt,
+                                                 accumulate);
+  }
+  return launch_status();
+}
+
+// Route Tc tokens (64-token sub-passes through the router and top-k kernels) into
+// idx/w [Tc][K] for the tensor-core path.
+k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+                          const uint16_t *wr, const float *bias, WsTc &wt, int32_t *idx,
+                          float *w, int32_t *status, cudaStream_t st) {
+  Ws ws{};
+  ws.sc = wt.sc;
+  ws.ch = wt.ch;
+  const int H = d->hidden, K = d->topk;
+  for (int t0 = 0; t0 < Tc; t0 += kDecodeTokens) {
+    const int n = (Tc - t0) < kDecodeTokens ? (Tc - t0) : kDecodeTokens;
+    const k3moe_status s = run_route(di, d, x + (size_t)t0 * H, n, wr, bias, nullptr, nullptr, ws,
+                                     idx + (size_t)t0 * K, w + (size_t)t0 * K, status, st, true);
+    if (s != K3MOE_OK) return s;
+  }
+  return K3MOE_OK;
+}
+
+// The tensor-core path applies from two tokens on, for the shapes it takes.
+bool use_tc(const k3moe_dims *d, int T) { return T >= 2 && tc_shape_ok(d); }
+
 }  // namespace
 
 // ---- scratch of k3moe_layer_static_scratch -------------------------------------------
@@ -436,7 +669,12 @@ k3moe_status k3moe_record_layout(const k3moe_dims *dims, int64_t offsets[7]) {
 size_t k3moe_workspace_size(const k3moe_dims *dims, int32_t T) {
   if (check_dims(dims) != K3MOE_OK || T < 0) return 0;
   if (T == 0) return 16;
-  return ws_layout(dims, T, nullptr).total;
+  const size_t base = ws_layout(dims, T, nullptr).total;
+  if (use_tc(dims, T)) {
+    const size_t tc = ws_tc_layout(dims, T, nullptr).total;
+    return tc > base ? tc : base;
+  }
+  return base;
 }
 
 k3moe_status k3moe_route(const k3moe_dims *dims, const uint16_t *x_bf16, const uint16_t *wr_bf16,
@@ -486,8 +724,20 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims *dims, const uint16_t *x_bf
   const DeviceInfo *di = device_info();
   if (!di) return K3MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  Ws ws = ws_layout(dims, T, workspace);
   const int H = dims->hidden, K = dims->topk;
+  if (use_tc(dims, T)) {
+    WsTc wt = ws_tc_layout(dims, T, workspace);
+    for (int t0 = 0; t0 < T; t0 += kTcTokens) {
+      const int Tc = (T - t0) < kTcTokens ? (T - t0) : kTcTokens;
+      s = run_ffn_tc(di, dims, x_bf16 + (size_t)t0 * H, Tc, experts, idx + (size_t)t0 * K,
+                     w + (size_t)t0 * K, nullptr, nullptr, nullptr, wt,
+                     static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt,
+                     accumulate, status_dev, st);
+      if (s != K3MOE_OK) return s;
+    }
+    return K3MOE_OK;
+  }
+  Ws ws = ws_layout(dims, T, workspace);
   for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
     const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
     s = run_ffn(di, dims, x_bf16 + (size_t)t0 * H, Tc, experts, idx + (size_t)t0 * K,
@@ -526,8 +776,25 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
   const DeviceInfo *di = device_info();
   if (!di) return K3MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  Ws ws = ws_layout(dims, T, workspace);
   const int H = dims->hidden, K = dims->topk;
+  if (use_tc(dims, T)) {
+    WsTc wt = ws_tc_layout(dims, T, workspace);
+    for (int t0 = 0; t0 < T; t0 += kTcTokens) {
+      const int Tc = (T - t0) < kTcTokens ? (T - t0) : kTcTokens;
+      int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : wt.idx;
+      float *w_c = w_out ? w_out + (size_t)t0 * K : wt.w;
+      const uint16_t *xc = x_bf16 + (size_t)t0 * H;
+      s = run_route_tc(di, dims, xc, Tc, wr_bf16, bias, wt, idx_c, w_c, status_dev, st);
+      if (s != K3MOE_OK) return s;
+      s = run_ffn_tc(di, dims, xc, Tc, experts, idx_c, w_c, shared ? sh_gate : nullptr,
+                     shared ? sh_up : nullptr, shared ? sh_down : nullptr, wt,
+                     static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt,
+                     accumulate, status_dev, st);
+      if (s != K3MOE_OK) return s;
+    }
+    return K3MOE_OK;
+  }
+  Ws ws = ws_layout(dims, T, workspace);
   for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
     const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
     int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : ws.idx;

@@ -1,0 +1,256 @@
+// k3moe_prefill.cu -- the kernels around the tensor-core grouped GEMM of the multi-token
+// path: expert dispatch (a stable counting sort of the (token, slot) pairs by expert),
+// activation encoding for the block-scaled MMA, and the router-order combine.
+//
+// The combine is the page's routed sum (README of FareedKhan-dev/kimi-k3-in-c, section 9,
+// LatentMoE listing, steps 3 and 6): y_t = sum_j w[t,j] d_j in slot order j, in float,
+// then the shared expert added unweighted; README of Maknee/Kimi-K3.cpp, "The
+// consumer-memory idea" item 7, fixes the router order of that sum.
+#include "k3moe_kernels.cuh"
+
+namespace k3 {
+
+// ------------------------------------------------------------------------------ dispatch
+// One block: per-expert pair counts, their exclusive prefix off[E+1], and the prefix of
+// 128-row tiles tile_off[E+1].  Pairs whose expert index is outside [0, E) are counted
+// nowhere, get inv = -1 (the combine skips them) and set K3MOE_ERR_BAD_EXPERT.
+__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int32_t *off,
+                             int32_t *tile_off, int32_t *inv, int32_t *status) {
+  extern __shared__ int32_t cnt[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = idx[p];
+    if (e >= 0 && e < E) {
+      atomicAdd(&cnt[e], 1);
+    } else {
+      inv[p] = -1;
+      set_status(status, K3MOE_ERR_BAD_EXPERT);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, to = 0;
+    for (int e = 0; e < E; e++) {
+      off[e] = o;
+      tile_off[e] = to;
+      o += cnt[e];
+      to += (cnt[e] + kTcRows - 1) / kTcRows;
+    }
+    off[E] = o;
+    tile_off[E] = to;
+  }
+}
+
+// Block e lists expert e's pairs in pair order: perm[off[e] + r] = p and inv[p] =
+// off[e] + r for the r-th pair routed to e.  Stable, so the slot order is deterministic.
+__global__ void k_route_scatter(const int32_t *__restrict__ idx, int P,
+                                const int32_t *__restrict__ off, int32_t *perm, int32_t *inv) {
+  __shared__ int wsum[32];
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int base = off[e];
+  if (off[e + 1] == base) return;
+  for (int p0 = 0; p0 < P; p0 += blockDim.x) {
+    const int p = p0 + threadIdx.x;
+    const bool hit = p < P && idx[p] == e;
+    const unsigned b = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) wsum[warp] = __popc(b);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < nw; w++) {
+      before += (w < warp) ? wsum[w] : 0;
+      total += wsum[w];
+    }
+    if (hit) {
+      const int pos = base + before + __popc(b & ((1u << lane) - 1u));
+      perm[pos] = p;
+      inv[p] = pos;
+    }
+    base += total;
+    __syncthreads();
+  }
+}
+
+// One group of 32 values -> NT MXFP4 terms: term i takes the residual left by terms
+// 0..i-1, with the E8M0 scale 2^e chosen so that max|r| <= 6 * 2^e and each value rounded
+// to the nearest E2M1 code (hardware conversion, round to nearest even); residuals are
+// exact in float.  Codes packed two per byte, the even element in the low nibble.
+template <int NT>
+__device__ __forceinline__ void encode_terms(float (&r)[32], uint4 (&q)[NT], uint8_t (&sb)[NT]) {
+#pragma unroll
+  for (int t = 0; t < NT; t++) {
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; k++) m = fmaxf(m, fabsf(r[k]));
+    int e = -127;
+    if (m > 0.f) {
+      e = exponent_of(m) - 2;
+      if (m > 6.f * pow2i(e)) e++;
+      e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    }
+    sb[t] = (uint8_t)(e + 127);
+    const float inv_s = pow2i(-e), s = pow2i(e);
+    uint32_t w[4];
+#pragma unroll
+    for (int wq = 0; wq < 4; wq++) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int bb = 0; bb < 4; bb++) {
+        const int k = 8 * wq + 2 * bb;
+        uint32_t byte;
+        asm("{ .reg .b8 t8; cvt.rn.satfinite.e2m1x2.f32 t8, %1, %2; cvt.u32.u8 %0, t8; }"
+            : "=r"(byte)
+            : "f"(r[k + 1] * inv_s), "f"(r[k] * inv_s));
+        word |= byte << (8 * bb);
+        // residual: subtract the decoded value (exact)
+        const uint32_t h2 = e2m1x2_to_f16x2(byte);
+        const __half2 hv = *reinterpret_cast<const __half2 *>(&h2);
+        r[k] = __fsub_rn(r[k], __low2float(hv) * s);
+        r[k + 1] = __fsub_rn(r[k + 1], __high2float(hv) * s);
+      }
+      w[wq] = word;
+    }
+    q[t] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// x [T][H] bf16 -> the kTcTermsX-term encoding of every (token, slot) pair's row, written
+// at the pair's sorted position: xq [term][P][H/2], xs [term][P][H/32].  One thread per
+// (token, group); the token's K slots receive the same bytes.
+__global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
+                          const int32_t *__restrict__ inv, int P, uint8_t *__restrict__ xq,
+                          uint8_t *__restrict__ xs) {
+  const int G = H / kGroup;
+  const long long n = (long long)T * G;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / G), g = (int)(i % G);
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H + g * kGroup);
+    float r[32];
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        r[8 * c + 2 * k] = bf16_lo(w4[k]);
+        r[8 * c + 2 * k + 1] = bf16_hi(w4[k]);
+      }
+    }
+    uint4 q[kTcTermsX];
+    uint8_t sb[kTcTermsX];
+    encode_terms<kTcTermsX>(r, q, sb);
+    for (int j = 0; j < K; j++) {
+      const int s = inv[(size_t)t * K + j];
+      if (s < 0) continue;
+#pragma unroll
+      for (int tt = 0; tt < kTcTermsX; tt++) {
+        reinterpret_cast<uint4 *>(xq + ((size_t)tt * P + s) * (H / 2))[g] = q[tt];
+        xs[((size_t)tt * P + s) * G + g] = sb[tt];
+      }
+    }
+  }
+}
+
+// act [P][I] float -> kTcTermsAct-term encoding: aq [term][P][I/2], as [term][P][I/32].
+__global__ void k_quant_act(const float *__restrict__ act, int P, int I,
+                            uint8_t *__restrict__ aq, uint8_t *__restrict__ as) {
+  const int G = I / kGroup;
+  const long long n = (long long)P * G;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(i / G), g = (int)(i % G);
+    const float4 *src = reinterpret_cast<const float4 *>(act + (size_t)s * I + g * kGroup);
+    float r[32];
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      const float4 v = __ldg(src + c);
+      r[4 * c] = v.x;
+      r[4 * c + 1] = v.y;
+      r[4 * c + 2] = v.z;
+      r[4 * c + 3] = v.w;
+    }
+    uint4 q[kTcTermsAct];
+    uint8_t sb[kTcTermsAct];
+    encode_terms<kTcTermsAct>(r, q, sb);
+#pragma unroll
+    for (int tt = 0; tt < kTcTermsAct; tt++) {
+      reinterpret_cast<uint4 *>(aq + ((size_t)tt * P + s) * (I / 2))[g] = q[tt];
+      as[((size_t)tt * P + s) * G + g] = sb[tt];
+    }
+  }
+}
+
+// float [n] -> two bf16 terms hi = bf16(v), lo = bf16(v - hi) (round to nearest even):
+// out[0][n] = hi, out[1][n] = lo.  hi + lo carries 16 significant bits of v.
+__global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t *__restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float f = v[i];
+    const uint16_t hi = f32_to_bf16(f);
+    const float r = __fsub_rn(f, __uint_as_float((uint32_t)hi << 16));
+    out[i] = hi;
+    out[n + i] = f32_to_bf16(r);
+  }
+}
+
+// Group table of a single dense group of n rows: off = {0, n}, tile_off = {0, tiles}.
+__global__ void k_group1(int n, int32_t *off, int32_t *tile_off) {
+  if (threadIdx.x == 0) {
+    off[0] = 0;
+    off[1] = n;
+    tile_off[0] = 0;
+    tile_off[1] = (n + kTcRows - 1) / kTcRows;
+  }
+}
+
+// y[t] (=|+=) sum_j w[t,j] * dpair[inv[t*K+j]] (float, slot order j) + ds[t] (shared
+// expert, unweighted, added last).  One block per token.
+__global__ void k_combine(int T, int H, int K, const float *__restrict__ w,
+                          const int32_t *__restrict__ inv, const float *__restrict__ dpair,
+                          const float *__restrict__ ds, void *y, int ydt, int accumulate) {
+  const int t = blockIdx.x;
+  extern __shared__ int32_t s_slot[];  // [K] slots, then [K] weights (as float bits)
+  float *s_w = reinterpret_cast<float *>(s_slot + K);
+  for (int j = threadIdx.x; j < K; j += blockDim.x) {
+    s_slot[j] = inv[(size_t)t * K + j];
+    s_w[j] = w[(size_t)t * K + j];
+  }
+  __syncthreads();
+  for (int h4 = threadIdx.x; h4 < H / 4; h4 += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < K; j++) {
+      const int s = s_slot[j];
+      if (s < 0) continue;
+      const float wj = s_w[j];
+      const float4 d = __ldg(reinterpret_cast<const float4 *>(dpair + (size_t)s * H) + h4);
+      acc.x = __fadd_rn(acc.x, __fmul_rn(wj, d.x));
+      acc.y = __fadd_rn(acc.y, __fmul_rn(wj, d.y));
+      acc.z = __fadd_rn(acc.z, __fmul_rn(wj, d.z));
+      acc.w = __fadd_rn(acc.w, __fmul_rn(wj, d.w));
+    }
+    if (ds) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(ds + (size_t)t * H) + h4);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    const float o[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (ydt == K3MOE_F32) {
+      float *yp = static_cast<float *>(y) + (size_t)t * H + 4 * h4;
+#pragma unroll
+      for (int c = 0; c < 4; c++) yp[c] = accumulate ? __fadd_rn(yp[c], o[c]) : o[c];
+    } else {
+      uint16_t *yp = static_cast<uint16_t *>(y) + (size_t)t * H + 4 * h4;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const float prev = accumulate ? __uint_as_float((uint32_t)yp[c] << 16) : 0.f;
+        yp[c] = f32_to_bf16(accumulate ? __fadd_rn(prev, o[c]) : o[c]);
+      }
+    }
+  }
+}
+
+}  // namespace k3

@@ -1,0 +1,517 @@
+// k3moe_tc.cu -- grouped GEMM on the 5th-generation tensor cores (tcgen05) for the
+// multi-token expert path (prefill and batched decode).
+//
+// What it computes (README of FareedKhan-dev/kimi-k3-in-c, section 4 for MXFP4 and
+// section 9, LatentMoE listing, for the expert FFN): for every group g (a routed expert,
+// or the shared expert) and every B row n routed to it,
+//     D[m][n] = sum_k A_g[m][k] * B[n][k]        (m: output feature, k: input feature)
+// with A_g the expert's weight matrix (rows = outputs, K-major) and B the activations of
+// the group's tokens.  Two kinds:
+//   MXF4: A is the expert's packed MXFP4 operand as stored in the record (E2M1 nibbles,
+//         one E8M0 scale per 32 along K) and B is the activation written as a sum of
+//         NT MXFP4 terms (each E2M1 with its own E8M0 scale per 32); every term is one
+//         block-scaled MMA (kind::mxf4, scale vectors of 2 per 64-wide K step), all
+//         accumulated in one fp32 accumulator.  Scale byte 255 of A (the page's "no
+//         contribution") is written to tensor memory as 0, i.e. 2^-127.
+//   F16:  A and B bf16 (kind::f16, fp32 accumulate); B may be NT bf16 terms (hi + lo).
+// Epilogues: SITU (two A matrices, gate and up: act = SiTU(D_gate, D_up)) or STORE
+// (one A matrix: D as is); both write fp32 [B row][feature].
+//
+// Design: one CTA per SM (persistent), work item = (group, 128-row tile of A, tile of up
+// to 128 B rows).  Warp roles: 0-3 write the scale vectors of each stage into tensor
+// memory (warp q owns TMEM lanes 32q..32q+31; A row m's scales sit in lane m, B's are
+// replicated in every lane quarter, column n / 32, lane n % 32), 4 issues TMA loads (128-byte swizzled
+// tiles of 128 rows x 128 bytes of K), 5 issues the MMAs (one thread), 6-13 drain the
+// accumulator (two warps per lane quarter).  Shared-memory stages and the scale slots in
+// tensor memory are released together by tcgen05.commit on the stage's "empty" barrier.
+#include <cuda.h>
+
+#include "k3moe_kernels.cuh"
+
+namespace k3 {
+
+namespace {
+
+constexpr int kTcThreads = 448;           // 14 warps
+constexpr int kTcWarpSf = 0;              // warps 0..3
+constexpr int kTcWarpTma = 4;
+constexpr int kTcWarpMma = 5;
+constexpr int kTcWarpEpi = 6;             // warps 6..13
+constexpr int kTcTile = kTcRows;          // A rows and B rows per tile
+constexpr int kTcChunkBytes = 128;        // K bytes per stage (one 128-byte swizzle atom)
+constexpr uint32_t kTcBox = kTcTile * kTcChunkBytes;  // bytes of one TMA box (16 KB)
+constexpr int kTcTmemCols = 512;
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, int cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, int cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;            // descriptor version
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// 3-D tiled TMA load (x = K byte, y = row, z = group or term) completing on `bar`.
+__device__ __forceinline__ void tma_load3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                           uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&f)[16]) {
+  uint32_t v[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int j = 0; j < 16; j++) f[j] = __uint_as_float(v[j]);
+}
+
+// Eight scale bytes of one row for K chunk c (groups 8c .. 8c+7), fewer at the row's end;
+// bytes past the row read 0.  Scale byte 255 becomes 0 when map255.
+__device__ __forceinline__ uint2 load_scales8(const uint8_t *row, int G, int c, bool map255) {
+  const int g0 = 8 * c;
+  uint32_t lo = 0, hi = 0;
+  if (g0 + 8 <= G && ((reinterpret_cast<uintptr_t>(row + g0) & 7) == 0)) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(row + g0));
+    lo = v.x;
+    hi = v.y;
+  } else {
+    for (int j = 0; j < 8; j++) {
+      const uint32_t b = (g0 + j < G) ? (uint32_t)__ldg(row + g0 + j) : 0u;
+      if (j < 4)
+        lo |= b << (8 * j);
+      else
+        hi |= b << (8 * (j - 4));
+    }
+  }
+  if (map255) {
+    lo &= ~__vcmpeq4(lo, 0xffffffffu);
+    hi &= ~__vcmpeq4(hi, 0xffffffffu);
+  }
+  return make_uint2(lo, hi);
+}
+// The two scale bytes of K step i (groups 2i, 2i+1 of the chunk), in bytes 0 and 1.
+__device__ __forceinline__ uint32_t step_scales(uint2 s, int i) {
+  const uint32_t w = (i < 2) ? s.x : s.y;
+  return (w >> (16 * (i & 1))) & 0xffffu;
+}
+
+}  // namespace
+
+struct TcItem {
+  int g, mt, brow0, nvalid;
+};
+
+// Maps a flat item index to (group, A-row tile, first B row, valid B rows).
+__device__ __forceinline__ TcItem tc_item(const TcGemmArgs &a, int item) {
+  TcItem it;
+  const int tile = item / a.mtiles;
+  it.mt = item - tile * a.mtiles;
+  int lo = 0, hi = a.ngroups - 1;  // last group with tile_off[g] <= tile
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.tile_off[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  it.g = lo;
+  const int nt = tile - a.tile_off[lo];
+  it.brow0 = a.off[lo] + nt * kTcTile;
+  const int rem = a.off[lo + 1] - it.brow0;
+  it.nvalid = rem < kTcTile ? rem : kTcTile;
+  return it;
+}
+
+template <int KIND, int NA, int NT, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_tc_gemm(const TcGemmArgs a, const __grid_constant__ CUtensorMap tmA0,
+              const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // barriers and the TMEM base address in the first 1 KB; stages 1024-aligned after it
+  uint8_t *smem = smem_raw;
+  const uint32_t base_u32 = smem_u32(smem);
+  const uint32_t pad = ((base_u32 + 1023u) & ~1023u) - base_u32;
+  smem += pad;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [NS]
+  uint64_t *sfull = full + 8;                           // [NS]
+  uint64_t *empty = full + 16;                          // [NS]
+  uint64_t *dfull = full + 24;
+  uint64_t *dempty = full + 25;
+  uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + 512);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 520);
+  uint8_t *stages = smem + 1024;
+  constexpr uint32_t kStageBytes = (uint32_t)(NA + NT) * kTcBox;
+  // TMEM columns per stage of scale vectors: B terms first (16 columns each), then the A
+  // matrices (16 each); multi-column accesses stay aligned to their width
+  constexpr int kSfSlot = (KIND == 0) ? 16 * (NT + NA) : 0;
+  const int NS = a.nstages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < NS; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&sfull[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(dfull, 1);
+    mbar_init(dempty, 8);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kTcWarpMma) tmem_alloc(tmem_base, kTcTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base;
+  const uint32_t sf_col0 = (uint32_t)(NA * kTcTile);  // scale slots after the accumulators
+
+  pdl_wait();
+  const int nitems = a.tile_off[a.ngroups] * a.mtiles;
+  const int G = a.sf_rowb;  // scale bytes per A / B row
+
+  if (warp == kTcWarpTma) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int it = 0;
+      for (int item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
+        const TcItem ti = tc_item(a, item);
+        const int ga = a.gid ? a.gid[ti.g] : ti.g;
+        for (int c = 0; c < a.kchunks; c++, it++) {
+          const int s = it % NS;
+          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t *st = stages + (size_t)s * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+          if (NA > 1)
+            tma_load3d(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+#pragma unroll
+          for (int t = 0; t < NT; t++)
+            tma_load3d(st + (NA + t) * kTcBox, &tmB, c * kTcChunkBytes, ti.brow0, t, &full[s]);
+        }
+      }
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- scale writers
+    if (KIND == 0) {
+      const int q = warp;
+      int it = 0;
+      for (int item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
+        const TcItem ti = tc_item(a, item);
+        const int ga = a.gid ? a.gid[ti.g] : ti.g;
+        const int row = ti.mt * kTcTile + 32 * q + lane;  // A row of this lane
+        const bool rok = row < a.M_rows;
+        for (int c = 0; c < a.kchunks; c++, it++) {
+          const int s = it % NS;
+          // scale bytes first (global loads), then wait for the slot
+          uint2 sa[NA];
+#pragma unroll
+          for (int m = 0; m < NA; m++)
+            sa[m] = rok ? load_scales8(a.sfa[m] + (long long)ga * a.sfa_gstride +
+                                           (long long)row * G,
+                                       G, c, true)
+                        : make_uint2(0u, 0u);
+          uint32_t vb[NT][16];
+          {
+#pragma unroll
+            for (int t = 0; t < NT; t++)
+#pragma unroll
+              for (int j = 0; j < 4; j++) {
+                const int n = 32 * j + lane;
+                const uint2 sb = (n < ti.nvalid)
+                                     ? load_scales8(a.sfb + (long long)t * a.sfb_tstride +
+                                                        (long long)(ti.brow0 + n) * G,
+                                                    G, c, false)
+                                     : make_uint2(0u, 0u);
+#pragma unroll
+                for (int i = 0; i < 4; i++) vb[t][4 * i + j] = step_scales(sb, i);
+              }
+          }
+          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
+          const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
+          // A: K step i of matrix m reads column slot + 16(NT + m) + 4i + (row / 32)
+#pragma unroll
+          for (int m = 0; m < NA; m++)
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+              tmem_st_x1(slot + lane_sel + 16 * (NT + m) + 4 * i + q, step_scales(sa[m], i));
+          // B: K step i of term t reads column slot + 16t + 4i + n/32 at lane n % 32 of
+          // every lane quarter (each 32-row quarter of the MMA reads its own copy)
+#pragma unroll
+          for (int t = 0; t < NT; t++) tmem_st_x16(slot + lane_sel + 16 * t, vb[t]);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfull[s]);
+        }
+      }
+    }
+  } else if (warp == kTcWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, n = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, n++) {
+        const TcItem ti = tc_item(a, item);
+        const int nmma = ((ti.nvalid + 15) / 16) * 16;
+        uint32_t idesc;
+        if (KIND == 0)
+          idesc = (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) | (1u << 23) |
+                  ((uint32_t)(kTcTile >> 4) << 24);
+        else
+          idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) |
+                  ((uint32_t)(kTcTile >> 4) << 24);
+        // the epilogue must have drained the previous item's accumulator
+        if (!mbar_wait(dempty, (n & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int c = 0; c < a.kchunks; c++, it++) {
+          const int s = it % NS;
+          const uint32_t par = (it / NS) & 1;
+          if (!mbar_wait(&full[s], par) || (KIND == 0 && !mbar_wait(&sfull[s], par))) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(stages + (size_t)s * kStageBytes);
+          const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
+          const int nk = (c == a.kchunks - 1) ? a.ksteps_last : 4;
+          for (int i = 0; i < nk; i++) {
+#pragma unroll
+            for (int m = 0; m < NA; m++) {
+              const uint64_t ad = sw128_desc(st + m * kTcBox + 32 * i);
+#pragma unroll
+              for (int t = 0; t < NT; t++) {
+                const uint64_t bd = sw128_desc(st + (NA + t) * kTcBox + 32 * i);
+                const uint32_t acc = (c > 0 || i > 0 || t > 0) ? 1u : 0u;
+                const uint32_t dcol = tmem + (uint32_t)(m * kTcTile);
+                if (KIND == 0)
+                  mma_mxf4(dcol, ad, bd, idesc, slot + 16 * (NT + m) + 4 * i, slot + 16 * t + 4 * i,
+                           acc);
+                else
+                  mma_f16(dcol, ad, bd, idesc, acc);
+              }
+            }
+          }
+          tc_commit(&empty[s]);
+        }
+        tc_commit(dfull);
+      }
+      // before the accumulator is freed: wait (bounded) for every MMA issued
+      if (!ok && it > 0) {
+        const int s = (it - 1) % NS;
+        mbar_wait(&empty[s], ((it - 1) / NS) & 1, 400000000LL);
+      }
+    }
+  } else if (warp >= kTcWarpEpi) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int half = (warp - kTcWarpEpi) >> 2;
+    int n = 0;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, n++) {
+      const TcItem ti = tc_item(a, item);
+      const bool got = mbar_wait(dfull, n & 1);
+      if (!got) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      tc_fence_after();
+      const int row = ti.mt * kTcTile + 32 * q + lane;
+      const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
+      if (got && !*abort_flag) {
+        for (int c0 = half * 64; c0 < half * 64 + 64 && c0 < ti.nvalid; c0 += 16) {
+          float d0[16], d1[16];
+          tmem_ld_x16(tmem + lane_sel + (uint32_t)c0, d0);
+          if (NA > 1) tmem_ld_x16(tmem + lane_sel + (uint32_t)(kTcTile + c0), d1);
+          if (row < a.M_rows) {
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+              const int col = c0 + j;
+              if (col < ti.nvalid) {
+                float v = d0[j];
+                if (EPI == 0) v = situ(d0[j], d1[j], a.b1, a.b2);
+                a.out[(long long)(ti.brow0 + col) * a.out_ld + row] = v;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);
+      if (!got) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kTcWarpMma) tmem_dealloc(tmem, kTcTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------
+// Host side: tensor maps (through the driver entry point, no link against libcuda) and
+// launches.
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+}  // namespace
+
+bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
+              unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
+              unsigned long long depth_stride) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_stride & 15) || (depth_stride & 15))
+    return false;
+  if (depth_stride == 0) depth_stride = row_stride * rows;
+  const cuuint64_t dims[3] = {inner_bytes, rows, depth};
+  const cuuint64_t strides[2] = {row_stride, depth_stride};
+  const cuuint32_t box[3] = {(cuuint32_t)kTcChunkBytes, (cuuint32_t)kTcTile, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_stages(int na, int nt) {
+  const size_t stage = (size_t)(na + nt) * kTcBox;
+  int ns = (int)((227 * 1024 - 2048) / stage);
+  return ns > 8 ? 8 : ns;
+}
+
+size_t tc_smem_bytes(int na, int nt) { return 2048 + (size_t)tc_stages(na, nt) * (na + nt) * kTcBox; }
+
+template <int KIND, int NA, int NT, int EPI>
+static cudaError_t launch_tc(const TcGemmArgs &a, const CUtensorMap &A0, const CUtensorMap &A1,
+                             const CUtensorMap &B, int grid, cudaStream_t st) {
+  auto fn = k_tc_gemm<KIND, NA, NT, EPI>;
+  const size_t smem = tc_smem_bytes(NA, NT);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  TcGemmArgs aa = a;
+  aa.nstages = tc_stages(NA, NT);
+  fn<<<grid, kTcThreads, smem, st>>>(aa, A0, A1, B);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &A0,
+                           const CUtensorMap &A1, const CUtensorMap &B, int grid,
+                           cudaStream_t st) {
+  switch (kind) {
+    case TcKind::kMxf4GateUp: return launch_tc<0, 2, 4, 0>(a, A0, A1, B, grid, st);
+    case TcKind::kMxf4Down: return launch_tc<0, 1, 5, 1>(a, A0, A1, B, grid, st);
+    case TcKind::kBf16GateUp: return launch_tc<1, 2, 1, 0>(a, A0, A1, B, grid, st);
+    case TcKind::kBf16Down: return launch_tc<1, 1, 2, 1>(a, A0, A1, B, grid, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace k3

@@ -45,8 +45,12 @@ def test_record_layout_and_workspace_queries():
     assert k3.record_layout(dims()) == [0, 5505024, 5849088, 11354112, 11698176, 17203200,
                                         17547264]
     assert k3.workspace_size(dims(), 0) == 16
-    w1, w64, w65 = (k3.workspace_size(dims(), t) for t in (1, 64, 65))
-    assert 0 < w1 < w64 == w65   # decode passes of at most 64 tokens reuse one workspace
+    w1, w2, w4096, w5000 = (k3.workspace_size(dims(), t) for t in (1, 2, 4096, 5000))
+    # multi-token passes of at most 4096 tokens reuse one workspace
+    assert 0 < w1 < w2 < w4096 == w5000
+    # shapes the tensor-core path does not take keep the 64-token decode passes
+    small = dims(hidden=96, inter=64, n_experts=5, topk=3, shared_inter=64)
+    assert k3.workspace_size(small, 64) == k3.workspace_size(small, 65)
     assert k3.workspace_size(dims(hidden=100), 1) == 0
 
 

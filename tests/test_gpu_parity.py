@@ -135,6 +135,13 @@ SHAPES = [
     (256, 128, 16, 2, 1, 65),
     (1024, 256, 24, 6, 2, 130),
     (2048, 512, 33, 8, 1, 2),
+    # tensor-core path (two tokens and up, H and I multiples of 64, at least 256): ragged
+    # 128-row tiles (I 320, H 320), a partial last 128-byte K chunk (H/2 = 160, I/2 = 160),
+    # more than 128 pairs on one expert (T 300 over 4 experts), no shared expert
+    (256, 256, 8, 2, 1, 5),
+    (320, 320, 6, 3, 1, 40),
+    (512, 384, 4, 2, 1, 300),
+    (768, 256, 12, 4, 0, 64),
 ]
 
 
@@ -193,6 +200,50 @@ def test_expert_ffn_bad_index_reports_and_drops_the_slot():
         want = oracle.moe_token(L.x[t], [L.expert_record(int(bad[t, j])) for j in keep],
                                 ow[t, keep], H, cfg.inter)
         assert rel_l2(gy[t], want) <= REL_L2_F32
+
+
+def test_expert_ffn_tensor_core_bad_index_reports_and_drops_the_slot():
+    cfg = dataclasses.replace(synth.config("tiny"), name="custom", hidden=512, inter=256,
+                              n_experts=8, topk=3, tokens=20, n_shared=0)
+    L = Layer(cfg, seed=9)
+    T, K, H = cfg.tokens, cfg.topk, cfg.hidden
+    oi, ow, _, _ = oracle.router(L.x, L.host["wr"], L.host["bias"], K)
+    bad = oi.copy()
+    bad[3, 2] = -1
+    bad[11, 0] = cfg.n_experts
+    idx = torch.from_numpy(bad).cuda()
+    w = torch.from_numpy(ow).cuda()
+    y = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    st = k3.new_status()
+    k3.k3moe_expert_ffn_mxfp4(L.dims, L.d_x, L.experts, L.stride, idx, w, y,
+                              k3.new_workspace(L.dims, T), st)
+    torch.cuda.synchronize()
+    assert st.item() == 7
+    gy = y.cpu().numpy()
+    for t in range(T):
+        keep = [j for j in range(K) if 0 <= bad[t, j] < cfg.n_experts]
+        want = oracle.moe_token(L.x[t], [L.expert_record(int(bad[t, j])) for j in keep],
+                                ow[t, keep], H, cfg.inter)
+        assert rel_l2(gy[t], want) <= REL_L2_F32
+
+
+def test_tensor_core_path_scale_255_and_0_groups():
+    # scale byte 255 (the group contributes nothing) and 0 (2^-127) in every operand
+    cfg = dataclasses.replace(synth.config("tiny"), name="custom", hidden=512, inter=256,
+                              n_experts=6, topk=2, tokens=9, n_shared=1)
+    L = Layer(cfg, seed=12)
+    off = cfg.record_offsets
+    rec = L._host_experts
+    rng = np.random.default_rng(3)
+    for op in (1, 3, 5):
+        seg = rec[:, off[op]:off[op + 1]]
+        m = rng.random(seg.shape) < 0.05
+        seg[m] = 255
+        m = rng.random(seg.shape) < 0.05
+        seg[m] = 0
+    view = L.experts.view(cfg.n_experts, L.stride)
+    view[:, :L.rec_bytes].copy_(torch.from_numpy(rec))
+    check_layer(L)
 
 
 def test_rmsnorm_bf16():

@@ -33,9 +33,10 @@ def test_static_scratch_size_matches_header_and_holds_the_model_shape():
     m = re.search(r"#define\s+K3MOE_STATIC_SCRATCH_BYTES\s+\((\d+)u \* (\d+)u \* (\d+)u\)", hdr)
     assert m, "K3MOE_STATIC_SCRATCH_BYTES not found"
     assert int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == k3.STATIC_SCRATCH_BYTES
-    # one pass holds at most 64 tokens, so the model shape fits at every T
-    for T in (1, 64, 4096):
+    # the model shape fits up to nine tokens, the size the header states
+    for T in (1, 2, 9):
         assert 0 < k3.workspace_size(model_dims(), T) <= k3.STATIC_SCRATCH_BYTES
+    assert k3.workspace_size(model_dims(), 10) > k3.STATIC_SCRATCH_BYTES
 
 
 def test_static_scratch_refuses_requests_beyond_its_size():
