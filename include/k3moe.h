@@ -148,7 +148,7 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
 /* Size of the library's static scratch array (8 MiB), the most scratch that
  * k3moe_layer_static_scratch can use.  At the model's shape (H 7168, I 1536, 896
  * experts, top 16, shared 1536) it holds the workspace of up to 9 tokens: 115,040 bytes
- * for one token, 8,238,848 for nine.                                                  */
+ * for one token, 8,275,200 for nine.                                                  */
 #define K3MOE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 /* k3moe_layer without a workspace argument: the same kernels, arguments, results and

@@ -128,12 +128,14 @@ k3moe_status launch_status() {
 enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KID_RMSNORM,
                 KID_DEQUANT, KID_GATEUP_T1, KID_DOWN_TMA, KID_ROUTE_HIST, KID_ROUTE_SCATTER,
                 KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
-                KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_COUNT };
+                KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_NORMS, KID_TC_ROUTER,
+                KID_ROUTE_CAND, KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {
     "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
     "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
     "k_route_scatter", "k_quant_x", "k_tc_gemm_gateup", "k_quant_act", "k_tc_gemm_down",
-    "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine"};
+    "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine",
+    "k_row_norms", "k_tc_gemm_router", "k_route_candidates"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -391,7 +393,10 @@ bool tc_shape_ok(const k3moe_dims *d) {
 
 // Workspace of one pass of up to kTcTokens tokens (P = Tc * K pairs).
 struct WsTc {
-  float *sc, *ch;                 // router scores of one 64-token sub-pass
+  float *sc, *ch;                 // router scores [Tc][E]
+  float *Lt;                      // screening logits [Tc][E]
+  float *xn, *wn;                 // row norms of x [Tc] and Wr [E]
+  int32_t *ncand;                 // candidates per token [Tc]
   int32_t *idx;
   float *w;
   int32_t *off, *tile_off, *inv, *perm, *off1, *tile_off1;
@@ -417,9 +422,12 @@ WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
     return reinterpret_cast<uint8_t *>(b + at);
   };
   WsTc w{};
-  const size_t Tr = Tc < kDecodeTokens ? Tc : kDecodeTokens;
-  w.sc = reinterpret_cast<float *>(take(Tr * E * 4));
-  w.ch = reinterpret_cast<float *>(take(Tr * E * 4));
+  w.sc = reinterpret_cast<float *>(take((size_t)Tc * E * 4));
+  w.ch = reinterpret_cast<float *>(take((size_t)Tc * E * 4));
+  w.Lt = reinterpret_cast<float *>(take((size_t)Tc * E * 4));
+  w.xn = reinterpret_cast<float *>(take((size_t)Tc * 4));
+  w.wn = reinterpret_cast<float *>(take(E * 4));
+  w.ncand = reinterpret_cast<int32_t *>(take((size_t)Tc * 4));
   w.idx = reinterpret_cast<int32_t *>(take(P * 4));
   w.w = reinterpret_cast<float *>(take(P * 4));
   w.off = reinterpret_cast<int32_t *>(take((E + 1) * 4));
@@ -588,22 +596,48 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   return launch_status();
 }
 
-// Route Tc tokens (64-token sub-passes through the router and top-k kernels) into
-// idx/w [Tc][K] for the tensor-core path.
+// Route Tc tokens into idx/w [Tc][K] for the tensor-core path: screening logits and
+// their error bounds on the tensor cores, exact scores for the candidates, then top-k.
 k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
                           const uint16_t *wr, const float *bias, WsTc &wt, int32_t *idx,
                           float *w, int32_t *status, cudaStream_t st) {
-  Ws ws{};
-  ws.sc = wt.sc;
-  ws.ch = wt.ch;
-  const int H = d->hidden, K = d->topk;
-  for (int t0 = 0; t0 < Tc; t0 += kDecodeTokens) {
-    const int n = (Tc - t0) < kDecodeTokens ? (Tc - t0) : kDecodeTokens;
-    const k3moe_status s = run_route(di, d, x + (size_t)t0 * H, n, wr, bias, nullptr, nullptr, ws,
-                                     idx + (size_t)t0 * K, w + (size_t)t0 * K, status, st, true);
-    if (s != K3MOE_OK) return s;
+  const int H = d->hidden, E = d->n_experts, K = d->topk;
+  {
+    TraceScope ts(KID_NORMS, st);
+    k_row_norms<<<(Tc + 7) / 8, 256, 0, st>>>(x, Tc, H, wt.xn);
+    k_row_norms<<<(E + 7) / 8, 256, 0, st>>>(wr, E, H, wt.wn);
   }
-  return K3MOE_OK;
+  k_group1<<<1, 32, 0, st>>>(Tc, wt.off1, wt.tile_off1);
+  CUtensorMap mw, mx;
+  if (!tc_map3d(&mw, wr, 2ull * H, E, 1, 2ull * H, 2ull * H * E) ||
+      !tc_map3d(&mx, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc))
+    return K3MOE_ERR_CUDA;
+  TcGemmArgs a{};
+  a.off = wt.off1;
+  a.tile_off = wt.tile_off1;
+  a.ngroups = 1;
+  a.mtiles = (E + kTcRows - 1) / kTcRows;
+  a.M_rows = E;
+  tc_k_split(2LL * H, a);
+  a.out_ld = E;
+  a.status = status;
+  {
+    TraceScope ts(KID_TC_ROUTER, st);
+    a.out = wt.Lt;
+    if (launch_tc_gemm(TcKind::kBf16Store, a, mw, mw, mx, di->sms, st) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+  }
+  {
+    TraceScope ts(KID_ROUTE_CAND, st);
+    k_route_candidates<<<Tc, 256, route_candidates_smem(H, E, K), st>>>(
+        wt.Lt, wt.xn, wt.wn, x, wr, bias, H, E, K, wt.sc, wt.ch, wt.ncand, status);
+  }
+  {
+    TraceScope ts(KID_TOPK, st);
+    k_topk<<<Tc, 512, (size_t)topk_scratch_keys(E, K) * 8, st>>>(
+        wt.sc, wt.ch, Tc, E, K, d->renorm, d->routed_scale, idx, w, status);
+  }
+  return launch_status();
 }
 
 // The tensor-core path applies from two tokens on, for the shapes it takes.

@@ -141,7 +141,7 @@ struct TcGemmArgs {
   int32_t *status;
 };
 
-enum class TcKind { kMxf4GateUp, kMxf4Down, kBf16GateUp, kBf16Down };
+enum class TcKind { kMxf4GateUp, kMxf4Down, kBf16GateUp, kBf16Down, kBf16Store };
 
 // 3-D tensor map of bytes (inner = K bytes, rows, depth) with 128 x 128-byte boxes and
 // 128-byte swizzle; false if the driver entry point is missing or the layout is refused.
@@ -163,6 +163,14 @@ __global__ void k_quant_act(const float *__restrict__ act, int P, int I,
                             uint8_t *__restrict__ aq, uint8_t *__restrict__ as);
 __global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t *__restrict__ out);
 __global__ void k_group1(int n, int32_t *off, int32_t *tile_off);
+__global__ void k_row_norms(const uint16_t *__restrict__ v, int R, int H, float *__restrict__ out);
+__global__ void k_route_candidates(const float *__restrict__ Lt, const float *__restrict__ xn,
+                                   const float *__restrict__ wn,
+                                   const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
+                                   const float *__restrict__ bias, int H, int E, int K,
+                                   float *__restrict__ sc, float *__restrict__ ch,
+                                   int32_t *__restrict__ ncand, int32_t *status);
+size_t route_candidates_smem(int H, int E, int K);
 __global__ void k_combine(int T, int H, int K, const float *__restrict__ w,
                           const int32_t *__restrict__ inv, const float *__restrict__ dpair,
                           const float *__restrict__ ds, void *y, int ydt, int accumulate);

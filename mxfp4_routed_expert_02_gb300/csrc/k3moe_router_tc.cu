@@ -1,0 +1,165 @@
+// k3moe_router_tc.cu -- the router of the multi-token path: tensor-core screening, then the
+// exact computation for the experts that can matter.
+//
+// The selection is the page's (README of FareedKhan-dev/kimi-k3-in-c, section 9 "Picking
+// 16 experts of 896"): logit = x . Wr[e] rounded to float, sc = logistic(logit), ch = sc +
+// bias, the K largest ch with the lower index first on ties, weights from sc.
+//
+// 1. L~[t][e] = x . Wr[e] with bf16 operands and fp32 accumulation on the tensor cores.
+//    Every bf16 product is exact in float, so the only error of L~ is the rounding of at
+//    most H additions, each within 2^-23 of a partial sum bounded by
+//    S = sum_k |x_k Wr[e][k]| <= |x|_2 |Wr[e]|_2 (Cauchy-Schwarz):
+//    |L~ - logit| <= H * 2^-23 * |x|_2 |Wr[e]|_2.  The bound is taken with a factor 2 to
+//    spare; the norms come from k_row_norms.
+// 2. Per token, from those intervals, a lower and an upper bound of every expert's ch.
+//    With tau the K-th largest lower bound, at least K experts have ch >= tau, so an
+//    expert whose upper bound is below tau is not among the K largest.  The others (the
+//    candidates, at least K) get their logit computed exactly as in the decode router (a
+//    float-float sum of the exact products, rounded once), then sc and ch as the page
+//    defines them; the rest get ch = -inf.
+// 3. The usual top-k kernel then selects among the candidates: same result as selecting
+//    among all experts with exact scores.
+#include "k3moe_kernels.cuh"
+
+namespace k3 {
+
+// Euclidean norm of each of R bf16 rows of width H (a multiple of 8), one warp per row,
+// rounded up by a relative 2^-10 so that it bounds the exact norm.
+__global__ void k_row_norms(const uint16_t *__restrict__ v, int R, int H, float *__restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (warp >= R) return;
+  const uint4 *row = reinterpret_cast<const uint4 *>(v + (size_t)warp * H);
+  double acc = 0.0;
+  for (int q = lane; q < H / 8; q += 32) {
+    const uint4 w = __ldg(row + q);
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const double lo = bf16_lo(a[k]), hi = bf16_hi(a[k]);
+      acc += lo * lo + hi * hi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) out[warp] = (float)(sqrt(acc) * (1.0 + 1.0 / 1024));
+}
+
+// Logistic in float for the bounds (a few ulp from the exact value; the slack covers it).
+__device__ __forceinline__ float logistic_f(float v) { return 1.f / (1.f + expf(-v)); }
+
+// One block per token.  Lt [T][E] screening logits, xn [T] / wn [E] row norms of x / Wr;
+// x [T][H], wr [E][H] bf16; writes sc/ch [T][E] (candidates: exact; others: sc 0,
+// ch -inf).  Dynamic shared memory: H bf16 of x, then the candidate list (E ints) and the
+// top-k scratch.
+__global__ void __launch_bounds__(256) k_route_candidates(
+    const float *__restrict__ Lt, const float *__restrict__ xn, const float *__restrict__ wn,
+    const uint16_t *__restrict__ x,
+    const uint16_t *__restrict__ wr, const float *__restrict__ bias, int H, int E, int K,
+    float *__restrict__ sc, float *__restrict__ ch, int32_t *__restrict__ ncand,
+    int32_t *status) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
+  int *clist = reinterpret_cast<int *>(smem + (size_t)H * 2);
+  unsigned long long *keys = reinterpret_cast<unsigned long long *>(
+      smem + (((size_t)H * 2 + (size_t)E * 4 + 15) & ~size_t(15)));
+  __shared__ int sel[32];
+  __shared__ float wsel[32];
+  __shared__ int count;
+  __shared__ float tau;
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float *Lrow = Lt + (size_t)t * E;
+  const float xnorm = xn[t];
+  float *scr = sc + (size_t)t * E;
+  float *chr = ch + (size_t)t * E;
+  const float nerr = (float)H * 2.384185791015625e-07f;  // H * 2^-22
+  if (threadIdx.x == 0) count = 0;
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+  }
+  // lower bounds of ch -> ch row (scratch for the K-th largest), upper bounds kept in sc row
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float L = Lrow[e], S = xnorm * wn[e], b = bias ? bias[e] : 0.f;
+    float lo, hi;
+    if (isfinite(L) && isfinite(S) && isfinite(b)) {
+      const float d = __fmaf_rn(nerr, S, 1e-30f);
+      const float slack = 2e-6f + 9.5367431640625e-07f * (fabsf(L) + fabsf(b));  // 2^-20
+      lo = logistic_f(__fsub_rn(L, d)) + b - slack;
+      hi = logistic_f(__fadd_rn(L, d)) + b + slack;
+    } else {  // decided exactly below (and reported there if not finite)
+      lo = -INFINITY;
+      hi = INFINITY;
+    }
+    chr[e] = lo;
+    scr[e] = hi;
+  }
+  __syncthreads();
+  cta_topk(chr, chr, E, K, 0, 1.f, keys, sel, wsel);  // ends with __syncthreads
+  if (threadIdx.x == 0) tau = chr[sel[K - 1]];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float hi = scr[e];
+    if (!(hi < tau)) clist[atomicAdd(&count, 1)] = e;
+  }
+  __syncthreads();
+  const int C = count;
+  if (threadIdx.x == 0 && ncand) ncand[t] = C;
+  // non-candidates: out of the selection
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    if (!(scr[e] < tau)) continue;
+    scr[e] = 0.f;
+    chr[e] = -INFINITY;
+  }
+  __syncthreads();  // the candidates' rows are rewritten below
+  // candidates: exact logit (float-float sum of exact products, fixed reduction tree)
+  const int nchunk = H >> 3;
+  const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
+  for (int c = warp; c < C; c += nw) {
+    const int e = clist[c];
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(wr + (size_t)e * H);
+    float hi = 0.f, lo = 0.f;
+    for (int q = lane; q < nchunk; q += 32) {
+      const uint4 wv = __ldg(w4 + q), xv = xs4[q];
+      const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w}, xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        float p = __fmul_rn(bf16_lo(wa[k]), bf16_lo(xa[k]));
+        float s, er;
+        two_sum(hi, p, s, er);
+        hi = s;
+        lo = __fadd_rn(lo, er);
+        p = __fmul_rn(bf16_hi(wa[k]), bf16_hi(xa[k]));
+        two_sum(hi, p, s, er);
+        hi = s;
+        lo = __fadd_rn(lo, er);
+      }
+    }
+    {
+      const float s = __fadd_rn(hi, lo);
+      lo = __fsub_rn(lo, __fsub_rn(s, hi));
+      hi = s;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+      const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+      ff_add(hi, lo, oh, ol);
+    }
+    if (lane == 0) {
+      const float sv = (float)(1.0 / (1.0 + exp(-(double)hi)));
+      const float cv = __fadd_rn(sv, bias ? bias[e] : 0.f);
+      scr[e] = sv;
+      chr[e] = cv;
+      if (!(fabsf(cv) <= 3.402823466e38f)) set_status(status, K3MOE_ERR_NONFINITE);
+    }
+  }
+}
+
+size_t route_candidates_smem(int H, int E, int K) {
+  return (((size_t)H * 2 + (size_t)E * 4 + 15) & ~size_t(15)) + (size_t)topk_scratch_keys(E, K) * 8;
+}
+
+}  // namespace k3

@@ -510,6 +510,7 @@ cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &
     case TcKind::kMxf4Down: return launch_tc<0, 1, 5, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16GateUp: return launch_tc<1, 2, 1, 0>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Down: return launch_tc<1, 1, 2, 1>(a, A0, A1, B, grid, st);
+    case TcKind::kBf16Store: return launch_tc<1, 1, 1, 1>(a, A0, A1, B, grid, st);
   }
   return cudaErrorInvalidValue;
 }

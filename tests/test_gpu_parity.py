@@ -83,6 +83,32 @@ def test_route_ties_and_bias_only_selects():
     assert np.all(w.cpu().numpy() == np.float32(0.5))         # unbiased, renormalised 0.5/1.0
 
 
+def test_layer_tensor_core_router_ties_and_bias():
+    # multi-token path: duplicated router rows give equal selection scores (the lower
+    # index must win), a large bias on one expert forces it in without changing weights
+    cfg = dataclasses.replace(synth.config("tiny"), name="custom", hidden=512, inter=256,
+                              n_experts=24, topk=5, tokens=33, n_shared=1)
+    L = Layer(cfg, seed=21)
+    wr = L.host["wr"].copy()
+    wr[7] = wr[3]
+    wr[12] = wr[3]
+    wr[20] = wr[9]
+    bias = L.host["bias"].copy()
+    bias[3] = bias[7] = bias[12] = 0.05
+    bias[17] = 2.0
+    L.host["wr"], L.host["bias"] = wr, bias
+    L.d_wr = torch.from_numpy(wr.view(np.int16)).cuda()
+    L.d_bias = torch.from_numpy(bias).cuda()
+    y, idx, w, st = L.run()
+    assert st == 0
+    oi, ow, oy = L.oracle()
+    gi = idx.cpu().numpy()
+    assert np.array_equal(gi, oi)
+    assert (gi == 17).any(axis=1).all()
+    assert np.allclose(w.cpu().numpy(), ow, rtol=2e-7, atol=0)
+    assert rel_l2(y.cpu().numpy(), oy) <= REL_L2_F32
+
+
 def test_route_nonfinite_sets_status():
     cfg = synth.config("tiny")
     dims = dims_of(cfg)
