@@ -437,10 +437,10 @@ WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
   w.off1 = reinterpret_cast<int32_t *>(take(8));
   w.tile_off1 = reinterpret_cast<int32_t *>(take(8));
   w.xq = take((size_t)kTcTermsX * P * (H / 2));
-  w.xs = take((size_t)kTcTermsX * P * (H / kGroup));
+  w.xs = take((size_t)kTcTermsX * ((H / kGroup + 7) / 8) * P * 8);
   w.act = reinterpret_cast<float *>(take(P * I * 4));
   w.aq = take((size_t)kTcTermsAct * P * (I / 2));
-  w.as = take((size_t)kTcTermsAct * P * (I / kGroup));
+  w.as = take((size_t)kTcTermsAct * ((I / kGroup + 7) / 8) * P * 8);
   w.dpair = reinterpret_cast<float *>(take(P * H * 4));
   if (SI > 0) {
     w.act_s = reinterpret_cast<float *>(take((size_t)Tc * SI * 4));
@@ -472,9 +472,15 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   record_offsets(d, off);
   const uint8_t *rec = ex->experts;
   const unsigned long long es = (unsigned long long)ex->expert_stride;
+  // B rows per tile: 1.25 x the mean number of pairs per expert, rounded up to 16, at
+  // least 32 and at most 128 (few experts then need a second tile)
+  const int used = P < E ? P : E;
+  int ntile = ((((5 * P + 4 * used - 1) / (4 * used)) + 15) / 16) * 16;
+  ntile = ntile < 32 ? 32 : (ntile > kTcRows ? kTcRows : ntile);
   {
     TraceScope ts(KID_ROUTE_HIST, st);
-    k_route_hist<<<1, 1024, (size_t)E * 4, st>>>(idx, P, E, ws.off, ws.tile_off, ws.inv, status);
+    k_route_hist<<<1, 1024, (size_t)E * 4, st>>>(idx, P, E, ntile, ws.off, ws.tile_off, ws.inv,
+                                                 status);
   }
   {
     TraceScope ts(KID_ROUTE_SCATTER, st);
@@ -489,17 +495,18 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   }
   if (launch_status() != K3MOE_OK) return K3MOE_ERR_CUDA;
   CUtensorMap mg, mu, md, mx, ma;
-  if (!tc_map3d(&mg, rec + off[0], H / 2, I, E, H / 2, es) ||
-      !tc_map3d(&mu, rec + off[4], H / 2, I, E, H / 2, es) ||
-      !tc_map3d(&md, rec + off[2], I / 2, H, E, I / 2, es) ||
-      !tc_map3d(&mx, ws.xq, H / 2, P, kTcTermsX, H / 2, (unsigned long long)P * (H / 2)) ||
-      !tc_map3d(&ma, ws.aq, I / 2, P, kTcTermsAct, I / 2, (unsigned long long)P * (I / 2)))
+  if (!tc_map3d(&mg, rec + off[0], H / 2, I, E, H / 2, es, kTcRows) ||
+      !tc_map3d(&mu, rec + off[4], H / 2, I, E, H / 2, es, kTcRows) ||
+      !tc_map3d(&md, rec + off[2], I / 2, H, E, I / 2, es, kTcRows) ||
+      !tc_map3d(&mx, ws.xq, H / 2, P, kTcTermsX, H / 2, (unsigned long long)P * (H / 2), ntile) ||
+      !tc_map3d(&ma, ws.aq, I / 2, P, kTcTermsAct, I / 2, (unsigned long long)P * (I / 2), ntile))
     return K3MOE_ERR_CUDA;
   TcGemmArgs g{};
   g.off = ws.off;
   g.tile_off = ws.tile_off;
   g.gid = nullptr;
   g.ngroups = E;
+  g.ntile = ntile;
   g.b1 = d->situ_b1;
   g.b2 = d->situ_b2;
   g.status = status;
@@ -513,7 +520,8 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     a.sfa_gstride = ex->expert_stride;
     a.sf_rowb = H / kGroup;
     a.sfb = ws.xs;
-    a.sfb_tstride = (long long)P * (H / kGroup);
+    a.sfb_cstride = (long long)P * 8;
+    a.sfb_tstride = (long long)a.kchunks * a.sfb_cstride;
     a.out = ws.act;
     a.out_ld = I;
     TraceScope ts(KID_TC_GATEUP, st);
@@ -537,7 +545,8 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     a.sfa_gstride = ex->expert_stride;
     a.sf_rowb = I / kGroup;
     a.sfb = ws.as;
-    a.sfb_tstride = (long long)P * (I / kGroup);
+    a.sfb_cstride = (long long)P * 8;
+    a.sfb_tstride = (long long)a.kchunks * a.sfb_cstride;
     a.out = ws.dpair;
     a.out_ld = H;
     TraceScope ts(KID_TC_DOWN, st);
@@ -546,17 +555,19 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   }
   if (SI > 0) {
     CUtensorMap msg, msu, msd, mxs, mhs;
-    if (!tc_map3d(&msg, sh_gate, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI) ||
-        !tc_map3d(&msu, sh_up, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI) ||
-        !tc_map3d(&msd, sh_down, 2ull * SI, H, 1, 2ull * SI, 2ull * SI * H) ||
-        !tc_map3d(&mxs, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc) ||
-        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc))
+    const int nt1 = kTcRows;
+    if (!tc_map3d(&msg, sh_gate, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
+        !tc_map3d(&msu, sh_up, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
+        !tc_map3d(&msd, sh_down, 2ull * SI, H, 1, 2ull * SI, 2ull * SI * H, kTcRows) ||
+        !tc_map3d(&mxs, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, nt1) ||
+        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc, nt1))
       return K3MOE_ERR_CUDA;
-    k_group1<<<1, 32, 0, st>>>(Tc, ws.off1, ws.tile_off1);
+    k_group1<<<1, 32, 0, st>>>(Tc, nt1, ws.off1, ws.tile_off1);
     TcGemmArgs s1 = g;
     s1.off = ws.off1;
     s1.tile_off = ws.tile_off1;
     s1.ngroups = 1;
+    s1.ntile = nt1;
     {
       TcGemmArgs a = s1;
       a.mtiles = (SI + kTcRows - 1) / kTcRows;
@@ -607,15 +618,16 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
     k_row_norms<<<(Tc + 7) / 8, 256, 0, st>>>(x, Tc, H, wt.xn);
     k_row_norms<<<(E + 7) / 8, 256, 0, st>>>(wr, E, H, wt.wn);
   }
-  k_group1<<<1, 32, 0, st>>>(Tc, wt.off1, wt.tile_off1);
+  k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, wt.off1, wt.tile_off1);
   CUtensorMap mw, mx;
-  if (!tc_map3d(&mw, wr, 2ull * H, E, 1, 2ull * H, 2ull * H * E) ||
-      !tc_map3d(&mx, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc))
+  if (!tc_map3d(&mw, wr, 2ull * H, E, 1, 2ull * H, 2ull * H * E, kTcRows) ||
+      !tc_map3d(&mx, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, kTcRows))
     return K3MOE_ERR_CUDA;
   TcGemmArgs a{};
   a.off = wt.off1;
   a.tile_off = wt.tile_off1;
   a.ngroups = 1;
+  a.ntile = kTcRows;
   a.mtiles = (E + kTcRows - 1) / kTcRows;
   a.M_rows = E;
   tc_k_split(2LL * H, a);

@@ -129,12 +129,15 @@ struct TcGemmArgs {
   int M_rows;        // rows of each A matrix (outputs)
   int kchunks;       // 128-byte chunks of K
   int ksteps_last;   // 32-byte MMA steps in the last chunk (1..4)
-  int nstages;       // set by the launcher
+  int ntile;         // B rows per tile (multiple of 16, at most 128)
+  int nstages;       // data stages, set by the launcher
+  int nsf;           // scale-byte slots, set by the launcher
   const uint8_t *sfa[2];   // MXF4: scale bytes of A matrix m for group 0, rows of sf_rowb
   long long sfa_gstride;   // bytes between consecutive groups' A scales
   int sf_rowb;             // scale bytes per row (K / 32)
-  const uint8_t *sfb;      // MXF4: B scale bytes [term][B row][sf_rowb]
+  const uint8_t *sfb;      // MXF4: B scale bytes [term][K chunk][B row][8]
   long long sfb_tstride;   // bytes between terms
+  long long sfb_cstride;   // bytes between K chunks (B rows x 8)
   float *out;              // [B row][out_ld]
   long long out_ld;
   float b1, b2;            // SiTU caps (gate/up epilogue)
@@ -143,17 +146,18 @@ struct TcGemmArgs {
 
 enum class TcKind { kMxf4GateUp, kMxf4Down, kBf16GateUp, kBf16Down, kBf16Store };
 
-// 3-D tensor map of bytes (inner = K bytes, rows, depth) with 128 x 128-byte boxes and
-// 128-byte swizzle; false if the driver entry point is missing or the layout is refused.
+// 3-D tensor map of bytes (inner = K bytes, rows, depth) with boxes of box_rows x 128
+// bytes and 128-byte swizzle; false if the driver entry point is missing or the layout is
+// refused.
 bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
               unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
-              unsigned long long depth_stride);
+              unsigned long long depth_stride, int box_rows);
 cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &A0,
                            const CUtensorMap &A1, const CUtensorMap &B, int grid,
                            cudaStream_t st);
 
-__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int32_t *off,
-                             int32_t *tile_off, int32_t *inv, int32_t *status);
+__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int ntile,
+                             int32_t *off, int32_t *tile_off, int32_t *inv, int32_t *status);
 __global__ void k_route_scatter(const int32_t *__restrict__ idx, int P,
                                 const int32_t *__restrict__ off, int32_t *perm, int32_t *inv);
 __global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
@@ -162,7 +166,7 @@ __global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
 __global__ void k_quant_act(const float *__restrict__ act, int P, int I,
                             uint8_t *__restrict__ aq, uint8_t *__restrict__ as);
 __global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t *__restrict__ out);
-__global__ void k_group1(int n, int32_t *off, int32_t *tile_off);
+__global__ void k_group1(int n, int ntile, int32_t *off, int32_t *tile_off);
 __global__ void k_row_norms(const uint16_t *__restrict__ v, int R, int H, float *__restrict__ out);
 __global__ void k_route_candidates(const float *__restrict__ Lt, const float *__restrict__ xn,
                                    const float *__restrict__ wn,

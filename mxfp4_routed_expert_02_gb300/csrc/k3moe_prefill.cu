@@ -12,10 +12,10 @@ namespace k3 {
 
 // ------------------------------------------------------------------------------ dispatch
 // One block: per-expert pair counts, their exclusive prefix off[E+1], and the prefix of
-// 128-row tiles tile_off[E+1].  Pairs whose expert index is outside [0, E) are counted
+// ntile-row tiles tile_off[E+1].  Pairs whose expert index is outside [0, E) are counted
 // nowhere, get inv = -1 (the combine skips them) and set K3MOE_ERR_BAD_EXPERT.
-__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int32_t *off,
-                             int32_t *tile_off, int32_t *inv, int32_t *status) {
+__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int ntile,
+                             int32_t *off, int32_t *tile_off, int32_t *inv, int32_t *status) {
   extern __shared__ int32_t cnt[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -35,7 +35,7 @@ __global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int3
       off[e] = o;
       tile_off[e] = to;
       o += cnt[e];
-      to += (cnt[e] + kTcRows - 1) / kTcRows;
+      to += (cnt[e] + ntile - 1) / ntile;
     }
     off[E] = o;
     tile_off[E] = to;
@@ -116,8 +116,9 @@ __device__ __forceinline__ void encode_terms(float (&r)[32], uint4 (&q)[NT], uin
 }
 
 // x [T][H] bf16 -> the kTcTermsX-term encoding of every (token, slot) pair's row, written
-// at the pair's sorted position: xq [term][P][H/2], xs [term][P][H/32].  One thread per
-// (token, group); the token's K slots receive the same bytes.
+// at the pair's sorted position: xq [term][P][H/2] and the scale bytes xs [term][K chunk]
+// [P][8] (chunk = 8 groups, the block-scaled GEMM's stage).  One thread per (token,
+// group); the token's K slots receive the same bytes.
 __global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
                           const int32_t *__restrict__ inv, int P, uint8_t *__restrict__ xq,
                           uint8_t *__restrict__ xs) {
@@ -147,13 +148,14 @@ __global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
 #pragma unroll
       for (int tt = 0; tt < kTcTermsX; tt++) {
         reinterpret_cast<uint4 *>(xq + ((size_t)tt * P + s) * (H / 2))[g] = q[tt];
-        xs[((size_t)tt * P + s) * G + g] = sb[tt];
+        xs[(((size_t)tt * ((G + 7) / 8) + g / 8) * P + s) * 8 + (g % 8)] = sb[tt];
       }
     }
   }
 }
 
-// act [P][I] float -> kTcTermsAct-term encoding: aq [term][P][I/2], as [term][P][I/32].
+// act [P][I] float -> kTcTermsAct-term encoding: aq [term][P][I/2], scale bytes as
+// [term][K chunk][P][8].
 __global__ void k_quant_act(const float *__restrict__ act, int P, int I,
                             uint8_t *__restrict__ aq, uint8_t *__restrict__ as) {
   const int G = I / kGroup;
@@ -177,7 +179,7 @@ __global__ void k_quant_act(const float *__restrict__ act, int P, int I,
 #pragma unroll
     for (int tt = 0; tt < kTcTermsAct; tt++) {
       reinterpret_cast<uint4 *>(aq + ((size_t)tt * P + s) * (I / 2))[g] = q[tt];
-      as[((size_t)tt * P + s) * G + g] = sb[tt];
+      as[(((size_t)tt * ((G + 7) / 8) + g / 8) * P + s) * 8 + (g % 8)] = sb[tt];
     }
   }
 }
@@ -196,12 +198,12 @@ __global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t 
 }
 
 // Group table of a single dense group of n rows: off = {0, n}, tile_off = {0, tiles}.
-__global__ void k_group1(int n, int32_t *off, int32_t *tile_off) {
+__global__ void k_group1(int n, int ntile, int32_t *off, int32_t *tile_off) {
   if (threadIdx.x == 0) {
     off[0] = 0;
     off[1] = n;
     tile_off[0] = 0;
-    tile_off[1] = (n + kTcRows - 1) / kTcRows;
+    tile_off[1] = (n + ntile - 1) / ntile;
   }
 }
 

@@ -41,6 +41,8 @@ constexpr int kTcTile = kTcRows;          // A rows and B rows per tile
 constexpr int kTcChunkBytes = 128;        // K bytes per stage (one 128-byte swizzle atom)
 constexpr uint32_t kTcBox = kTcTile * kTcChunkBytes;  // bytes of one TMA box (16 KB)
 constexpr int kTcTmemCols = 512;
+constexpr int kTcItemTable = 512;         // per-CTA work items kept in shared memory
+constexpr uint32_t kTcItemTableBytes = kTcItemTable * 16;
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, int cols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -190,10 +192,56 @@ __device__ __forceinline__ TcItem tc_item(const TcGemmArgs &a, int item) {
   }
   it.g = lo;
   const int nt = tile - a.tile_off[lo];
-  it.brow0 = a.off[lo] + nt * kTcTile;
+  it.brow0 = a.off[lo] + nt * a.ntile;
   const int rem = a.off[lo + 1] - it.brow0;
-  it.nvalid = rem < kTcTile ? rem : kTcTile;
+  it.nvalid = rem < a.ntile ? rem : a.ntile;
   return it;
+}
+
+// Non-blocking test of an mbarrier phase (unlike try_wait, never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, "
+      "p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared memory after the 1 KB header: NS data stages [A_0 .. A_{NA-1}: 128 rows x 128 B]
+// [B_0 .. B_{NT-1}: ntile rows x 128 B] (1 KB aligned), then NSF scale slots [A scales:
+// NA x 128 rows x 8 B][B scales: NT x ntile rows x 8 B].
+__host__ __device__ inline uint32_t tc_stage_bytes(int na, int nt, int ntile) {
+  const uint32_t b = (uint32_t)na * kTcBox + (uint32_t)nt * ntile * kTcChunkBytes;
+  return (b + 1023u) & ~1023u;
+}
+__host__ __device__ inline uint32_t tc_sf_bytes(int na, int nt, int ntile) {
+  return ((uint32_t)na * kTcTile * 8 + (uint32_t)nt * ntile * 8 + 15u) & ~15u;
+}
+
+// SiTU-GLU in the tensor-core epilogue: b1 tanh(g/b1) sigmoid(g) * b2 tanh(u/b2) with the
+// fast exponential; within ~1e-6 of the value (absolute near zero), far inside the layer
+// tolerance.
+__device__ __forceinline__ float tanh_fast(float y) {
+  const float e = __expf(-2.f * fabsf(y));
+  return copysignf(__fdividef(1.f - e, 1.f + e), y);
+}
+__device__ __forceinline__ float situ_fast(float g, float u, float b1, float ib1, float b2,
+                                           float ib2) {
+  const float sg = __fdividef(1.f, 1.f + __expf(-g));
+  return (b1 * tanh_fast(g * ib1)) * sg * (b2 * tanh_fast(u * ib2));
 }
 
 template <int KIND, int NA, int NT, int EPI>
@@ -206,19 +254,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t base_u32 = smem_u32(smem);
   const uint32_t pad = ((base_u32 + 1023u) & ~1023u) - base_u32;
   smem += pad;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [NS]
-  uint64_t *sfull = full + 8;                           // [NS]
-  uint64_t *empty = full + 16;                          // [NS]
-  uint64_t *dfull = full + 24;
-  uint64_t *dempty = full + 25;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [NS] TMA landed
+  uint64_t *sfull = full + 8;                           // [NS] scale vectors in TMEM
+  uint64_t *empty = full + 16;                          // [NS] MMAs of the stage done
+  uint64_t *sfload = full + 24;                         // [NSF] scale bytes landed
+  uint64_t *sffree = full + 32;                         // [NSF] scale slot read by all
+  uint64_t *dfull = full + 40;
+  uint64_t *dempty = full + 41;
   uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + 512);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 520);
   uint8_t *stages = smem + 1024;
-  constexpr uint32_t kStageBytes = (uint32_t)(NA + NT) * kTcBox;
+  uint8_t *sfring = stages + (size_t)a.nstages * tc_stage_bytes(NA, NT, a.ntile);
+  constexpr bool kScales = (KIND == 0);
   // TMEM columns per stage of scale vectors: B terms first (16 columns each), then the A
   // matrices (16 each); multi-column accesses stay aligned to their width
-  constexpr int kSfSlot = (KIND == 0) ? 16 * (NT + NA) : 0;
-  const int NS = a.nstages;
+  constexpr int kSfSlot = kScales ? 16 * (NT + NA) : 0;
+  const int NS = a.nstages, NSF = a.nsf, ntile = a.ntile;
+  const uint32_t stage_bytes = tc_stage_bytes(NA, NT, ntile);
+  const uint32_t tma_bytes = (uint32_t)NA * kTcBox + (uint32_t)NT * ntile * kTcChunkBytes;
+  const uint32_t sf_bytes = tc_sf_bytes(NA, NT, ntile);
+  const uint32_t off_sfa = 0, off_sfb = (uint32_t)NA * kTcTile * 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -226,6 +281,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&sfull[s], 4);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < NSF; s++) {
+      mbar_init(&sfload[s], 128);
+      mbar_init(&sffree[s], 4);
     }
     mbar_init(dfull, 1);
     mbar_init(dempty, 8);
@@ -237,105 +296,159 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base;
-  const uint32_t sf_col0 = (uint32_t)(NA * kTcTile);  // scale slots after the accumulators
+  // accumulators: matrix m at columns [m * ntile, (m+1) * ntile); scale slots after them
+  const uint32_t sf_col0 = (uint32_t)((NA * ntile + 15) & ~15);
 
   pdl_wait();
   const int nitems = a.tile_off[a.ngroups] * a.mtiles;
-  const int G = a.sf_rowb;  // scale bytes per A / B row
+  const int my_items = nitems > (int)blockIdx.x ? (nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int total = my_items * a.kchunks;  // stages this CTA runs
+  const int G = a.sf_rowb;                 // scale bytes per A row
+  // this CTA's work items (the k-th is item blockIdx.x + k * gridDim.x), looked up once
+  int4 *itab = reinterpret_cast<int4 *>(sfring + (size_t)NSF * sf_bytes);
+  for (int k = tid; k < my_items && k < kTcItemTable; k += blockDim.x) {
+    const TcItem ti = tc_item(a, (int)blockIdx.x + k * (int)gridDim.x);
+    itab[k] = make_int4(ti.g, ti.mt, ti.brow0, ti.nvalid);
+  }
+  __syncthreads();
+  auto item_at = [&](int k) -> TcItem {
+    if (k < kTcItemTable) {
+      const int4 v = itab[k];
+      return TcItem{v.x, v.y, v.z, v.w};
+    }
+    return tc_item(a, (int)blockIdx.x + k * (int)gridDim.x);
+  };
 
   if (warp == kTcWarpTma) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      int it = 0;
-      for (int item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
-        const TcItem ti = tc_item(a, item);
+      for (int it = 0; it < total && !*abort_flag; it++) {
+        const int c = it % a.kchunks;
+        const TcItem ti = item_at(it / a.kchunks);
         const int ga = a.gid ? a.gid[ti.g] : ti.g;
-        for (int c = 0; c < a.kchunks; c++, it++) {
-          const int s = it % NS;
-          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
-            set_status(a.status, K3MOE_ERR_TIMEOUT);
-            *abort_flag = 1;
-            break;
-          }
-          uint8_t *st = stages + (size_t)s * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
-          tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
-          if (NA > 1)
-            tma_load3d(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
-#pragma unroll
-          for (int t = 0; t < NT; t++)
-            tma_load3d(st + (NA + t) * kTcBox, &tmB, c * kTcChunkBytes, ti.brow0, t, &full[s]);
+        const int s = it % NS;
+        if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
         }
+        uint8_t *st = stages + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], tma_bytes);
+        tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+        if (NA > 1) tma_load3d(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+#pragma unroll
+        for (int t = 0; t < NT; t++)
+          tma_load3d(st + NA * kTcBox + t * ntile * kTcChunkBytes, &tmB, c * kTcChunkBytes,
+                     ti.brow0, t, &full[s]);
       }
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- scale writers
-    if (KIND == 0) {
+    // Two streams: load stage ld's scale bytes into scale slot ld % NSF (cp.async, arriving
+    // on sfload) as soon as every writer has finished with that slot's previous stage (up
+    // to NSF stages ahead), and place stage stn's bytes in TMEM once they have landed and
+    // the stage's TMEM slot is free.
+    if (kScales) {
       const int q = warp;
-      int it = 0;
-      for (int item = blockIdx.x; item < nitems && !*abort_flag; item += gridDim.x) {
-        const TcItem ti = tc_item(a, item);
-        const int ga = a.gid ? a.gid[ti.g] : ti.g;
-        const int row = ti.mt * kTcTile + 32 * q + lane;  // A row of this lane
-        const bool rok = row < a.M_rows;
-        for (int c = 0; c < a.kchunks; c++, it++) {
-          const int s = it % NS;
-          // scale bytes first (global loads), then wait for the slot
-          uint2 sa[NA];
+      const bool g8 = (G % 8) == 0;
+      const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
+      int ld = 0, stn = 0;
+      while (stn < total && !*abort_flag) {
+        while (ld < total && ld < stn + NSF &&
+               (ld == stn ? mbar_wait(&sffree[ld % NSF], ((ld / NSF) & 1) ^ 1)
+                          : mbar_test(&sffree[ld % NSF], ((ld / NSF) & 1) ^ 1))) {
+          const int c = ld % a.kchunks;
+          const TcItem ti = item_at(ld / a.kchunks);
+          const int ga = a.gid ? a.gid[ti.g] : ti.g;
+          const int k = ld % NSF;
+          uint8_t *sfs = sfring + (size_t)k * sf_bytes;
+          const int r = 32 * q + lane;  // this thread's A row and B row in the tile
+          const int row = ti.mt * kTcTile + r;
 #pragma unroll
-          for (int m = 0; m < NA; m++)
-            sa[m] = rok ? load_scales8(a.sfa[m] + (long long)ga * a.sfa_gstride +
-                                           (long long)row * G,
-                                       G, c, true)
-                        : make_uint2(0u, 0u);
-          uint32_t vb[NT][16];
-          {
-#pragma unroll
-            for (int t = 0; t < NT; t++)
-#pragma unroll
-              for (int j = 0; j < 4; j++) {
-                const int n = 32 * j + lane;
-                const uint2 sb = (n < ti.nvalid)
-                                     ? load_scales8(a.sfb + (long long)t * a.sfb_tstride +
-                                                        (long long)(ti.brow0 + n) * G,
-                                                    G, c, false)
-                                     : make_uint2(0u, 0u);
-#pragma unroll
-                for (int i = 0; i < 4; i++) vb[t][4 * i + j] = step_scales(sb, i);
-              }
+          for (int m = 0; m < NA; m++) {
+            uint8_t *dst = sfs + off_sfa + (m * kTcTile + r) * 8;
+            const uint8_t *src = a.sfa[m] + (long long)ga * a.sfa_gstride + (long long)row * G;
+            if (row < a.M_rows && g8 && 8 * c + 8 <= G) {
+              cp_async8(dst, src + 8 * c);
+            } else {
+              const uint2 v = row < a.M_rows ? load_scales8(src, G, c, false) : make_uint2(0u, 0u);
+              *reinterpret_cast<uint2 *>(dst) = v;
+            }
           }
-          if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
-            set_status(a.status, K3MOE_ERR_TIMEOUT);
-            *abort_flag = 1;
-            break;
+          if (r < ntile) {
+#pragma unroll
+            for (int t = 0; t < NT; t++) {
+              uint8_t *dst = sfs + off_sfb + (t * ntile + r) * 8;
+              if (r < ti.nvalid)
+                cp_async8(dst, a.sfb + (long long)t * a.sfb_tstride +
+                                   (long long)c * a.sfb_cstride + (long long)(ti.brow0 + r) * 8);
+              else
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
+            }
           }
-          tc_fence_after();
-          const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
-          const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
-          // A: K step i of matrix m reads column slot + 16(NT + m) + 4i + (row / 32)
-#pragma unroll
-          for (int m = 0; m < NA; m++)
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-              tmem_st_x1(slot + lane_sel + 16 * (NT + m) + 4 * i + q, step_scales(sa[m], i));
-          // B: K step i of term t reads column slot + 16t + 4i + n/32 at lane n % 32 of
-          // every lane quarter (each 32-row quarter of the MMA reads its own copy)
-#pragma unroll
-          for (int t = 0; t < NT; t++) tmem_st_x16(slot + lane_sel + 16 * t, vb[t]);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sfull[s]);
+          cp_async_arrive(&sfload[k]);
+          ld++;
         }
+        if (stn >= ld) {  // the slot wait above timed out
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        const int k = stn % NSF, sj = stn % NS;
+        if (!mbar_wait(&sfload[k], (stn / NSF) & 1) ||
+            !mbar_wait(&empty[sj], ((stn / NS) & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t *sfs = sfring + (size_t)k * sf_bytes;
+        const uint32_t slot = tmem + sf_col0 + (uint32_t)(sj * kSfSlot);
+        // A: K step i of matrix m reads column slot + 16(NT + m) + 4i + (row / 32);
+        // scale byte 255 (no contribution) becomes 0
+#pragma unroll
+        for (int m = 0; m < NA; m++) {
+          uint2 v = *reinterpret_cast<const uint2 *>(sfs + off_sfa + (m * kTcTile + 32 * q + lane) * 8);
+          v.x &= ~__vcmpeq4(v.x, 0xffffffffu);
+          v.y &= ~__vcmpeq4(v.y, 0xffffffffu);
+#pragma unroll
+          for (int i = 0; i < 4; i++)
+            tmem_st_x1(slot + lane_sel + 16 * (NT + m) + 4 * i + q, step_scales(v, i));
+        }
+        // B: K step i of term t reads column slot + 16t + 4i + n/32 at lane n % 32 of
+        // every lane quarter (each 32-row quarter of the MMA reads its own copy)
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+          uint32_t vb[16];
+#pragma unroll
+          for (int jj = 0; jj < 4; jj++) {
+            const int n = 32 * jj + lane;
+            const uint2 v = (n < ntile) ? *reinterpret_cast<const uint2 *>(sfs + off_sfb + (t * ntile + n) * 8)
+                                        : make_uint2(0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 4; i++) vb[4 * i + jj] = step_scales(v, i);
+          }
+          tmem_st_x16(slot + lane_sel + 16 * t, vb);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sfull[sj]);
+          mbar_arrive(&sffree[k]);
+        }
+        stn++;
       }
+      // every cp.async of this thread must land before the CTA can exit
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else if (warp == kTcWarpMma) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       int it = 0, n = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, n++) {
-        const TcItem ti = tc_item(a, item);
+      for (; n < my_items && ok; n++) {
+        const TcItem ti = item_at(n);
         const int nmma = ((ti.nvalid + 15) / 16) * 16;
         uint32_t idesc;
         if (KIND == 0)
@@ -355,30 +468,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c = 0; c < a.kchunks; c++, it++) {
           const int s = it % NS;
           const uint32_t par = (it / NS) & 1;
-          if (!mbar_wait(&full[s], par) || (KIND == 0 && !mbar_wait(&sfull[s], par))) {
+          if (!mbar_wait(&full[s], par) || (kScales && !mbar_wait(&sfull[s], par))) {
             set_status(a.status, K3MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(stages + (size_t)s * kStageBytes);
+          // descriptors: the stage base plus constant offsets (address field in 16-byte
+          // units, no carry out of it below 256 KB)
+          const uint64_t dbase = sw128_desc(smem_u32(stages + (size_t)s * stage_bytes));
           const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
+          const uint32_t boff = (uint32_t)(NA * kTcBox) >> 4, tstep = (uint32_t)(ntile * kTcChunkBytes) >> 4;
           const int nk = (c == a.kchunks - 1) ? a.ksteps_last : 4;
-          for (int i = 0; i < nk; i++) {
 #pragma unroll
-            for (int m = 0; m < NA; m++) {
-              const uint64_t ad = sw128_desc(st + m * kTcBox + 32 * i);
+          for (int i = 0; i < 4; i++) {
+            if (i < nk) {
 #pragma unroll
-              for (int t = 0; t < NT; t++) {
-                const uint64_t bd = sw128_desc(st + (NA + t) * kTcBox + 32 * i);
-                const uint32_t acc = (c > 0 || i > 0 || t > 0) ? 1u : 0u;
-                const uint32_t dcol = tmem + (uint32_t)(m * kTcTile);
-                if (KIND == 0)
-                  mma_mxf4(dcol, ad, bd, idesc, slot + 16 * (NT + m) + 4 * i, slot + 16 * t + 4 * i,
-                           acc);
-                else
-                  mma_f16(dcol, ad, bd, idesc, acc);
+              for (int m = 0; m < NA; m++) {
+                const uint64_t ad = dbase + (uint64_t)((m * kTcBox + 32 * i) >> 4);
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                  const uint64_t bd = dbase + (uint64_t)(boff + t * tstep + 2 * i);
+                  const uint32_t acc = (c > 0 || i > 0 || t > 0) ? 1u : 0u;
+                  const uint32_t dcol = tmem + (uint32_t)(m * ntile);
+                  if (KIND == 0)
+                    mma_mxf4(dcol, ad, bd, idesc, slot + 16 * (NT + m) + 4 * i,
+                             slot + 16 * t + 4 * i, acc);
+                  else
+                    mma_f16(dcol, ad, bd, idesc, acc);
+                }
               }
             }
           }
@@ -396,9 +515,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - kTcWarpEpi) >> 2;
-    int n = 0;
-    for (int item = blockIdx.x; item < nitems; item += gridDim.x, n++) {
-      const TcItem ti = tc_item(a, item);
+    const int hcols = ((ntile / 2) + 15) & ~15;  // columns per half (multiple of 16)
+    const float ib1 = 1.f / a.b1, ib2 = 1.f / a.b2;
+    for (int n = 0; n < my_items; n++) {
+      const TcItem ti = item_at(n);
       const bool got = mbar_wait(dfull, n & 1);
       if (!got) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
@@ -408,17 +528,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int row = ti.mt * kTcTile + 32 * q + lane;
       const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
       if (got && !*abort_flag) {
-        for (int c0 = half * 64; c0 < half * 64 + 64 && c0 < ti.nvalid; c0 += 16) {
+        for (int c0 = half * hcols; c0 < (half + 1) * hcols && c0 < ti.nvalid; c0 += 16) {
           float d0[16], d1[16];
           tmem_ld_x16(tmem + lane_sel + (uint32_t)c0, d0);
-          if (NA > 1) tmem_ld_x16(tmem + lane_sel + (uint32_t)(kTcTile + c0), d1);
+          if (NA > 1) tmem_ld_x16(tmem + lane_sel + (uint32_t)(ntile + c0), d1);
           if (row < a.M_rows) {
 #pragma unroll
             for (int j = 0; j < 16; j++) {
               const int col = c0 + j;
               if (col < ti.nvalid) {
                 float v = d0[j];
-                if (EPI == 0) v = situ(d0[j], d1[j], a.b1, a.b2);
+                if (EPI == 0) v = situ_fast(d0[j], d1[j], a.b1, ib1, a.b2, ib2);
                 a.out[(long long)(ti.brow0 + col) * a.out_ld + row] = v;
               }
             }
@@ -465,7 +585,7 @@ EncodeTiledFn encode_fn() {
 
 bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
               unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
-              unsigned long long depth_stride) {
+              unsigned long long depth_stride, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_stride & 15) || (depth_stride & 15))
@@ -473,7 +593,7 @@ bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
   if (depth_stride == 0) depth_stride = row_stride * rows;
   const cuuint64_t dims[3] = {inner_bytes, rows, depth};
   const cuuint64_t strides[2] = {row_stride, depth_stride};
-  const cuuint32_t box[3] = {(cuuint32_t)kTcChunkBytes, (cuuint32_t)kTcTile, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)kTcChunkBytes, (cuuint32_t)box_rows, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -481,23 +601,42 @@ bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int tc_stages(int na, int nt) {
-  const size_t stage = (size_t)(na + nt) * kTcBox;
-  int ns = (int)((227 * 1024 - 2048) / stage);
-  return ns > 8 ? 8 : ns;
+// Ring depths: NSF scale slots (8 when they fit), then as many data stages as fit in
+// shared memory (and, with scale slots, in TMEM next to the accumulators), at most 8.
+static void tc_depths(int na, int nt, int ntile, bool scales, int *ns, int *nsf) {
+  const size_t budget = 227 * 1024 - 2048 - kTcItemTableBytes;
+  const size_t stage = tc_stage_bytes(na, nt, ntile), sfb = scales ? tc_sf_bytes(na, nt, ntile) : 0;
+  int f = scales ? 8 : 0;
+  int s = 0;
+  for (;; f = f > 2 ? f - 2 : 0) {
+    s = (int)((budget - f * sfb) / stage);
+    if (s >= 2 || f == 0) break;
+  }
+  if (scales) {
+    const int free_cols = kTcTmemCols - ((na * ntile + 15) & ~15);
+    const int by_tmem = free_cols / (16 * (na + nt));
+    if (s > by_tmem) s = by_tmem;
+  }
+  *ns = s > 8 ? 8 : s;
+  *nsf = f;
 }
-
-size_t tc_smem_bytes(int na, int nt) { return 2048 + (size_t)tc_stages(na, nt) * (na + nt) * kTcBox; }
 
 template <int KIND, int NA, int NT, int EPI>
 static cudaError_t launch_tc(const TcGemmArgs &a, const CUtensorMap &A0, const CUtensorMap &A1,
                              const CUtensorMap &B, int grid, cudaStream_t st) {
   auto fn = k_tc_gemm<KIND, NA, NT, EPI>;
-  const size_t smem = tc_smem_bytes(NA, NT);
+  if (a.ntile < 16 || a.ntile > kTcTile || a.ntile % 16) return cudaErrorInvalidValue;
+  int ns = 0, nsf = 0;
+  tc_depths(NA, NT, a.ntile, KIND == 0, &ns, &nsf);
+  if (ns < 2 || (KIND == 0 && nsf < 2)) return cudaErrorInvalidValue;
+  const size_t smem = 2048 + (size_t)ns * tc_stage_bytes(NA, NT, a.ntile) +
+                      (size_t)nsf * (KIND == 0 ? tc_sf_bytes(NA, NT, a.ntile) : 0) +
+                      kTcItemTableBytes;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   TcGemmArgs aa = a;
-  aa.nstages = tc_stages(NA, NT);
+  aa.nstages = ns;
+  aa.nsf = nsf;
   fn<<<grid, kTcThreads, smem, st>>>(aa, A0, A1, B);
   return cudaGetLastError();
 }
