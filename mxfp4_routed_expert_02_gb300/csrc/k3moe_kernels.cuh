@@ -116,7 +116,7 @@ namespace k3 {
 
 constexpr int kTcRows = 128;     // A rows / B rows per tensor-core tile
 constexpr int kTcTermsX = 4;     // MXFP4 terms of the layer input x (bf16)
-constexpr int kTcTermsAct = 5;   // MXFP4 terms of the SiTU activations (float)
+constexpr int kTcTermsAct = 4;   // MXFP4 terms of the SiTU activations (float)
 constexpr int kTcTokens = 4096;  // tokens per pass of the multi-token path
 
 // Arguments of k_tc_gemm.  Groups g = 0..ngroups-1 own B rows [off[g], off[g+1]) and
@@ -132,6 +132,7 @@ struct TcGemmArgs {
   int ntile;         // B rows per tile (multiple of 16, at most 128)
   int nstages;       // data stages, set by the launcher
   int nsf;           // scale-byte slots, set by the launcher
+  int nacc;          // accumulator buffers (1 or 2), set by the launcher
   const uint8_t *sfa[2];   // MXF4: scale bytes of A matrix m for group 0, rows of sf_rowb
   long long sfa_gstride;   // bytes between consecutive groups' A scales
   int sf_rowb;             // scale bytes per row (K / 32)

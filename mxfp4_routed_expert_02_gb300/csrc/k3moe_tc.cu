@@ -9,7 +9,8 @@
 // the group's tokens.  Two kinds:
 //   MXF4: A is the expert's packed MXFP4 operand as stored in the record (E2M1 nibbles,
 //         one E8M0 scale per 32 along K) and B is the activation written as a sum of
-//         NT MXFP4 terms (each E2M1 with its own E8M0 scale per 32); every term is one
+//         NT MXFP4 terms (each E2M1 with its own E8M0 scale per 32; 4 for x and for the
+//         activations, relative error ~4e-5 and ~3e-4 of a row's product); every term is one
 //         block-scaled MMA (kind::mxf4, scale vectors of 2 per 64-wide K step), all
 //         accumulated in one fp32 accumulator.  Scale byte 255 of A (the page's "no
 //         contribution") is written to tensor memory as 0, i.e. 2^-127.
@@ -120,6 +121,29 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for this thread's outstanding tcgen05.ld; the registers are passed through so the
+// compiler cannot read them before the wait.
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&v)[16], uint32_t (&w)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(w[0]), "+r"(w[1]),
+                 "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7]),
+                 "+r"(w[8]), "+r"(w[9]), "+r"(w[10]), "+r"(w[11]), "+r"(w[12]), "+r"(w[13]),
+                 "+r"(w[14]), "+r"(w[15])
+               :
+               : "memory");
 }
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&f)[16]) {
   uint32_t v[16];
@@ -259,8 +283,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t *empty = full + 16;                          // [NS] MMAs of the stage done
   uint64_t *sfload = full + 24;                         // [NSF] scale bytes landed
   uint64_t *sffree = full + 32;                         // [NSF] scale slot read by all
-  uint64_t *dfull = full + 40;
-  uint64_t *dempty = full + 41;
+  uint64_t *dfull = full + 40;   // [2] accumulator buffer complete
+  uint64_t *dempty = full + 42;  // [2] accumulator buffer drained
   uint32_t *tmem_base = reinterpret_cast<uint32_t *>(smem + 512);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 520);
   uint8_t *stages = smem + 1024;
@@ -286,8 +310,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sfload[s], 128);
       mbar_init(&sffree[s], 4);
     }
-    mbar_init(dfull, 1);
-    mbar_init(dempty, 8);
+    for (int b = 0; b < 2; b++) {
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dempty[b], 8);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -296,8 +322,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base;
-  // accumulators: matrix m at columns [m * ntile, (m+1) * ntile); scale slots after them
-  const uint32_t sf_col0 = (uint32_t)((NA * ntile + 15) & ~15);
+  // accumulators: buffer b, matrix m at columns (b * NA + m) * ntile; scale slots after them
+  const int ND = a.nacc;
+  const uint32_t sf_col0 = (uint32_t)((ND * NA * ntile + 15) & ~15);
 
   pdl_wait();
   const int nitems = a.tile_off[a.ngroups] * a.mtiles;
@@ -457,8 +484,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else
           idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) |
                   ((uint32_t)(kTcTile >> 4) << 24);
-        // the epilogue must have drained the previous item's accumulator
-        if (!mbar_wait(dempty, (n & 1) ^ 1)) {
+        // the epilogue must have drained this accumulator buffer's previous item
+        const int db = n % ND;
+        if (!mbar_wait(&dempty[db], ((n / ND) & 1) ^ 1)) {
           set_status(a.status, K3MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           ok = false;
@@ -491,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int t = 0; t < NT; t++) {
                   const uint64_t bd = dbase + (uint64_t)(boff + t * tstep + 2 * i);
                   const uint32_t acc = (c > 0 || i > 0 || t > 0) ? 1u : 0u;
-                  const uint32_t dcol = tmem + (uint32_t)(m * ntile);
+                  const uint32_t dcol = tmem + (uint32_t)((db * NA + m) * ntile);
                   if (KIND == 0)
                     mma_mxf4(dcol, ad, bd, idesc, slot + 16 * (NT + m) + 4 * i,
                              slot + 16 * t + 4 * i, acc);
@@ -503,7 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_commit(&empty[s]);
         }
-        tc_commit(dfull);
+        tc_commit(&dfull[db]);
       }
       // before the accumulator is freed: wait (bounded) for every MMA issued
       if (!ok && it > 0) {
@@ -519,7 +547,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float ib1 = 1.f / a.b1, ib2 = 1.f / a.b2;
     for (int n = 0; n < my_items; n++) {
       const TcItem ti = item_at(n);
-      const bool got = mbar_wait(dfull, n & 1);
+      const int db = n % ND;
+      const bool got = mbar_wait(&dfull[db], (n / ND) & 1);
       if (!got) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
         *abort_flag = 1;
@@ -528,18 +557,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int row = ti.mt * kTcTile + 32 * q + lane;
       const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
       if (got && !*abort_flag) {
+        const uint32_t dbase = tmem + lane_sel + (uint32_t)(db * NA * ntile);
         for (int c0 = half * hcols; c0 < (half + 1) * hcols && c0 < ti.nvalid; c0 += 16) {
-          float d0[16], d1[16];
-          tmem_ld_x16(tmem + lane_sel + (uint32_t)c0, d0);
-          if (NA > 1) tmem_ld_x16(tmem + lane_sel + (uint32_t)(ntile + c0), d1);
+          uint32_t d0[16], d1[16];
+          tmem_ld16_nowait(dbase + (uint32_t)c0, d0);
+          if (NA > 1) tmem_ld16_nowait(dbase + (uint32_t)(ntile + c0), d1);
+          tmem_wait_ld2(d0, d1);
           if (row < a.M_rows) {
+            float *orow = a.out + (long long)(ti.brow0 + c0) * a.out_ld + row;
 #pragma unroll
             for (int j = 0; j < 16; j++) {
-              const int col = c0 + j;
-              if (col < ti.nvalid) {
-                float v = d0[j];
-                if (EPI == 0) v = situ_fast(d0[j], d1[j], a.b1, ib1, a.b2, ib2);
-                a.out[(long long)(ti.brow0 + col) * a.out_ld + row] = v;
+              if (c0 + j < ti.nvalid) {
+                float v = __uint_as_float(d0[j]);
+                if (EPI == 0)
+                  v = situ_fast(v, __uint_as_float(d1[j]), a.b1, ib1, a.b2, ib2);
+                orow[(long long)j * a.out_ld] = v;
               }
             }
           }
@@ -547,7 +579,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dempty);
+      if (lane == 0) mbar_arrive(&dempty[db]);
       if (!got) break;
     }
   }
@@ -621,6 +653,13 @@ static void tc_depths(int na, int nt, int ntile, bool scales, int *ns, int *nsf)
   *nsf = f;
 }
 
+// Accumulator buffers: two (the epilogue of one item overlaps the next item's MMAs) when
+// they fit in TMEM next to the scale slots, else one.
+static int tc_nacc(int na, int nt, int ntile, bool scales, int ns) {
+  const int sf = scales ? ns * 16 * (na + nt) : 0;
+  return (((2 * na * ntile + 15) & ~15) + sf <= kTcTmemCols) ? 2 : 1;
+}
+
 template <int KIND, int NA, int NT, int EPI>
 static cudaError_t launch_tc(const TcGemmArgs &a, const CUtensorMap &A0, const CUtensorMap &A1,
                              const CUtensorMap &B, int grid, cudaStream_t st) {
@@ -637,6 +676,7 @@ static cudaError_t launch_tc(const TcGemmArgs &a, const CUtensorMap &A0, const C
   TcGemmArgs aa = a;
   aa.nstages = ns;
   aa.nsf = nsf;
+  aa.nacc = tc_nacc(NA, NT, a.ntile, KIND == 0, ns);
   fn<<<grid, kTcThreads, smem, st>>>(aa, A0, A1, B);
   return cudaGetLastError();
 }
@@ -645,8 +685,8 @@ cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &
                            const CUtensorMap &A1, const CUtensorMap &B, int grid,
                            cudaStream_t st) {
   switch (kind) {
-    case TcKind::kMxf4GateUp: return launch_tc<0, 2, 4, 0>(a, A0, A1, B, grid, st);
-    case TcKind::kMxf4Down: return launch_tc<0, 1, 5, 1>(a, A0, A1, B, grid, st);
+    case TcKind::kMxf4GateUp: return launch_tc<0, 2, kTcTermsX, 0>(a, A0, A1, B, grid, st);
+    case TcKind::kMxf4Down: return launch_tc<0, 1, kTcTermsAct, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16GateUp: return launch_tc<1, 2, 1, 0>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Down: return launch_tc<1, 1, 2, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Store: return launch_tc<1, 1, 1, 1>(a, A0, A1, B, grid, st);
