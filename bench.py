@@ -342,6 +342,162 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+BATCH_WORKLOADS = {
+    "decode64_zipf": "decode64_zipf: 64 tokens/step through one full-shape MoE layer, expert "
+                     "popularity Zipf(1.1) through the correction bias",
+    "prefill4096": "prefill4096: 4096 tokens/step through one full-shape MoE layer, uniform "
+                   "routing (grouped MXFP4 GEMM on tcgen05)",
+    "stacked8": "stacked8: 1 token/step through 8 stacked full-shape MoE layers (126 GB of "
+                "MXFP4 resident) with RMSNorm and the residual stream between them",
+}
+
+
+def useful_flops(cfg, P, T):
+    """Multiply-adds x 2 of the expert GEMMs for P (token, slot) pairs and T tokens."""
+    H, I, SI = cfg.hidden, cfg.inter, cfg.shared_inter
+    return 2.0 * P * 3 * H * I + 2.0 * T * 3 * H * SI
+
+
+def run_batch(args):
+    """The multi-token and stacked workloads (one JSON line each, same contract)."""
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    import synth
+    import synth.device as sd
+    import mxfp4_routed_expert_02_gb300 as k3
+
+    name = args.workload
+    cfg = synth.config("decode1" if name == "stacked8" else name)
+    L = 8 if name == "stacked8" else 1
+    T = 1 if name == "stacked8" else cfg.tokens
+    seed = 0
+    dev = torch.device("cuda", local)
+    H, I, E, K = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
+    dims = k3.LayerDims(H, I, E, K, cfg.shared_inter)
+    stride = (cfg.record_bytes + 4095) // 4096 * 4096
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    layers = []
+    for l in range(L):
+        ex = torch.empty(E * stride, dtype=torch.uint8, device=dev)
+        sd.fill_experts(ex, cfg, seed, l, stride=stride)
+        w = synth.layer_weights(cfg, seed, l)
+        layers.append(dict(wr=t(w["wr"].view(np.int16)), bias=t(w["bias"]), experts=ex,
+                           stride=stride, sh_gate=t(w["sh_gate"].view(np.int16)),
+                           sh_up=t(w["sh_up"].view(np.int16)),
+                           sh_down=t(w["sh_down"].view(np.int16))))
+    ws = k3.new_workspace(dims, T, dev)
+    status = k3.new_status(dev)
+    NX = 4
+    xs_host = [synth.activations(cfg, seed + 1 + rank * NX + j, T) for j in range(NX)]
+    xs = [t(a.view(np.int16)) for a in xs_host]
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    idx = torch.empty((L, T, K), dtype=torch.int32, device=dev)
+    wts = torch.empty((L, T, K), dtype=torch.float32, device=dev)
+    h = torch.empty((T, H), dtype=torch.float32, device=dev)
+    h.copy_(torch.from_numpy((xs_host[0].astype(np.uint32) << 16).view(np.float32)).to(dev))
+    xsc = torch.empty((T, H), dtype=torch.int16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    lw = layers[0]
+
+    def step(s):
+        if name == "stacked8":
+            k3.k3moe_decode_stack(dims, layers, h, xsc, ws, status, eps=cfg.rms_eps,
+                                  idx_out=idx, w_out=wts)
+        else:
+            k3.k3moe_layer(dims, xs[s % NX], lw["wr"], lw["bias"], lw["experts"], stride,
+                           lw["sh_gate"], lw["sh_up"], lw["sh_down"], y, ws, status,
+                           idx_out=idx[0], w_out=wts[0])
+
+    for s in range(args.warmup):
+        if name != "stacked8":
+            flush.fill_(s & 255)
+        step(s)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = Clocks("/tmp/k3moe_bench_clocks_%d_%d.csv" % (os.getpid(), rank))
+    with clocks:
+        for s in range(args.steps):
+            if name != "stacked8":
+                flush.fill_((s + 7) & 255)
+            ev[s][0].record(stream)
+            step(args.warmup + s)
+            ev[s][1].record(stream)
+        torch.cuda.synchronize()
+    assert status.item() == 0, k3.status_str(status.item())
+    ms = [a.elapsed_time(b) for a, b in ev]
+    t_dev = sum(ms) / 1e3
+    # per-kernel device time from a traced pass
+    k3.k3moe_trace_enable(True)
+    for s in range(min(args.steps, 3)):
+        step(args.warmup + s)
+    torch.cuda.synchronize()
+    trace = k3.k3moe_trace_read()
+    k3.k3moe_trace_enable(False)
+    nsteps_tr = min(args.steps, 3)
+    kernels = {k: {"ms_avg": v[0] / v[1], "launches_per_step": v[1] / nsteps_tr}
+               for k, v in trace.items() if v[1]}
+    launches = int(sum(v[1] for v in trace.values()) / nsteps_tr * args.steps)
+    # distinct experts of the last step, per layer
+    ids = idx.cpu().numpy()
+    U = [len(set(ids[l].ravel().tolist())) for l in range(L)]
+    op = I * H // 2 + I * H // 32
+    layer_bytes = [u * 3 * op + E * H * 2 + 3 * cfg.shared_inter * H * 2 + T * H * 6 for u in U]
+    step_bytes_v = sum(layer_bytes)
+    pk = peaks()
+    peak_hbm = pk["hbm_gbs"] if pk else 6800.0
+    peak_bf16 = pk["bf16_tflops"] if pk else 1900.0
+    sec = t_dev / args.steps
+    if name == "prefill4096":
+        P = T * K
+        fl = useful_flops(cfg, P, T)
+        gk = kernels.get("k_tc_gemm_gateup", {}).get("ms_avg")
+        dk = kernels.get("k_tc_gemm_down", {}).get("ms_avg")
+        gfl = 2.0 * P * 2 * H * I
+        roofline = {"bound": "tensor", "kernel": "k_tc_gemm_gateup",
+                    "achieved": gfl / (gk * 1e-3) / 1e12, "peak": 6 * peak_bf16,
+                    "unit": "TFLOP/s", "frac": gfl / (gk * 1e-3) / 1e12 / (6 * peak_bf16),
+                    "traffic": None,
+                    "peak_source": "MXFP4 dense = measured bf16 x 6 (nominal 13.5 / 2.25)",
+                    "useful_flops": gfl,
+                    "issued_mma_flops": gfl * k3.k3moe.TC_TERMS_X,
+                    "hbm_frac_step": step_bytes_v / sec / 1e9 / peak_hbm}
+        extra = {"useful_tflops_step": fl / sec / 1e12,
+                 "down_kernel_tflops": 2.0 * P * H * I / (dk * 1e-3) / 1e12 if dk else None}
+    else:
+        dom = "k_tc_gemm_gateup" if name == "decode64_zipf" else "k_gateup_t1"
+        dk = kernels.get(dom, {}).get("ms_avg")
+        db = sum(u * 2 * op for u in U) / L
+        roofline = {"bound": "hbm", "kernel": dom,
+                    "achieved": db / (dk * 1e-3) / 1e9 if dk else None, "peak": peak_hbm,
+                    "unit": "GB/s", "frac": db / (dk * 1e-3) / 1e9 / peak_hbm if dk else None,
+                    "traffic": None, "algorithmic_bytes": db,
+                    "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else
+                                   "fallback 6.8 TB/s (of fallback)"}
+        extra = {}
+    lat = sorted(ms)
+    line = {
+        "metric": METRIC, "value": T * args.steps * world / t_dev, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": BATCH_WORKLOADS[name], "tokens_per_step": T, "layers": L,
+                   "seed": seed, "distinct_experts_per_layer": U,
+                   "l2": ("inputs larger than L2 (2.9 GB of weights per step)" if L > 1 else
+                          "flushed between timed steps (256 MB write)")},
+        "hbm_gbs_step": step_bytes_v / sec / 1e9,
+        "algorithmic_bytes_per_step": step_bytes_v,
+        "latency_ms": {"p50": lat[len(lat) // 2], "p99": lat[min(len(lat) - 1, int(len(lat) * 0.99))]},
+        "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
+        "clocks": clocks.summary(local), "cpu_baseline": None,
+    }
+    line.update(extra)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,6 +505,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode1",
+                    choices=["decode1", "decode64_zipf", "prefill4096", "stacked8"])
     ap.add_argument("--experts", type=int, default=896,
                     help="routed experts resident (896 = the workload; fewer only to keep "
                          "profiler captures small)")
@@ -357,6 +515,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "decode1":
+        run_batch(args)
     else:
         run_ours(args)
 

@@ -179,6 +179,29 @@ k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *
                                         k3moe_dtype ydt, int32_t accumulate,
                                         int32_t *status_dev, k3moe_stream_t stream);
 
+/* Weights of one layer of a stack (the arguments k3moe_layer takes for it). */
+typedef struct {
+    const uint16_t *wr_bf16;  /* [E][H] */
+    const float *bias;        /* [E] or NULL */
+    k3moe_experts experts;
+    const uint16_t *sh_gate, *sh_up, *sh_down;  /* NULL when shared_inter == 0 */
+} k3moe_layer_weights;
+
+/* Decode through L stacked MoE layers with the residual stream between them (the
+ * decoder loop of kimi-k3-in-c, section 5 for RMSNorm and section 9 for the layer): for
+ * l = 0 .. L-1,
+ *     x = bf16(RMSNorm(h))        (k3moe_rmsnorm_bf16 with eps; weight 1)
+ *     h = h + layer_l(x)          (k3moe_layer, float output added to h)
+ * h float [T][H] is updated in place; x_scratch bf16 [T][H] is caller scratch;
+ * idx_out / w_out ([L][T][K] each) receive every layer's route when not NULL.
+ * layers is a HOST array of L entries (device pointers inside).  Needs
+ * k3moe_workspace_size(dims, T) bytes of workspace, shared by the layers in turn.     */
+k3moe_status k3moe_decode_stack(const k3moe_dims *dims, int32_t L,
+                                const k3moe_layer_weights *layers, int32_t T, float *h,
+                                float eps, uint16_t *x_scratch, int32_t *idx_out, float *w_out,
+                                void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                k3moe_stream_t stream);
+
 /* RMSNorm then bf16 (kimi-k3-in-c, section 5): for each of T rows of width n,
  *   inv = 1 / sqrt(mean(h^2) + eps) (sum of squares in double), out = bf16(h * inv),
  * round to nearest even.  h float [T][n], out bf16 [T][n].  The step between stacked

@@ -877,6 +877,33 @@ k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *
                      stream);
 }
 
+// The stacked decode loop: per layer, RMSNorm of the residual stream into bf16, then the
+// layer step added to the stream (k3moe_layer with accumulate).
+k3moe_status k3moe_decode_stack(const k3moe_dims *dims, int32_t L,
+                                const k3moe_layer_weights *layers, int32_t T, float *h,
+                                float eps, uint16_t *x_scratch, int32_t *idx_out, float *w_out,
+                                void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                k3moe_stream_t stream) {
+  k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (L < 1 || T < 0 || !layers) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!h || !x_scratch || !workspace || !status_dev) return K3MOE_ERR_ARG;
+  if ((idx_out == nullptr) != (w_out == nullptr)) return K3MOE_ERR_ARG;
+  const int H = dims->hidden, K = dims->topk;
+  for (int l = 0; l < L; l++) {
+    s = k3moe_rmsnorm_bf16(h, T, H, eps, x_scratch, stream);
+    if (s != K3MOE_OK) return s;
+    const k3moe_layer_weights &lw = layers[l];
+    const size_t ro = (size_t)l * T * K;
+    s = k3moe_layer(dims, x_scratch, T, lw.wr_bf16, lw.bias, &lw.experts, lw.sh_gate, lw.sh_up,
+                    lw.sh_down, idx_out ? idx_out + ro : nullptr, w_out ? w_out + ro : nullptr, h,
+                    K3MOE_F32, 1, workspace, ws_bytes, status_dev, stream);
+    if (s != K3MOE_OK) return s;
+  }
+  return K3MOE_OK;
+}
+
 k3moe_status k3moe_rmsnorm_bf16(const float *h, int32_t T, int32_t n, float eps, uint16_t *out,
                                 k3moe_stream_t stream) {
   if (T < 0 || n < 1 || !(eps >= 0.f)) return K3MOE_ERR_ARG;

@@ -19,6 +19,8 @@ STATUS_NAMES = {
     6: "ERR_TIMEOUT", 7: "ERR_BAD_EXPERT", 8: "ERR_NONFINITE", 9: "ERR_SCRATCH_LIMIT",
 }
 K3MOE_ERR_SCRATCH_LIMIT = 9
+# MXFP4 terms of the activations in the multi-token path (x, SiTU output); informational.
+TC_TERMS_X, TC_TERMS_ACT = 4, 4
 # Bytes of the library's static scratch array (K3MOE_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 F32, BF16 = 0, 1
@@ -26,7 +28,7 @@ F32, BF16 = 0, 1
 # Every symbol include/k3moe.h declares.
 EXPORTS = (
     "k3moe_record_layout", "k3moe_workspace_size", "k3moe_route", "k3moe_expert_ffn_mxfp4",
-    "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4", "k3moe_trace_enable",
+    "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_decode_stack", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4", "k3moe_trace_enable",
     "k3moe_trace_read", "k3moe_status_str",
 )
 
@@ -47,6 +49,12 @@ class Dims(ctypes.Structure):
 
 class Experts(ctypes.Structure):
     _fields_ = [("experts", ctypes.c_void_p), ("expert_stride", ctypes.c_int64)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("wr_bf16", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("experts", Experts),
+                ("sh_gate", ctypes.c_void_p), ("sh_up", ctypes.c_void_p),
+                ("sh_down", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -84,6 +92,9 @@ def lib(build_if_missing: bool = True):
     L.k3moe_layer_static_scratch.restype = i32
     L.k3moe_layer_static_scratch.argtypes = [dp, vp, i32, vp, vp, ep, vp, vp, vp, vp, vp, vp,
                                              i32, i32, vp, vp]
+    L.k3moe_decode_stack.restype = i32
+    L.k3moe_decode_stack.argtypes = [dp, i32, ctypes.POINTER(LayerWeights), i32, vp,
+                                     ctypes.c_float, vp, vp, vp, vp, sz, vp, vp]
     L.k3moe_rmsnorm_bf16.restype = i32
     L.k3moe_rmsnorm_bf16.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
     L.k3moe_dequant_mxfp4.restype = i32
@@ -229,6 +240,29 @@ def k3moe_layer_static_scratch(dims: LayerDims, x, wr, bias, experts, expert_str
         ctypes.byref(d), _ptr(x), T, _ptr(wr), _ptr(bias), ctypes.byref(ex), _ptr(sh_gate),
         _ptr(sh_up), _ptr(sh_down), _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
         int(bool(accumulate)), _ptr(status), _stream(stream)))
+
+
+def k3moe_decode_stack(dims: LayerDims, layers, h, x_scratch, workspace, status, eps: float = 1e-5,
+                       idx_out=None, w_out=None, stream=None):
+    """h (float [T][H], updated in place) through the stacked layers; ``layers`` is a
+    list of dicts with wr, bias, experts, stride and (optional) sh_gate, sh_up, sh_down."""
+    d = dims.c()
+    arr = (LayerWeights * len(layers))()
+    keep = []
+    for i, lw in enumerate(layers):
+        wr = _bits16(lw["wr"], "wr")
+        sh = [lw.get(k) for k in ("sh_gate", "sh_up", "sh_down")]
+        sh = [None if t is None else _bits16(t, k) for t, k in zip(sh, ("sh_gate", "sh_up", "sh_down"))]
+        keep += [wr] + sh
+        arr[i] = LayerWeights(_ptr(wr), _ptr(lw.get("bias")),
+                              Experts(ctypes.c_void_p(lw["experts"].data_ptr()), int(lw["stride"])),
+                              *[_ptr(t) for t in sh])
+    T = h.shape[0]
+    x_scratch = _bits16(x_scratch, "x_scratch")
+    _check("k3moe_decode_stack", lib().k3moe_decode_stack(
+        ctypes.byref(d), len(layers), arr, T, _ptr(h), float(eps), _ptr(x_scratch),
+        _ptr(idx_out), _ptr(w_out), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)))
 
 
 def k3moe_rmsnorm_bf16(h, out, eps: float = 1e-5, stream=None):

@@ -259,6 +259,30 @@ def moe_layer(x_bf16, wr_bf16, bias, get_expert, topk: int, H: int, I: int, sh_g
     return idx, w, y
 
 
+def stacked_decode_step(h, layers, topk: int, H: int, I: int, eps: float = 1e-5,
+                        renorm: bool = True, routed_scale: float = 1.0, b1: float = 4.0,
+                        b2: float = 25.0, nthreads: int = 0):
+    """One token through stacked MoE layers with the residual stream between them.
+
+    The decoder loop of kimi-k3-in-c: RMSNorm with weight 1 (section 5 "Kernels with a
+    floating point contract"), the layer input rounded to bf16 (the page's layers take
+    bf16 activations), the layer step of section 9, and its output added to the residual
+    stream in float.  ``layers`` holds dicts with wr, bias, get_expert and (optional)
+    sh_gate, sh_up, sh_down.  Returns (h_new, [idx per layer], [w per layer]).
+    """
+    h = np.array(h, dtype=np.float32)
+    idxs, ws = [], []
+    for lw in layers:
+        x = f32_to_bf16(rmsnorm(h, eps=eps))
+        idx, w, y = moe_layer(x[None, :], lw["wr"], lw["bias"], lw["get_expert"], topk, H, I,
+                              lw.get("sh_gate"), lw.get("sh_up"), lw.get("sh_down"), renorm,
+                              routed_scale, b1, b2, nthreads=nthreads)
+        h = (h + y[0]).astype(np.float32)
+        idxs.append(idx[0])
+        ws.append(w[0])
+    return h, idxs, ws
+
+
 def num_threads() -> int:
     """Threads the oracle's parallel loops use by default (OpenMP)."""
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
