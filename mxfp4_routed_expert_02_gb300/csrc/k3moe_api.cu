@@ -216,7 +216,7 @@ k3moe_status run_route(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
     TraceScope ts(KID_ROUTER, st);
     const cudaError_t e =
         (Tc == 1) ? launch_router_t1(st, x, H, wr, E, bias, sh_gate, sh_up, SI, d->situ_b1,
-                                     d->situ_b2, ws.sc, ws.ch, ws.act_s, status)
+                                     d->situ_b2, ws.sc, ws.ch, ws.act_s, status, !g_trace.on)
                   : launch_router_shared(tc, grid, (size_t)tc * H * 2, st, x, Tc, H, wr, E, bias,
                                          sh_gate, sh_up, SI, d->situ_b1, d->situ_b2, ws.sc,
                                          ws.ch, ws.act_s, status);
@@ -910,9 +910,21 @@ k3moe_status k3moe_rmsnorm_bf16(const float *h, int32_t T, int32_t n, float eps,
   if (T == 0) return K3MOE_OK;
   if (!h || !out) return K3MOE_ERR_ARG;
   if (!aligned16(h) || !aligned16(out)) return K3MOE_ERR_ALIGN;
-  TraceScope ts(KID_RMSNORM, reinterpret_cast<cudaStream_t>(stream));
-  k_rmsnorm_bf16<<<T, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(h, T, n, eps, out);
-  return launch_status();
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TraceScope ts(KID_RMSNORM, st);
+  // launched as a programmatic dependent (outside tracing): its launch overlaps the tail
+  // of the kernel that wrote h, and the kernel waits for that kernel before reading
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(kRmsThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = g_trace.on ? 0 : 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_bf16, h, T, n, eps, out) == cudaSuccess ? K3MOE_OK
+                                                                                  : K3MOE_ERR_CUDA;
 }
 
 k3moe_status k3moe_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int32_t rows,

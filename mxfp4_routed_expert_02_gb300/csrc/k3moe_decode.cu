@@ -332,6 +332,9 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
   }
   __syncthreads();
   pdl_wait();
+  // the next kernel (a following layer's first kernel) may launch now; it waits for this
+  // grid to complete before it reads anything
+  pdl_launch_dependents();
 
   const int U = a.disp[0];
   const int *uexp = a.disp + 4;

@@ -488,23 +488,64 @@ __global__ void k_dequant(const uint8_t *__restrict__ packed, const uint8_t *__r
 // ------------------------------------------------------------------------------------
 // RMSNorm to bf16 (kimi-k3-in-c, section 5): one CTA per row; sum of squares in double.
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_rmsnorm_bf16(const float *__restrict__ h, int T, int n,
-                                                      float eps, uint16_t *__restrict__ out) {
-  __shared__ double wsum[8];
+__global__ void __launch_bounds__(kRmsThreads) k_rmsnorm_bf16(const float *__restrict__ h, int T,
+                                                              int n, float eps,
+                                                              uint16_t *__restrict__ out) {
+  // Each thread loads its (up to kRmsVec) float4 of the row at once and keeps them for the
+  // output pass; the sum of squares is exact per product in double, reduced in a fixed
+  // tree.  Rows whose width is not a multiple of 4 or above kRmsThreads * 4 * kRmsVec take
+  // the strided loop.
+  __shared__ double wsum[kRmsThreads / 32];
+  __shared__ float s_inv;
   const int t = blockIdx.x;
+  pdl_wait();  // h is written by the previous kernel when launched as a dependent
+  pdl_launch_dependents();
   if (t >= T) return;
   const float *row = h + (size_t)t * n;
+  const bool vec = (n % 4 == 0) && (n <= kRmsThreads * 4 * kRmsVec);
+  float4 v[kRmsVec];
   double ss = 0.0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) ss += (double)row[i] * (double)row[i];
+  if (vec) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+    for (int k = 0; k < kRmsVec; k++) {
+      const int i = threadIdx.x + k * kRmsThreads;
+      v[k] = (4 * i < n) ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kRmsVec; k++)
+      ss += (double)v[k].x * v[k].x + (double)v[k].y * v[k].y + (double)v[k].z * v[k].z +
+            (double)v[k].w * v[k].w;
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) ss += (double)row[i] * (double)row[i];
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
   __syncthreads();
-  double tot = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += wsum[w];
-  const float inv = (float)(1.0 / sqrt(tot / (double)n + (double)eps));
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    out[(size_t)t * n + i] = f32_to_bf16(__fmul_rn(row[i], inv));
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += wsum[w];
+    s_inv = (float)(1.0 / sqrt(tot / (double)n + (double)eps));
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  uint16_t *orow = out + (size_t)t * n;
+  if (vec) {
+#pragma unroll
+    for (int k = 0; k < kRmsVec; k++) {
+      const int i = threadIdx.x + k * kRmsThreads;
+      if (4 * i < n) {
+        const uint32_t lo = (uint32_t)f32_to_bf16(__fmul_rn(v[k].x, inv)) |
+                            ((uint32_t)f32_to_bf16(__fmul_rn(v[k].y, inv)) << 16);
+        const uint32_t hi = (uint32_t)f32_to_bf16(__fmul_rn(v[k].z, inv)) |
+                            ((uint32_t)f32_to_bf16(__fmul_rn(v[k].w, inv)) << 16);
+        reinterpret_cast<uint2 *>(orow)[i] = make_uint2(lo, hi);
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) orow[i] = f32_to_bf16(__fmul_rn(row[i], inv));
+  }
 }
 
 }  // namespace k3

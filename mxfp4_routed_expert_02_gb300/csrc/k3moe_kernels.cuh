@@ -29,7 +29,7 @@ cudaError_t set_router_smem_limits(int bytes);
 cudaError_t launch_router_t1(cudaStream_t st, const uint16_t *x, int H, const uint16_t *wr,
                              int E, const float *bias, const uint16_t *sh_gate,
                              const uint16_t *sh_up, int SI, float b1, float b2, float *sc,
-                             float *ch, float *act_s, int32_t *status);
+                             float *ch, float *act_s, int32_t *status, bool pdl);
 
 __global__ void k_topk(const float *__restrict__ scores, const float *__restrict__ choice, int T,
                        int E, int K, int renorm, float routed_scale, int32_t *__restrict__ idx,
@@ -106,6 +106,8 @@ __global__ void k_dequant(const uint8_t *__restrict__ packed, const uint8_t *__r
 
 __global__ void k_rmsnorm_bf16(const float *__restrict__ h, int T, int n, float eps,
                                uint16_t *__restrict__ out);
+constexpr int kRmsThreads = 256;  // threads per row of k_rmsnorm_bf16
+constexpr int kRmsVec = 8;        // float4 per thread held in registers (rows up to 8192)
 
 }  // namespace k3
 

@@ -261,12 +261,21 @@ __global__ void __launch_bounds__(256) k_router_t1(const uint16_t *__restrict__ 
 cudaError_t launch_router_t1(cudaStream_t st, const uint16_t *x, int H, const uint16_t *wr,
                              int E, const float *bias, const uint16_t *sh_gate,
                              const uint16_t *sh_up, int SI, float b1, float b2, float *sc,
-                             float *ch, float *act_s, int32_t *status) {
+                             float *ch, float *act_s, int32_t *status, bool pdl) {
   const int Ep = E + (E & 1);
   const int units = Ep + 2 * SI;
-  k_router_t1<<<(units + 7) / 8, 256, (size_t)H * 2, st>>>(x, H, wr, E, bias, sh_gate, sh_up, SI,
-                                                          b1, b2, sc, ch, act_s, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((units + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = (size_t)H * 2;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_router_t1, x, H, wr, E, bias, sh_gate, sh_up, SI, b1, b2, sc,
+                            ch, act_s, status);
 }
 
 cudaError_t launch_router_shared(int tc, int grid, size_t smem, cudaStream_t st, const uint16_t *x,
