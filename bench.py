@@ -37,8 +37,9 @@ TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode.cu",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_device.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_topk.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_kernels.cuh"]
-TRAFFIC_CAPTURED = {"sources": "b8ab8a1046096a01",
-                    "bytes": {"k_gateup_t1": 190563840, "k_down_tma": 126093824}}
+TRAFFIC_CAPTURED = {"sources": "d9c26cc9dfd3b3cd",
+                    "bytes": {"k_gateup_t1": 190744320, "k_down_tma": 126194944,
+                              "k_router_t1": 45018368}}
 
 
 def traffic_of(kernel):
@@ -369,8 +370,10 @@ def run_batch(args):
 
     name = args.workload
     cfg = synth.config("decode1" if name == "stacked8" else name)
+    if args.experts != cfg.n_experts:   # smaller expert pool: profiling captures only
+        cfg = synth.config(cfg.name, n_experts=args.experts)
     L = 8 if name == "stacked8" else 1
-    T = 1 if name == "stacked8" else cfg.tokens
+    T = 1 if name == "stacked8" else (args.tokens or cfg.tokens)
     seed = 0
     dev = torch.device("cuda", local)
     H, I, E, K = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
@@ -507,6 +510,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="decode1",
                     choices=["decode1", "decode64_zipf", "prefill4096", "stacked8"])
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per step of a batch workload (0 = the workload's own; "
+                         "other values only for small profiler captures)")
     ap.add_argument("--experts", type=int, default=896,
                     help="routed experts resident (896 = the workload; fewer only to keep "
                          "profiler captures small)")
