@@ -230,20 +230,21 @@ k3moe_status run_route(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
   return launch_status();
 }
 
-// Row-block size of the single-token gate/up kernel: 4 rows if 4 rows of scale bytes are
-// 16-byte multiples, else 8 or 16; 0 if the kernel does not apply (fewer than 32 or more
+// Row-block size of the single-token gate/up kernel: 8 rows (fewer, larger stages: less
+// per-stage work in the consumers and larger bulk copies) when 8 rows of scale bytes are
+// a 16-byte multiple, else 16; 0 if the kernel does not apply (fewer than 32 or more
 // than 224 groups per row, or a stage above 64 KB).
 int t1_row_block(int H) {
   const int G = H / kGroup;
   if (G < 32 || G > 224) return 0;
-  const int rb = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 8 : 16;
+  const int rb = (G % 2 == 0) ? 8 : 16;
   if ((size_t)2 * rb * (H / 2 + G) > 64 * 1024) return 0;
   return rb;
 }
 
 // Ring slots of the bulk-copy down kernel for this shape (0: use the register kernel) and
 // whether the activations of all pairs are staged in its shared memory.
-int down_slots(int I, int Tc, int K, bool *act_smem) {
+int down_slots(int I, int Tc, int K, int ntl, bool *act_smem) {
   const int G2 = I / kGroup;
   *act_smem = false;
   if (G2 % 16 != 0 || G2 / 16 > 8) return 0;
@@ -251,12 +252,12 @@ int down_slots(int I, int Tc, int K, bool *act_smem) {
   const size_t stage = (size_t)8 * (I / 2 + G2);  // 8-row half tiles
   const size_t avail = 227 * 1024;
   // one slot per consumer warp (16): all of them when they fit
-  const size_t fa = down_tma_smem(I, Tc, P, 0, true);
+  const size_t fa = down_tma_smem(I, Tc, P, 0, true, ntl);
   if (fa + 16 * stage <= avail) {
     *act_smem = true;
     return 16;
   }
-  const size_t fg = down_tma_smem(I, Tc, P, 0, false);
+  const size_t fg = down_tma_smem(I, Tc, P, 0, false, ntl);
   if (fg + stage > avail) return 0;
   const int ns = (int)((avail - fg) / stage);
   return ns > 16 ? 16 : ns;
@@ -282,7 +283,9 @@ k3moe_status run_down(const DeviceInfo *di, const k3moe_dims *d, int Tc, const E
   const int P = Tc * K;
   const int LR = down_lanes(I);
   bool act_smem = false;
-  const int ns = down_slots(I, Tc, K, &act_smem);
+  int dgrid = H / kDownRows;
+  if (dgrid > di->sms) dgrid = di->sms;
+  const int ns = down_slots(I, Tc, K, (H / kDownRows + dgrid - 1) / dgrid, &act_smem);
   TraceScope ts(ns >= 1 ? KID_DOWN_TMA : KID_DOWN, st);
   if (ns >= 1) {
     DownArgs a;
@@ -293,9 +296,7 @@ k3moe_status run_down(const DeviceInfo *di, const k3moe_dims *d, int Tc, const E
     a.sh_down = sh_down; a.SI = sh_down ? d->shared_inter : 0; a.act_s = ws.act_s;
     a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate; a.LR = LR; a.NS = ns;
     a.status = status;
-    int grid = H / kDownRows;
-    if (grid > di->sms) grid = di->sms;
-    return launch_down_tma(a, grid, st, pdl, act_smem) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+    return launch_down_tma(a, dgrid, st, pdl, act_smem) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
   }
   const size_t dsmem = ((size_t)P * kDownRows + 256 * kDownRows + (size_t)Tc * kDownRows) * 4;
   k_down_combine<<<H / kDownRows, 256, dsmem, st>>>(Tc, H, I, K, ea, idx, w, ws.disp, P,

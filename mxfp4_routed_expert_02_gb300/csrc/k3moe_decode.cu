@@ -309,11 +309,14 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + 32;
   uint64_t *actbar = empty + 32;
+  const int ntl = (ntiles + gridDim.x - 1) / gridDim.x;  // row tiles per CTA (at most)
   float *dbuf = reinterpret_cast<float *>(smem + 1024);   // [P][16]
-  float *ds = dbuf + (size_t)P * kDownRows;               // [T][16]
+  float *ds = dbuf + (size_t)P * kDownRows;               // [ntl][T][16] shared-expert rows
+  float *wsm = ds + (size_t)ntl * T * kDownRows;          // [P] route weights
   // byte offsets inside the dynamic shared array (kept as smem + offset so the compiler
   // sees shared-space accesses)
-  const size_t o_act = (1024 + ((size_t)P * kDownRows + (size_t)T * kDownRows) * 4 + 127) & ~size_t(127);
+  const size_t o_act = (1024 + ((size_t)P * kDownRows + (size_t)ntl * T * kDownRows + P) * 4 +
+                        127) & ~size_t(127);
   const size_t n_act = ACT_SMEM ? (size_t)P * I * 2 : 0;
   uint16_t *s_hi = reinterpret_cast<uint16_t *>(smem + o_act);      // [P][I] (ACT_SMEM)
   uint16_t *s_lo = reinterpret_cast<uint16_t *>(smem + o_act + n_act);
@@ -397,11 +400,42 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
   const uint16_t *act_lo = ACT_SMEM ? s_lo : a.act_lo;
   const int32_t *act_ex = ACT_SMEM ? s_ex : a.act_ex;
 
-  int it0 = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int r0 = tile * kDownRows;
-    const int srow = tid >> 5, ls = lane;  // shared expert: one warp per row
+  // Before the first tile, while the ring fills: the route weights into shared memory and
+  // the shared expert's rows of every tile of this CTA (bf16 weights, prefetched into L2
+  // by the producer, x fp32 activations; one warp per row).
+  for (int i = tid; i < P; i += NC) wsm[i] = a.w[i];
+  if (a.sh_down != nullptr) {
     const int nch = a.SI >> 3;
+    for (int n = 0; n < ntl; n++) {
+      const int tile = blockIdx.x + n * gridDim.x;
+      if (tile >= ntiles) break;
+      const int row = tile * kDownRows + warp;  // warp < 16 = kDownRows
+      const uint4 *w4 = reinterpret_cast<const uint4 *>(a.sh_down + (size_t)row * a.SI);
+      for (int t = 0; t < T; t++) {
+        const float4 *a4 = reinterpret_cast<const float4 *>(a.act_s + (size_t)t * a.SI);
+        float sacc = 0.f;
+        for (int c = lane; c < nch; c += 32) {
+          const uint4 wv = __ldg(w4 + c);
+          const float4 a0 = a4[2 * c], a1 = a4[2 * c + 1];
+          sacc = fmaf(bf16_lo(wv.x), a0.x, sacc);
+          sacc = fmaf(bf16_hi(wv.x), a0.y, sacc);
+          sacc = fmaf(bf16_lo(wv.y), a0.z, sacc);
+          sacc = fmaf(bf16_hi(wv.y), a0.w, sacc);
+          sacc = fmaf(bf16_lo(wv.z), a1.x, sacc);
+          sacc = fmaf(bf16_hi(wv.z), a1.y, sacc);
+          sacc = fmaf(bf16_lo(wv.w), a1.z, sacc);
+          sacc = fmaf(bf16_hi(wv.w), a1.w, sacc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+        if (lane == 0) ds[((size_t)n * T + t) * kDownRows + warp] = sacc;
+      }
+    }
+  }
+
+  int it0 = 0, ntl_i = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ntl_i++) {
+    const int r0 = tile * kDownRows;
     for (int i = tid; i < P * kDownRows; i += NC) dbuf[i] = 0.f;
     asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
     // this warp's stages of the tile: those in its own slot (it % NS == warp)
@@ -459,38 +493,14 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
     }
     it0 += 2 * U;
 
-    // shared expert rows r0..r0+15: bf16 weights (prefetched into L2 by the producer at
-    // the start of the tile) x fp32 activations; one warp per row
-    if (a.sh_down != nullptr && srow < kDownRows) {
-      const uint4 *w4 = reinterpret_cast<const uint4 *>(a.sh_down + (size_t)(r0 + srow) * a.SI);
-      for (int t = 0; t < T; t++) {
-        const float4 *a4 = reinterpret_cast<const float4 *>(a.act_s + (size_t)t * a.SI);
-        float sacc = 0.f;
-        for (int c = ls; c < nch; c += 32) {
-          const uint4 wv = __ldg(w4 + c);
-          const float4 a0 = a4[2 * c], a1 = a4[2 * c + 1];
-          sacc = fmaf(bf16_lo(wv.x), a0.x, sacc);
-          sacc = fmaf(bf16_hi(wv.x), a0.y, sacc);
-          sacc = fmaf(bf16_lo(wv.y), a0.z, sacc);
-          sacc = fmaf(bf16_hi(wv.y), a0.w, sacc);
-          sacc = fmaf(bf16_lo(wv.z), a1.x, sacc);
-          sacc = fmaf(bf16_hi(wv.z), a1.y, sacc);
-          sacc = fmaf(bf16_lo(wv.w), a1.z, sacc);
-          sacc = fmaf(bf16_hi(wv.w), a1.w, sacc);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
-        if (ls == 0) ds[t * kDownRows + srow] = sacc;
-      }
-    }
     asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
 
     for (int q = tid; q < T * kDownRows; q += NC) {
       const int t = q / kDownRows, row = q % kDownRows;
       float sum = 0.f;
       for (int j = 0; j < K; j++)
-        sum = __fadd_rn(sum, __fmul_rn(a.w[t * K + j], dbuf[(size_t)(t * K + j) * kDownRows + row]));
-      if (a.sh_down != nullptr) sum = __fadd_rn(sum, ds[t * kDownRows + row]);
+        sum = __fadd_rn(sum, __fmul_rn(wsm[t * K + j], dbuf[(size_t)(t * K + j) * kDownRows + row]));
+      if (a.sh_down != nullptr) sum = __fadd_rn(sum, ds[((size_t)ntl_i * T + t) * kDownRows + row]);
       const size_t o = (size_t)t * H + r0 + row;
       if (aborted) sum = 0.f;
       if (a.ydt == K3MOE_F32) {
@@ -506,11 +516,13 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
   }
 }
 
-// Shared memory of k_down_tma: barriers, dbuf, ds, [activations], NS ring slots.
-size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem) {
+// Shared memory of k_down_tma for ntl row tiles per CTA: barriers, dbuf, shared-expert
+// rows, route weights, [activations], NS ring slots.
+size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem, int ntl) {
   const int G2 = I / kGroup;
   const size_t stage = (size_t)kDnStageRows * (I / 2 + G2);
-  size_t b = (1024 + ((size_t)P * kDownRows + (size_t)T * kDownRows) * 4 + 127) & ~size_t(127);
+  size_t b = (1024 + ((size_t)P * kDownRows + (size_t)ntl * T * kDownRows + P) * 4 + 127) &
+             ~size_t(127);
   if (act_smem) b += (size_t)P * I * 4 + (size_t)P * G2 * 4;
   b = (b + 127) & ~size_t(127);
   return b + NS * stage;
@@ -521,7 +533,8 @@ cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool p
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDnWarps * 32 + 32);
-  cfg.dynamicSmemBytes = down_tma_smem(a.I, a.T, a.P, a.NS, act_smem);
+  cfg.dynamicSmemBytes =
+      down_tma_smem(a.I, a.T, a.P, a.NS, act_smem, (a.H / kDownRows + grid - 1) / grid);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -137,6 +137,10 @@ __host__ __device__ __forceinline__ size_t act_index(int i, int I, int gg, int k
 // is the E8M0 scale byte and ex the exponent the activation group was scaled by; a
 // scale byte of 255 contributes nothing.
 __device__ __forceinline__ float group_factor(uint32_t s, int ex) {
+  // normal results (biased exponent s + ex in 1..254) are the exponent bits themselves;
+  // subnormal, overflowing and s = 255 cases take the general path
+  const uint32_t b = (uint32_t)((int)s + ex);
+  if (s != 255u && b - 1u < 254u) return __uint_as_float(b << 23);
   return (s == 255u) ? 0.f : pow2i((int)s - 127 + ex);
 }
 

@@ -96,7 +96,7 @@ struct DownArgs {
 
 size_t gateup_t1_smem(int H, int E, int K, int RB, int NS);
 cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl);
-size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem);
+size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem, int ntl);
 cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool pdl,
                             bool act_smem);
 cudaError_t set_decode_smem_limits();
