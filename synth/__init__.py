@@ -78,9 +78,10 @@ class Config:
         return self.inter * self.n_shared
 
 
-# Bias strength for the Zipf(1.1) decode workload; derived by synth/calibrate_zipf.py
-# (a seeded simulation of iid N(0,1) router logits over 10^5 tokens).
-ZIPF_BETA_1P1 = 0.0625
+# Bias strength for the Zipf(1.1) decode workload, from tests/golden/zipf_calibration.py:
+# routing 4096 seeded tokens with this bias gives selection counts whose log-log slope
+# against the popularity rank is -1.1 over ranks 17..256 (tests/golden/zipf_beta.json).
+ZIPF_BETA_1P1 = 0.0551
 
 CONFIGS = {
     "tiny": Config("tiny", 256, 128, 16, 2, 4),
@@ -190,13 +191,20 @@ def activations(cfg: Config, seed: int, tokens: int = None) -> np.ndarray:
     return normal_bf16(seed, 0, T_X, (T, cfg.hidden), 1.0)
 
 
-def zipf_bias(cfg: Config, seed: int, layer: int) -> np.ndarray:
-    """Correction bias making expert popularity follow Zipf(s): a seeded permutation
-    ranks the experts, bias_e = beta ln(p_e / p_max) + U(-0.1, 0.1), p_e ~ rank^-s."""
+def zipf_ranks(cfg: Config, seed: int, layer: int) -> np.ndarray:
+    """Popularity rank (1 = most popular) of every expert: a seeded permutation."""
     E = cfg.n_experts
     perm = _rng(seed, layer, T_ZIPF_PERM).permutation(E)
     rank = np.empty(E, dtype=np.int64)
     rank[perm] = np.arange(1, E + 1)
+    return rank
+
+
+def zipf_bias(cfg: Config, seed: int, layer: int) -> np.ndarray:
+    """Correction bias making expert popularity follow Zipf(s): a seeded permutation
+    ranks the experts, bias_e = beta ln(p_e / p_max) + U(-0.1, 0.1), p_e ~ rank^-s."""
+    E = cfg.n_experts
+    rank = zipf_ranks(cfg, seed, layer)
     logp = -cfg.zipf_s * np.log(rank.astype(np.float64))
     jit = _rng(seed, layer, T_ZIPF_JIT).uniform(-0.1, 0.1, E)
     return (cfg.zipf_beta * logp + jit).astype(np.float32)

@@ -50,3 +50,20 @@ def test_zipf_bias_ranks():
     assert b.shape == (896,) and np.isfinite(b).all()
     # the strongest-biased expert is rank 1: bias within the jitter of 0
     assert b.max() <= 0.1 + 1e-6
+
+
+def test_zipf_beta_is_the_calibrated_value():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "zipf_beta.json")))
+    assert synth.ZIPF_BETA_1P1 == g["beta"]
+    assert synth.config("decode64_zipf").zipf_beta == g["beta"]
+    # the calibration bracketed the target slope
+    slopes = [s for _, s, _ in g["grid"]]
+    assert min(slopes) < -g["zipf_s"] < max(slopes)
+
+
+def test_zipf_ranks_are_a_permutation():
+    cfg = synth.config("decode64_zipf")
+    r = synth.zipf_ranks(cfg, 0, 0)
+    assert sorted(r.tolist()) == list(range(1, cfg.n_experts + 1))
