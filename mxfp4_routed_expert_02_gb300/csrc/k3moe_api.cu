@@ -7,7 +7,7 @@
 #include <mutex>
 #include <vector>
 
-#include "k3moe_kernels.cuh"
+#include "k3moe_tc.cuh"
 
 using namespace k3;
 
@@ -42,6 +42,8 @@ const DeviceInfo *device_info() {
             cudaSuccess ||
         cudaFuncSetAttribute(k_dispatch, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
             cudaSuccess ||
+        cudaFuncSetAttribute(k_route_candidates, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             128 * 1024) != cudaSuccess ||
         set_decode_smem_limits() != cudaSuccess)
       return nullptr;
     d.attrs_set = true;
@@ -495,12 +497,21 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     k_quant_x<<<grid, 256, 0, st>>>(x, Tc, H, K, ws.inv, P, ws.xq, ws.xs);
   }
   if (launch_status() != K3MOE_OK) return K3MOE_ERR_CUDA;
-  CUtensorMap mg, mu, md, mx, ma;
-  if (!tc_map3d(&mg, rec + off[0], H / 2, I, E, H / 2, es, kTcRows) ||
-      !tc_map3d(&mu, rec + off[4], H / 2, I, E, H / 2, es, kTcRows) ||
+  // gate and up packed matrices of every expert as one 4-D map (K bytes, rows, matrix,
+  // expert): the up matrix sits at a fixed offset after the gate matrix in each record
+  CUtensorMap mgu, md, mx, ma;
+  const unsigned long long gu_dims[4] = {(unsigned long long)H / 2, (unsigned long long)I, 2,
+                                         (unsigned long long)E};
+  const unsigned long long gu_strides[3] = {(unsigned long long)H / 2,
+                                            (unsigned long long)(off[4] - off[0]),
+                                            (unsigned long long)es};
+  const unsigned gu_box[4] = {128u, (unsigned)kTcRows, 2, 1};  // 128 bytes of K x 128 rows x both
+  if (!tc_map(&mgu, rec + off[0], 4, gu_dims, gu_strides, gu_box) ||
       !tc_map3d(&md, rec + off[2], I / 2, H, E, I / 2, es, kTcRows) ||
-      !tc_map3d(&mx, ws.xq, H / 2, P, kTcTermsX, H / 2, (unsigned long long)P * (H / 2), ntile) ||
-      !tc_map3d(&ma, ws.aq, I / 2, P, kTcTermsAct, I / 2, (unsigned long long)P * (I / 2), ntile))
+      !tc_map3d(&mx, ws.xq, H / 2, P, kTcTermsX, H / 2, (unsigned long long)P * (H / 2), ntile,
+                kTcTermsX) ||
+      !tc_map3d(&ma, ws.aq, I / 2, P, kTcTermsAct, I / 2, (unsigned long long)P * (I / 2), ntile,
+                kTcTermsAct))
     return K3MOE_ERR_CUDA;
   TcGemmArgs g{};
   g.off = ws.off;
@@ -525,8 +536,9 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     a.sfb_tstride = (long long)a.kchunks * a.sfb_cstride;
     a.out = ws.act;
     a.out_ld = I;
+    a.a_pair = 1;
     TraceScope ts(KID_TC_GATEUP, st);
-    if (launch_tc_gemm(TcKind::kMxf4GateUp, a, mg, mu, mx, di->sms, st) != cudaSuccess)
+    if (launch_tc_gemm(TcKind::kMxf4GateUp, a, mgu, mgu, mx, di->sms, st) != cudaSuccess)
       return K3MOE_ERR_CUDA;
   }
   {
@@ -561,7 +573,7 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
         !tc_map3d(&msu, sh_up, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
         !tc_map3d(&msd, sh_down, 2ull * SI, H, 1, 2ull * SI, 2ull * SI * H, kTcRows) ||
         !tc_map3d(&mxs, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, nt1) ||
-        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc, nt1))
+        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc, nt1, 2))
       return K3MOE_ERR_CUDA;
     k_group1<<<1, 32, 0, st>>>(Tc, nt1, ws.off1, ws.tile_off1);
     TcGemmArgs s1 = g;
@@ -601,7 +613,7 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   }
   {
     TraceScope ts(KID_COMBINE, st);
-    k_combine<<<Tc, 256, (size_t)2 * K * 4, st>>>(Tc, H, K, w, ws.inv, ws.dpair,
+    k_combine<<<dim3(Tc, (H / 4 + 255) / 256), 256, (size_t)2 * K * 4, st>>>(Tc, H, K, w, ws.inv, ws.dpair,
                                                  SI > 0 ? ws.ds : nullptr, y, (int)ydt,
                                                  accumulate);
   }
@@ -616,8 +628,8 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
   const int H = d->hidden, E = d->n_experts, K = d->topk;
   {
     TraceScope ts(KID_NORMS, st);
-    k_row_norms<<<(Tc + 7) / 8, 256, 0, st>>>(x, Tc, H, wt.xn);
-    k_row_norms<<<(E + 7) / 8, 256, 0, st>>>(wr, E, H, wt.wn);
+    k_row_norms<<<(Tc + 3) / 4, 128, 0, st>>>(x, Tc, H, wt.xn);
+    k_row_norms<<<(E + 3) / 4, 128, 0, st>>>(wr, E, H, wt.wn);
   }
   k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, wt.off1, wt.tile_off1);
   CUtensorMap mw, mx;
@@ -642,7 +654,9 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
   }
   {
     TraceScope ts(KID_ROUTE_CAND, st);
-    k_route_candidates<<<Tc, 256, route_candidates_smem(H, E, K), st>>>(
+    // enough blocks per token to cover the SMs twice, at most 8
+    const int split = std::max(1, std::min(8, (2 * di->sms + Tc - 1) / Tc));
+    k_route_candidates<<<dim3(Tc, split), 256, route_candidates_smem(H, E, K), st>>>(
         wt.Lt, wt.xn, wt.wn, x, wr, bias, H, E, K, wt.sc, wt.ch, wt.ncand, status);
   }
   {

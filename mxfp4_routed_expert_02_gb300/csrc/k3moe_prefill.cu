@@ -6,7 +6,7 @@
 // LatentMoE listing, steps 3 and 6): y_t = sum_j w[t,j] d_j in slot order j, in float,
 // then the shared expert added unweighted; README of Maknee/Kimi-K3.cpp, "The
 // consumer-memory idea" item 7, fixes the router order of that sum.
-#include "k3moe_kernels.cuh"
+#include "k3moe_tc.cuh"
 
 namespace k3 {
 
@@ -29,16 +29,50 @@ __global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int 
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, to = 0;
-    for (int e = 0; e < E; e++) {
-      off[e] = o;
-      tile_off[e] = to;
-      o += cnt[e];
-      to += (cnt[e] + ntile - 1) / ntile;
+  // exclusive scans of the counts and of the tile counts: thread i takes a run of
+  // consecutive experts, the run totals are scanned across the block by warp shuffles
+  __shared__ int wsum[2][32];
+  const int nt = blockDim.x, per = (E + nt - 1) / nt;
+  const int e0 = min(E, threadIdx.x * per), e1 = min(E, e0 + per);
+  int c = 0, tl = 0;
+  for (int e = e0; e < e1; e++) {
+    c += cnt[e];
+    tl += (cnt[e] + ntile - 1) / ntile;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = nt >> 5;
+  int ic = c, it = tl;  // inclusive scans within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, o), b = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) {
+      ic += a;
+      it += b;
     }
-    off[E] = o;
-    tile_off[E] = to;
+  }
+  if (lane == 31) {
+    wsum[0][warp] = ic;
+    wsum[1][warp] = it;
+  }
+  __syncthreads();
+  int o = ic - c, to = it - tl;
+  for (int w = 0; w < warp; w++) {
+    o += wsum[0][w];
+    to += wsum[1][w];
+  }
+  for (int e = e0; e < e1; e++) {
+    off[e] = o;
+    tile_off[e] = to;
+    o += cnt[e];
+    to += (cnt[e] + ntile - 1) / ntile;
+  }
+  if (threadIdx.x == nt - 1) {
+    int so = 0, st = 0;
+    for (int w = 0; w < nw; w++) {
+      so += wsum[0][w];
+      st += wsum[1][w];
+    }
+    off[E] = so;
+    tile_off[E] = st;
   }
 }
 
@@ -220,7 +254,7 @@ __global__ void k_combine(int T, int H, int K, const float *__restrict__ w,
     s_w[j] = w[(size_t)t * K + j];
   }
   __syncthreads();
-  for (int h4 = threadIdx.x; h4 < H / 4; h4 += blockDim.x) {
+  for (int h4 = blockIdx.y * blockDim.x + threadIdx.x; h4 < H / 4; h4 += gridDim.y * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < K; j++) {
       const int s = s_slot[j];

@@ -19,39 +19,50 @@
 //    defines them; the rest get ch = -inf.
 // 3. The usual top-k kernel then selects among the candidates: same result as selecting
 //    among all experts with exact scores.
-#include "k3moe_kernels.cuh"
+#include "k3moe_tc.cuh"
 
 namespace k3 {
 
 // Euclidean norm of each of R bf16 rows of width H (a multiple of 8), one warp per row,
-// rounded up by a relative 2^-10 so that it bounds the exact norm.
-__global__ void k_row_norms(const uint16_t *__restrict__ v, int R, int H, float *__restrict__ out) {
+// rounded up by a relative 2^-10 so that it bounds the exact norm.  The squares of bf16
+// values are exact in float (8-bit significands); a lane adds n = 8 * ceil(H / 256) of them
+// in order and five shuffle levels follow, so the float sum S' has |S' - S| <= g S with
+// g = m u / (1 - m u), m = n + 4 additions on any path, u = 2^-24.  With the square root
+// and the final product rounded up, the result is >= sqrt(S) whenever g < 2^-9, that is for
+// H below 2^20 (hidden sizes are at most 8192 here).
+__global__ void __launch_bounds__(128) k_row_norms(const uint16_t *__restrict__ v, int R, int H,
+                                                   float *__restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (warp >= R) return;
   const uint4 *row = reinterpret_cast<const uint4 *>(v + (size_t)warp * H);
-  double acc = 0.0;
+  float acc = 0.f;
+#pragma unroll 4
   for (int q = lane; q < H / 8; q += 32) {
     const uint4 w = __ldg(row + q);
     const uint32_t a[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-      const double lo = bf16_lo(a[k]), hi = bf16_hi(a[k]);
-      acc += lo * lo + hi * hi;
+      const float lo = bf16_lo(a[k]), hi = bf16_hi(a[k]);
+      acc = __fmaf_rn(lo, lo, acc);
+      acc = __fmaf_rn(hi, hi, acc);
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) out[warp] = (float)(sqrt(acc) * (1.0 + 1.0 / 1024));
+  for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  if (lane == 0) out[warp] = __fmul_ru(__fsqrt_ru(acc), 1.0009765625f);  // 1 + 2^-10
 }
 
 // Logistic in float for the bounds (a few ulp from the exact value; the slack covers it).
 __device__ __forceinline__ float logistic_f(float v) { return 1.f / (1.f + expf(-v)); }
 
-// One block per token.  Lt [T][E] screening logits, xn [T] / wn [E] row norms of x / Wr;
-// x [T][H], wr [E][H] bf16; writes sc/ch [T][E] (candidates: exact; others: sc 0,
-// ch -inf).  Dynamic shared memory: H bf16 of x, then the candidate list (E ints) and the
-// top-k scratch.
+// gridDim.y blocks per token (blockIdx.x = token).  Lt [T][E] screening logits, xn [T] /
+// wn [E] row norms of x / Wr; x [T][H], wr [E][H] bf16.  Every block of a token computes
+// all E bounds and the threshold (cheap, and identical in every block); block y then owns
+// the experts e with e % gridDim.y == y: it computes the exact sc / ch of its candidates and
+// writes sc 0, ch -inf for its other experts, so no two blocks write the same entry.
+// Dynamic shared memory: H bf16 of x, the lower and upper bounds (2E floats), the
+// block's candidate list (E ints) and the top-k scratch.
 __global__ void __launch_bounds__(256) k_route_candidates(
     const float *__restrict__ Lt, const float *__restrict__ xn, const float *__restrict__ wn,
     const uint16_t *__restrict__ x,
@@ -60,32 +71,36 @@ __global__ void __launch_bounds__(256) k_route_candidates(
     int32_t *status) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
-  int *clist = reinterpret_cast<int *>(smem + (size_t)H * 2);
+  float *blo = reinterpret_cast<float *>(smem + (size_t)H * 2);
+  float *bhi = blo + E;
+  int *clist = reinterpret_cast<int *>(bhi + E);
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(
-      smem + (((size_t)H * 2 + (size_t)E * 4 + 15) & ~size_t(15)));
+      smem + (((size_t)H * 2 + (size_t)E * 12 + 15) & ~size_t(15)));
   __shared__ int sel[32];
   __shared__ float wsel[32];
-  __shared__ int count;
+  __shared__ int count, total;
   __shared__ float tau;
-  const int t = blockIdx.x;
+  const int t = blockIdx.x, S = gridDim.y, y = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float *Lrow = Lt + (size_t)t * E;
   const float xnorm = xn[t];
   float *scr = sc + (size_t)t * E;
   float *chr = ch + (size_t)t * E;
   const float nerr = (float)H * 2.384185791015625e-07f;  // H * 2^-22
-  if (threadIdx.x == 0) count = 0;
+  if (threadIdx.x == 0) {
+    count = 0;
+    total = 0;
+  }
   {
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
     uint4 *dst = reinterpret_cast<uint4 *>(xs);
     for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
   }
-  // lower bounds of ch -> ch row (scratch for the K-th largest), upper bounds kept in sc row
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const float L = Lrow[e], S = xnorm * wn[e], b = bias ? bias[e] : 0.f;
+    const float L = Lrow[e], Sn = xnorm * wn[e], b = bias ? bias[e] : 0.f;
     float lo, hi;
-    if (isfinite(L) && isfinite(S) && isfinite(b)) {
-      const float d = __fmaf_rn(nerr, S, 1e-30f);
+    if (isfinite(L) && isfinite(Sn) && isfinite(b)) {
+      const float d = __fmaf_rn(nerr, Sn, 1e-30f);
       const float slack = 2e-6f + 9.5367431640625e-07f * (fabsf(L) + fabsf(b));  // 2^-20
       lo = logistic_f(__fsub_rn(L, d)) + b - slack;
       hi = logistic_f(__fadd_rn(L, d)) + b + slack;
@@ -93,27 +108,33 @@ __global__ void __launch_bounds__(256) k_route_candidates(
       lo = -INFINITY;
       hi = INFINITY;
     }
-    chr[e] = lo;
-    scr[e] = hi;
+    blo[e] = lo;
+    bhi[e] = hi;
   }
   __syncthreads();
-  cta_topk(chr, chr, E, K, 0, 1.f, keys, sel, wsel);  // ends with __syncthreads
-  if (threadIdx.x == 0) tau = chr[sel[K - 1]];
+  cta_topk(blo, blo, E, K, 0, 1.f, keys, sel, wsel);  // ends with __syncthreads
+  if (threadIdx.x == 0) tau = blo[sel[K - 1]];
   __syncthreads();
+  int mine = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const float hi = scr[e];
-    if (!(hi < tau)) clist[atomicAdd(&count, 1)] = e;
+    if (bhi[e] < tau) continue;
+    mine++;
+    if (e % S == y) clist[atomicAdd(&count, 1)] = e;
   }
-  __syncthreads();
-  const int C = count;
-  if (threadIdx.x == 0 && ncand) ncand[t] = C;
-  // non-candidates: out of the selection
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    if (!(scr[e] < tau)) continue;
+  if (y == 0 && ncand) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    if (lane == 0) atomicAdd(&total, mine);
+  }
+  // the block's non-candidates: out of the selection
+  for (int e = y + S * threadIdx.x; e < E; e += S * blockDim.x) {
+    if (!(bhi[e] < tau)) continue;
     scr[e] = 0.f;
     chr[e] = -INFINITY;
   }
-  __syncthreads();  // the candidates' rows are rewritten below
+  __syncthreads();
+  const int C = count;
+  if (y == 0 && threadIdx.x == 0 && ncand) ncand[t] = total;
   // candidates: exact logit (float-float sum of exact products, fixed reduction tree)
   const int nchunk = H >> 3;
   const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
@@ -159,7 +180,7 @@ __global__ void __launch_bounds__(256) k_route_candidates(
 }
 
 size_t route_candidates_smem(int H, int E, int K) {
-  return (((size_t)H * 2 + (size_t)E * 4 + 15) & ~size_t(15)) + (size_t)topk_scratch_keys(E, K) * 8;
+  return (((size_t)H * 2 + (size_t)E * 12 + 15) & ~size_t(15)) + (size_t)topk_scratch_keys(E, K) * 8;
 }
 
 }  // namespace k3

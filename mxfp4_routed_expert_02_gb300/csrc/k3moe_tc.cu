@@ -27,7 +27,7 @@
 // tensor memory are released together by tcgen05.commit on the stage's "empty" barrier.
 #include <cuda.h>
 
-#include "k3moe_kernels.cuh"
+#include "k3moe_tc.cuh"
 
 namespace k3 {
 
@@ -96,6 +96,61 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// The same, issued by one elected lane of a converged warp (the whole warp computes the
+// operands, so they stay warp-uniform).
+__device__ __forceinline__ void mma_mxf4_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %6, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, "
+      "[%4], [%5], p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %4, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The MMAs below take a descriptor as its low word plus this constant high word (stride
+// 1024 bytes between 8-row groups, descriptor version 1, 128-byte swizzle); offsets within
+// shared memory change only the address field of the low word, which cannot carry out of it
+// below 256 KB.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+__device__ __forceinline__ void mma_mxf4_el_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t hi,
+                                               uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                               uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; .reg .b64 da, db; elect.sync r|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %7, 0; mov.b64 da, {%1, %3}; mov.b64 db, {%2, %3};\n"
+      "  @e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], da, db, %4, "
+      "[%5], [%6], p; }" ::"r"(d),
+      "r"(alo), "r"(blo), "r"(hi), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_el_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t hi,
+                                              uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; .reg .b64 da, db; elect.sync r|e, 0xffffffff;\n"
+      "  setp.ne.b32 p, %5, 0; mov.b64 da, {%1, %3}; mov.b64 db, {%2, %3};\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p; }" ::"r"(d),
+      "r"(alo), "r"(blo), "r"(hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_el(uint64_t *bar) {
+  asm volatile(
+      "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff;\n"
+      "  @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
 
 // 3-D tiled TMA load (x = K byte, y = row, z = group or term) completing on `bar`.
 __device__ __forceinline__ void tma_load3d(void *dst, const CUtensorMap *map, int x, int y, int z,
@@ -104,6 +159,15 @@ __device__ __forceinline__ void tma_load3d(void *dst, const CUtensorMap *map, in
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
       "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load4d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                           int w, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -268,6 +332,37 @@ __device__ __forceinline__ float situ_fast(float g, float u, float b1, float ib1
   return (b1 * tanh_fast(g * ib1)) * sg * (b2 * tanh_fast(u * ib2));
 }
 
+// The MMAs of one stage, issued by a converged warp: NQ groups of B terms side by side, NA A
+// matrices, K steps 0 .. nk-1 of the stage's 128-byte chunk.  Everything but the stage's
+// descriptor low word, its scale-slot column, the accumulator columns and the first-chunk
+// flag is a compile-time offset, so the issuing warp spends few instructions per MMA (the
+// issue loop runs on the pipeline's critical path: commit, refill, landing, issue).
+template <int KIND, int NA, int NQ>
+__device__ __forceinline__ void tc_issue_stage(uint32_t alo, uint32_t blo, uint32_t bstep, int nk,
+                                               uint32_t slot, uint32_t dcol0, uint32_t dcol1,
+                                               uint32_t idesc, bool first) {
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    if (i < nk) {
+#pragma unroll
+      for (int m = 0; m < NA; m++) {
+        const uint32_t a_lo = alo + (uint32_t)((m * kTcBox + 32 * i) >> 4);
+        const uint32_t dcol = m == 0 ? dcol0 : dcol1;
+#pragma unroll
+        for (int u = 0; u < NQ; u++) {
+          const uint32_t b_lo = blo + (uint32_t)u * bstep + (uint32_t)(2 * i);
+          const uint32_t acc = (i == 0 && u == 0 && first) ? 0u : 1u;
+          if (KIND == 0)
+            mma_mxf4_el_lo(dcol, a_lo, b_lo, kDescHi, idesc, slot + 16 * (NQ + m) + 4 * i,
+                           slot + 16 * u + 4 * i, acc);
+          else
+            mma_f16_el_lo(dcol, a_lo, b_lo, kDescHi, idesc, acc);
+        }
+      }
+    }
+  }
+}
+
 template <int KIND, int NA, int NT, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_tc_gemm(const TcGemmArgs a, const __grid_constant__ CUtensorMap tmA0,
@@ -290,10 +385,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t *stages = smem + 1024;
   uint8_t *sfring = stages + (size_t)a.nstages * tc_stage_bytes(NA, NT, a.ntile);
   constexpr bool kScales = (KIND == 0);
-  // TMEM columns per stage of scale vectors: B terms first (16 columns each), then the A
-  // matrices (16 each); multi-column accesses stay aligned to their width
-  constexpr int kSfSlot = kScales ? 16 * (NT + NA) : 0;
+  // B terms side by side: one MMA of N = TG * ntile columns covers TG terms (their tiles
+  // are adjacent in the stage), NQ = NT / TG such groups per K step accumulate into the
+  // same TG column blocks, which the epilogue adds up
+  const int TG = a.tgroup, NQ = NT / TG;
+  // TMEM columns per stage of scale vectors: B term groups first (16 columns each), then
+  // the A matrices (16 each); multi-column accesses stay aligned to their width
+  const int kSfSlot = kScales ? 16 * (NQ + NA) : 0;
   const int NS = a.nstages, NSF = a.nsf, ntile = a.ntile;
+  const int aw = TG * ntile;  // accumulator columns of one A matrix
   const uint32_t stage_bytes = tc_stage_bytes(NA, NT, ntile);
   const uint32_t tma_bytes = (uint32_t)NA * kTcBox + (uint32_t)NT * ntile * kTcChunkBytes;
   const uint32_t sf_bytes = tc_sf_bytes(NA, NT, ntile);
@@ -322,9 +422,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base;
-  // accumulators: buffer b, matrix m at columns (b * NA + m) * ntile; scale slots after them
+  // accumulators: buffer b, matrix m at columns (b * NA + m) * aw; scale slots after them
   const int ND = a.nacc;
-  const uint32_t sf_col0 = (uint32_t)((ND * NA * ntile + 15) & ~15);
+  const uint32_t sf_col0 = (uint32_t)((ND * NA * aw + 15) & ~15);
 
   pdl_wait();
   const int nitems = a.tile_off[a.ngroups] * a.mtiles;
@@ -361,12 +461,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         uint8_t *st = stages + (size_t)s * stage_bytes;
         mbar_arrive_expect_tx(&full[s], tma_bytes);
-        tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
-        if (NA > 1) tma_load3d(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
-#pragma unroll
-        for (int t = 0; t < NT; t++)
-          tma_load3d(st + NA * kTcBox + t * ntile * kTcChunkBytes, &tmB, c * kTcChunkBytes,
-                     ti.brow0, t, &full[s]);
+        // few large copies: a stage costs the TMA unit about the same whether it moves 4 KB
+        // or 32 KB, so both A matrices come in one 4-D box where their layout allows, and
+        // all NT terms of B in one box of depth NT
+        if (NA > 1 && a.a_pair) {
+          tma_load4d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, 0, ga, &full[s]);
+        } else {
+          tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+          if (NA > 1) tma_load3d(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+        }
+        tma_load3d(st + NA * kTcBox, &tmB, c * kTcChunkBytes, ti.brow0, 0, &full[s]);
       }
     }
   } else if (warp < 4) {
@@ -431,7 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint8_t *sfs = sfring + (size_t)k * sf_bytes;
         const uint32_t slot = tmem + sf_col0 + (uint32_t)(sj * kSfSlot);
-        // A: K step i of matrix m reads column slot + 16(NT + m) + 4i + (row / 32);
+        // A: K step i of matrix m reads column slot + 16(NQ + m) + 4i + (row / 32);
         // scale byte 255 (no contribution) becomes 0
 #pragma unroll
         for (int m = 0; m < NA; m++) {
@@ -440,22 +544,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           v.y &= ~__vcmpeq4(v.y, 0xffffffffu);
 #pragma unroll
           for (int i = 0; i < 4; i++)
-            tmem_st_x1(slot + lane_sel + 16 * (NT + m) + 4 * i + q, step_scales(v, i));
+            tmem_st_x1(slot + lane_sel + 16 * (NQ + m) + 4 * i + q, step_scales(v, i));
         }
-        // B: K step i of term t reads column slot + 16t + 4i + n/32 at lane n % 32 of
-        // every lane quarter (each 32-row quarter of the MMA reads its own copy)
+        // B: K step i of term group u reads column slot + 16u + 4i + n/32 at lane n % 32
+        // of every lane quarter (each 32-row quarter of the MMA reads its own copy), for
+        // the group's rows n = 0 .. aw-1 (term u*TG + n / ntile, row n % ntile; those are
+        // consecutive in the staged scale bytes)
 #pragma unroll
-        for (int t = 0; t < NT; t++) {
-          uint32_t vb[16];
+        for (int u = 0; u < NT; u++) {
+          if (u < NQ) {
+            uint32_t vb[16];
 #pragma unroll
-          for (int jj = 0; jj < 4; jj++) {
-            const int n = 32 * jj + lane;
-            const uint2 v = (n < ntile) ? *reinterpret_cast<const uint2 *>(sfs + off_sfb + (t * ntile + n) * 8)
-                                        : make_uint2(0u, 0u);
+            for (int jj = 0; jj < 4; jj++) {
+              const int n = 32 * jj + lane;
+              const uint2 v = (n < aw) ? *reinterpret_cast<const uint2 *>(sfs + off_sfb + (u * aw + n) * 8)
+                                       : make_uint2(0u, 0u);
 #pragma unroll
-            for (int i = 0; i < 4; i++) vb[4 * i + jj] = step_scales(v, i);
+              for (int i = 0; i < 4; i++) vb[4 * i + jj] = step_scales(v, i);
+            }
+            tmem_st_x16(slot + lane_sel + 16 * u, vb);
           }
-          tmem_st_x16(slot + lane_sel + 16 * t, vb);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -471,12 +579,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == kTcWarpMma) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (waits and operands warp-uniform); one elected lane
+    // issues each tcgen05 instruction.
+    {
       int it = 0, n = 0;
       bool ok = true;
+      // B: group u of TG terms starts TG * ntile rows of 128 bytes after group u - 1
+      const uint32_t bstep = (uint32_t)(TG * ntile * kTcChunkBytes) >> 4;
       for (; n < my_items && ok; n++) {
         const TcItem ti = item_at(n);
-        const int nmma = ((ti.nvalid + 15) / 16) * 16;
+        // the last term block of a group needs only the tile's valid rows
+        const int nmma = (TG - 1) * ntile + ((ti.nvalid + 15) / 16) * 16;
         uint32_t idesc;
         if (KIND == 0)
           idesc = (1u << 7) | (1u << 10) | ((uint32_t)(nmma >> 3) << 17) | (1u << 23) |
@@ -486,9 +599,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   ((uint32_t)(kTcTile >> 4) << 24);
         // the epilogue must have drained this accumulator buffer's previous item
         const int db = n % ND;
-        if (!mbar_wait(&dempty[db], ((n / ND) & 1) ^ 1)) {
-          set_status(a.status, K3MOE_ERR_TIMEOUT);
-          *abort_flag = 1;
+        const uint32_t dcol0 = tmem + (uint32_t)((db * NA) * aw);
+        const uint32_t dcol1 = dcol0 + (uint32_t)aw;
+        if (!__all_sync(0xffffffffu, mbar_wait(&dempty[db], ((n / ND) & 1) ^ 1))) {
+          if (lane == 0) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+          }
           ok = false;
           break;
         }
@@ -496,48 +613,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c = 0; c < a.kchunks; c++, it++) {
           const int s = it % NS;
           const uint32_t par = (it / NS) & 1;
-          if (!mbar_wait(&full[s], par) || (kScales && !mbar_wait(&sfull[s], par))) {
-            set_status(a.status, K3MOE_ERR_TIMEOUT);
-            *abort_flag = 1;
+          const bool got = mbar_wait(&full[s], par) && (!kScales || mbar_wait(&sfull[s], par));
+          if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) {
+              set_status(a.status, K3MOE_ERR_TIMEOUT);
+              *abort_flag = 1;
+            }
             ok = false;
             break;
           }
           tc_fence_after();
-          // descriptors: the stage base plus constant offsets (address field in 16-byte
-          // units, no carry out of it below 256 KB)
-          const uint64_t dbase = sw128_desc(smem_u32(stages + (size_t)s * stage_bytes));
-          const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
-          const uint32_t boff = (uint32_t)(NA * kTcBox) >> 4, tstep = (uint32_t)(ntile * kTcChunkBytes) >> 4;
-          const int nk = (c == a.kchunks - 1) ? a.ksteps_last : 4;
-#pragma unroll
-          for (int i = 0; i < 4; i++) {
-            if (i < nk) {
-#pragma unroll
-              for (int m = 0; m < NA; m++) {
-                const uint64_t ad = dbase + (uint64_t)((m * kTcBox + 32 * i) >> 4);
-#pragma unroll
-                for (int t = 0; t < NT; t++) {
-                  const uint64_t bd = dbase + (uint64_t)(boff + t * tstep + 2 * i);
-                  const uint32_t acc = (c > 0 || i > 0 || t > 0) ? 1u : 0u;
-                  const uint32_t dcol = tmem + (uint32_t)((db * NA + m) * ntile);
-                  if (KIND == 0)
-                    mma_mxf4(dcol, ad, bd, idesc, slot + 16 * (NT + m) + 4 * i,
-                             slot + 16 * t + 4 * i, acc);
-                  else
-                    mma_f16(dcol, ad, bd, idesc, acc);
-                }
-              }
-            }
+          {
+            const uint32_t alo = sw128_desc_lo(smem_u32(stages + (size_t)s * stage_bytes));
+            const uint32_t blo = alo + ((uint32_t)(NA * kTcBox) >> 4);
+            const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
+            const int nk = (c == a.kchunks - 1) ? a.ksteps_last : 4;
+            if (NQ == 1)
+              tc_issue_stage<KIND, NA, 1>(alo, blo, bstep, nk, slot, dcol0, dcol1, idesc, c == 0);
+            else if (NQ == 2)
+              tc_issue_stage<KIND, NA, (NT >= 2 ? 2 : 1)>(alo, blo, bstep, nk, slot, dcol0, dcol1,
+                                                          idesc, c == 0);
+            else
+              tc_issue_stage<KIND, NA, (NT >= 4 ? 4 : 1)>(alo, blo, bstep, nk, slot, dcol0, dcol1,
+                                                          idesc, c == 0);
           }
-          tc_commit(&empty[s]);
+          tc_commit_el(&empty[s]);
         }
-        tc_commit(&dfull[db]);
+        tc_commit_el(&dfull[db]);
       }
       // before the accumulator is freed: wait (bounded) for every MMA issued
       if (!ok && it > 0) {
         const int s = (it - 1) % NS;
         mbar_wait(&empty[s], ((it - 1) / NS) & 1, 400000000LL);
       }
+      __syncwarp();
     }
   } else if (warp >= kTcWarpEpi) {
     // ---------------------------------------------------------------- epilogue
@@ -557,12 +666,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int row = ti.mt * kTcTile + 32 * q + lane;
       const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
       if (got && !*abort_flag) {
-        const uint32_t dbase = tmem + lane_sel + (uint32_t)(db * NA * ntile);
+        const uint32_t dbase = tmem + lane_sel + (uint32_t)(db * NA * aw);
         for (int c0 = half * hcols; c0 < (half + 1) * hcols && c0 < ti.nvalid; c0 += 16) {
+          // the sum of the TG term blocks of each matrix
           uint32_t d0[16], d1[16];
           tmem_ld16_nowait(dbase + (uint32_t)c0, d0);
-          if (NA > 1) tmem_ld16_nowait(dbase + (uint32_t)(ntile + c0), d1);
+          if (NA > 1) tmem_ld16_nowait(dbase + (uint32_t)(aw + c0), d1);
           tmem_wait_ld2(d0, d1);
+          for (int tb = 1; tb < TG; tb++) {
+            uint32_t e0[16], e1[16];
+            tmem_ld16_nowait(dbase + (uint32_t)(tb * ntile + c0), e0);
+            if (NA > 1) tmem_ld16_nowait(dbase + (uint32_t)(aw + tb * ntile + c0), e1);
+            tmem_wait_ld2(e0, e1);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+              d0[j] = __float_as_uint(__uint_as_float(d0[j]) + __uint_as_float(e0[j]));
+              if (NA > 1) d1[j] = __float_as_uint(__uint_as_float(d1[j]) + __uint_as_float(e1[j]));
+            }
+          }
           if (row < a.M_rows) {
             float *orow = a.out + (long long)(ti.brow0 + c0) * a.out_ld + row;
 #pragma unroll
@@ -615,27 +736,41 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
+bool tc_map(CUtensorMap *m, const void *base, int rank, const unsigned long long *dims,
+            const unsigned long long *strides, const unsigned *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rank < 3 || rank > 5) return false;
+  if (reinterpret_cast<uintptr_t>(base) & 15) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; i++) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) {
+      if (strides[i] & 15) return false;
+      st[i] = strides[i];
+    }
+  }
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void *>(base), d, st,
+            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
               unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
-              unsigned long long depth_stride, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_stride & 15) || (depth_stride & 15))
-    return false;
+              unsigned long long depth_stride, int box_rows, int box_depth) {
   if (depth_stride == 0) depth_stride = row_stride * rows;
-  const cuuint64_t dims[3] = {inner_bytes, rows, depth};
-  const cuuint64_t strides[2] = {row_stride, depth_stride};
-  const cuuint32_t box[3] = {(cuuint32_t)kTcChunkBytes, (cuuint32_t)box_rows, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const unsigned long long dims[3] = {inner_bytes, rows, depth};
+  const unsigned long long strides[2] = {row_stride, depth_stride};
+  const unsigned box[3] = {(unsigned)kTcChunkBytes, (unsigned)box_rows, (unsigned)box_depth};
+  return tc_map(m, base, 3, dims, strides, box);
 }
 
 // Ring depths: NSF scale slots (8 when they fit), then as many data stages as fit in
 // shared memory (and, with scale slots, in TMEM next to the accumulators), at most 8.
-static void tc_depths(int na, int nt, int ntile, bool scales, int *ns, int *nsf) {
+// tg: B terms per MMA (accumulator columns tg * ntile per A matrix).
+static void tc_depths(int na, int nt, int ntile, int tg, bool scales, int *ns, int *nsf) {
   const size_t budget = 227 * 1024 - 2048 - kTcItemTableBytes;
   const size_t stage = tc_stage_bytes(na, nt, ntile), sfb = scales ? tc_sf_bytes(na, nt, ntile) : 0;
   int f = scales ? 8 : 0;
@@ -645,8 +780,8 @@ static void tc_depths(int na, int nt, int ntile, bool scales, int *ns, int *nsf)
     if (s >= 2 || f == 0) break;
   }
   if (scales) {
-    const int free_cols = kTcTmemCols - ((na * ntile + 15) & ~15);
-    const int by_tmem = free_cols / (16 * (na + nt));
+    const int free_cols = kTcTmemCols - ((na * tg * ntile + 15) & ~15);
+    const int by_tmem = free_cols / (16 * (na + nt / tg));
     if (s > by_tmem) s = by_tmem;
   }
   *ns = s > 8 ? 8 : s;
@@ -655,9 +790,25 @@ static void tc_depths(int na, int nt, int ntile, bool scales, int *ns, int *nsf)
 
 // Accumulator buffers: two (the epilogue of one item overlaps the next item's MMAs) when
 // they fit in TMEM next to the scale slots, else one.
-static int tc_nacc(int na, int nt, int ntile, bool scales, int ns) {
-  const int sf = scales ? ns * 16 * (na + nt) : 0;
-  return (((2 * na * ntile + 15) & ~15) + sf <= kTcTmemCols) ? 2 : 1;
+static int tc_nacc(int na, int nt, int ntile, int tg, bool scales, int ns) {
+  const int sf = scales ? ns * 16 * (na + nt / tg) : 0;
+  return (((2 * na * tg * ntile + 15) & ~15) + sf <= kTcTmemCols) ? 2 : 1;
+}
+
+// B terms per MMA: the largest divisor of nt with tg * ntile <= 128 (the scale layout of
+// up to four 32-row column groups) that still leaves room for two accumulator buffers and
+// two data stages; else the largest that leaves two stages.
+static int tc_tgroup(int na, int nt, int ntile, bool scales) {
+  int best = 1, best2 = 0;
+  for (int tg = 1; tg <= nt; tg *= 2) {
+    if (nt % tg || tg * ntile > 128) continue;
+    int ns = 0, nsf = 0;
+    tc_depths(na, nt, ntile, tg, scales, &ns, &nsf);
+    if (ns < 2) continue;
+    best = tg;
+    if (tc_nacc(na, nt, ntile, tg, scales, ns) == 2) best2 = tg;
+  }
+  return best2 ? best2 : best;
 }
 
 template <int KIND, int NA, int NT, int EPI>
@@ -665,8 +816,9 @@ static cudaError_t launch_tc(const TcGemmArgs &a, const CUtensorMap &A0, const C
                              const CUtensorMap &B, int grid, cudaStream_t st) {
   auto fn = k_tc_gemm<KIND, NA, NT, EPI>;
   if (a.ntile < 16 || a.ntile > kTcTile || a.ntile % 16) return cudaErrorInvalidValue;
+  const int tg = tc_tgroup(NA, NT, a.ntile, KIND == 0);
   int ns = 0, nsf = 0;
-  tc_depths(NA, NT, a.ntile, KIND == 0, &ns, &nsf);
+  tc_depths(NA, NT, a.ntile, tg, KIND == 0, &ns, &nsf);
   if (ns < 2 || (KIND == 0 && nsf < 2)) return cudaErrorInvalidValue;
   const size_t smem = 2048 + (size_t)ns * tc_stage_bytes(NA, NT, a.ntile) +
                       (size_t)nsf * (KIND == 0 ? tc_sf_bytes(NA, NT, a.ntile) : 0) +
@@ -676,7 +828,8 @@ static cudaError_t launch_tc(const TcGemmArgs &a, const CUtensorMap &A0, const C
   TcGemmArgs aa = a;
   aa.nstages = ns;
   aa.nsf = nsf;
-  aa.nacc = tc_nacc(NA, NT, a.ntile, KIND == 0, ns);
+  aa.nacc = tc_nacc(NA, NT, a.ntile, tg, KIND == 0, ns);
+  aa.tgroup = tg;
   fn<<<grid, kTcThreads, smem, st>>>(aa, A0, A1, B);
   return cudaGetLastError();
 }

@@ -1,0 +1,84 @@
+// k3moe_tc.cuh -- declarations of the multi-token path: the tensor-core grouped GEMM
+// (k3moe_tc.cu), its routing and quantisation helpers (k3moe_prefill.cu) and the screening
+// router (k3moe_router_tc.cu).
+#pragma once
+#include <cuda.h>
+#include "k3moe_kernels.cuh"
+
+namespace k3 {
+
+constexpr int kTcRows = 128;     // A rows / B rows per tensor-core tile
+constexpr int kTcTermsX = 4;     // MXFP4 terms of the layer input x (bf16)
+constexpr int kTcTermsAct = 4;   // MXFP4 terms of the SiTU activations (float)
+constexpr int kTcTokens = 4096;  // tokens per pass of the multi-token path
+
+// Arguments of k_tc_gemm.  Groups g = 0..ngroups-1 own B rows [off[g], off[g+1]) and
+// tile_off[g] = sum over earlier groups of ceil(rows / 128); gid[g] is the A index of
+// group g in the A tensor map's third dimension (NULL: g itself).
+struct TcGemmArgs {
+  const int32_t *off, *tile_off, *gid;
+  int ngroups;
+  int mtiles;        // ceil(M_rows / 128)
+  int M_rows;        // rows of each A matrix (outputs)
+  int kchunks;       // 128-byte chunks of K
+  int ksteps_last;   // 32-byte MMA steps in the last chunk (1..4)
+  int ntile;         // B rows per tile (multiple of 16, at most 128)
+  int nstages;       // data stages, set by the launcher
+  int nsf;           // scale-byte slots, set by the launcher
+  int nacc;          // accumulator buffers (1 or 2), set by the launcher
+  int tgroup;        // B terms side by side in one MMA (divides the term count), set by
+                     // the launcher
+  int a_pair;        // 1: A matrices 0 and 1 are one 4-D map (third dimension = matrix),
+                     // fetched by one copy per stage
+  const uint8_t *sfa[2];   // MXF4: scale bytes of A matrix m for group 0, rows of sf_rowb
+  long long sfa_gstride;   // bytes between consecutive groups' A scales
+  int sf_rowb;             // scale bytes per row (K / 32)
+  const uint8_t *sfb;      // MXF4: B scale bytes [term][K chunk][B row][8]
+  long long sfb_tstride;   // bytes between terms
+  long long sfb_cstride;   // bytes between K chunks (B rows x 8)
+  float *out;              // [B row][out_ld]
+  long long out_ld;
+  float b1, b2;            // SiTU caps (gate/up epilogue)
+  int32_t *status;
+};
+
+enum class TcKind { kMxf4GateUp, kMxf4Down, kBf16GateUp, kBf16Down, kBf16Store };
+
+// Tensor map of bytes of rank 3..5 (dims[0] = K bytes, innermost; strides in bytes of
+// dims 1..rank-1) with 128-byte swizzle and boxes of box[0] = 128 bytes x box[1..]; false if
+// the driver entry point is missing or the layout is refused.
+bool tc_map(CUtensorMap *m, const void *base, int rank, const unsigned long long *dims,
+            const unsigned long long *strides, const unsigned *box);
+// The 3-D case (inner = K bytes, rows, depth) with boxes of 128 bytes x box_rows x
+// box_depth.
+bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
+              unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
+              unsigned long long depth_stride, int box_rows, int box_depth = 1);
+cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &A0,
+                           const CUtensorMap &A1, const CUtensorMap &B, int grid,
+                           cudaStream_t st);
+
+__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int ntile,
+                             int32_t *off, int32_t *tile_off, int32_t *inv, int32_t *status);
+__global__ void k_route_scatter(const int32_t *__restrict__ idx, int P,
+                                const int32_t *__restrict__ off, int32_t *perm, int32_t *inv);
+__global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
+                          const int32_t *__restrict__ inv, int P, uint8_t *__restrict__ xq,
+                          uint8_t *__restrict__ xs);
+__global__ void k_quant_act(const float *__restrict__ act, int P, int I,
+                            uint8_t *__restrict__ aq, uint8_t *__restrict__ as);
+__global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t *__restrict__ out);
+__global__ void k_group1(int n, int ntile, int32_t *off, int32_t *tile_off);
+__global__ void k_row_norms(const uint16_t *__restrict__ v, int R, int H, float *__restrict__ out);
+__global__ void k_route_candidates(const float *__restrict__ Lt, const float *__restrict__ xn,
+                                   const float *__restrict__ wn,
+                                   const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
+                                   const float *__restrict__ bias, int H, int E, int K,
+                                   float *__restrict__ sc, float *__restrict__ ch,
+                                   int32_t *__restrict__ ncand, int32_t *status);
+size_t route_candidates_smem(int H, int E, int K);
+__global__ void k_combine(int T, int H, int K, const float *__restrict__ w,
+                          const int32_t *__restrict__ inv, const float *__restrict__ dpair,
+                          const float *__restrict__ ds, void *y, int ydt, int accumulate);
+
+}  // namespace k3

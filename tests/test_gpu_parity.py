@@ -163,11 +163,14 @@ SHAPES = [
     (2048, 512, 33, 8, 1, 2),
     # tensor-core path (two tokens and up, H and I multiples of 64, at least 256): ragged
     # 128-row tiles (I 320, H 320), a partial last 128-byte K chunk (H/2 = 160, I/2 = 160),
-    # more than 128 pairs on one expert (T 300 over 4 experts), no shared expert
+    # more than 128 pairs on one expert (T 300 over 4 experts), no shared expert; B tiles
+    # of 32, 48, 64 and 128 rows (several activation terms side by side in one MMA, or one)
     (256, 256, 8, 2, 1, 5),
     (320, 320, 6, 3, 1, 40),
     (512, 384, 4, 2, 1, 300),
     (768, 256, 12, 4, 0, 64),
+    (256, 320, 8, 2, 1, 150),
+    (384, 256, 8, 2, 0, 200),
 ]
 
 
