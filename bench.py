@@ -33,7 +33,8 @@ WORKLOAD = ("decode1: 1 token/step through one full-shape MoE layer (hidden 7168
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each decode kernel, keyed to a hash of the sources the kernels are built
 # from: a changed kernel reports null until it is captured again.
-TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode.cu",
+TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode_fused.cu",
+                   "mxfp4_routed_expert_02_gb300/csrc/k3moe_decode.cu",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_router.cu",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_device.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_topk.cuh",
@@ -66,10 +67,12 @@ def step_bytes(cfg, U):
     op = I * H // 2 + I * H // 32            # one MXFP4 operand (packed + scales)
     gate_up = U * 2 * op                    # W1 and W3 of each distinct expert
     down = U * op + H * SI * 2 + H * 4       # W2 of each distinct expert, shared W2s, y
+    router = E * H * 2 + 2 * SI * H * 2 + H * 2   # Wr, shared W1s/W3s, x
     return {
-        "k_router_shared": E * H * 2 + 2 * SI * H * 2 + H * 2,   # Wr, shared W1s/W3s, x
+        "k_router_shared": router, "k_router_t1": router,
         "k_expert_gateup": gate_up, "k_gateup_t1": gate_up,
         "k_down_combine": down, "k_down_tma": down,
+        "k_decode_fused": router + gate_up + down,  # the whole step in one kernel
     }
 
 
@@ -274,7 +277,7 @@ def run_ours(args):
     used = [len(set(steps_idx[(args.warmup + s) % NX].tolist())) for s in range(args.steps)]
     U = statistics.mean(used)
     nb = step_bytes(cfg, U)
-    bytes_step = nb["k_router_shared"] + nb["k_gateup_t1"] + nb["k_down_tma"]
+    bytes_step = nb["k_decode_fused"]
     launches = sum(v[1] for v in trace.values())
     kernels = {k: {"ms_avg": v[0] / v[1], "launches": v[1]} for k, v in trace.items() if v[1]}
     # the dominant kernel: most device time among the kernels that stream the weights
@@ -471,9 +474,13 @@ def run_batch(args):
         extra = {"useful_tflops_step": fl / sec / 1e12,
                  "down_kernel_tflops": 2.0 * P * H * I / (dk * 1e-3) / 1e12 if dk else None}
     else:
-        dom = "k_tc_gemm_gateup" if name == "decode64_zipf" else "k_gateup_t1"
+        if name == "decode64_zipf":
+            dom = "k_tc_gemm_gateup"
+            db = sum(u * 2 * op for u in U) / L        # gate/up bytes of the distinct experts
+        else:
+            dom = "k_decode_fused"                      # one kernel per layer: all its bytes
+            db = sum(layer_bytes) / L
         dk = kernels.get(dom, {}).get("ms_avg")
-        db = sum(u * 2 * op for u in U) / L
         roofline = {"bound": "hbm", "kernel": dom,
                     "achieved": db / (dk * 1e-3) / 1e9 if dk else None, "peak": peak_hbm,
                     "unit": "GB/s", "frac": db / (dk * 1e-3) / 1e9 / peak_hbm if dk else None,

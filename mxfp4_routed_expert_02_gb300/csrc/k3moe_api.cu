@@ -4,6 +4,7 @@
 // the path runs in this library's kernels; nothing here computes on the host.
 #include <cstdio>
 #include <cstring>
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -44,7 +45,7 @@ const DeviceInfo *device_info() {
             cudaSuccess ||
         cudaFuncSetAttribute(k_route_candidates, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              128 * 1024) != cudaSuccess ||
-        set_decode_smem_limits() != cudaSuccess)
+        set_decode_smem_limits() != cudaSuccess || set_fused_smem_limit() != cudaSuccess)
       return nullptr;
     d.attrs_set = true;
   }
@@ -95,6 +96,7 @@ struct Ws {
   uint16_t *act_hi, *act_lo;
   int32_t *act_ex;
   float *act_s;
+  unsigned *bar;  // grid-barrier counters of the single-token fused kernel
   size_t total;
 };
 
@@ -118,6 +120,7 @@ Ws ws_layout(const k3moe_dims *d, int T, void *base) {
   w.act_lo = reinterpret_cast<uint16_t *>(take(P * d->inter * 2));
   w.act_ex = reinterpret_cast<int32_t *>(take(P * (d->inter / kGroup) * 4));
   w.act_s = reinterpret_cast<float *>(take((size_t)Tc * (d->shared_inter > 0 ? d->shared_inter : 1) * 4));
+  w.bar = reinterpret_cast<unsigned *>(take(16));
   w.total = o;
   return w;
 }
@@ -131,13 +134,13 @@ enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KI
                 KID_DEQUANT, KID_GATEUP_T1, KID_DOWN_TMA, KID_ROUTE_HIST, KID_ROUTE_SCATTER,
                 KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
                 KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_NORMS, KID_TC_ROUTER,
-                KID_ROUTE_CAND, KID_COUNT };
+                KID_ROUTE_CAND, KID_DECODE_FUSED, KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {
     "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
     "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
     "k_route_scatter", "k_quant_x", "k_tc_gemm_gateup", "k_quant_act", "k_tc_gemm_down",
     "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine",
-    "k_row_norms", "k_tc_gemm_router", "k_route_candidates"};
+    "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -341,6 +344,15 @@ k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *
   return run_down(di, d, Tc, ea, idx, w, sh_down, ws, y, ydt, accumulate, status, st, false);
 }
 
+// Exponent e with |b1 b2| 2^-e < 2^15 (at least one binade of headroom below the f16
+// maximum), clamped to a range where every scale is a normal float.
+int act_scale_exp(float b1, float b2) {
+  const double m = std::fabs((double)b1 * (double)b2);
+  int e = -100;
+  if (m > 0.0) e = std::ilogb(m) + 1 - 15;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
 // The whole layer for Tc tokens.  One token with a supported width: router kernel, then
 // the single-token gate/up kernel (top-k and dispatch fused), then the down kernel, the
 // last two launched as programmatic dependents so their prologues overlap the previous
@@ -350,6 +362,29 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
                        const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
                        Ws &ws, int32_t *idx, float *w, void *y, k3moe_dtype ydt, int accumulate,
                        int32_t *status, cudaStream_t st) {
+  if (Tc == 1 &&
+      fused_t1_smem(d->hidden, d->inter, d->n_experts, d->topk, d->shared_inter, di->sms) > 0) {
+    // the whole step in one cooperative kernel; its two grid-barrier counters start at zero
+    if (cudaMemsetAsync(ws.bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return K3MOE_ERR_CUDA;
+    FusedT1Args a;
+    a.x = x; a.H = d->hidden; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
+    a.SI = d->shared_inter;
+    a.wr = wr; a.bias = bias;
+    a.sh_gate = sh_gate; a.sh_up = sh_up; a.sh_down = sh_down;
+    a.ex = expert_args(d, ex);
+    a.renorm = d->renorm; a.routed_scale = d->routed_scale;
+    a.b1 = d->situ_b1; a.b2 = d->situ_b2;
+    a.sc = ws.sc; a.ch = ws.ch; a.act_s = ws.act_s;
+    a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
+    a.bar = ws.bar;
+    // |SiTU| <= b1 b2: scale the activations so that the largest stays below 2^15
+    a.act_exp = act_scale_exp(d->situ_b1, d->situ_b2);
+    a.idx_out = idx; a.w_out = w;
+    a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate;
+    a.status = status;
+    TraceScope ts(KID_DECODE_FUSED, st);
+    return launch_fused_t1(a, di->sms, st) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+  }
   const int rb = t1_row_block(d->hidden);
   if (Tc == 1 && rb > 0) {
     k3moe_status s = run_route(di, d, x, Tc, wr, bias, sh_gate, sh_up, ws, idx, w, status, st,

@@ -1,0 +1,888 @@
+// k3moe_decode_fused.cu -- the whole MoE layer step for one decode token in one persistent
+// kernel: one CTA per SM, launched cooperatively so that every CTA is resident, with two
+// grid-wide dependencies (bounded waits on a counter pair in the workspace).
+//
+// What it computes is the single-token layer step of the other decode kernels (README of
+// FareedKhan-dev/kimi-k3-in-c: section 9 "Picking 16 experts of 896" for the router and
+// the top-k, the LatentMoE listing steps 3 and 6 for the expert FFN, the routed sum and
+// the shared expert, the activation listing for SiTU; section 4 for the MXFP4 format;
+// README of Maknee/Kimi-K3.cpp, "The consumer-memory idea" item 7, for the router order of
+// the sum).  The schedule is what changes: every weight byte -- router rows, the shared
+// expert, the selected experts -- goes through one ring of bulk-copy stages per SM, in
+// the order
+//
+//   X  the token's input (once per CTA: every consumer thread takes its inputs from it)
+//   R  router rows (two per stage)           -> logits, scores, selection scores
+//   S  shared-expert gate/up row pairs       -> SiTU activations of the shared expert
+//   G  the selected experts' gate/up rows    -> SiTU activations of the 16 experts
+//   D  down rows of 16-row output tiles: the selected experts (two per stage) and the
+//      shared expert, then the router-order combine of the tile
+//
+// so the stream never drains: the top-k needs every CTA's R rows (dependency 1: a counter
+// the epilogue warps bump once their router rows are written) and is computed by the
+// consumer warps of every CTA while the ring fills with S stages; D needs every
+// activation (dependency 2: all worker warps of every CTA), while the ring already holds
+// the first D stages.
+//
+// Warp roles: workers 0..2n-1 (n = H/1024) consume X, R, S and G stages (thread (h, g):
+// input group g, row parity h) and select the top-k; warp 14 reduces their partial sums
+// (logits and scores, SiTU); warp 16 issues the bulk copies.  In D all 16 worker warps
+// consume.
+// Every wait is bounded: on expiry the kernel reports K3MOE_ERR_TIMEOUT, keeps arriving on
+// the barriers it owes, and writes zeros.
+#include "k3moe_kernels.cuh"
+
+namespace k3 {
+
+namespace {
+
+constexpr int kFuWorkers = 16;   // worker warps
+constexpr int kFuEpi = 14;       // warp index of the reduction epilogue
+constexpr int kFuProducer = 16;  // warp index of the bulk-copy producer
+constexpr int kFuThreads = 32 * (kFuWorkers + 1);
+constexpr int kFuRB = 4;         // gate/up rows per G stage
+constexpr int kFuItemRows = 8;   // gate/up rows per reduction item (two G stages)
+constexpr int kFuNSD = 4;        // D ring slots (one per group of four worker warps)
+constexpr int kFuMaxNS = 8;      // R/S/G ring slots at most
+constexpr int kFuDownRows = 16;  // output rows per down tile
+constexpr int kFuRedBytes = 2 * 16 * 64 * 4;  // partial sums [parity][warp][row][2]
+constexpr int kBarDown = 1;      // named barrier of the 16 worker warps (0 is __syncthreads)
+constexpr int kBarCons = 2;      // named barrier of the R/S/G consumer warps
+
+// shared-memory map: barriers and small arrays; the ring (X/R/S/G slots, then D slots);
+// the partial sums
+constexpr int kFuBars = 0;       // fullG[8] emptyG[8] fullD[4] emptyD[4] redbar[2] redfree[2]
+                                 // selbar
+constexpr int kFuSel = 256;      // int[32]
+constexpr int kFuWsel = 384;     // float[32]
+constexpr int kFuMisc = 512;     // int[8]: top-k scratch [0..3], abort flag [4]
+constexpr int kFuGDone = 576;    // int[8]: X/R/S/G slot s fully consumed (set by its owner)
+constexpr int kFuSmall = 1024;   // top-k: histogram [256], selected keys [32], warp or/and;
+                                 // D: dbuf [K][16] + ds [16]
+constexpr int kFuSmallBytes = 4096;
+constexpr int kFuRing = kFuSmall + kFuSmallBytes;
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Order this thread's generic-proxy accesses before later async-proxy (bulk copy) ones.
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until a counter (zeroed by the host before the launch) reaches n.
+__device__ bool wait_count(const unsigned *cnt, unsigned n) {
+  const long long t0 = clock64();
+  while (ld_acquire_u32(cnt) < n) {
+    if (clock64() - t0 > kWaitBudget) return false;
+    __nanosleep(64);  // let the other lanes of the warp issue
+  }
+  return true;
+}
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
+  return __shfl_xor_sync(0xffffffffu, v, o);
+}
+
+// Top-k of one token by the nt consumer threads (named barrier bar, nt a multiple of 32).
+// Keys as in cta_topk: the selection score's order-preserving bits, then the complemented
+// expert index, so the unsigned order is (score desc, index asc) and keys are distinct.
+// The K-th largest key is found by radix selection from the highest bit where the keys
+// differ (the bits above it are common to all of them): per pass an 8-bit digit, a
+// histogram of the keys that share the prefix found so far, and the digit where the count
+// from the top reaches K; the search stops once that digit's keys are all selected.  The
+// K keys >= the prefix are then sorted by warp 0.  E <= 8 nt, K <= 32.
+__device__ void topk_cta(const float *sc, const float *ch, int E, int K, int renorm,
+                         float routed_scale, int nt, int bar, uint32_t *hist,
+                         unsigned long long *list, unsigned long long *wred, int *misc,
+                         int *sel, float *wsel) {
+  constexpr int KPT = 8;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = nt >> 5;
+  unsigned long long key[KPT];
+  unsigned long long kor = 0ull, kand = ~0ull;
+#pragma unroll
+  for (int k = 0; k < KPT; k++) {
+    const int e = t + nt * k;
+    key[k] = 0ull;
+    if (e < E) {
+      float c = __fadd_rn(__ldcg(ch + e), 0.f);     // -0 -> +0
+      if (c != c) c = -__int_as_float(0x7f800000);  // a NaN never wins (it is reported)
+      key[k] = ((unsigned long long)float_order_key(c) << 32) |
+               (unsigned long long)(0xffffffffu - (uint32_t)e);
+      kor |= key[k];
+      kand &= key[k];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kor |= shfl_xor_u64(kor, o);
+    kand &= shfl_xor_u64(kand, o);
+  }
+  if (lane == 0) {
+    wred[2 * warp] = kor;
+    wred[2 * warp + 1] = kand;
+  }
+  if (t == 0) misc[3] = 0;
+  named_bar_sync(bar, nt);
+  kor = 0ull;
+  kand = ~0ull;
+  for (int w = 0; w < nw; w++) {
+    kor |= wred[2 * w];
+    kand &= wred[2 * w + 1];
+  }
+  const unsigned long long diff = kor ^ kand;
+  const int b = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
+  unsigned long long mask = (b >= 63) ? 0ull : ~((2ull << b) - 1ull);
+  unsigned long long prefix = kand & mask;
+  int need = K;
+  for (int top = b;; top -= 8) {
+    const int lowb = top - 7 > 0 ? top - 7 : 0;
+    const unsigned dmask = (1u << (top - lowb + 1)) - 1u;
+    for (int i = t; i < 256; i += nt) hist[i] = 0u;
+    named_bar_sync(bar, nt);
+#pragma unroll
+    for (int k = 0; k < KPT; k++)
+      if (key[k] != 0ull && (key[k] & mask) == prefix)
+        atomicAdd(&hist[(unsigned)(key[k] >> lowb) & dmask], 1u);
+    named_bar_sync(bar, nt);
+    if (warp == 0) {
+      // lane l takes digits 255-8l down to 248-8l; counts are scanned from the top
+      uint32_t c[8], s = 0;
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        c[q] = hist[255 - 8 * lane - q];
+        s += c[q];
+      }
+      uint32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - s;
+      if (lane == 0) misc[2] = -1;
+      __syncwarp();
+      if (excl < (uint32_t)need && (uint32_t)need <= incl) {
+        uint32_t ab = excl;
+        for (int q = 0; q < 8; q++) {
+          if (ab + c[q] >= (uint32_t)need) {
+            misc[0] = 255 - 8 * lane - q;
+            misc[1] = (int)ab;
+            misc[2] = (int)c[q];
+            break;
+          }
+          ab += c[q];
+        }
+      }
+    }
+    named_bar_sync(bar, nt);
+    const int digit = misc[0], above = misc[1], cnt = misc[2];
+    if (cnt < 0) break;  // not reached: need <= the keys left under the prefix
+    need -= above;
+    prefix |= (unsigned long long)digit << lowb;
+    mask |= (unsigned long long)dmask << lowb;
+    if (cnt == need || lowb == 0) break;
+  }
+  // every key >= prefix is selected (exactly K of them)
+#pragma unroll
+  for (int k = 0; k < KPT; k++)
+    if (key[k] != 0ull && key[k] >= prefix) {
+      const int at = atomicAdd(&misc[3], 1);
+      if (at < 32) list[at] = key[k];
+    }
+  named_bar_sync(bar, nt);
+  if (warp == 0) {
+    const int nsel = misc[3];
+    unsigned long long v = (lane < K && lane < nsel) ? list[lane] : 0ull;
+    // bitonic sort of 32 keys, descending
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned long long o = shfl_xor_u64(v, stride);
+        const bool lower = (lane & stride) == 0;
+        const bool desc = (lane & size) == 0;
+        v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    }
+    int e = 0;
+    float s = 0.f;
+    if (lane < K) {
+      e = (v == 0ull) ? 0 : (int)(0xffffffffu - (uint32_t)(v & 0xffffffffull));
+      s = __ldcg(sc + e);
+    }
+    float wsum = 0.f;  // float sum of the chosen scores in selection order
+    for (int j = 0; j < K; j++) wsum = __fadd_rn(wsum, __shfl_sync(0xffffffffu, s, j));
+    if (lane < K) {
+      float w = s;
+      if (renorm && wsum > 0.f) w = __fdiv_rn(w, wsum);
+      sel[lane] = e;
+      wsel[lane] = __fmul_rn(w, routed_scale);
+    }
+  }
+  named_bar_sync(bar, nt);
+}
+
+}  // namespace
+
+// ---- layout of the fused kernel, shared by the host and the device ----------------------
+// [small arrays | ring | partial sums].  The ring holds NSG X/R/S/G slots (the largest of
+// a G stage -- kFuRB rows of gate and of up, packed + scales -- and an R/S stage of two
+// bf16 rows of H); in phase D the same bytes hold kFuNSD D slots: the larger of a routed
+// stage (16 rows of two experts, packed + scales, and those experts' activations) and a
+// shared stage (8 bf16 rows of the shared down matrix and its activations).
+__host__ __device__ inline uint32_t fused_gslot_bytes(int H) {
+  const uint32_t g = (uint32_t)(2 * kFuRB * (H / 2 + H / kGroup));
+  const uint32_t r = (uint32_t)(2 * H * 2);
+  return ((g > r ? g : r) + 127u) & ~127u;
+}
+__host__ __device__ inline uint32_t fused_dexp_bytes(int I) {  // one expert's 16 down rows
+  return (uint32_t)(kFuDownRows * (I / 2 + I / kGroup));
+}
+__host__ __device__ inline uint32_t fused_dslot_bytes(int I, int SI) {
+  const uint32_t r = 2 * fused_dexp_bytes(I) + 2u * (uint32_t)I * 4u;
+  const uint32_t sh = SI > 0 ? 8u * (uint32_t)SI * 2u + (uint32_t)SI * 4u : 0u;
+  return ((r > sh ? r : sh) + 127u) & ~127u;
+}
+constexpr size_t kFuSmemMax = 227 * 1024;
+__host__ __device__ inline int fused_nsg(int H) {
+  const int ns = (int)((kFuSmemMax - kFuRing - kFuRedBytes) / fused_gslot_bytes(H));
+  return ns > kFuMaxNS ? kFuMaxNS : ns;
+}
+__host__ __device__ inline uint32_t fused_ring_bytes(int H, int I, int SI) {
+  const uint32_t g = (uint32_t)fused_nsg(H) * fused_gslot_bytes(H);
+  const uint32_t d = (uint32_t)kFuNSD * fused_dslot_bytes(I, SI);
+  return g > d ? g : d;
+}
+
+__global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = a.H, I = a.I, K = a.K, E = a.E, SI = a.SI;
+  const int G = H / kGroup, nwc = G / 32;  // consumer warps per row parity
+  const int rowb = H / 2;                  // packed bytes of a gate/up row
+  const int rowh = H * 2;                  // bytes of a bf16 row of H
+  const uint32_t gstage = (uint32_t)(2 * kFuRB * (rowb + G));
+  const int G2 = I / kGroup, rowb2 = I / 2;
+  const uint32_t dexp = fused_dexp_bytes(I);    // one expert's 16 down rows
+  const uint32_t gslot = fused_gslot_bytes(H);
+  const uint32_t dslot = fused_dslot_bytes(I, SI);
+  const int NSG = fused_nsg(H);
+  constexpr int RS = 8;                          // shared down rows per D stage
+  const int nSD = SI > 0 ? kFuDownRows / RS : 0;  // shared-down stages per tile
+  const int bx = blockIdx.x, nb = gridDim.x;
+  // this CTA's work
+  const int cntR = bx < E ? (E - bx + nb - 1) / nb : 0;  // router rows bx + nb k
+  const int nR = (cntR + 1) / 2;                          // R stages
+  const int nS = bx < SI ? (SI - bx + nb - 1) / nb : 0;   // shared pairs bx + nb k
+  const int blocks = I / kFuItemRows;                     // 8-row blocks per expert
+  const int nitems = K * blocks;
+  const int nI = bx < nitems ? (nitems - bx + nb - 1) / nb : 0;  // items bx + nb k
+  const int tR = 1, tS = 1 + nR, tG = 1 + nR + nS;          // first X, R, S, G stages
+  const int nRSG = tG + 2 * nI;
+  const int ntiles = H / kFuDownRows;
+  const int nT = bx < ntiles ? (ntiles - bx + nb - 1) / nb : 0;  // tiles bx + nb k
+  const int hk = K / 2;
+  const int dpt = hk + nSD;  // D stages per tile
+  const int nD = nT * dpt;
+
+  uint8_t *ring = smem + kFuRing;
+  auto slot_ptr = [&](int s) -> uint8_t * { return ring + (size_t)s * gslot; };
+  auto dslot_ptr = [&](int d) -> uint8_t * { return ring + (size_t)d * dslot; };
+  uint64_t *fullG = reinterpret_cast<uint64_t *>(smem + kFuBars);
+  uint64_t *emptyG = fullG + 8;
+  uint64_t *fullD = fullG + 16;
+  uint64_t *emptyD = fullG + 20;
+  uint64_t *redbar = fullG + 24;
+  uint64_t *redfree = fullG + 26;
+  uint64_t *selbar = fullG + 28;
+  int *sel = reinterpret_cast<int *>(smem + kFuSel);
+  float *wsel = reinterpret_cast<float *>(smem + kFuWsel);
+  int *misc = reinterpret_cast<int *>(smem + kFuMisc);
+  volatile int *abort_flag = misc + 4;
+  volatile int *gdone = reinterpret_cast<volatile int *>(smem + kFuGDone);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kFuSmall);
+  unsigned long long *list = reinterpret_cast<unsigned long long *>(smem + kFuSmall + 1024);
+  unsigned long long *wred = reinterpret_cast<unsigned long long *>(smem + kFuSmall + 1280);
+  float *dbuf = reinterpret_cast<float *>(smem + kFuSmall);  // [K][16] (D)
+  float *ds = dbuf + K * kFuDownRows;                        // [16] (D)
+  float *red = reinterpret_cast<float *>(ring + fused_ring_bytes(H, I, SI));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < NSG; s++) {
+      mbar_init(&fullG[s], 1);
+      mbar_init(&emptyG[s], 2 * nwc);
+    }
+    for (int d = 0; d < kFuNSD; d++) {
+      mbar_init(&fullD[d], 1);
+      mbar_init(&emptyD[d], 4);
+    }
+    for (int p = 0; p < 2; p++) {
+      mbar_init(&redbar[p], 2 * nwc);
+      mbar_init(&redfree[p], 1);
+    }
+    mbar_init(selbar, 1);
+    misc[4] = 0;
+    for (int s = 0; s < kFuMaxNS; s++) gdone[s] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kFuProducer) {
+    // ---------------- producer: lane p < NSG owns ring slot p ----------------
+    bool ab = false;
+    int last_g = -1;  // this lane's last R/S/G stage
+    if (lane < NSG) {
+      bool have_sel = false;
+      for (int t = lane; t < nRSG; t += NSG) {
+        if (t >= tG && !have_sel) {  // routed stages need the top-k
+          if (!mbar_wait(selbar, 0)) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            ab = true;
+            break;
+          }
+          have_sel = true;
+        }
+        if (!mbar_wait(&emptyG[lane], ((t / NSG) & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          ab = true;
+          break;
+        }
+        uint8_t *dst = slot_ptr(lane);
+        if (t == 0) {
+          mbar_arrive_expect_tx(&fullG[lane], (uint32_t)rowh);
+          bulk_g2s(dst, a.x, rowh, &fullG[lane]);
+        } else if (t < tS) {
+          const int k0 = 2 * (t - tR);
+          const int nrow = cntR - k0 < 2 ? cntR - k0 : 2;
+          mbar_arrive_expect_tx(&fullG[lane], (uint32_t)(nrow * rowh));
+          for (int rr = 0; rr < nrow; rr++)
+            bulk_g2s(dst + rr * rowh, a.wr + (size_t)(bx + nb * (k0 + rr)) * H, rowh,
+                     &fullG[lane]);
+        } else if (t < tG) {
+          const int p = bx + nb * (t - tS);
+          mbar_arrive_expect_tx(&fullG[lane], (uint32_t)(2 * rowh));
+          bulk_g2s(dst, a.sh_gate + (size_t)p * H, rowh, &fullG[lane]);
+          bulk_g2s(dst + rowh, a.sh_up + (size_t)p * H, rowh, &fullG[lane]);
+        } else {
+          const int tg = t - tG;
+          const int item = bx + nb * (tg >> 1);
+          const int j = item / blocks, blk = item % blocks;
+          const int r = blk * kFuItemRows + (tg & 1) * kFuRB;
+          const uint8_t *rec = a.ex.base + (long long)sel[j] * a.ex.stride;
+          mbar_arrive_expect_tx(&fullG[lane], gstage);
+          bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, kFuRB * rowb, &fullG[lane]);
+          bulk_g2s(dst + kFuRB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, kFuRB * rowb,
+                   &fullG[lane]);
+          bulk_g2s(dst + 2 * kFuRB * rowb, rec + a.ex.off[1] + (size_t)r * G, kFuRB * G,
+                   &fullG[lane]);
+          bulk_g2s(dst + 2 * kFuRB * rowb + kFuRB * G, rec + a.ex.off[5] + (size_t)r * G,
+                   kFuRB * G, &fullG[lane]);
+        }
+        last_g = t;
+      }
+    }
+    // D stages: stage i = (tile n = i / dpt, m = i % dpt): m < hk the routed experts
+    // 2m, 2m+1 with their activations, else rows (m - hk) RS .. of the shared expert with
+    // its activations; D slot i % 4, issued by lane i % 4 once the X/R/S/G slots that
+    // share its bytes are consumed.  Weights go in flight at once; the activations only
+    // once every CTA has written them (dependency 2, polled here).
+    // every lane waits for the consumption of its own slot's last stage (a parity wait is
+    // only safe on a barrier at most one phase behind: the owner's) and publishes it
+    if (lane < NSG) {
+      if (!ab && last_g >= 0 && !mbar_wait(&emptyG[lane], (last_g / NSG) & 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        ab = true;
+      }
+      __threadfence_block();
+      gdone[lane] = 1;
+    }
+    int iD = lane;
+    if (lane < kFuNSD && !ab && nD > 0) {
+      const int g0 = (int)((uint32_t)lane * dslot / gslot);
+      int g1 = (int)((((uint32_t)lane + 1u) * dslot - 1u) / gslot);
+      g1 = g1 < NSG - 1 ? g1 : NSG - 1;
+      for (int gs = g0; gs <= g1 && !ab; gs++) {
+        const long long t0 = clock64();
+        while (!gdone[gs]) {
+          if (clock64() - t0 > kWaitBudget) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            ab = true;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      __threadfence_block();
+      if (!ab && !mbar_wait(selbar, 0)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        ab = true;
+      }
+      bool dep2 = false;
+      for (; !ab && iD < nD; iD += kFuNSD) {
+        const int q = iD & 3, u = iD >> 2;
+        if (!mbar_wait(&emptyD[q], (u & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          ab = true;
+          break;
+        }
+        const int n = iD / dpt, m = iD % dpt;
+        const int r0 = (bx + nb * n) * kFuDownRows;
+        uint8_t *dst = dslot_ptr(q);
+        const bool routed = m < hk;
+        const uint32_t wbytes = routed ? 2 * dexp : (uint32_t)(RS * SI * 2);
+        const uint32_t abytes = routed ? (uint32_t)(2 * I * 4) : (uint32_t)(SI * 4);
+        mbar_arrive_expect_tx(&fullD[q], wbytes + abytes);
+        if (routed) {
+          for (int e2 = 0; e2 < 2; e2++) {
+            const uint8_t *rec = a.ex.base + (long long)sel[2 * m + e2] * a.ex.stride;
+            bulk_g2s(dst + e2 * dexp, rec + a.ex.off[2] + (size_t)r0 * rowb2,
+                     kFuDownRows * rowb2, &fullD[q]);
+            bulk_g2s(dst + e2 * dexp + kFuDownRows * rowb2,
+                     rec + a.ex.off[3] + (size_t)r0 * G2, kFuDownRows * G2, &fullD[q]);
+          }
+        } else {
+          const int rs0 = r0 + (m - hk) * RS;
+          bulk_g2s(dst, a.sh_down + (size_t)rs0 * SI, wbytes, &fullD[q]);
+        }
+        if (!dep2) {
+          if (!wait_count(a.bar + 1, (unsigned)nb)) {
+            set_status(a.status, K3MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          fence_proxy_async_all();
+          dep2 = true;
+        }
+        if (routed) {
+          // experts 2m, 2m+1: hi then lo, I values each, after the weights
+          for (int e2 = 0; e2 < 2; e2++) {
+            uint8_t *ad = dst + 2 * dexp + e2 * (I * 4);
+            bulk_g2s(ad, a.act_hi + (size_t)(2 * m + e2) * I, (uint32_t)(I * 2), &fullD[q]);
+            bulk_g2s(ad + I * 2, a.act_lo + (size_t)(2 * m + e2) * I, (uint32_t)(I * 2),
+                     &fullD[q]);
+          }
+        } else {
+          bulk_g2s(dst + wbytes, a.act_s, abytes, &fullD[q]);
+        }
+      }
+    }
+    if (ab) {
+      // bounded waits for this lane's copies still in flight
+      if (lane < NSG && last_g >= 0) mbar_wait(&fullG[lane], (last_g / NSG) & 1, 400000000LL);
+      if (lane < kFuNSD && iD - kFuNSD >= 0 && iD - kFuNSD < nD)
+        mbar_wait(&fullD[lane], ((iD - kFuNSD) >> 2) & 1, 400000000LL);
+    }
+    return;
+  }
+
+  if (warp == kFuEpi) {
+    // ---------------- epilogue: the partial sums of each reduction item ----------------
+    int n = 0;
+    auto take = [&](int nn) -> const float * {
+      const int par = nn & 1;
+      if (!mbar_wait(&redbar[par], (nn >> 1) & 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      return red + par * (16 * 64);
+    };
+    auto release = [&](int nn) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&redfree[nn & 1]);
+    };
+    // R: router rows 2s, 2s+1 of this CTA -> logit (float-float sum of the warps' pairs),
+    // collected in lane 2s + r; then every lane's unbiased score (logistic in double,
+    // rounded once; the slow double pipe runs once for all rows) and selection score
+    float mylogit = 0.f;
+    for (int s = 0; s < nR; s++, n++) {
+      const float *rt = take(n);
+      float hi = 0.f, lo = 0.f;
+      if (lane < 2) {
+        for (int w = lane * nwc; w < (lane + 1) * nwc; w++) ff_add(hi, lo, rt[w * 64], rt[w * 64 + 1]);
+      }
+      release(n);
+      const float h0 = __shfl_sync(0xffffffffu, hi, 0), h1 = __shfl_sync(0xffffffffu, hi, 1);
+      if (lane == 2 * s) mylogit = h0;
+      if (lane == 2 * s + 1) mylogit = h1;
+    }
+    if (lane < cntR) {
+      const int row = bx + nb * lane;
+      const float sv = (float)(1.0 / (1.0 + exp(-(double)mylogit)));
+      const float cv = __fadd_rn(sv, a.bias ? a.bias[row] : 0.f);
+      a.sc[row] = sv;
+      a.ch[row] = cv;
+      if (!(fabsf(cv) <= 3.402823466e38f)) set_status(a.status, K3MOE_ERR_NONFINITE);
+      __threadfence();
+    }
+    __syncwarp();
+    if (lane == 0) {  // dependency 1: this CTA's router rows are written
+      __threadfence();
+      atomicAdd(a.bar, 1u);
+    }
+    // S: shared pair p -> SiTU(gate, up)
+    for (int s = 0; s < nS; s++, n++) {
+      const float *rt = take(n);
+      float gs = 0.f, us = 0.f;
+      if (lane == 0) {
+        for (int w = 0; w < nwc; w++) gs += rt[w * 64];
+        for (int w = nwc; w < 2 * nwc; w++) us += rt[w * 64];
+      }
+      release(n);
+      if (lane == 0) a.act_s[bx + nb * s] = situ(gs, us, a.b1, a.b2);
+    }
+    // G: rows of an 8-row block of expert slot j -> SiTU -> f16 hi + lo at the fixed scale
+    // 2^-act_exp (|SiTU| <= b1 b2, so the scaled value stays below 2^15)
+    const float inv = pow2i(-a.act_exp);
+    for (int s = 0; s < nI; s++, n++) {
+      const float *rt = take(n);
+      const int item = bx + nb * s;
+      const int j = item / blocks, blk = item % blocks;
+      const int r = lane & (kFuItemRows - 1), hp = r & 1;
+      float gs = 0.f, us = 0.f;
+      for (int w = hp * nwc; w < (hp + 1) * nwc; w++) {
+        gs += rt[(w * 32 + r) * 2];
+        us += rt[(w * 32 + r) * 2 + 1];
+      }
+      release(n);
+      if (lane < kFuItemRows) {
+        float act = situ(gs, us, a.b1, a.b2);
+        if (*abort_flag) act = 0.f;
+        const float sa = act * inv;
+        const __half hh = __float2half_rn(sa);
+        const __half hl = __float2half_rn(sa - __half2float(hh));
+        const int row = blk * kFuItemRows + r;
+        const size_t o = act_index(j, I, row / kTileRows, row % kTileRows);
+        a.act_hi[o] = __half_as_ushort(hh);
+        a.act_lo[o] = __half_as_ushort(hl);
+      }
+    }
+  } else if (warp < 2 * nwc) {
+    // ---------------- consumers: thread (h, g) ----------------
+    const int h = tid / G, g = tid % G;
+    const int nt = 2 * nwc * 32;  // consumer threads
+    int t = 0, n = 0;
+    bool aborted = false;
+    auto begin_item = [&](int nn) -> float * {
+      const int par = nn & 1;
+      if (!aborted && !mbar_wait(&redfree[par], ((nn >> 1) & 1) ^ 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        aborted = true;
+        *abort_flag = 1;
+      }
+      return red + par * (16 * 64);
+    };
+    auto stage_in = [&](int tt) -> const uint8_t * {
+      const int s = tt % NSG;
+      if (!aborted && !mbar_wait(&fullG[s], (tt / NSG) & 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        aborted = true;
+        *abort_flag = 1;
+      }
+      return slot_ptr(s);
+    };
+    auto stage_out = [&](int tt) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&emptyG[tt % NSG]);
+    };
+    auto end_item = [&](int nn) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&redbar[nn & 1]);  // also when aborted: no one hangs
+    };
+    // X: MXFP4 rows use input group g (32 inputs prescaled to f16); bf16 rows use the
+    // 16-byte chunks g + G c (c < 4) of the row, so a warp reads consecutive chunks
+    uint32_t xr[16];
+    int xe;
+    uint4 xb[4];
+    {
+      const uint4 *xs = reinterpret_cast<const uint4 *>(stage_in(t));
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const uint4 c = xs[g * 4 + q];
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          v[8 * q + 2 * k] = bf16_lo(w4[k]);
+          v[8 * q + 2 * k + 1] = bf16_hi(w4[k]);
+        }
+      }
+      xe = prescale_group_f16(v, xr);
+#pragma unroll
+      for (int c = 0; c < 4; c++) xb[c] = xs[g + G * c];
+      stage_out(t);
+      t++;
+    }
+    // R: row h of the stage, exact bf16 products summed as a float-float pair
+    for (int s = 0; s < nR; s++, t++, n++) {
+      float *rt = begin_item(n);
+      const uint8_t *st = stage_in(t);
+      float hi = 0.f, lo = 0.f;
+      if (!aborted && 2 * s + h < cntR) {
+        const uint4 *w4 = reinterpret_cast<const uint4 *>(st + h * rowh);
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          const uint4 wv = w4[g + G * c];
+          const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+          const uint32_t xa[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            float p = __fmul_rn(bf16_lo(wa[q]), bf16_lo(xa[q]));
+            float sx, ex;
+            two_sum(hi, p, sx, ex);
+            hi = sx;
+            lo = __fadd_rn(lo, ex);
+            p = __fmul_rn(bf16_hi(wa[q]), bf16_hi(xa[q]));
+            two_sum(hi, p, sx, ex);
+            hi = sx;
+            lo = __fadd_rn(lo, ex);
+          }
+        }
+      }
+      stage_out(t);
+      {
+        const float sx = __fadd_rn(hi, lo);
+        lo = __fsub_rn(lo, __fsub_rn(sx, hi));
+        hi = sx;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+        ff_add(hi, lo, oh, ol);
+      }
+      if (lane == 0) {
+        rt[warp * 64] = hi;
+        rt[warp * 64 + 1] = lo;
+      }
+      end_item(n);
+    }
+    // top-k, once every CTA's router rows are in the workspace; the ring meanwhile fills
+    // with S stages
+    if (tid == 0 && !wait_count(a.bar, (unsigned)nb)) {
+      set_status(a.status, K3MOE_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    named_bar_sync(kBarCons, nt);
+    topk_cta(a.sc, a.ch, E, K, a.renorm, a.routed_scale, nt, kBarCons, hist, list, wred, misc,
+             sel, wsel);
+    if (bx == 0 && tid < K && a.idx_out) {
+      a.idx_out[tid] = sel[tid];
+      a.w_out[tid] = wsel[tid];
+    }
+    if (tid == 0) mbar_arrive(selbar);
+    // S: gate row (h = 0) or up row (h = 1) of shared pair s, fp32 sums of exact products
+    for (int s = 0; s < nS; s++, t++, n++) {
+      float *rt = begin_item(n);
+      const uint8_t *st = stage_in(t);
+      float acc = 0.f;
+      if (!aborted) {
+        const uint4 *w4 = reinterpret_cast<const uint4 *>(st + h * rowh);
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          const uint4 wv = w4[g + G * c];
+          const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+          const uint32_t xa[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            acc = fmaf(bf16_lo(wa[q]), bf16_lo(xa[q]), acc);
+            acc = fmaf(bf16_hi(wa[q]), bf16_hi(xa[q]), acc);
+          }
+        }
+      }
+      stage_out(t);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) rt[warp * 64] = acc;
+      end_item(n);
+    }
+    // G: an 8-row block = two stages of kFuRB gate and up rows; thread (h, g) takes the
+    // rows of parity h in input group g
+    constexpr int V = 2 * kFuRB;  // (2 rows x 2 matrices) x 2 stages
+    for (int s = 0; s < nI; s++, n++) {
+      float *rt = begin_item(n);
+      float vals[V];
+#pragma unroll
+      for (int v = 0; v < V; v++) vals[v] = 0.f;
+#pragma unroll
+      for (int b2 = 0; b2 < 2; b2++, t++) {
+        const uint8_t *st = stage_in(t);
+        if (!aborted) {
+          const uint8_t *sgs = st + 2 * kFuRB * rowb;
+          const uint8_t *sus = sgs + kFuRB * G;
+#pragma unroll
+          for (int k = 0; k < kFuRB / 2; k++) {
+            const int q = h + 2 * k;  // row within the stage
+            const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
+            const uint4 wu = reinterpret_cast<const uint4 *>(st + (kFuRB + q) * rowb)[g];
+            const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
+            if (sg != 255u) vals[b2 * kFuRB + 2 * k] = group_dot(xr, wg) * group_factor(sg, xe);
+            if (su != 255u)
+              vals[b2 * kFuRB + 2 * k + 1] = group_dot(xr, wu) * group_factor(su, xe);
+          }
+        }
+        stage_out(t);
+      }
+      // value v = b2*RB + 2k + m  ->  block row b2*RB + h + 2k, matrix m
+      const float tot = warp_transpose_reduce<V>(vals);
+      if (lane < V) {
+        const int b2 = lane / kFuRB, k = (lane % kFuRB) / 2, m = lane & 1;
+        rt[(warp * 32 + b2 * kFuRB + h + 2 * k) * 2 + m] = tot;
+      }
+      end_item(n);
+    }
+  }
+
+  // ---------------- dependency 2: this CTA's activations are written ----------------
+  // (the producer waits for every CTA's before it copies activations into D stages)
+  constexpr int NDT = kFuWorkers * 32;  // worker threads
+  fence_proxy_async_all();              // generic writes before the bulk copies that read them
+  named_bar_sync(kBarDown, NDT);
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(a.bar + 1, 1u);
+  }
+
+  // ---------------- D: down rows, shared down rows, router-order combine ----------------
+  const int q = warp >> 2, v = warp & 3;  // D slot, unit within the stage
+  bool aborted = *abort_flag != 0;
+  const int NG = G2 / 16;                   // groups per lane
+  const int rq = lane >> 4, l = lane & 15;  // row quarter (4 rows), group lane
+  const int e2 = a.act_exp;
+  for (int n = 0; n < nT; n++) {
+    const int r0 = (bx + nb * n) * kFuDownRows;
+    for (int i = tid; i < (K + 1) * kFuDownRows; i += NDT) dbuf[i] = 0.f;  // dbuf and ds
+    named_bar_sync(kBarDown, NDT);
+    for (int m = 0; m < dpt; m++) {
+      const int i = n * dpt + m;
+      if ((i & 3) != q) continue;
+      if (!aborted && !mbar_wait(&fullD[q], (i >> 2) & 1)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        aborted = true;
+      }
+      const uint8_t *st = dslot_ptr(q);
+      if (!aborted && m < hk) {
+        // expert slot j = 2m + v/2, rows (v & 1) 8 .. + 8 of the tile
+        const int j = 2 * m + (v >> 1), rh = v & 1;
+        const uint8_t *sp = st + (v >> 1) * dexp;
+        const uint8_t *ss = sp + kFuDownRows * rowb2;
+        const uint16_t *s_hi = reinterpret_cast<const uint16_t *>(st + 2 * dexp + (v >> 1) * (I * 4));
+        const uint16_t *s_lo = s_hi + I;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int qq = 0; qq < NG; qq++) {
+          // the 16 group lanes read 16 consecutive 16-byte weight chunks of a row
+          const int gg = qq * 16 + l;
+          uint32_t xh[16], xl[16];
+          const uint4 *ph = reinterpret_cast<const uint4 *>(s_hi + act_index(0, I, gg, 0));
+          const uint4 *pl = reinterpret_cast<const uint4 *>(s_lo + act_index(0, I, gg, 0));
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            const uint4 x0 = ph[c * G2], x1 = pl[c * G2];
+            xh[4 * c] = x0.x; xh[4 * c + 1] = x0.y; xh[4 * c + 2] = x0.z; xh[4 * c + 3] = x0.w;
+            xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
+          }
+#pragma unroll
+          for (int r = 0; r < 4; r++) {
+            const int row = rh * 8 + rq * 4 + r;
+            const uint4 wv = reinterpret_cast<const uint4 *>(sp + row * rowb2)[gg];
+            const uint32_t sv = ss[row * G2 + gg];
+            if (sv != 255u) acc[r] += group_dot2(xh, xl, wv) * group_factor(sv, e2);
+          }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+          for (int r = 0; r < 4; r++) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+        }
+        if (l == 0) {
+#pragma unroll
+          for (int r = 0; r < 4; r++) dbuf[j * kFuDownRows + rh * 8 + rq * 4 + r] = acc[r];
+        }
+      } else if (!aborted) {
+        // shared expert: rows v, v + 4, .. < RS of this stage; bf16 weights, fp32 inputs
+        const int nch = SI >> 3;
+        for (int rr = v; rr < RS; rr += 4) {
+          const uint4 *w4 = reinterpret_cast<const uint4 *>(st + (size_t)rr * SI * 2);
+          const float4 *a4 = reinterpret_cast<const float4 *>(st + RS * SI * 2);
+          float sacc = 0.f;
+          for (int c = lane; c < nch; c += 32) {
+            const uint4 wv = w4[c];
+            const float4 a0 = a4[2 * c], a1 = a4[2 * c + 1];
+            sacc = fmaf(bf16_lo(wv.x), a0.x, sacc);
+            sacc = fmaf(bf16_hi(wv.x), a0.y, sacc);
+            sacc = fmaf(bf16_lo(wv.y), a0.z, sacc);
+            sacc = fmaf(bf16_hi(wv.y), a0.w, sacc);
+            sacc = fmaf(bf16_lo(wv.z), a1.x, sacc);
+            sacc = fmaf(bf16_hi(wv.z), a1.y, sacc);
+            sacc = fmaf(bf16_lo(wv.w), a1.z, sacc);
+            sacc = fmaf(bf16_hi(wv.w), a1.w, sacc);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+          if (lane == 0) ds[(m - hk) * RS + rr] = sacc;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&emptyD[q]);
+    }
+    if (aborted) *abort_flag = 1;
+    named_bar_sync(kBarDown, NDT);
+    if (tid < kFuDownRows) {
+      const int row = tid;
+      float sum = 0.f;
+      for (int j = 0; j < K; j++)
+        sum = __fadd_rn(sum, __fmul_rn(wsel[j], dbuf[j * kFuDownRows + row]));
+      if (SI > 0) sum = __fadd_rn(sum, ds[row]);  // the shared expert, unweighted, last
+      if (*abort_flag) sum = 0.f;
+      const size_t o = (size_t)r0 + row;
+      if (a.ydt == K3MOE_F32) {
+        float *yf = reinterpret_cast<float *>(a.y);
+        yf[o] = a.accumulate ? __fadd_rn(yf[o], sum) : sum;
+      } else {
+        uint16_t *yb = reinterpret_cast<uint16_t *>(a.y);
+        const float vv = a.accumulate ? __fadd_rn(bf16_lo(yb[o]), sum) : sum;
+        yb[o] = f32_to_bf16(vv);
+      }
+    }
+    named_bar_sync(kBarDown, NDT);
+  }
+}
+
+size_t fused_t1_smem(int H, int I, int E, int K, int SI, int grid) {
+  const int G = H / kGroup, G2 = I / kGroup;
+  if (H % 1024 != 0 || G / 32 < 1 || G / 32 > 7) return 0;  // 2 G/32 consumer warps <= 14
+  if (I % 512 != 0 || G2 / 16 > 8) return 0;               // 16 group lanes, <= 8 groups each
+  if (K < 2 || K > 16 || K % 2 != 0) return 0;             // two experts per down stage
+  if (SI < 0 || SI % 256 != 0) return 0;                   // shared rows in 32 lanes x 8
+  if (grid < 1) return 0;
+  if (E > 8 * 64 * (G / 32) || (E + grid - 1) / grid > 32) return 0;  // top-k keys, R rows
+  if (fused_nsg(H) < 2) return 0;
+  const size_t total = (size_t)kFuRing + fused_ring_bytes(H, I, SI) + kFuRedBytes;
+  return total <= kFuSmemMax ? total : 0;
+}
+
+cudaError_t set_fused_smem_limit() {
+  return cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              227 * 1024);
+}
+
+// Cooperative launch: the runtime refuses it unless every CTA can be resident at once,
+// which the grid-wide dependencies need.
+cudaError_t launch_fused_t1(const FusedT1Args &a, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFuThreads);
+  cfg.dynamicSmemBytes = fused_t1_smem(a.H, a.I, a.E, a.K, a.SI, grid);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_decode_fused, a);
+}
+
+}  // namespace k3

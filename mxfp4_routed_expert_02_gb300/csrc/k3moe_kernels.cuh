@@ -94,6 +94,33 @@ struct DownArgs {
   int32_t *status;
 };
 
+// ---- the single-token layer step as one persistent kernel (k3moe_decode_fused.cu)
+struct FusedT1Args {
+  const uint16_t *x;  // [H] bf16
+  int H, I, E, K, SI;
+  const uint16_t *wr;  // [E][H]
+  const float *bias;   // [E] or null
+  const uint16_t *sh_gate, *sh_up, *sh_down;  // null when SI == 0
+  ExpertArgs ex;
+  int renorm;
+  float routed_scale, b1, b2;
+  float *sc, *ch;       // [E] workspace
+  float *act_s;         // [SI] workspace
+  uint16_t *act_hi, *act_lo;  // [K][I] workspace
+  int32_t *act_ex;            // [K][I/32] workspace
+  unsigned *bar;              // two grid-wide counters, zeroed before the launch
+  int act_exp;                // activations are stored as f16 hi + lo of act * 2^-act_exp
+  int32_t *idx_out;
+  float *w_out;  // [K] or null
+  void *y;
+  int ydt, accumulate;
+  int32_t *status;
+};
+// Shared memory the fused kernel needs for this shape (0: the shape does not fit it).
+size_t fused_t1_smem(int H, int I, int E, int K, int SI, int grid);
+cudaError_t launch_fused_t1(const FusedT1Args &a, int grid, cudaStream_t st);
+cudaError_t set_fused_smem_limit();
+
 size_t gateup_t1_smem(int H, int E, int K, int RB, int NS);
 cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl);
 size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem, int ntl);

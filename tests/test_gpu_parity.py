@@ -171,6 +171,14 @@ SHAPES = [
     (768, 256, 12, 4, 0, 64),
     (256, 320, 8, 2, 1, 150),
     (384, 256, 8, 2, 0, 200),
+    # one token through the fused single-token kernel (H a multiple of 1024, I of 512, top-k
+    # even): 1..7 consumer warps per row parity, 1..2 groups per down lane, an odd number of
+    # down stages per tile (top-6), top-16, two shared experts or none, more experts than
+    # top-k threads (200)
+    (1024, 512, 24, 6, 1, 1),
+    (2048, 512, 40, 16, 2, 1),
+    (3072, 1024, 40, 4, 0, 1),
+    (1024, 512, 200, 8, 1, 1),
 ]
 
 
@@ -179,6 +187,60 @@ def test_layer_shapes(H, I, E, K, NS, T):
     cfg = dataclasses.replace(synth.config("tiny"), name="custom", hidden=H, inter=I,
                               n_experts=E, topk=K, tokens=T, n_shared=NS)
     check_layer(Layer(cfg, seed=H + T))
+
+
+def fused_layer(seed, **kw):
+    """A one-token layer at a shape the fused single-token kernel takes."""
+    base = dict(hidden=1024, inter=512, n_experts=24, topk=6, tokens=1, n_shared=1)
+    base.update(kw)
+    cfg = dataclasses.replace(synth.config("tiny"), name="custom", **base)
+    return Layer(cfg, seed=seed)
+
+
+def test_fused_single_token_ties_bias_bf16_accumulate():
+    # equal selection scores (duplicated router rows: the lower index wins), a large bias
+    # that forces one expert in without changing the weights, bf16 output, y += layer,
+    # and bitwise reproducibility across calls
+    L = fused_layer(31)
+    wr = L.host["wr"].copy()
+    wr[7] = wr[3]
+    wr[12] = wr[3]
+    wr[20] = wr[9]
+    bias = L.host["bias"].copy()
+    bias[3] = bias[7] = bias[12] = 1.5
+    bias[17] = 3.0
+    L.host["wr"], L.host["bias"] = wr, bias
+    L.d_wr = torch.from_numpy(wr.view(np.int16)).cuda()
+    L.d_bias = torch.from_numpy(bias).cuda()
+    oi, ow, oy = L.oracle()
+    assert oi[0, :4].tolist() == [17, 3, 7, 12]
+    y1, idx, w, st = L.run()
+    assert st == 0
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    assert np.allclose(w.cpu().numpy(), ow, rtol=2e-7, atol=0)
+    assert rel_l2(y1.cpu().numpy(), oy) <= REL_L2_F32
+    y2, _, _, _ = L.run()
+    assert torch.equal(y1, y2)
+    base = torch.randn_like(y1)
+    y3, _, _, st = L.run(y=base.clone(), accumulate=True)
+    assert st == 0 and torch.equal(y3, base + y1)
+    yb, _, _, st = L.run(ydt=torch.bfloat16)
+    assert st == 0 and max_rel(yb.float().cpu().numpy(), oy) <= MAX_REL_BF16
+
+
+def test_fused_single_token_scale_255_and_0_groups():
+    L = fused_layer(32, topk=8, n_experts=16, n_shared=0)
+    cfg = L.cfg
+    off = cfg.record_offsets
+    rec = L._host_experts
+    rng = np.random.default_rng(5)
+    for op in (1, 3, 5):
+        seg = rec[:, off[op]:off[op + 1]]
+        seg[rng.random(seg.shape) < 0.05] = 255
+        seg[rng.random(seg.shape) < 0.05] = 0
+    view = L.experts.view(cfg.n_experts, L.stride)
+    view[:, :L.rec_bytes].copy_(torch.from_numpy(rec))
+    check_layer(L)
 
 
 def test_layer_accumulate_and_determinism():
