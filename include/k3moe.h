@@ -27,6 +27,11 @@
  *   - Pointers must be 16-byte aligned (K3MOE_ERR_ALIGN otherwise).
  *   - Thread safety: calls are independent; two calls may run concurrently only if
  *     they use different workspaces.
+ *   - Workspace: zero-fill it once before its first use (e.g. one cudaMemsetAsync).  Its
+ *     first 256 bytes hold counters of the single-token kernel that must be zero when a
+ *     call starts; every call leaves them zero, so a workspace can be reused across calls,
+ *     entry points, shapes and token counts without clearing it again.  Do not write to
+ *     a workspace between calls.  The rest is scratch.
  */
 #ifndef K3MOE_H
 #define K3MOE_H
@@ -147,8 +152,8 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
 
 /* Size of the library's static scratch array (8 MiB), the most scratch that
  * k3moe_layer_static_scratch can use.  At the model's shape (H 7168, I 1536, 896
- * experts, top 16, shared 1536) it holds the workspace of up to 9 tokens: 115,040 bytes
- * for one token, 8,275,200 for nine.                                                  */
+ * experts, top 16, shared 1536) it holds the workspace of up to 9 tokens: 115,296 bytes
+ * for one token, 8,157,952 for nine.                                                  */
 #define K3MOE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
 /* k3moe_layer without a workspace argument: the same kernels, arguments, results and
@@ -165,8 +170,9 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
  *     looks up the device address of the array (which may load the library's device
  *     code) and sets kernel attributes.  Make that first call before any stream capture
  *     starts on the device.  K3MOE_ERR_CUDA if the lookup fails.
- *   - Nothing in the array has to start at zero: each call writes every scratch word
- *     before it reads it.
+ *   - The array is zero when the library loads, and every call leaves the counter words
+ *     at its start zero again (see Workspace above); the rest is written before it is
+ *     read.
  *   - Every call on a device shares the one array.  Calls ordered on one stream are
  *     safe; two calls whose work can overlap on the device (different streams without
  *     an ordering between them, or concurrent host threads) race on the array and

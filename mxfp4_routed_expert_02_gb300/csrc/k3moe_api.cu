@@ -100,10 +100,15 @@ struct Ws {
   size_t total;
 };
 
+// The first kWsHeader bytes of every workspace hold the single-token kernel's grid-wide
+// counters, which must be zero before a call and are zero again after it; no layout
+// places anything else there.
+constexpr size_t kWsHeader = 256;
+
 Ws ws_layout(const k3moe_dims *d, int T, void *base) {
   const int Tc = T < kDecodeTokens ? T : kDecodeTokens;
   const size_t P = (size_t)Tc * d->topk;
-  size_t o = 0;
+  size_t o = kWsHeader;
   Ws w{};
   const uintptr_t b = reinterpret_cast<uintptr_t>(base);
   auto take = [&](size_t bytes) {
@@ -120,7 +125,7 @@ Ws ws_layout(const k3moe_dims *d, int T, void *base) {
   w.act_lo = reinterpret_cast<uint16_t *>(take(P * d->inter * 2));
   w.act_ex = reinterpret_cast<int32_t *>(take(P * (d->inter / kGroup) * 4));
   w.act_s = reinterpret_cast<float *>(take((size_t)Tc * (d->shared_inter > 0 ? d->shared_inter : 1) * 4));
-  w.bar = reinterpret_cast<unsigned *>(take(16));
+  w.bar = reinterpret_cast<unsigned *>(b);  // the header
   w.total = o;
   return w;
 }
@@ -364,8 +369,8 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
                        int32_t *status, cudaStream_t st) {
   if (Tc == 1 &&
       fused_t1_smem(d->hidden, d->inter, d->n_experts, d->topk, d->shared_inter, di->sms) > 0) {
-    // the whole step in one cooperative kernel; its two grid-barrier counters start at zero
-    if (cudaMemsetAsync(ws.bar, 0, 2 * sizeof(unsigned), st) != cudaSuccess) return K3MOE_ERR_CUDA;
+    // the whole step in one cooperative kernel; its grid-wide counters (workspace header)
+    // are zero on entry and left zero by the kernel's last CTA
     FusedT1Args a;
     a.x = x; a.H = d->hidden; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
     a.SI = d->shared_inter;
@@ -452,7 +457,7 @@ WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
   const int Tc = T < kTcTokens ? T : kTcTokens;
   const size_t H = d->hidden, I = d->inter, E = d->n_experts, SI = d->shared_inter;
   const size_t P = (size_t)Tc * d->topk;
-  size_t o = 0;
+  size_t o = kWsHeader;
   const uintptr_t b = reinterpret_cast<uintptr_t>(base);
   auto take = [&](size_t bytes) {
     const size_t at = o;

@@ -1,6 +1,7 @@
 // k3moe_decode_fused.cu -- the whole MoE layer step for one decode token in one persistent
 // kernel: one CTA per SM, launched cooperatively so that every CTA is resident, with two
-// grid-wide dependencies (bounded waits on a counter pair in the workspace).
+// grid-wide dependencies (bounded waits on counters in the workspace header, which the
+// last CTA to finish leaves zero for the next call).
 //
 // What it computes is the single-token layer step of the other decode kernels (README of
 // FareedKhan-dev/kimi-k3-in-c: section 9 "Picking 16 experts of 896" for the router and
@@ -708,8 +709,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
 #pragma unroll
       for (int v = 0; v < V; v++) vals[v] = 0.f;
 #pragma unroll
-      for (int b2 = 0; b2 < 2; b2++, t++) {
-        const uint8_t *st = stage_in(t);
+      // both stages of the item first: eight independent dot products per thread
+      const uint8_t *stA = stage_in(t);
+      const uint8_t *stB = stage_in(t + 1);
+#pragma unroll
+      for (int b2 = 0; b2 < 2; b2++) {
+        const uint8_t *st = b2 ? stB : stA;
         if (!aborted) {
           const uint8_t *sgs = st + 2 * kFuRB * rowb;
           const uint8_t *sus = sgs + kFuRB * G;
@@ -719,13 +724,15 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
             const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
             const uint4 wu = reinterpret_cast<const uint4 *>(st + (kFuRB + q) * rowb)[g];
             const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
-            if (sg != 255u) vals[b2 * kFuRB + 2 * k] = group_dot(xr, wg) * group_factor(sg, xe);
-            if (su != 255u)
-              vals[b2 * kFuRB + 2 * k + 1] = group_dot(xr, wu) * group_factor(su, xe);
+            // group_factor is 0 for scale byte 255 and the dot is finite: no branch
+            vals[b2 * kFuRB + 2 * k] = group_dot(xr, wg) * group_factor(sg, xe);
+            vals[b2 * kFuRB + 2 * k + 1] = group_dot(xr, wu) * group_factor(su, xe);
           }
         }
-        stage_out(t);
       }
+      stage_out(t);
+      stage_out(t + 1);
+      t += 2;
       // value v = b2*RB + 2k + m  ->  block row b2*RB + h + 2k, matrix m
       const float tot = warp_transpose_reduce<V>(vals);
       if (lane < V) {
@@ -848,6 +855,18 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       }
     }
     named_bar_sync(kBarDown, NDT);
+  }
+  // exit: every use of the counters by this CTA is over (its producer read the second
+  // one before it copied the activations its D stages needed); the last CTA to get here
+  // leaves all three zero for the next call
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.bar + 2, 1u) == (unsigned)nb - 1) {
+      a.bar[0] = 0u;
+      a.bar[1] = 0u;
+      a.bar[2] = 0u;
+      __threadfence();
+    }
   }
 }
 

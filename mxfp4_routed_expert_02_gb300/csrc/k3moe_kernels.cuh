@@ -108,7 +108,7 @@ struct FusedT1Args {
   float *act_s;         // [SI] workspace
   uint16_t *act_hi, *act_lo;  // [K][I] workspace
   int32_t *act_ex;            // [K][I/32] workspace
-  unsigned *bar;              // two grid-wide counters, zeroed before the launch
+  unsigned *bar;              // dependency 1, dependency 2, exit: zero on entry and on exit
   int act_exp;                // activations are stored as f16 hi + lo of act * 2^-act_exp
   int32_t *idx_out;
   float *w_out;  // [K] or null

@@ -169,8 +169,9 @@ def workspace_size(dims: LayerDims, T: int) -> int:
 
 
 def new_workspace(dims: LayerDims, T: int, device=None) -> torch.Tensor:
+    """A workspace for T tokens, zero-filled as the C ABI requires before first use."""
     n = workspace_size(dims, T)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def new_status(device=None) -> torch.Tensor:
