@@ -43,7 +43,7 @@ constexpr int kFuProducer = 16;  // warp index of the bulk-copy producer
 constexpr int kFuThreads = 32 * (kFuWorkers + 1);
 constexpr int kFuRB = 4;         // gate/up rows per G stage
 constexpr int kFuItemRows = 8;   // gate/up rows per reduction item (two G stages)
-constexpr int kFuNSD = 4;        // D ring slots (one per group of four worker warps)
+constexpr int kFuNSD = 4;        // D ring slots: two per group of eight worker warps
 constexpr int kFuMaxNS = 8;      // R/S/G ring slots at most
 constexpr int kFuDownRows = 16;  // output rows per down tile
 constexpr int kFuRedBytes = 2 * 16 * 64 * 4;  // partial sums [parity][warp][row][2]
@@ -84,6 +84,12 @@ __device__ bool wait_count(const unsigned *cnt, unsigned n) {
     __nanosleep(64);  // let the other lanes of the warp issue
   }
   return true;
+}
+// D slot of D stage i: stages alternate between the two worker groups (i % 2), and each
+// group between its two slots, so a group computes on one slot while the other fills.
+__host__ __device__ __forceinline__ int d_slot_of(int i) {
+  const int r = i & 3;
+  return r == 1 ? 2 : (r == 2 ? 1 : r);
 }
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
   return __shfl_xor_sync(0xffffffffu, v, o);
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     }
     for (int d = 0; d < kFuNSD; d++) {
       mbar_init(&fullD[d], 1);
-      mbar_init(&emptyD[d], 4);
+      mbar_init(&emptyD[d], 8);
     }
     for (int p = 0; p < 2; p++) {
       mbar_init(&redbar[p], 2 * nwc);
@@ -389,7 +395,8 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     }
     // D stages: stage i = (tile n = i / dpt, m = i % dpt): m < hk the routed experts
     // 2m, 2m+1 with their activations, else rows (m - hk) RS .. of the shared expert with
-    // its activations; D slot i % 4, issued by lane i % 4 once the X/R/S/G slots that
+    // its activations.  Stage i goes to worker group i % 2 and to that group's slots in
+    // turn (d_slot_of); lane d issues the stages of slot d once the X/R/S/G slots that
     // share its bytes are consumed.  Weights go in flight at once; the activations only
     // once every CTA has written them (dependency 2, polled here).
     // every lane waits for the consumption of its own slot's last stage (a parity wait is
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       __threadfence_block();
       gdone[lane] = 1;
     }
-    int iD = lane;
+    int iD = d_slot_of(lane);  // the first stage of slot `lane` (d_slot_of is an involution)
     if (lane < kFuNSD && !ab && nD > 0) {
       const int g0 = (int)((uint32_t)lane * dslot / gslot);
       int g1 = (int)((((uint32_t)lane + 1u) * dslot - 1u) / gslot);
@@ -425,7 +432,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       }
       bool dep2 = false;
       for (; !ab && iD < nD; iD += kFuNSD) {
-        const int q = iD & 3, u = iD >> 2;
+        const int q = lane, u = iD >> 2;
         if (!mbar_wait(&emptyD[q], (u & 1) ^ 1)) {
           set_status(a.status, K3MOE_ERR_TIMEOUT);
           ab = true;
@@ -708,7 +715,6 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       float vals[V];
 #pragma unroll
       for (int v = 0; v < V; v++) vals[v] = 0.f;
-#pragma unroll
       // both stages of the item first: eight independent dot products per thread
       const uint8_t *stA = stage_in(t);
       const uint8_t *stB = stage_in(t + 1);
@@ -754,10 +760,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
   }
 
   // ---------------- D: down rows, shared down rows, router-order combine ----------------
-  const int q = warp >> 2, v = warp & 3;  // D slot, unit within the stage
+  // worker group gD (eight warps) takes the D stages i with i % 2 == gD; warp wg of the
+  // group takes expert wg / 4 of a routed stage, rows 4 (wg % 4) .. + 4
+  const int gD = warp >> 3, wg = warp & 7;
   bool aborted = *abort_flag != 0;
   const int NG = G2 / 16;                   // groups per lane
-  const int rq = lane >> 4, l = lane & 15;  // row quarter (4 rows), group lane
+  const int rp = lane >> 4, l = lane & 15;  // row pair, group lane
   const int e2 = a.act_exp;
   for (int n = 0; n < nT; n++) {
     const int r0 = (bx + nb * n) * kFuDownRows;
@@ -765,20 +773,21 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     named_bar_sync(kBarDown, NDT);
     for (int m = 0; m < dpt; m++) {
       const int i = n * dpt + m;
-      if ((i & 3) != q) continue;
+      if ((i & 1) != gD) continue;
+      const int q = d_slot_of(i);
       if (!aborted && !mbar_wait(&fullD[q], (i >> 2) & 1)) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
         aborted = true;
       }
       const uint8_t *st = dslot_ptr(q);
       if (!aborted && m < hk) {
-        // expert slot j = 2m + v/2, rows (v & 1) 8 .. + 8 of the tile
-        const int j = 2 * m + (v >> 1), rh = v & 1;
-        const uint8_t *sp = st + (v >> 1) * dexp;
+        // expert slot j = 2m + wg/4; each lane: rows rb + 2 rp, +1 over NG input groups
+        const int ex = wg >> 2, j = 2 * m + ex, rb = (wg & 3) * 4 + rp * 2;
+        const uint8_t *sp = st + ex * dexp;
         const uint8_t *ss = sp + kFuDownRows * rowb2;
-        const uint16_t *s_hi = reinterpret_cast<const uint16_t *>(st + 2 * dexp + (v >> 1) * (I * 4));
+        const uint16_t *s_hi = reinterpret_cast<const uint16_t *>(st + 2 * dexp + ex * (I * 4));
         const uint16_t *s_lo = s_hi + I;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[2] = {0.f, 0.f};
         for (int qq = 0; qq < NG; qq++) {
           // the 16 group lanes read 16 consecutive 16-byte weight chunks of a row
           const int gg = qq * 16 + l;
@@ -792,26 +801,26 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
             xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
           }
 #pragma unroll
-          for (int r = 0; r < 4; r++) {
-            const int row = rh * 8 + rq * 4 + r;
+          for (int r = 0; r < 2; r++) {
+            const int row = rb + r;
             const uint4 wv = reinterpret_cast<const uint4 *>(sp + row * rowb2)[gg];
             const uint32_t sv = ss[row * G2 + gg];
-            if (sv != 255u) acc[r] += group_dot2(xh, xl, wv) * group_factor(sv, e2);
+            acc[r] += group_dot2(xh, xl, wv) * group_factor(sv, e2);  // 0 for byte 255
           }
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) {
-#pragma unroll
-          for (int r = 0; r < 4; r++) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+          acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+          acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
         }
         if (l == 0) {
-#pragma unroll
-          for (int r = 0; r < 4; r++) dbuf[j * kFuDownRows + rh * 8 + rq * 4 + r] = acc[r];
+          dbuf[j * kFuDownRows + rb] = acc[0];
+          dbuf[j * kFuDownRows + rb + 1] = acc[1];
         }
       } else if (!aborted) {
-        // shared expert: rows v, v + 4, .. < RS of this stage; bf16 weights, fp32 inputs
+        // shared expert: row wg of this stage; bf16 weights, fp32 inputs
         const int nch = SI >> 3;
-        for (int rr = v; rr < RS; rr += 4) {
+        for (int rr = wg; rr < RS; rr += 8) {
           const uint4 *w4 = reinterpret_cast<const uint4 *>(st + (size_t)rr * SI * 2);
           const float4 *a4 = reinterpret_cast<const float4 *>(st + RS * SI * 2);
           float sacc = 0.f;
