@@ -39,9 +39,8 @@ TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode_fused.cu",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_device.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_topk.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_kernels.cuh"]
-TRAFFIC_CAPTURED = {"sources": "0101231a7c9f9f76",
-                    "bytes": {"k_gateup_t1": 190727424, "k_down_tma": 118842368,
-                              "k_router_t1": 45020416}}
+TRAFFIC_CAPTURED = {"sources": "44ad470b12421a77",
+                    "bytes": {"k_decode_fused": 351343104}}
 
 
 def traffic_of(kernel):
@@ -91,6 +90,9 @@ class Clocks:
             self.f = open(self.path, "w")
             self.p = subprocess.Popen(["nvidia-smi", "--query-gpu=" + q, "--format=csv,noheader",
                                        "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)  # sampling is running before the timed region starts
         except OSError:
             self.p = None
         return self
@@ -512,7 +514,9 @@ def run_batch(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (0 = the workload's default: long enough for the "
+                         "200 ms clock sampler to see the timed region)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -525,6 +529,9 @@ def main():
                     help="routed experts resident (896 = the workload; fewer only to keep "
                          "profiler captures small)")
     args = ap.parse_args()
+    if args.steps <= 0:
+        args.steps = {"decode1": 3000, "decode64_zipf": 200, "prefill4096": 40,
+                      "stacked8": 256}[args.workload]
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
