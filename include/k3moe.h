@@ -198,7 +198,9 @@ typedef struct {
  * l = 0 .. L-1,
  *     x = bf16(RMSNorm(h))        (k3moe_rmsnorm_bf16 with eps; weight 1)
  *     h = h + layer_l(x)          (k3moe_layer, float output added to h)
- * h float [T][H] is updated in place; x_scratch bf16 [T][H] is caller scratch;
+ * h float [T][H] is updated in place; x_scratch bf16 [T][H] is caller scratch (for one
+ * token at the shapes of the single-token kernel the RMSNorm runs inside that kernel, one
+ * launch per layer, and x_scratch is not written);
  * idx_out / w_out ([L][T][K] each) receive every layer's route when not NULL.
  * layers is a HOST array of L entries (device pointers inside).  Needs
  * k3moe_workspace_size(dims, T) bytes of workspace, shared by the layers in turn.     */

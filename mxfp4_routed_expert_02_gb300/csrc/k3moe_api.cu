@@ -358,6 +358,40 @@ int act_scale_exp(float b1, float b2) {
   return e < -100 ? -100 : (e > 100 ? 100 : e);
 }
 
+// Whether the single-token fused kernel takes this shape.
+bool fused_takes(const DeviceInfo *di, const k3moe_dims *d) {
+  return fused_t1_smem(d->hidden, d->inter, d->n_experts, d->topk, d->shared_inter, di->sms) > 0;
+}
+
+// One token through the fused kernel: input x (bf16), or h (float, the residual stream)
+// normalised in the kernel (x = bf16(RMSNorm(h)) with eps).  Its grid-wide counters
+// (workspace header) are zero on entry and left zero by the kernel's last CTA.
+k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x,
+                       const float *h, float eps, const uint16_t *wr, const float *bias,
+                       const k3moe_experts *ex, const uint16_t *sh_gate, const uint16_t *sh_up,
+                       const uint16_t *sh_down, Ws &ws, int32_t *idx, float *w, void *y,
+                       k3moe_dtype ydt, int accumulate, int32_t *status, cudaStream_t st) {
+  FusedT1Args a;
+  a.x = x; a.h = h; a.eps = eps;
+  a.H = d->hidden; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
+  a.SI = d->shared_inter;
+  a.wr = wr; a.bias = bias;
+  a.sh_gate = sh_gate; a.sh_up = sh_up; a.sh_down = sh_down;
+  a.ex = expert_args(d, ex);
+  a.renorm = d->renorm; a.routed_scale = d->routed_scale;
+  a.b1 = d->situ_b1; a.b2 = d->situ_b2;
+  a.sc = ws.sc; a.ch = ws.ch; a.act_s = ws.act_s;
+  a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
+  a.bar = ws.bar;
+  // |SiTU| <= b1 b2: scale the activations so that the largest stays below 2^15
+  a.act_exp = act_scale_exp(d->situ_b1, d->situ_b2);
+  a.idx_out = idx; a.w_out = w;
+  a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate;
+  a.status = status;
+  TraceScope ts(KID_DECODE_FUSED, st);
+  return launch_fused_t1(a, di->sms, st) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
 // The whole layer for Tc tokens.  One token with a supported width: router kernel, then
 // the single-token gate/up kernel (top-k and dispatch fused), then the down kernel, the
 // last two launched as programmatic dependents so their prologues overlap the previous
@@ -367,29 +401,9 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
                        const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
                        Ws &ws, int32_t *idx, float *w, void *y, k3moe_dtype ydt, int accumulate,
                        int32_t *status, cudaStream_t st) {
-  if (Tc == 1 &&
-      fused_t1_smem(d->hidden, d->inter, d->n_experts, d->topk, d->shared_inter, di->sms) > 0) {
-    // the whole step in one cooperative kernel; its grid-wide counters (workspace header)
-    // are zero on entry and left zero by the kernel's last CTA
-    FusedT1Args a;
-    a.x = x; a.H = d->hidden; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
-    a.SI = d->shared_inter;
-    a.wr = wr; a.bias = bias;
-    a.sh_gate = sh_gate; a.sh_up = sh_up; a.sh_down = sh_down;
-    a.ex = expert_args(d, ex);
-    a.renorm = d->renorm; a.routed_scale = d->routed_scale;
-    a.b1 = d->situ_b1; a.b2 = d->situ_b2;
-    a.sc = ws.sc; a.ch = ws.ch; a.act_s = ws.act_s;
-    a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
-    a.bar = ws.bar;
-    // |SiTU| <= b1 b2: scale the activations so that the largest stays below 2^15
-    a.act_exp = act_scale_exp(d->situ_b1, d->situ_b2);
-    a.idx_out = idx; a.w_out = w;
-    a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate;
-    a.status = status;
-    TraceScope ts(KID_DECODE_FUSED, st);
-    return launch_fused_t1(a, di->sms, st) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
-  }
+  if (Tc == 1 && fused_takes(di, d))
+    return run_fused(di, d, x, nullptr, 0.f, wr, bias, ex, sh_gate, sh_up, sh_down, ws, idx, w,
+                     y, ydt, accumulate, status, st);
   const int rb = t1_row_block(d->hidden);
   if (Tc == 1 && rb > 0) {
     k3moe_status s = run_route(di, d, x, Tc, wr, bias, sh_gate, sh_up, ws, idx, w, status, st,
@@ -850,17 +864,20 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims *dims, const uint16_t *x_bf
   return K3MOE_OK;
 }
 
-k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
-                         const uint16_t *wr_bf16, const float *bias, const k3moe_experts *experts,
-                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
-                         int32_t *idx_out, float *w_out, void *y, k3moe_dtype ydt,
-                         int32_t accumulate, void *workspace, size_t ws_bytes,
-                         int32_t *status_dev, k3moe_stream_t stream) {
+// Host-side argument checks of k3moe_layer (x is the layer input, or the residual
+// stream of a stacked step; only its pointer and alignment are checked).
+static k3moe_status check_layer_args(const k3moe_dims *dims, const void *x, int32_t T,
+                                     const uint16_t *wr_bf16, const float *bias,
+                                     const k3moe_experts *experts, const uint16_t *sh_gate,
+                                     const uint16_t *sh_up, const uint16_t *sh_down,
+                                     const int32_t *idx_out, const float *w_out, const void *y,
+                                     k3moe_dtype ydt, const void *workspace, size_t ws_bytes,
+                                     const int32_t *status_dev) {
   k3moe_status s = check_dims(dims);
   if (s != K3MOE_OK) return s;
   if (T < 0 || (ydt != K3MOE_F32 && ydt != K3MOE_BF16)) return K3MOE_ERR_ARG;
   if (T == 0) return K3MOE_OK;
-  if (!x_bf16 || !wr_bf16 || !experts || !experts->experts || !y || !workspace || !status_dev)
+  if (!x || !wr_bf16 || !experts || !experts->experts || !y || !workspace || !status_dev)
     return K3MOE_ERR_ARG;
   const bool shared = dims->shared_inter > 0;
   if (shared && (!sh_gate || !sh_up || !sh_down)) return K3MOE_ERR_ARG;
@@ -868,12 +885,26 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
   int64_t off[7];
   record_offsets(dims, off);
   if (experts->expert_stride < off[6] || experts->expert_stride % 16) return K3MOE_ERR_ALIGN;
-  if (!aligned16(x_bf16) || !aligned16(wr_bf16) || !aligned16(experts->experts) ||
+  if (!aligned16(x) || !aligned16(wr_bf16) || !aligned16(experts->experts) ||
       !aligned16(y) || !aligned16(workspace) || (bias && !aligned16(bias)) ||
       (idx_out && (!aligned16(idx_out) || !aligned16(w_out))) ||
       (shared && (!aligned16(sh_gate) || !aligned16(sh_up) || !aligned16(sh_down))))
     return K3MOE_ERR_ALIGN;
   if (ws_bytes < k3moe_workspace_size(dims, T)) return K3MOE_ERR_WORKSPACE;
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                         const uint16_t *wr_bf16, const float *bias, const k3moe_experts *experts,
+                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
+                         int32_t *idx_out, float *w_out, void *y, k3moe_dtype ydt,
+                         int32_t accumulate, void *workspace, size_t ws_bytes,
+                         int32_t *status_dev, k3moe_stream_t stream) {
+  k3moe_status s = check_layer_args(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up,
+                                    sh_down, idx_out, w_out, y, ydt, workspace, ws_bytes,
+                                    status_dev);
+  if (s != K3MOE_OK || T == 0) return s;
+  const bool shared = dims->shared_inter > 0;
   const DeviceInfo *di = device_info();
   if (!di) return K3MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -946,6 +977,29 @@ k3moe_status k3moe_decode_stack(const k3moe_dims *dims, int32_t L,
   if (!h || !x_scratch || !workspace || !status_dev) return K3MOE_ERR_ARG;
   if ((idx_out == nullptr) != (w_out == nullptr)) return K3MOE_ERR_ARG;
   const int H = dims->hidden, K = dims->topk;
+  const DeviceInfo *di = device_info();
+  if (!di) return K3MOE_ERR_CUDA;
+  if (T == 1 && fused_takes(di, dims) && eps >= 0.f) {
+    // one launch per layer: the fused kernel normalises h itself (RMSNorm in every CTA)
+    // and adds the layer's output to it; x_scratch is not used
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Ws ws = ws_layout(dims, T, workspace);
+    for (int l = 0; l < L; l++) {
+      const k3moe_layer_weights &lw = layers[l];
+      const bool shared = dims->shared_inter > 0;
+      s = check_layer_args(dims, h, T, lw.wr_bf16, lw.bias, &lw.experts, lw.sh_gate, lw.sh_up,
+                           lw.sh_down, idx_out, w_out, h, K3MOE_F32, workspace, ws_bytes,
+                           status_dev);
+      if (s != K3MOE_OK) return s;
+      const size_t ro = (size_t)l * K;
+      s = run_fused(di, dims, nullptr, h, eps, lw.wr_bf16, lw.bias, &lw.experts,
+                    shared ? lw.sh_gate : nullptr, shared ? lw.sh_up : nullptr,
+                    shared ? lw.sh_down : nullptr, ws, idx_out ? idx_out + ro : ws.idx,
+                    w_out ? w_out + ro : ws.w, h, K3MOE_F32, 1, status_dev, st);
+      if (s != K3MOE_OK) return s;
+    }
+    return K3MOE_OK;
+  }
   for (int l = 0; l < L; l++) {
     s = k3moe_rmsnorm_bf16(h, T, H, eps, x_scratch, stream);
     if (s != K3MOE_OK) return s;

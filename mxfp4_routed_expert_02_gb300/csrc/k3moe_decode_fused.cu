@@ -102,11 +102,12 @@ __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v,
 // differ (the bits above it are common to all of them): per pass an 8-bit digit, a
 // histogram of the keys that share the prefix found so far, and the digit where the count
 // from the top reaches K; the search stops once that digit's keys are all selected.  The
-// K keys >= the prefix are then sorted by warp 0.  E <= 8 nt, K <= 32.
+// K keys >= the prefix are then sorted by warp 0.  sc_s: E floats of shared scratch.
+// E <= 8 nt, K <= 32.
 __device__ void topk_cta(const float *sc, const float *ch, int E, int K, int renorm,
                          float routed_scale, int nt, int bar, uint32_t *hist,
                          unsigned long long *list, unsigned long long *wred, int *misc,
-                         int *sel, float *wsel) {
+                         float *sc_s, int *sel, float *wsel) {
   constexpr int KPT = 8;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = nt >> 5;
   unsigned long long key[KPT];
@@ -116,6 +117,7 @@ __device__ void topk_cta(const float *sc, const float *ch, int E, int K, int ren
     const int e = t + nt * k;
     key[k] = 0ull;
     if (e < E) {
+      sc_s[e] = __ldcg(sc + e);  // the unbiased scores, loaded with the selection scores
       float c = __fadd_rn(__ldcg(ch + e), 0.f);     // -0 -> +0
       if (c != c) c = -__int_as_float(0x7f800000);  // a NaN never wins (it is reported)
       key[k] = ((unsigned long long)float_order_key(c) << 32) |
@@ -220,7 +222,7 @@ __device__ void topk_cta(const float *sc, const float *ch, int E, int K, int ren
     float s = 0.f;
     if (lane < K) {
       e = (v == 0ull) ? 0 : (int)(0xffffffffu - (uint32_t)(v & 0xffffffffull));
-      s = __ldcg(sc + e);
+      s = sc_s[e];  // written before the barriers above
     }
     float wsum = 0.f;  // float sum of the chosen scores in selection order
     for (int j = 0; j < K; j++) wsum = __fadd_rn(wsum, __shfl_sync(0xffffffffu, s, j));
@@ -361,8 +363,11 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         }
         uint8_t *dst = slot_ptr(lane);
         if (t == 0) {
-          mbar_arrive_expect_tx(&fullG[lane], (uint32_t)rowh);
-          bulk_g2s(dst, a.x, rowh, &fullG[lane]);
+          // the token's input: bf16 x, or the float residual stream to normalise
+          const uint32_t xbytes = a.h ? (uint32_t)(H * 4) : (uint32_t)rowh;
+          mbar_arrive_expect_tx(&fullG[lane], xbytes);
+          bulk_g2s(dst, a.h ? static_cast<const void *>(a.h) : static_cast<const void *>(a.x),
+                   xbytes, &fullG[lane]);
         } else if (t < tS) {
           const int k0 = 2 * (t - tR);
           const int nrow = cntR - k0 < 2 ? cntR - k0 : 2;
@@ -605,7 +610,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     uint32_t xr[16];
     int xe;
     uint4 xb[4];
-    {
+    if (a.h == nullptr) {
       const uint4 *xs = reinterpret_cast<const uint4 *>(stage_in(t));
       float v[32];
 #pragma unroll
@@ -621,6 +626,65 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       xe = prescale_group_f16(v, xr);
 #pragma unroll
       for (int c = 0; c < 4; c++) xb[c] = xs[g + G * c];
+      stage_out(t);
+      t++;
+    } else {
+      // x = bf16(h * inv), inv = 1 / sqrt(mean(h^2) + eps) (kimi-k3-in-c, section 5): the
+      // sum of squares as a float-float sum of exact squares (parity-0 threads cover each
+      // input group once; fixed warp and cross-warp order), one double-precision root
+      const float *hs = reinterpret_cast<const float *>(stage_in(t));
+      float sh = 0.f, sl = 0.f;
+      if (h == 0) {
+        const float4 *h4 = reinterpret_cast<const float4 *>(hs + g * kGroup);
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+          const float4 c = h4[q];
+          const float e4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int k = 0; k < 4; k++) {
+            const float p = __fmul_rn(e4[k], e4[k]);
+            const float pe = fmaf(e4[k], e4[k], -p);  // exact square = p + pe
+            float sx, ex;
+            two_sum(sh, p, sx, ex);
+            sh = sx;
+            sl = __fadd_rn(sl, __fadd_rn(ex, pe));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
+        ff_add(sh, sl, oh, ol);
+      }
+      float *wss = reinterpret_cast<float *>(wred);  // [warp][2], idle until the top-k
+      if (lane == 0) {
+        wss[2 * warp] = sh;
+        wss[2 * warp + 1] = sl;
+      }
+      named_bar_sync(kBarCons, nt);
+      if (tid == 0) {
+        float th = 0.f, tl = 0.f;
+        for (int w = 0; w < nwc; w++) ff_add(th, tl, wss[2 * w], wss[2 * w + 1]);
+        const double tot = (double)th + (double)tl;
+        misc[5] = __float_as_int((float)(1.0 / sqrt(tot / (double)H + (double)a.eps)));
+      }
+      named_bar_sync(kBarCons, nt);
+      const float inv = __int_as_float(misc[5]);
+      float v[32];
+#pragma unroll
+      for (int k = 0; k < 32; k++)
+        v[k] = bf16_lo(f32_to_bf16(__fmul_rn(hs[g * kGroup + k], inv)));
+      xe = prescale_group_f16(v, xr);
+      auto pair = [&](const float *p2) -> uint32_t {
+        return (uint32_t)f32_to_bf16(__fmul_rn(p2[0], inv)) |
+               ((uint32_t)f32_to_bf16(__fmul_rn(p2[1], inv)) << 16);
+      };
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const float *p8 = hs + 8 * (g + G * c);
+        xb[c] = make_uint4(pair(p8), pair(p8 + 2), pair(p8 + 4), pair(p8 + 6));
+      }
       stage_out(t);
       t++;
     }
@@ -675,8 +739,10 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       *abort_flag = 1;
     }
     named_bar_sync(kBarCons, nt);
+    // the partial-sum buffer is idle here (the epilogue finished the R items before
+    // dependency 1; S items start after the top-k): it holds the scores meanwhile
     topk_cta(a.sc, a.ch, E, K, a.renorm, a.routed_scale, nt, kBarCons, hist, list, wred, misc,
-             sel, wsel);
+             red, sel, wsel);
     if (bx == 0 && tid < K && a.idx_out) {
       a.idx_out[tid] = sel[tid];
       a.w_out[tid] = wsel[tid];
@@ -887,6 +953,7 @@ size_t fused_t1_smem(int H, int I, int E, int K, int SI, int grid) {
   if (SI < 0 || SI % 256 != 0) return 0;                   // shared rows in 32 lanes x 8
   if (grid < 1) return 0;
   if (E > 8 * 64 * (G / 32) || (E + grid - 1) / grid > 32) return 0;  // top-k keys, R rows
+  if (E * 4 > kFuRedBytes) return 0;  // the top-k's scores in the partial-sum buffer
   if (fused_nsg(H) < 2) return 0;
   const size_t total = (size_t)kFuRing + fused_ring_bytes(H, I, SI) + kFuRedBytes;
   return total <= kFuSmemMax ? total : 0;

@@ -96,7 +96,9 @@ struct DownArgs {
 
 // ---- the single-token layer step as one persistent kernel (k3moe_decode_fused.cu)
 struct FusedT1Args {
-  const uint16_t *x;  // [H] bf16
+  const uint16_t *x;  // [H] bf16 (unused when h is set)
+  const float *h;     // [H] residual stream: when set, x = bf16(RMSNorm(h)) in the kernel
+  float eps;          // RMSNorm epsilon (with h)
   int H, I, E, K, SI;
   const uint16_t *wr;  // [E][H]
   const float *bias;   // [E] or null
