@@ -702,13 +702,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
           const uint32_t xa[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
 #pragma unroll
           for (int q = 0; q < 4; q++) {
-            float p = __fmul_rn(bf16_lo(wa[q]), bf16_lo(xa[q]));
-            float sx, ex;
-            two_sum(hi, p, sx, ex);
+            float p0, p1, sx, ex;
+            mul2_bf16_f32(xa[q], wa[q], p0, p1);  // exact products
+            two_sum(hi, p0, sx, ex);
             hi = sx;
             lo = __fadd_rn(lo, ex);
-            p = __fmul_rn(bf16_hi(wa[q]), bf16_hi(xa[q]));
-            two_sum(hi, p, sx, ex);
+            two_sum(hi, p1, sx, ex);
             hi = sx;
             lo = __fadd_rn(lo, ex);
           }
@@ -761,10 +760,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
           const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
           const uint32_t xa[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
 #pragma unroll
-          for (int q = 0; q < 4; q++) {
-            acc = fmaf(bf16_lo(wa[q]), bf16_lo(xa[q]), acc);
-            acc = fmaf(bf16_hi(wa[q]), bf16_hi(xa[q]), acc);
-          }
+          for (int q = 0; q < 4; q++) acc = fma2_bf16_f32(xa[q], wa[q], acc);
         }
       }
       stage_out(t);

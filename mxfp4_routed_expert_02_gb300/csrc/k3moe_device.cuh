@@ -77,6 +77,27 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t x2, uint32_t w2, float c)
   return d;
 }
 
+// c + x.lo * w.lo + x.hi * w.hi with bf16 operands and an f32 accumulator (mixed-precision
+// FMA: each bf16 x bf16 product is exact in f32, each add rounds once) -- the same result
+// as widening both to f32 first, without the widening instructions.
+__device__ __forceinline__ float fma2_bf16_f32(uint32_t x2, uint32_t w2, float c) {
+  float d;
+  asm("{ .reg .b16 xl, xh, wl, wh; mov.b32 {xl, xh}, %1; mov.b32 {wl, wh}, %2;\n"
+      "  fma.rn.f32.bf16 %0, xl, wl, %3; fma.rn.f32.bf16 %0, xh, wh, %0; }"
+      : "=f"(d)
+      : "r"(x2), "r"(w2), "f"(c));
+  return d;
+}
+
+// The two exact products x.lo * w.lo and x.hi * w.hi of bf16 pairs, as floats (an FMA
+// with -0 added keeps the sign of a zero product).
+__device__ __forceinline__ void mul2_bf16_f32(uint32_t x2, uint32_t w2, float &p0, float &p1) {
+  asm("{ .reg .b16 xl, xh, wl, wh; mov.b32 {xl, xh}, %2; mov.b32 {wl, wh}, %3;\n"
+      "  fma.rn.f32.bf16 %0, xl, wl, 0f80000000; fma.rn.f32.bf16 %1, xh, wh, 0f80000000; }"
+      : "=f"(p0), "=f"(p1)
+      : "r"(x2), "r"(w2));
+}
+
 // Sum over the 32 columns of one MXFP4 group: sum_k x'[k] * e2m1[k] (unscaled), with
 // x' given as 16 f16x2 registers (pair p = columns 2p, 2p+1) and the weights as the 16
 // packed bytes of the group (4 words).  Two accumulators for latency.
