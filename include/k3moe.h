@@ -224,6 +224,17 @@ k3moe_status k3moe_rmsnorm_bf16(const float *h, int32_t T, int32_t n, float eps,
 k3moe_status k3moe_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, int32_t rows,
                                  int32_t cols, float *out, k3moe_stream_t stream);
 
+/* Test hook for failure detection, not on the hot path.  While on (on != 0), every
+ * single-token step that runs as one fused kernel (k3moe_layer and k3moe_decode_stack
+ * with T == 1 at shapes that kernel takes) makes its second grid-wide dependency, the
+ * one on every CTA's activations, wait for one arrival more than there are CTAs, with a
+ * limit of about 0.1 s instead of the usual ~2 s.  The wait runs out: the launch
+ * completes with the layer's output taken as zero (y = 0, or y unchanged when
+ * accumulating, as the residual stream of a stack is) and *status_dev set to
+ * K3MOE_ERR_TIMEOUT; the workspace counters are left zero, so the context and the
+ * workspace stay usable.  Other kernels ignore it.  Process-wide; returns K3MOE_OK.     */
+k3moe_status k3moe_test_expire_wait(int32_t on);
+
 /* Tracing (no counterpart in the pages, which time whole tokens on the host).  When on,
  * every kernel the library launches is bracketed by two CUDA events on its stream and
  * its device duration is summed per kernel.  k3moe_trace_enable(1) clears the sums and

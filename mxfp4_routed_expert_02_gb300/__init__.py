@@ -9,6 +9,6 @@ and raises if it cannot.
 from .k3moe import (  # noqa: F401
     LayerDims, K3MoeError, k3moe_route, k3moe_expert_ffn_mxfp4, k3moe_layer,
     k3moe_layer_static_scratch, STATIC_SCRATCH_BYTES, k3moe_decode_stack,
-    k3moe_rmsnorm_bf16, k3moe_dequant_mxfp4, k3moe_trace_enable, k3moe_trace_read,
+    k3moe_rmsnorm_bf16, k3moe_dequant_mxfp4, k3moe_test_expire_wait, k3moe_trace_enable, k3moe_trace_read,
     record_layout, workspace_size, new_workspace, new_status, status_str, lib, EXPORTS,
 )

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <cmath>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -366,6 +367,10 @@ bool fused_takes(const DeviceInfo *di, const k3moe_dims *d) {
 // One token through the fused kernel: input x (bf16), or h (float, the residual stream)
 // normalised in the kernel (x = bf16(RMSNorm(h)) with eps).  Its grid-wide counters
 // (workspace header) are zero on entry and left zero by the kernel's last CTA.
+// While set, single-token fused launches wait for an arrival that never comes (test of the
+// bounded-wait path).
+std::atomic<int> g_expire_wait{0};
+
 k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x,
                        const float *h, float eps, const uint16_t *wr, const float *bias,
                        const k3moe_experts *ex, const uint16_t *sh_gate, const uint16_t *sh_up,
@@ -388,6 +393,7 @@ k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
   a.idx_out = idx; a.w_out = w;
   a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate;
   a.status = status;
+  a.expire_dep2 = g_expire_wait.load(std::memory_order_relaxed);
   TraceScope ts(KID_DECODE_FUSED, st);
   return launch_fused_t1(a, di->sms, st) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
 }
@@ -1049,6 +1055,11 @@ k3moe_status k3moe_dequant_mxfp4(const uint8_t *packed, const uint8_t *scales, i
   k_dequant<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(packed, scales, rows, cols,
                                                                     out);
   return launch_status();
+}
+
+k3moe_status k3moe_test_expire_wait(int32_t on) {
+  g_expire_wait.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
+  return K3MOE_OK;
 }
 
 k3moe_status k3moe_trace_enable(int32_t on) {

@@ -49,6 +49,7 @@ constexpr int kFuDownRows = 16;  // output rows per down tile
 constexpr int kFuRedBytes = 2 * 16 * 64 * 4;  // partial sums [parity][warp][row][2]
 constexpr int kBarDown = 1;      // named barrier of the 16 worker warps (0 is __syncthreads)
 constexpr int kBarCons = 2;      // named barrier of the R/S/G consumer warps
+constexpr long long kExpireBudget = 200000000LL;  // ~0.1 s: the expiry test's wait limit
 
 // shared-memory map: barriers and small arrays; the ring (X/R/S/G slots, then D slots);
 // the partial sums
@@ -77,10 +78,10 @@ __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 // Bounded wait until a counter (zeroed by the host before the launch) reaches n.
-__device__ bool wait_count(const unsigned *cnt, unsigned n) {
+__device__ bool wait_count(const unsigned *cnt, unsigned n, long long budget = kWaitBudget) {
   const long long t0 = clock64();
   while (ld_acquire_u32(cnt) < n) {
-    if (clock64() - t0 > kWaitBudget) return false;
+    if (clock64() - t0 > budget) return false;
     __nanosleep(64);  // let the other lanes of the warp issue
   }
   return true;
@@ -463,9 +464,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
           bulk_g2s(dst, a.sh_down + (size_t)rs0 * SI, wbytes, &fullD[q]);
         }
         if (!dep2) {
-          if (!wait_count(a.bar + 1, (unsigned)nb)) {
+          // (the expiry test waits for one arrival more than there are CTAs, briefly)
+          const unsigned need = (unsigned)nb + (a.expire_dep2 ? 1u : 0u);
+          if (!wait_count(a.bar + 1, need, a.expire_dep2 ? kExpireBudget : kWaitBudget)) {
             set_status(a.status, K3MOE_ERR_TIMEOUT);
             *abort_flag = 1;
+            __threadfence_block();  // before the copies whose landing the workers wait for
           }
           fence_proxy_async_all();
           dep2 = true;
@@ -483,12 +487,13 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         }
       }
     }
-    if (ab) {
-      // bounded waits for this lane's copies still in flight
-      if (lane < NSG && last_g >= 0) mbar_wait(&fullG[lane], (last_g / NSG) & 1, 400000000LL);
-      if (lane < kFuNSD && iD - kFuNSD >= 0 && iD - kFuNSD < nD)
-        mbar_wait(&fullD[lane], ((iD - kFuNSD) >> 2) & 1, 400000000LL);
-    }
+    // bounded waits for this lane's copies still in flight: the last D stage always (a
+    // worker whose wait expired no longer waits for it, and the CTA must not exit before
+    // it lands), the last R/S/G stage after an expiry here
+    if (ab && lane < NSG && last_g >= 0)
+      mbar_wait(&fullG[lane], (last_g / NSG) & 1, 400000000LL);
+    if (lane < kFuNSD && iD - kFuNSD >= 0 && iD - kFuNSD < nD)
+      mbar_wait(&fullD[lane], ((iD - kFuNSD) >> 2) & 1, 400000000LL);
     return;
   }
 

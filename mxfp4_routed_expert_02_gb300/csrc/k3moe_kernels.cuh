@@ -117,6 +117,7 @@ struct FusedT1Args {
   void *y;
   int ydt, accumulate;
   int32_t *status;
+  int expire_dep2;  // test of the expiry path: dependency 2 cannot complete, its wait is short
 };
 // Shared memory the fused kernel needs for this shape (0: the shape does not fit it).
 size_t fused_t1_smem(int H, int I, int E, int K, int SI, int grid);

@@ -28,8 +28,8 @@ F32, BF16 = 0, 1
 # Every symbol include/k3moe.h declares.
 EXPORTS = (
     "k3moe_record_layout", "k3moe_workspace_size", "k3moe_route", "k3moe_expert_ffn_mxfp4",
-    "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_decode_stack", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4", "k3moe_trace_enable",
-    "k3moe_trace_read", "k3moe_status_str",
+    "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_decode_stack", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4",
+    "k3moe_test_expire_wait", "k3moe_trace_enable", "k3moe_trace_read", "k3moe_status_str",
 )
 
 
@@ -99,6 +99,8 @@ def lib(build_if_missing: bool = True):
     L.k3moe_rmsnorm_bf16.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
     L.k3moe_dequant_mxfp4.restype = i32
     L.k3moe_dequant_mxfp4.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.k3moe_test_expire_wait.restype = i32
+    L.k3moe_test_expire_wait.argtypes = [i32]
     L.k3moe_trace_enable.restype = i32
     L.k3moe_trace_enable.argtypes = [i32]
     L.k3moe_trace_read.restype = i32
@@ -280,6 +282,12 @@ def k3moe_dequant_mxfp4(packed, scales, rows: int, cols: int, out, stream=None):
 
 def status_str(code: int) -> str:
     return lib().k3moe_status_str(int(code)).decode()
+
+
+def k3moe_test_expire_wait(on: bool = True):
+    """While on, the single-token fused step's second grid dependency cannot complete and its
+    wait gives up after ~0.1 s (status K3MOE_ERR_TIMEOUT, output taken as zero)."""
+    _check("k3moe_test_expire_wait", lib().k3moe_test_expire_wait(int(bool(on))))
 
 
 def k3moe_trace_enable(on: bool = True):

@@ -5,6 +5,8 @@ Tolerances (fp32 output: relative L2 error <= 1e-3 over the [T][H] output; bf16 
 max |y - y_ref| / max |y_ref| <= 2e-2) are those the layer step is specified to; expert
 indices must match exactly.
 """
+import dataclasses
+
 import numpy as np
 import torch
 
@@ -100,3 +102,11 @@ class Layer:
                                 cfg.hidden, cfg.inter, *sh, renorm=bool(cfg.renorm),
                                 routed_scale=cfg.routed_scale, b1=cfg.situ_b1, b2=cfg.situ_b2,
                                 tokens=tokens, nthreads=nthreads)
+
+
+def fused_layer(seed, **kw):
+    """A one-token layer at a shape the fused single-token kernel takes."""
+    base = dict(hidden=1024, inter=512, n_experts=24, topk=6, tokens=1, n_shared=1)
+    base.update(kw)
+    cfg = dataclasses.replace(synth.config("tiny"), name="custom", **base)
+    return Layer(cfg, seed=seed)

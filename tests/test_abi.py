@@ -35,6 +35,13 @@ def test_oracle_is_not_linked_into_the_library():
             getattr(L, name)
 
 
+def test_expiry_hook_needs_no_device():
+    # the hook only sets a host flag the next fused launch reads
+    L = k3.lib()
+    assert L.k3moe_test_expire_wait(1) == 0
+    assert L.k3moe_test_expire_wait(0) == 0
+
+
 def dims(**kw):
     base = dict(hidden=7168, inter=1536, n_experts=896, topk=16, shared_inter=1536)
     base.update(kw)

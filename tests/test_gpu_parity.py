@@ -10,7 +10,7 @@ import torch
 import oracle
 import synth
 import mxfp4_routed_expert_02_gb300 as k3
-from parity import Layer, rel_l2, max_rel, REL_L2_F32, MAX_REL_BF16, dims_of
+from parity import Layer, fused_layer, rel_l2, max_rel, REL_L2_F32, MAX_REL_BF16, dims_of
 
 pytestmark = pytest.mark.gpu
 
@@ -187,14 +187,6 @@ def test_layer_shapes(H, I, E, K, NS, T):
     cfg = dataclasses.replace(synth.config("tiny"), name="custom", hidden=H, inter=I,
                               n_experts=E, topk=K, tokens=T, n_shared=NS)
     check_layer(Layer(cfg, seed=H + T))
-
-
-def fused_layer(seed, **kw):
-    """A one-token layer at a shape the fused single-token kernel takes."""
-    base = dict(hidden=1024, inter=512, n_experts=24, topk=6, tokens=1, n_shared=1)
-    base.update(kw)
-    cfg = dataclasses.replace(synth.config("tiny"), name="custom", **base)
-    return Layer(cfg, seed=seed)
 
 
 def test_fused_single_token_ties_bias_bf16_accumulate():
