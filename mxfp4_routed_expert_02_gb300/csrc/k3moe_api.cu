@@ -386,7 +386,7 @@ k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
   a.renorm = d->renorm; a.routed_scale = d->routed_scale;
   a.b1 = d->situ_b1; a.b2 = d->situ_b2;
   a.sc = ws.sc; a.ch = ws.ch; a.act_s = ws.act_s;
-  a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
+  a.act = ws.act_hi;
   a.bar = ws.bar;
   // |SiTU| <= b1 b2: scale the activations so that the largest stays below 2^15
   a.act_exp = act_scale_exp(d->situ_b1, d->situ_b2);

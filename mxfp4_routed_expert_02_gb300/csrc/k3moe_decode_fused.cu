@@ -43,7 +43,7 @@ constexpr int kFuProducer = 16;  // warp index of the bulk-copy producer
 constexpr int kFuThreads = 32 * (kFuWorkers + 1);
 constexpr int kFuRB = 4;         // gate/up rows per G stage
 constexpr int kFuItemRows = 8;   // gate/up rows per reduction item (two G stages)
-constexpr int kFuNSD = 4;        // D ring slots: two per group of eight worker warps
+constexpr int kFuNSD = 6;        // D ring slots: three per group of eight worker warps
 constexpr int kFuMaxNS = 8;      // R/S/G ring slots at most
 constexpr int kFuDownRows = 16;  // output rows per down tile
 constexpr int kFuRedBytes = 2 * 16 * 64 * 4;  // partial sums [parity][warp][row][2]
@@ -53,15 +53,17 @@ constexpr long long kExpireBudget = 200000000LL;  // ~0.1 s: the expiry test's w
 
 // shared-memory map: barriers and small arrays; the ring (X/R/S/G slots, then D slots);
 // the partial sums
-constexpr int kFuBars = 0;       // fullG[8] emptyG[8] fullD[4] emptyD[4] redbar[2] redfree[2]
+constexpr int kFuBars = 0;       // fullG[8] emptyG[8] fullD[6] emptyD[6] redbar[2] redfree[2]
                                  // selbar
-constexpr int kFuSel = 256;      // int[32]
-constexpr int kFuWsel = 384;     // float[32]
-constexpr int kFuMisc = 512;     // int[8]: top-k scratch [0..3], abort flag [4]
-constexpr int kFuGDone = 576;    // int[8]: X/R/S/G slot s fully consumed (set by its owner)
+constexpr int kFuSel = 384;      // int[32]
+constexpr int kFuWsel = 512;     // float[32]
+constexpr int kFuMisc = 640;     // int[8]: top-k scratch [0..3], abort flag [4]
+constexpr int kFuGDone = 704;    // int[8]: X/R/S/G slot s fully consumed (set by its owner)
 constexpr int kFuSmall = 1024;   // top-k: histogram [256], selected keys [32], warp or/and;
                                  // D: dbuf [K][16] + ds [16]
 constexpr int kFuSmallBytes = 4096;
+static_assert((16 + 2 * kFuNSD + 5) * 8 <= kFuSel, "the barriers overlap the small arrays");
+static_assert(kFuNSD % 2 == 0, "every D slot serves one worker group");
 constexpr int kFuRing = kFuSmall + kFuSmallBytes;
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -86,12 +88,10 @@ __device__ bool wait_count(const unsigned *cnt, unsigned n, long long budget = k
   }
   return true;
 }
-// D slot of D stage i: stages alternate between the two worker groups (i % 2), and each
-// group between its two slots, so a group computes on one slot while the other fills.
-__host__ __device__ __forceinline__ int d_slot_of(int i) {
-  const int r = i & 3;
-  return r == 1 ? 2 : (r == 2 ? 1 : r);
-}
+// D slot of D stage i: stages alternate between the two worker groups (i % 2, which is
+// also the slot's parity), and each group cycles through its three slots, so a group
+// computes on one slot while the other two fill.
+__host__ __device__ __forceinline__ int d_slot_of(int i) { return i % kFuNSD; }
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
   return __shfl_xor_sync(0xffffffffu, v, o);
 }
@@ -254,7 +254,7 @@ __host__ __device__ inline uint32_t fused_dexp_bytes(int I) {  // one expert's 1
   return (uint32_t)(kFuDownRows * (I / 2 + I / kGroup));
 }
 __host__ __device__ inline uint32_t fused_dslot_bytes(int I, int SI) {
-  const uint32_t r = 2 * fused_dexp_bytes(I) + 2u * (uint32_t)I * 4u;
+  const uint32_t r = 2 * fused_dexp_bytes(I) + 2u * (uint32_t)I * 2u;
   const uint32_t sh = SI > 0 ? 8u * (uint32_t)SI * 2u + (uint32_t)SI * 4u : 0u;
   return ((r > sh ? r : sh) + 127u) & ~127u;
 }
@@ -305,10 +305,10 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
   uint64_t *fullG = reinterpret_cast<uint64_t *>(smem + kFuBars);
   uint64_t *emptyG = fullG + 8;
   uint64_t *fullD = fullG + 16;
-  uint64_t *emptyD = fullG + 20;
-  uint64_t *redbar = fullG + 24;
-  uint64_t *redfree = fullG + 26;
-  uint64_t *selbar = fullG + 28;
+  uint64_t *emptyD = fullD + kFuNSD;
+  uint64_t *redbar = emptyD + kFuNSD;
+  uint64_t *redfree = redbar + 2;
+  uint64_t *selbar = redfree + 2;
   int *sel = reinterpret_cast<int *>(smem + kFuSel);
   float *wsel = reinterpret_cast<float *>(smem + kFuWsel);
   int *misc = reinterpret_cast<int *>(smem + kFuMisc);
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       __threadfence_block();
       gdone[lane] = 1;
     }
-    int iD = d_slot_of(lane);  // the first stage of slot `lane` (d_slot_of is an involution)
+    int iD = lane;  // the first stage of slot `lane`
     if (lane < kFuNSD && !ab && nD > 0) {
       const int g0 = (int)((uint32_t)lane * dslot / gslot);
       int g1 = (int)((((uint32_t)lane + 1u) * dslot - 1u) / gslot);
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       }
       bool dep2 = false;
       for (; !ab && iD < nD; iD += kFuNSD) {
-        const int q = lane, u = iD >> 2;
+        const int q = lane, u = iD / kFuNSD;
         if (!mbar_wait(&emptyD[q], (u & 1) ^ 1)) {
           set_status(a.status, K3MOE_ERR_TIMEOUT);
           ab = true;
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         uint8_t *dst = dslot_ptr(q);
         const bool routed = m < hk;
         const uint32_t wbytes = routed ? 2 * dexp : (uint32_t)(RS * SI * 2);
-        const uint32_t abytes = routed ? (uint32_t)(2 * I * 4) : (uint32_t)(SI * 4);
+        const uint32_t abytes = routed ? (uint32_t)(2 * I * 2) : (uint32_t)(SI * 4);
         mbar_arrive_expect_tx(&fullD[q], wbytes + abytes);
         if (routed) {
           for (int e2 = 0; e2 < 2; e2++) {
@@ -475,13 +475,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
           dep2 = true;
         }
         if (routed) {
-          // experts 2m, 2m+1: hi then lo, I values each, after the weights
-          for (int e2 = 0; e2 < 2; e2++) {
-            uint8_t *ad = dst + 2 * dexp + e2 * (I * 4);
-            bulk_g2s(ad, a.act_hi + (size_t)(2 * m + e2) * I, (uint32_t)(I * 2), &fullD[q]);
-            bulk_g2s(ad + I * 2, a.act_lo + (size_t)(2 * m + e2) * I, (uint32_t)(I * 2),
-                     &fullD[q]);
-          }
+          // experts 2m, 2m+1: I f16 activations each, after the weights
+          bulk_g2s(dst + 2 * dexp, a.act + (size_t)(2 * m) * I, (uint32_t)(2 * I * 2),
+                   &fullD[q]);
         } else {
           bulk_g2s(dst + wbytes, a.act_s, abytes, &fullD[q]);
         }
@@ -493,7 +489,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     if (ab && lane < NSG && last_g >= 0)
       mbar_wait(&fullG[lane], (last_g / NSG) & 1, 400000000LL);
     if (lane < kFuNSD && iD - kFuNSD >= 0 && iD - kFuNSD < nD)
-      mbar_wait(&fullD[lane], ((iD - kFuNSD) >> 2) & 1, 400000000LL);
+      mbar_wait(&fullD[lane], ((iD - kFuNSD) / kFuNSD) & 1, 400000000LL);
     return;
   }
 
@@ -552,7 +548,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       release(n);
       if (lane == 0) a.act_s[bx + nb * s] = situ(gs, us, a.b1, a.b2);
     }
-    // G: rows of an 8-row block of expert slot j -> SiTU -> f16 hi + lo at the fixed scale
+    // G: rows of an 8-row block of expert slot j -> SiTU -> f16 at the fixed scale
     // 2^-act_exp (|SiTU| <= b1 b2, so the scaled value stays below 2^15)
     const float inv = pow2i(-a.act_exp);
     for (int s = 0; s < nI; s++, n++) {
@@ -570,12 +566,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         float act = situ(gs, us, a.b1, a.b2);
         if (*abort_flag) act = 0.f;
         const float sa = act * inv;
-        const __half hh = __float2half_rn(sa);
-        const __half hl = __float2half_rn(sa - __half2float(hh));
         const int row = blk * kFuItemRows + r;
         const size_t o = act_index(j, I, row / kTileRows, row % kTileRows);
-        a.act_hi[o] = __half_as_ushort(hh);
-        a.act_lo[o] = __half_as_ushort(hl);
+        a.act[o] = __half_as_ushort(__float2half_rn(sa));
       }
     }
   } else if (warp < 2 * nwc) {
@@ -842,7 +835,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       const int i = n * dpt + m;
       if ((i & 1) != gD) continue;
       const int q = d_slot_of(i);
-      if (!aborted && !mbar_wait(&fullD[q], (i >> 2) & 1)) {
+      if (!aborted && !mbar_wait(&fullD[q], (i / kFuNSD) & 1)) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
         aborted = true;
       }
@@ -852,27 +845,24 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         const int ex = wg >> 2, j = 2 * m + ex, rb = (wg & 3) * 4 + rp * 2;
         const uint8_t *sp = st + ex * dexp;
         const uint8_t *ss = sp + kFuDownRows * rowb2;
-        const uint16_t *s_hi = reinterpret_cast<const uint16_t *>(st + 2 * dexp + ex * (I * 4));
-        const uint16_t *s_lo = s_hi + I;
+        const uint16_t *s_act = reinterpret_cast<const uint16_t *>(st + 2 * dexp + ex * (I * 2));
         float acc[2] = {0.f, 0.f};
         for (int qq = 0; qq < NG; qq++) {
           // the 16 group lanes read 16 consecutive 16-byte weight chunks of a row
           const int gg = qq * 16 + l;
-          uint32_t xh[16], xl[16];
-          const uint4 *ph = reinterpret_cast<const uint4 *>(s_hi + act_index(0, I, gg, 0));
-          const uint4 *pl = reinterpret_cast<const uint4 *>(s_lo + act_index(0, I, gg, 0));
+          uint32_t xa[16];
+          const uint4 *pa = reinterpret_cast<const uint4 *>(s_act + act_index(0, I, gg, 0));
 #pragma unroll
           for (int c = 0; c < 4; c++) {
-            const uint4 x0 = ph[c * G2], x1 = pl[c * G2];
-            xh[4 * c] = x0.x; xh[4 * c + 1] = x0.y; xh[4 * c + 2] = x0.z; xh[4 * c + 3] = x0.w;
-            xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
+            const uint4 x0 = pa[c * G2];
+            xa[4 * c] = x0.x; xa[4 * c + 1] = x0.y; xa[4 * c + 2] = x0.z; xa[4 * c + 3] = x0.w;
           }
 #pragma unroll
           for (int r = 0; r < 2; r++) {
             const int row = rb + r;
             const uint4 wv = reinterpret_cast<const uint4 *>(sp + row * rowb2)[gg];
             const uint32_t sv = ss[row * G2 + gg];
-            acc[r] += group_dot2(xh, xl, wv) * group_factor(sv, e2);  // 0 for byte 255
+            acc[r] += group_dot(xa, wv) * group_factor(sv, e2);  // 0 for byte 255
           }
         }
 #pragma unroll

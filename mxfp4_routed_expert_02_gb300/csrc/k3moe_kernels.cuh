@@ -108,10 +108,9 @@ struct FusedT1Args {
   float routed_scale, b1, b2;
   float *sc, *ch;       // [E] workspace
   float *act_s;         // [SI] workspace
-  uint16_t *act_hi, *act_lo;  // [K][I] workspace
-  int32_t *act_ex;            // [K][I/32] workspace
+  uint16_t *act;              // [K][I] workspace
   unsigned *bar;              // dependency 1, dependency 2, exit: zero on entry and on exit
-  int act_exp;                // activations are stored as f16 hi + lo of act * 2^-act_exp
+  int act_exp;                // activations are stored as f16 of act * 2^-act_exp
   int32_t *idx_out;
   float *w_out;  // [K] or null
   void *y;
