@@ -39,6 +39,7 @@ namespace {
 
 constexpr int kFuWorkers = 16;   // worker warps
 constexpr int kFuEpi = 14;       // warp index of the reduction epilogue
+constexpr int kFuTopk = 15;      // warp index of the top-k (a worker only in D)
 constexpr int kFuProducer = 16;  // warp index of the bulk-copy producer
 constexpr int kFuThreads = 32 * (kFuWorkers + 1);
 constexpr int kFuRB = 4;         // gate/up rows per G stage
@@ -54,15 +55,16 @@ constexpr long long kExpireBudget = 200000000LL;  // ~0.1 s: the expiry test's w
 // shared-memory map: barriers and small arrays; the ring (X/R/S/G slots, then D slots);
 // the partial sums
 constexpr int kFuBars = 0;       // fullG[8] emptyG[8] fullD[6] emptyD[6] redbar[2] redfree[2]
-                                 // selbar
+                                 // selbar topbar
 constexpr int kFuSel = 384;      // int[32]
 constexpr int kFuWsel = 512;     // float[32]
-constexpr int kFuMisc = 640;     // int[8]: top-k scratch [0..3], abort flag [4]
+constexpr int kFuMisc = 640;     // int[8]: abort flag [4], RMSNorm factor [5], selections
+                                 // published [7]
 constexpr int kFuGDone = 704;    // int[8]: X/R/S/G slot s fully consumed (set by its owner)
-constexpr int kFuSmall = 1024;   // top-k: histogram [256], selected keys [32], warp or/and;
+constexpr int kFuSmall = 1024;   // X (RMSNorm): per-warp sums; top-k: the selection scores;
                                  // D: dbuf [K][16] + ds [16]
 constexpr int kFuSmallBytes = 4096;
-static_assert((16 + 2 * kFuNSD + 5) * 8 <= kFuSel, "the barriers overlap the small arrays");
+static_assert((16 + 2 * kFuNSD + 6) * 8 <= kFuSel, "the barriers overlap the small arrays");
 static_assert(kFuNSD % 2 == 0, "every D slot serves one worker group");
 constexpr int kFuRing = kFuSmall + kFuSmallBytes;
 
@@ -92,149 +94,77 @@ __device__ bool wait_count(const unsigned *cnt, unsigned n, long long budget = k
 // also the slot's parity), and each group cycles through its three slots, so a group
 // computes on one slot while the other two fill.
 __host__ __device__ __forceinline__ int d_slot_of(int i) { return i % kFuNSD; }
-__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int o) {
-  return __shfl_xor_sync(0xffffffffu, v, o);
-}
 
-// Top-k of one token by the nt consumer threads (named barrier bar, nt a multiple of 32).
-// Keys as in cta_topk: the selection score's order-preserving bits, then the complemented
-// expert index, so the unsigned order is (score desc, index asc) and keys are distinct.
-// The K-th largest key is found by radix selection from the highest bit where the keys
-// differ (the bits above it are common to all of them): per pass an 8-bit digit, a
-// histogram of the keys that share the prefix found so far, and the digit where the count
-// from the top reaches K; the search stops once that digit's keys are all selected.  The
-// K keys >= the prefix are then sorted by warp 0.  sc_s: E floats of shared scratch.
-// E <= 8 nt, K <= 32.
-__device__ void topk_cta(const float *sc, const float *ch, int E, int K, int renorm,
-                         float routed_scale, int nt, int bar, uint32_t *hist,
-                         unsigned long long *list, unsigned long long *wred, int *misc,
-                         float *sc_s, int *sel, float *wsel) {
-  constexpr int KPT = 8;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = nt >> 5;
-  unsigned long long key[KPT];
-  unsigned long long kor = 0ull, kand = ~0ull;
+// Top-k of one token by one warp, once every CTA's scores are in the workspace.  Keys as
+// in cta_topk: the selection score's order-preserving bits, then the complemented expert
+// index, so the unsigned order is (score desc, index asc) and keys are distinct.  Lane l
+// scans experts l, l + 32, ... and keeps its kTopQ largest keys in order; K rounds of a
+// warp-wide maximum over the lanes' first keys then pick the selection in order, the
+// winning lane dropping its first key.  A lane whose kept keys run out rescans its
+// experts for the kTopQ largest below the last one it gave up, so the result is exact
+// whatever the distribution.  The selection scores are read from ch_s (a shared-memory
+// copy) when given, else from ch.  Selection j goes to sel[j] as soon as it is known, and
+// *ready = j + 1 publishes it.  Lane j < K returns selection j: its expert index and its
+// weight (the unbiased score, divided by the sum of the K scores in selection order when
+// renorm is set, times routed_scale).
+constexpr int kTopQ = 4;
+__device__ void topk_warp(const float *sc, const float *ch, const float *ch_s, int E, int K,
+                          int renorm, float routed_scale, int *sel, volatile int *ready,
+                          int &e_out, float &w_out) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long top[kTopQ];
+  // the kTopQ largest keys of this lane's experts that are below `below`
+  auto scan = [&](unsigned long long below) {
 #pragma unroll
-  for (int k = 0; k < KPT; k++) {
-    const int e = t + nt * k;
-    key[k] = 0ull;
-    if (e < E) {
-      sc_s[e] = __ldcg(sc + e);  // the unbiased scores, loaded with the selection scores
-      float c = __fadd_rn(__ldcg(ch + e), 0.f);     // -0 -> +0
+    for (int q = 0; q < kTopQ; q++) top[q] = 0ull;
+#pragma unroll 4
+    for (int e = lane; e < E; e += 32) {
+      float c = __fadd_rn(ch_s ? ch_s[e] : __ldcg(ch + e), 0.f);  // -0 -> +0
       if (c != c) c = -__int_as_float(0x7f800000);  // a NaN never wins (it is reported)
-      key[k] = ((unsigned long long)float_order_key(c) << 32) |
-               (unsigned long long)(0xffffffffu - (uint32_t)e);
-      kor |= key[k];
-      kand &= key[k];
-    }
-  }
+      const unsigned long long k = ((unsigned long long)float_order_key(c) << 32) |
+                                   (unsigned long long)(0xffffffffu - (uint32_t)e);
+      if (k < below && k > top[kTopQ - 1]) {
+        top[kTopQ - 1] = k;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kor |= shfl_xor_u64(kor, o);
-    kand &= shfl_xor_u64(kand, o);
-  }
-  if (lane == 0) {
-    wred[2 * warp] = kor;
-    wred[2 * warp + 1] = kand;
-  }
-  if (t == 0) misc[3] = 0;
-  named_bar_sync(bar, nt);
-  kor = 0ull;
-  kand = ~0ull;
-  for (int w = 0; w < nw; w++) {
-    kor |= wred[2 * w];
-    kand &= wred[2 * w + 1];
-  }
-  const unsigned long long diff = kor ^ kand;
-  const int b = diff ? 63 - __clzll((long long)diff) : 0;  // highest differing bit
-  unsigned long long mask = (b >= 63) ? 0ull : ~((2ull << b) - 1ull);
-  unsigned long long prefix = kand & mask;
-  int need = K;
-  for (int top = b;; top -= 8) {
-    const int lowb = top - 7 > 0 ? top - 7 : 0;
-    const unsigned dmask = (1u << (top - lowb + 1)) - 1u;
-    for (int i = t; i < 256; i += nt) hist[i] = 0u;
-    named_bar_sync(bar, nt);
-#pragma unroll
-    for (int k = 0; k < KPT; k++)
-      if (key[k] != 0ull && (key[k] & mask) == prefix)
-        atomicAdd(&hist[(unsigned)(key[k] >> lowb) & dmask], 1u);
-    named_bar_sync(bar, nt);
-    if (warp == 0) {
-      // lane l takes digits 255-8l down to 248-8l; counts are scanned from the top
-      uint32_t c[8], s = 0;
-#pragma unroll
-      for (int q = 0; q < 8; q++) {
-        c[q] = hist[255 - 8 * lane - q];
-        s += c[q];
-      }
-      uint32_t incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const uint32_t excl = incl - s;
-      if (lane == 0) misc[2] = -1;
-      __syncwarp();
-      if (excl < (uint32_t)need && (uint32_t)need <= incl) {
-        uint32_t ab = excl;
-        for (int q = 0; q < 8; q++) {
-          if (ab + c[q] >= (uint32_t)need) {
-            misc[0] = 255 - 8 * lane - q;
-            misc[1] = (int)ab;
-            misc[2] = (int)c[q];
-            break;
+        for (int q = kTopQ - 1; q > 0; q--) {
+          if (top[q] > top[q - 1]) {
+            const unsigned long long tk = top[q];
+            top[q] = top[q - 1];
+            top[q - 1] = tk;
           }
-          ab += c[q];
         }
       }
     }
-    named_bar_sync(bar, nt);
-    const int digit = misc[0], above = misc[1], cnt = misc[2];
-    if (cnt < 0) break;  // not reached: need <= the keys left under the prefix
-    need -= above;
-    prefix |= (unsigned long long)digit << lowb;
-    mask |= (unsigned long long)dmask << lowb;
-    if (cnt == need || lowb == 0) break;
-  }
-  // every key >= prefix is selected (exactly K of them)
-#pragma unroll
-  for (int k = 0; k < KPT; k++)
-    if (key[k] != 0ull && key[k] >= prefix) {
-      const int at = atomicAdd(&misc[3], 1);
-      if (at < 32) list[at] = key[k];
+  };
+  scan(~0ull);
+  unsigned long long mine = 0ull;
+#pragma unroll 1
+  for (int j = 0; j < K; j++) {
+    const unsigned long long head = top[0];
+    const unsigned hi = (unsigned)(head >> 32), lo = (unsigned)head;
+    const unsigned mhi = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+    const unsigned long long best = ((unsigned long long)mhi << 32) | mlo;
+    if (lane == j) mine = best;
+    if (lane == 0) {  // publish selection j at once: the producer waits for it
+      sel[j] = best ? (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull)) : 0;
+      __threadfence_block();
+      *ready = j + 1;
     }
-  named_bar_sync(bar, nt);
-  if (warp == 0) {
-    const int nsel = misc[3];
-    unsigned long long v = (lane < K && lane < nsel) ? list[lane] : 0ull;
-    // bitonic sort of 32 keys, descending
+    if (head == best && head != 0ull) {  // distinct keys: one lane at most
 #pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        const unsigned long long o = shfl_xor_u64(v, stride);
-        const bool lower = (lane & stride) == 0;
-        const bool desc = (lane & size) == 0;
-        v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
-      }
-    }
-    int e = 0;
-    float s = 0.f;
-    if (lane < K) {
-      e = (v == 0ull) ? 0 : (int)(0xffffffffu - (uint32_t)(v & 0xffffffffull));
-      s = sc_s[e];  // written before the barriers above
-    }
-    float wsum = 0.f;  // float sum of the chosen scores in selection order
-    for (int j = 0; j < K; j++) wsum = __fadd_rn(wsum, __shfl_sync(0xffffffffu, s, j));
-    if (lane < K) {
-      float w = s;
-      if (renorm && wsum > 0.f) w = __fdiv_rn(w, wsum);
-      sel[lane] = e;
-      wsel[lane] = __fmul_rn(w, routed_scale);
+      for (int q = 0; q < kTopQ - 1; q++) top[q] = top[q + 1];
+      top[kTopQ - 1] = 0ull;
+      if (top[0] == 0ull) scan(best);  // kept keys used up: the next ones below `best`
     }
   }
-  named_bar_sync(bar, nt);
+  e_out = (lane < K && mine != 0ull) ? (int)(0xffffffffu - (uint32_t)(mine & 0xffffffffull)) : 0;
+  const float s = lane < K ? __ldcg(sc + e_out) : 0.f;
+  float wsum = 0.f;  // float sum of the chosen scores in selection order
+  for (int j = 0; j < K; j++) wsum = __fadd_rn(wsum, __shfl_sync(0xffffffffu, s, j));
+  float w = s;
+  if (renorm && wsum > 0.f) w = __fdiv_rn(w, wsum);
+  w_out = __fmul_rn(w, routed_scale);
 }
 
 }  // namespace
@@ -309,14 +239,14 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
   uint64_t *redbar = emptyD + kFuNSD;
   uint64_t *redfree = redbar + 2;
   uint64_t *selbar = redfree + 2;
+  uint64_t *topbar = selbar + 1;
   int *sel = reinterpret_cast<int *>(smem + kFuSel);
   float *wsel = reinterpret_cast<float *>(smem + kFuWsel);
   int *misc = reinterpret_cast<int *>(smem + kFuMisc);
   volatile int *abort_flag = misc + 4;
+  volatile int *selready = misc + 7;  // selections 0 .. *selready-1 are in sel
   volatile int *gdone = reinterpret_cast<volatile int *>(smem + kFuGDone);
-  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kFuSmall);
-  unsigned long long *list = reinterpret_cast<unsigned long long *>(smem + kFuSmall + 1024);
-  unsigned long long *wred = reinterpret_cast<unsigned long long *>(smem + kFuSmall + 1280);
+  float *wss = reinterpret_cast<float *>(smem + kFuSmall);  // [warp][2] (X)
   float *dbuf = reinterpret_cast<float *>(smem + kFuSmall);  // [K][16] (D)
   float *ds = dbuf + K * kFuDownRows;                        // [16] (D)
   float *red = reinterpret_cast<float *>(ring + fused_ring_bytes(H, I, SI));
@@ -336,7 +266,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       mbar_init(&redfree[p], 1);
     }
     mbar_init(selbar, 1);
+    mbar_init(topbar, 1);
     misc[4] = 0;
+    misc[7] = 0;
     for (int s = 0; s < kFuMaxNS; s++) gdone[s] = 0;
     fence_barrier_init();
   }
@@ -347,15 +279,23 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     bool ab = false;
     int last_g = -1;  // this lane's last R/S/G stage
     if (lane < NSG) {
-      bool have_sel = false;
+      int ready = 0;  // selections this lane has seen published
       for (int t = lane; t < nRSG; t += NSG) {
-        if (t >= tG && !have_sel) {  // routed stages need the top-k
-          if (!mbar_wait(selbar, 0)) {
-            set_status(a.status, K3MOE_ERR_TIMEOUT);
-            ab = true;
-            break;
+        if (t >= tG) {  // a routed stage needs its expert slot's selection
+          const int j = (bx + nb * ((t - tG) >> 1)) / blocks;
+          if (j >= ready) {
+            const long long t0 = clock64();
+            while ((ready = *selready) <= j) {
+              if (clock64() - t0 > kWaitBudget) {
+                set_status(a.status, K3MOE_ERR_TIMEOUT);
+                ab = true;
+                break;
+              }
+              __nanosleep(32);
+            }
+            if (ab) break;
+            __threadfence_block();  // the published selections before their use
           }
-          have_sel = true;
         }
         if (!mbar_wait(&emptyG[lane], ((t / NSG) & 1) ^ 1)) {
           set_status(a.status, K3MOE_ERR_TIMEOUT);
@@ -655,7 +595,6 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
         ff_add(sh, sl, oh, ol);
       }
-      float *wss = reinterpret_cast<float *>(wred);  // [warp][2], idle until the top-k
       if (lane == 0) {
         wss[2 * warp] = sh;
         wss[2 * warp + 1] = sl;
@@ -729,22 +668,6 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       }
       end_item(n);
     }
-    // top-k, once every CTA's router rows are in the workspace; the ring meanwhile fills
-    // with S stages
-    if (tid == 0 && !wait_count(a.bar, (unsigned)nb)) {
-      set_status(a.status, K3MOE_ERR_TIMEOUT);
-      *abort_flag = 1;
-    }
-    named_bar_sync(kBarCons, nt);
-    // the partial-sum buffer is idle here (the epilogue finished the R items before
-    // dependency 1; S items start after the top-k): it holds the scores meanwhile
-    topk_cta(a.sc, a.ch, E, K, a.renorm, a.routed_scale, nt, kBarCons, hist, list, wred, misc,
-             red, sel, wsel);
-    if (bx == 0 && tid < K && a.idx_out) {
-      a.idx_out[tid] = sel[tid];
-      a.w_out[tid] = wsel[tid];
-    }
-    if (tid == 0) mbar_arrive(selbar);
     // S: gate row (h = 0) or up row (h = 1) of shared pair s, fp32 sums of exact products
     for (int s = 0; s < nS; s++, t++, n++) {
       float *rt = begin_item(n);
@@ -807,6 +730,54 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       }
       end_item(n);
     }
+  } else if (warp == kFuTopk) {
+    // ---------------- top-k, once every CTA's router rows are in the workspace ----------
+    // (meanwhile the consumers take the S stages; the producer issues G stages once the
+    // selection is published)
+    // the selection scores come into shared memory in one bulk copy when they fit
+    const uint32_t chb = ((uint32_t)E * 4u + 15u) & ~15u;  // the workspace pads them to 16
+    const bool bulk = chb <= (uint32_t)kFuSmallBytes;
+    bool ok = true;
+    if (lane == 0) {
+      if (!wait_count(a.bar, (unsigned)nb)) {
+        set_status(a.status, K3MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (bulk) {
+        fence_proxy_async_all();  // the other CTAs' score writes before the async-proxy read
+        mbar_arrive_expect_tx(topbar, chb);
+        bulk_g2s(smem + kFuSmall, a.ch, chb, topbar);
+      }
+    }
+    __syncwarp();
+    if (bulk && !mbar_wait(topbar, 0)) {
+      set_status(a.status, K3MOE_ERR_TIMEOUT);
+      *abort_flag = 1;
+      ok = false;
+      mbar_wait(topbar, 0, 400000000LL);  // bounded wait for the copy still in flight
+    }
+    int e_sel = 0;
+    float w_sel = 0.f;
+    if (__all_sync(0xffffffffu, ok)) {
+      topk_warp(a.sc, a.ch, bulk ? reinterpret_cast<const float *>(smem + kFuSmall) : nullptr, E,
+                K, a.renorm, a.routed_scale, sel, selready, e_sel, w_sel);
+    } else {  // after an expiry: expert 0 everywhere, output zero (the abort flag is set)
+      if (lane < K) sel[lane] = 0;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        *selready = K;
+      }
+    }
+    if (lane < K) {
+      wsel[lane] = w_sel;
+      if (bx == 0 && a.idx_out) {
+        a.idx_out[lane] = e_sel;
+        a.w_out[lane] = w_sel;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(selbar);
   }
 
   // ---------------- dependency 2: this CTA's activations are written ----------------
@@ -943,8 +914,7 @@ size_t fused_t1_smem(int H, int I, int E, int K, int SI, int grid) {
   if (K < 2 || K > 16 || K % 2 != 0) return 0;             // two experts per down stage
   if (SI < 0 || SI % 256 != 0) return 0;                   // shared rows in 32 lanes x 8
   if (grid < 1) return 0;
-  if (E > 8 * 64 * (G / 32) || (E + grid - 1) / grid > 32) return 0;  // top-k keys, R rows
-  if (E * 4 > kFuRedBytes) return 0;  // the top-k's scores in the partial-sum buffer
+  if ((E + grid - 1) / grid > 32) return 0;  // R rows of a CTA: one epilogue lane each
   if (fused_nsg(H) < 2) return 0;
   const size_t total = (size_t)kFuRing + fused_ring_bytes(H, I, SI) + kFuRedBytes;
   return total <= kFuSmemMax ? total : 0;

@@ -220,6 +220,21 @@ def test_fused_single_token_ties_bias_bf16_accumulate():
     assert st == 0 and max_rel(yb.float().cpu().numpy(), oy) <= MAX_REL_BF16
 
 
+def test_fused_topk_one_lane_holds_most_of_the_selection():
+    # The single-token kernel's top-k lane l scans experts l, l + 32, ... and keeps its
+    # four best; boosting every expert 5 + 32 i puts the first 12 picks in one lane, which
+    # must rescan for more three times.  The rest of the selection comes from the others.
+    L = fused_layer(34, n_experts=384, topk=16)
+    bias = L.host["bias"].copy()
+    for i in range(12):
+        bias[5 + 32 * i] = 10.0 + i
+    L.host["bias"] = bias
+    L.d_bias = torch.from_numpy(bias).cuda()
+    oi, ow, oy = L.oracle()
+    assert oi[0, :12].tolist() == [5 + 32 * i for i in range(11, -1, -1)]
+    check_layer(L)
+
+
 def test_fused_single_token_scale_255_and_0_groups():
     L = fused_layer(32, topk=8, n_experts=16, n_shared=0)
     cfg = L.cfg
