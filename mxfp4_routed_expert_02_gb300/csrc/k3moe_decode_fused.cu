@@ -452,6 +452,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     // collected in lane 2s + r; then every lane's unbiased score (logistic in double,
     // rounded once; the slow double pipe runs once for all rows) and selection score
     float mylogit = 0.f;
+    // this lane's router-row bias, fetched now: by the time it is added the stream of
+    // weight stages keeps every memory queue long
+    const float mybias = (a.bias && lane < cntR) ? __ldg(a.bias + bx + nb * lane) : 0.f;
     for (int s = 0; s < nR; s++, n++) {
       const float *rt = take(n);
       float hi = 0.f, lo = 0.f;
@@ -466,13 +469,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     if (lane < cntR) {
       const int row = bx + nb * lane;
       const float sv = (float)(1.0 / (1.0 + exp(-(double)mylogit)));
-      const float cv = __fadd_rn(sv, a.bias ? a.bias[row] : 0.f);
+      const float cv = __fadd_rn(sv, mybias);
       a.sc[row] = sv;
       a.ch[row] = cv;
       if (!(fabsf(cv) <= 3.402823466e38f)) set_status(a.status, K3MOE_ERR_NONFINITE);
-      __threadfence();
     }
-    __syncwarp();
+    __syncwarp();  // the lanes' score writes before lane 0's fence, which covers them all
     if (lane == 0) {  // dependency 1: this CTA's router rows are written
       __threadfence();
       atomicAdd(a.bar, 1u);
