@@ -20,15 +20,16 @@
 //      shared expert, then the router-order combine of the tile
 //
 // so the stream never drains: the top-k needs every CTA's R rows (dependency 1: a counter
-// the epilogue warps bump once their router rows are written) and is computed by the
-// consumer warps of every CTA while the ring fills with S stages; D needs every
-// activation (dependency 2: all worker warps of every CTA), while the ring already holds
-// the first D stages.
+// the epilogue warp bumps once its router rows are written) and is computed by one warp
+// of every CTA while the consumers take the S stages; each selection is published as soon
+// as it is known, and the G stages of an expert slot go out once its selection is; D
+// needs every activation (dependency 2: all worker warps of every CTA), while the ring
+// already holds the first D stages.
 //
 // Warp roles: workers 0..2n-1 (n = H/1024) consume X, R, S and G stages (thread (h, g):
-// input group g, row parity h) and select the top-k; warp 14 reduces their partial sums
-// (logits and scores, SiTU); warp 16 issues the bulk copies.  In D all 16 worker warps
-// consume.
+// input group g, row parity h); warp 14 reduces their partial sums (logits and scores,
+// SiTU); warp 15 selects the top-k; warp 16 issues the bulk copies (lane s owns ring slot
+// s).  In D all 16 worker warps (0..15) consume.
 // Every wait is bounded: on expiry the kernel reports K3MOE_ERR_TIMEOUT, keeps arriving on
 // the barriers it owes, and writes zeros.
 #include "k3moe_kernels.cuh"
