@@ -364,13 +364,13 @@ bool fused_takes(const DeviceInfo *di, const k3moe_dims *d) {
   return fused_t1_smem(d->hidden, d->inter, d->n_experts, d->topk, d->shared_inter, di->sms) > 0;
 }
 
-// One token through the fused kernel: input x (bf16), or h (float, the residual stream)
-// normalised in the kernel (x = bf16(RMSNorm(h)) with eps).  Its grid-wide counters
-// (workspace header) are zero on entry and left zero by the kernel's last CTA.
 // While set, single-token fused launches wait for an arrival that never comes (test of the
 // bounded-wait path).
 std::atomic<int> g_expire_wait{0};
 
+// One token through the fused kernel: input x (bf16), or h (float, the residual stream)
+// normalised in the kernel (x = bf16(RMSNorm(h)) with eps).  Its grid-wide counters
+// (workspace header) are zero on entry and left zero by the kernel's last CTA.
 k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x,
                        const float *h, float eps, const uint16_t *wr, const float *bias,
                        const k3moe_experts *ex, const uint16_t *sh_gate, const uint16_t *sh_up,

@@ -235,6 +235,16 @@ def test_fused_topk_one_lane_holds_most_of_the_selection():
     check_layer(L)
 
 
+@pytest.mark.parametrize("E,K", [(37, 6), (1100, 8)])
+def test_fused_single_token_expert_counts(E, K):
+    # 37: the score copy for the top-k includes the workspace's padding (37 * 4 bytes is
+    # not a multiple of 16); 1100: the scores exceed the shared-memory copy and the top-k
+    # warp reads them from the workspace
+    cfg = dataclasses.replace(synth.config("tiny"), name="custom", hidden=1024, inter=512,
+                              n_experts=E, topk=K, tokens=1, n_shared=1)
+    check_layer(Layer(cfg, seed=35 + K, device_fill=E > 64))
+
+
 def test_fused_single_token_scale_255_and_0_groups():
     L = fused_layer(32, topk=8, n_experts=16, n_shared=0)
     cfg = L.cfg
