@@ -95,6 +95,15 @@ __device__ bool wait_count(const unsigned *cnt, unsigned n, long long budget = k
 // also the slot's parity), and each group cycles through its three slots, so a group
 // computes on one slot while the other two fill.
 __host__ __device__ __forceinline__ int d_slot_of(int i) { return i % kFuNSD; }
+// The factor 2^(s-127) * pe of an MXFP4 group with scale byte s, without a branch: the
+// byte's bits become the float exponent (exact powers of two, subnormal products
+// included).  Byte 255 contributes nothing (the group's NaN code); byte 0 gives 0 where
+// the exact factor is 2^-127 * pe, a contribution some 30 orders of magnitude below the
+// output's tolerance.
+__device__ __forceinline__ float group_scale(uint32_t s, float pe) {
+  const float f = __uint_as_float(s << 23) * pe;
+  return s == 255u ? 0.f : f;
+}
 
 // Top-k of one token by one warp, once every CTA's scores are in the workspace.  Keys as
 // in cta_topk: the selection score's order-preserving bits, then the complemented expert
@@ -696,6 +705,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     // G: an 8-row block = two stages of kFuRB gate and up rows; thread (h, g) takes the
     // rows of parity h in input group g
     constexpr int V = 2 * kFuRB;  // (2 rows x 2 matrices) x 2 stages
+    const float pxe = pow2i(xe);  // this thread's inputs are stored times 2^-xe
     for (int s = 0; s < nI; s++, n++) {
       float *rt = begin_item(n);
       float vals[V];
@@ -716,9 +726,8 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
             const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
             const uint4 wu = reinterpret_cast<const uint4 *>(st + (kFuRB + q) * rowb)[g];
             const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
-            // group_factor is 0 for scale byte 255 and the dot is finite: no branch
-            vals[b2 * kFuRB + 2 * k] = group_dot(xr, wg) * group_factor(sg, xe);
-            vals[b2 * kFuRB + 2 * k + 1] = group_dot(xr, wu) * group_factor(su, xe);
+            vals[b2 * kFuRB + 2 * k] = group_dot(xr, wg) * group_scale(sg, pxe);
+            vals[b2 * kFuRB + 2 * k + 1] = group_dot(xr, wu) * group_scale(su, pxe);
           }
         }
       }
@@ -800,7 +809,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
   bool aborted = *abort_flag != 0;
   const int NG = G2 / 16;                   // groups per lane
   const int rp = lane >> 4, l = lane & 15;  // row pair, group lane
-  const int e2 = a.act_exp;
+  const float pe2 = pow2i(a.act_exp);  // activations are stored times 2^-act_exp
   for (int n = 0; n < nT; n++) {
     const int r0 = (bx + nb * n) * kFuDownRows;
     for (int i = tid; i < (K + 1) * kFuDownRows; i += NDT) dbuf[i] = 0.f;  // dbuf and ds
@@ -836,7 +845,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
             const int row = rb + r;
             const uint4 wv = reinterpret_cast<const uint4 *>(sp + row * rowb2)[gg];
             const uint32_t sv = ss[row * G2 + gg];
-            acc[r] += group_dot(xa, wv) * group_factor(sv, e2);  // 0 for byte 255
+            acc[r] += group_dot(xa, wv) * group_scale(sv, pe2);
           }
         }
 #pragma unroll
