@@ -194,6 +194,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def reduce_max(dist, value, device):
+    """The largest of the ranks' values, returned on every rank (the value itself when
+    there is one rank): the job's time is its slowest rank's."""
+    if dist is None:
+        return value
+    import torch
+    tt = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(units_per_rank, world, seconds):
+    """Whole-job throughput of independent replicas: the units all ranks processed over
+    the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -260,11 +277,7 @@ def run_ours(args):
         dist.barrier()
     assert status.item() == 0, k3.status_str(status.item())
     ms = [a.elapsed_time(b) for a, b in ev]
-    t_dev = sum(ms) / 1e3
-    if dist:
-        tt = torch.tensor([t_dev], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_dev = float(tt.item())
+    t_dev = reduce_max(dist, sum(ms) / 1e3, dev)
 
     # per-kernel device time: the same steps again with the library's event tracing on
     # (tracing brackets every launch with events, so it also turns off the programmatic
@@ -316,19 +329,15 @@ def run_ours(args):
         yh.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    t_e2e = e0.elapsed_time(e1) / 1e3
-    if dist:
-        tt = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = reduce_max(dist, e0.elapsed_time(e1) / 1e3, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, seed, 2)
     if rank == 0:
-        tokens = args.steps * world
         line = {
-            "metric": METRIC, "value": tokens / t_dev, "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": job_rate(args.steps, world, t_dev), "unit": "tokens/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_dev / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -342,7 +351,8 @@ def run_ours(args):
             "kernels": kernels,
             "gpu_launches": launches,
             "clocks": clocks.summary(local),
-            "e2e": {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": H * 2,
+            "e2e": {"value": job_rate(args.steps, world, t_e2e), "unit": "tokens/s",
+                    "h2d_bytes_per_step": H * 2,
                     "d2h_bytes_per_step": H * 4},
             "cpu_baseline": cpu,
             "wall_s": t_wall,
@@ -373,6 +383,10 @@ def run_batch(args):
     import torch
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
     import synth
     import synth.device as sd
     import mxfp4_routed_expert_02_gb300 as k3
@@ -430,6 +444,9 @@ def run_batch(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     clocks = Clocks("/tmp/k3moe_bench_clocks_%d_%d.csv" % (os.getpid(), rank))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
     with clocks:
         for s in range(args.steps):
             if name != "stacked8":
@@ -438,9 +455,11 @@ def run_batch(args):
             step(args.warmup + s)
             ev[s][1].record(stream)
         torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     assert status.item() == 0, k3.status_str(status.item())
     ms = [a.elapsed_time(b) for a, b in ev]
-    t_dev = sum(ms) / 1e3
+    t_dev = reduce_max(dist, sum(ms) / 1e3, torch.device("cuda", local))
     # per-kernel device time from a traced pass
     k3.k3moe_trace_enable(True)
     for s in range(min(args.steps, 3)):
@@ -495,7 +514,7 @@ def run_batch(args):
         extra = {}
     lat = sorted(ms)
     line = {
-        "metric": METRIC, "value": T * args.steps * world / t_dev, "unit": "tokens/s",
+        "metric": METRIC, "value": job_rate(T * args.steps, world, t_dev), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -512,6 +531,8 @@ def run_batch(args):
     line.update(extra)
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 def main():
