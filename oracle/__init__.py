@@ -7,9 +7,11 @@ ctypes and numpy; it shares no code with the CUDA library.
 Every function names the passage it follows; "kimi-k3-in-c" is the README of
 FareedKhan-dev/kimi-k3-in-c, "Kimi-K3.cpp" the README of Maknee/Kimi-K3.cpp.
 
-Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against
-values the pages print, closed forms, invariants or brute force (see the design notes'
-pin table); none is "parity unpinned".
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``: the
+number formats by the page's printed E2M1 table and the closed form of E8M0, the
+products and the top-k by brute force on tiny inputs, the router weights, SiTU and the
+layer composition by invariants and special cases, the routed sum by sums whose float
+result depends on the order of the terms.  None is "parity unpinned".
 """
 import ctypes
 import os
@@ -51,6 +53,7 @@ def lib():
                                          f32p, c_int]),
             "k3o_moe_token": (None, [c_int, c_int, c_int, c_int, u16p, ctypes.POINTER(u8p), f32p,
                                      u16p, u16p, u16p, c_float, c_float, f32p, c_int]),
+            "k3o_combine": (None, [c_int, c_int, f32p, f32p, f32p, f32p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -212,9 +215,26 @@ def shared_expert(gate, up, down, x_f32, b1: float = 4.0, b2: float = 25.0,
     return ds
 
 
+def combine(w, d, ds=None) -> np.ndarray:
+    """Routed sum in router order plus the shared expert (section 9, LatentMoE listing
+    steps 3 and 6): acc = 0; acc = acc + w[j] * d[j] for j = 0..K-1 in float, one
+    rounding per product and per sum; then acc + ds (one float add) when ds is given.
+    d is [K][H]."""
+    w = _c(w, np.float32)
+    d = _c(np.atleast_2d(d), np.float32)
+    K, H = d.shape
+    assert w.shape == (K,)
+    dsa = None if ds is None else _c(ds, np.float32)
+    y = np.empty(H, dtype=np.float32)
+    lib().k3o_combine(H, K, _p(w, ctypes.c_float), _p(d, ctypes.c_float),
+                      _p(dsa, ctypes.c_float), _p(y, ctypes.c_float))
+    return y
+
+
 def moe_token(x_bf16, recs, w, H: int, I: int, sh_gate=None, sh_up=None, sh_down=None,
               b1: float = 4.0, b2: float = 25.0, nthreads: int = 0) -> np.ndarray:
-    """Layer output for one routed token: sum_j w_j d_j in router order + shared(x)."""
+    """Layer output for one routed token: the float sum of w_j d_j in router order, then
+    the shared expert's output added unweighted (``combine``)."""
     x = _c(x_bf16, np.uint16)
     K = len(recs)
     recs = [_c(r, np.uint8) for r in recs]

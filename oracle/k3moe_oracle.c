@@ -25,10 +25,12 @@
  *                                              Kimi-K3.cpp "The consumer-memory idea" 7
  *
  * Precision: every sum the page accumulates in double is accumulated in double here,
- * every value the page stores as float is rounded to float here.  Where the page uses a
- * float libm call (expf, tanhf) the oracle evaluates the same function in double and
- * rounds once to float (the reading recorded in the design notes: the float libm result
- * is platform dependent, the double-then-round one is not).
+ * every sum the page accumulates in float (the routed sum in router order, the shared
+ * expert's add) is a float sum here, term by term in the page's order, and every value
+ * the page stores as float is rounded to float here.  Where the page uses a float libm
+ * call (expf, tanhf) the oracle evaluates the same function in double and rounds once to
+ * float: the float libm result differs from one C library to another, the
+ * double-then-round one does not, so CPU and GPU can agree on it.
  *
  * Build: gcc -std=c11 -O2 -ffp-contract=off -fopenmp -fPIC -shared (see build.py).
  */
@@ -281,30 +283,41 @@ void k3o_shared_expert(int H, int SI, const uint16_t *gate, const uint16_t *up,
     free(act);
 }
 
+/* The routed sum and the shared expert (section 9, LatentMoE listing steps 3 and 6):
+ *   acc[i] = 0.0f;  for j = 0 .. K-1 in router order:  acc[i] = acc[i] + w[j] * d[j][i]
+ * with one float product and one float sum per term (the build turns off contraction,
+ * so no fused multiply-add), then y[i] = acc[i] + ds[i], one float add (skipped when ds
+ * is NULL).  Float addition is not associative: the order of the terms is part of the
+ * result.  d is [K][H]. */
+void k3o_combine(int H, int K, const float *w, const float *d, const float *ds, float *y) {
+    for (int i = 0; i < H; i++) {
+        float acc = 0.0f;
+        for (int j = 0; j < K; j++) {
+            const float p = w[j] * d[(size_t)j * H + i];
+            acc = acc + p;
+        }
+        y[i] = ds ? acc + ds[i] : acc;
+    }
+}
+
 /* The layer for ONE token whose route is already known.
  *   recs[j]  : the expert record of the j-th selected expert (router order)
  *   w[j]     : its weight
- *   y[i]     = sum_{j=0}^{K-1} w[j] d_j[i]   (accumulated in router order, in double)
- *              + shared(x)[i]                (unweighted; skipped when gate == NULL)
- * rounded once to float.  x is the token's bf16 input. */
+ *   y        = the float router-order sum of w[j] d_j plus the shared expert's output
+ *              (unweighted; no shared expert when gate == NULL), as k3o_combine forms it.
+ * x is the token's bf16 input. */
 void k3o_moe_token(int H, int I, int K, int SI, const uint16_t *x,
                    const uint8_t *const *recs, const float *w, const uint16_t *sh_gate,
                    const uint16_t *sh_up, const uint16_t *sh_down, float b1, float b2,
                    float *y, int nthreads) {
     float *xf = (float *)malloc(sizeof(float) * (size_t)H);
-    float *d = (float *)malloc(sizeof(float) * (size_t)H);
-    double *acc = (double *)calloc((size_t)H, sizeof(double));
+    float *d = (float *)malloc(sizeof(float) * (size_t)H * (size_t)(K > 0 ? K : 1));
+    float *ds = sh_gate ? (float *)malloc(sizeof(float) * (size_t)H) : NULL;
     for (int i = 0; i < H; i++) xf[i] = k3o_bf16_to_f32(x[i]);
-    for (int j = 0; j < K; j++) {
-        k3o_expert(H, I, recs[j], xf, b1, b2, d, nthreads);
-        for (int i = 0; i < H; i++) acc[i] += (double)w[j] * (double)d[i];
-    }
-    if (sh_gate) {
-        k3o_shared_expert(H, SI, sh_gate, sh_up, sh_down, xf, b1, b2, d, nthreads);
-        for (int i = 0; i < H; i++) acc[i] += (double)d[i];
-    }
-    for (int i = 0; i < H; i++) y[i] = (float)acc[i];
+    for (int j = 0; j < K; j++) k3o_expert(H, I, recs[j], xf, b1, b2, d + (size_t)j * H, nthreads);
+    if (sh_gate) k3o_shared_expert(H, SI, sh_gate, sh_up, sh_down, xf, b1, b2, ds, nthreads);
+    k3o_combine(H, K, w, d, ds, y);
     free(xf);
     free(d);
-    free(acc);
+    free(ds);
 }

@@ -135,3 +135,50 @@ def test_router_order_weighted_sum_and_unweighted_shared():
     for t in range(2):
         d = oracle.expert(recs[idx1[t][0]], oracle.bf16_to_f32(x[t]), H, I)
         assert np.allclose(y1[t], np.float64(w1[t][0]) * d, rtol=1e-6, atol=1e-7)
+
+
+def test_combine_is_a_float_sum_in_router_order():
+    # kimi-k3-in-c, section 9, LatentMoE listing steps 3 and 6: acc += w[j] * d_j[i] in
+    # float, j in router order, then the shared output added.  2^24 + 1 rounds back to
+    # 2^24, so the three terms sum to 0 left to right and to 1 right to left (and in
+    # double).
+    big = 2.0 ** 24
+    assert oracle.combine([1, 1, 1], [[big], [1.0], [-big]])[0] == 0.0
+    assert oracle.combine([1, 1, 1], [[-big], [1.0], [big]])[0] == 1.0
+    # each product is rounded to float before it is added (no fused multiply-add):
+    # (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24 rounds to 1 + 2^-11
+    a = 1.0 + 2.0 ** -12
+    assert oracle.combine([-1.0, a], [[1.0], [a]])[0] == 2.0 ** -11
+    # the shared expert's output comes after the routed sum: added first, 1 + 2^24 would
+    # round away the 1
+    assert oracle.combine([1, 1], [[big], [-big]], ds=[1.0])[0] == 1.0
+    assert oracle.combine([1, 1], [[big], [-big]])[0] == 0.0
+
+
+def test_routed_sum_in_router_order_through_the_layer():
+    # records built so that each output row's float sum is exactly 0 or exactly the one
+    # small term, depending only on where that term sits in the router order
+    import order_probe
+    H, I, K = 96, 64, 4
+    recs, pat = order_probe.records(H, I, K, seed=11)
+    rng = np.random.default_rng(12)
+    x = oracle.f32_to_bf16(rng.standard_normal(H).astype(np.float32))
+    xf = oracle.bf16_to_f32(x)
+    w = np.full(K, 0.25, np.float32)
+    y = oracle.moe_token(x, list(recs), w, H, I)
+    zero = order_probe.zero_rows(pat)
+    assert zero.any() and (~zero).any()
+    assert np.all(y[zero] == 0.0)
+    r = order_probe.small_term_position(pat)
+    d = np.stack([oracle.expert(recs[k], xf, H, I) for k in range(K)])
+    want = w[r] * d[r, np.arange(H)]            # one float32 product per row
+    assert want.dtype == np.float32 and np.all(want[~zero] != 0)
+    assert np.array_equal(y[~zero], want[~zero])
+    # the same experts in another order: the rows that vanish follow the new order
+    perm = [2, 0, 3, 1]                          # position n holds expert perm[n]
+    y2 = oracle.moe_token(x, [recs[k] for k in perm], w, H, I)
+    pos = np.argsort(perm)                       # expert k sits at position pos[k]
+    zero2 = order_probe.zero_rows(pos[pat])
+    assert not np.array_equal(zero, zero2)
+    assert np.all(y2[zero2] == 0.0)
+    assert np.array_equal(y2[~zero2], want[~zero2])
