@@ -1,19 +1,32 @@
 """Benchmark of the MoE layer step on GB300.
 
-Workload (one step = one pass of the whole layer step over one batch):
-  decode1: one decode token through one full-shape layer -- hidden 7168, expert
-  intermediate 1536, 896 routed MXFP4 experts resident in HBM (15.7 GB), top-16, one bf16
-  shared expert 7168x1536.  Synthetic seeded inputs (synth/), distinct tokens per step so
-  every step routes to its own experts; L2 is flushed (a 256 MB write) between timed steps.
+One full-shape layer -- hidden 7168, expert intermediate 1536, 896 routed MXFP4 experts
+resident in HBM (15.7 GB), top-16, one bf16 shared expert 7168x1536 -- with seeded
+synthetic inputs (synth/).  The default run times, in one process and on one resident
+expert pool:
 
-Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the reference
-arm of this comparison), on the same workload, metric and unit.
+  decode1        1 token per step (the headline: value, e2e, roofline, cpu_baseline);
+  decode64_zipf  64 tokens per step, expert popularity Zipf(1.1) through the bias;
+  prefill4096    4096 tokens per step, uniform routing, grouped GEMMs on tcgen05;
+  stacked8       1 token per step through 8 stacked layers (126 GB of MXFP4 resident),
+                 RMSNorm and the residual stream in between;
+
+the last three as nested entries of the one JSON line (``workloads``).  ``--workload``
+times one of them alone as the line's headline.  Timed regions: blocks of exactly K
+steps, each between a barrier and a synchronize, repeated until at least a second of
+load has passed so that the clock sampler sees the timed work; every step between CUDA
+events on the launching stream; L2 flushed between steps (outside the events) except
+for stacked8, whose inputs are larger than L2.
+
+``--impl reference`` times the CPU oracle instead (the reference arm of this
+comparison), on the decode1 workload, metric and unit.
 
 N > 1 (torchrun): the layer step does not shard without an exchange step, so every rank
 runs an independent replica; value = tokens processed by all ranks / max rank time.
 """
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -26,9 +39,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer decode tokens/s & HBM GB/s vs ~8 TB/s; prefill tcgen05 % peak"
-WORKLOAD = ("decode1: 1 token/step through one full-shape MoE layer (hidden 7168, inter 1536, "
-            "896 MXFP4 experts top-16, 1 bf16 shared expert 7168x1536)")
-
+WORKLOADS = {
+    "decode1": "decode1: 1 token/step through one full-shape MoE layer (hidden 7168, inter "
+               "1536, 896 MXFP4 experts top-16, 1 bf16 shared expert 7168x1536)",
+    "decode64_zipf": "decode64_zipf: 64 tokens/step through one full-shape MoE layer, expert "
+                     "popularity Zipf(1.1) through the correction bias",
+    "prefill4096": "prefill4096: 4096 tokens/step through one full-shape MoE layer, uniform "
+                   "routing (grouped MXFP4 GEMM on tcgen05)",
+    "stacked8": "stacked8: 1 token/step through 8 stacked full-shape MoE layers (126 GB of "
+                "MXFP4 resident) with RMSNorm and the residual stream between them",
+}
+WORKLOAD = WORKLOADS["decode1"]
+DEFAULT_STEPS = {"decode1": 3000, "decode64_zipf": 200, "prefill4096": 40, "stacked8": 256}
+MIN_TIMED_SECONDS = 1.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of each decode kernel, keyed to a hash of the sources the kernels are built
@@ -211,100 +234,169 @@ def job_rate(units_per_rank, world, seconds):
     return units_per_rank * world / seconds
 
 
-def run_ours(args):
-    import torch
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    import synth
-    import synth.device as sd
-    import mxfp4_routed_expert_02_gb300 as k3
+def blocks_needed(block_seconds, min_seconds=MIN_TIMED_SECONDS):
+    """Timed blocks of K steps so that the timed work lasts at least min_seconds."""
+    if block_seconds <= 0:
+        return 1
+    return max(1, int(math.ceil(min_seconds / block_seconds)))
 
-    cfg = synth.config("decode1")
-    if args.experts != cfg.n_experts:   # smaller expert pool: profiling captures only
-        cfg = synth.config("decode1", n_experts=args.experts)
-    seed = 0
-    dev = torch.device("cuda", local)
-    H, I, E, K = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
-    dims = k3.LayerDims(H, I, E, K, cfg.shared_inter)
-    stride = (cfg.record_bytes + 4095) // 4096 * 4096
-    experts = torch.empty(E * stride, dtype=torch.uint8, device=dev)
-    sd.fill_experts(experts, cfg, seed, 0, stride=stride)
-    w = synth.layer_weights(cfg, seed)
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    wr, bias = t(w["wr"].view(np.int16)), t(w["bias"])
-    sg, su, sdn = (t(w[k].view(np.int16)) for k in ("sh_gate", "sh_up", "sh_down"))
-    NX = 256
-    xs_host = synth.activations(cfg, seed + 1 + rank, NX)
-    xs = t(xs_host.view(np.int16))
-    y = torch.empty((1, H), dtype=torch.float32, device=dev)
-    idx = torch.empty((NX, K), dtype=torch.int32, device=dev)
-    wt = torch.empty((NX, K), dtype=torch.float32, device=dev)
-    ws = k3.new_workspace(dims, 1, dev)
-    status = k3.new_status(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
 
-    def step(s):
-        j = s % NX
-        k3.k3moe_layer(dims, xs[j:j + 1], wr, bias, experts, stride, sg, su, sdn, y, ws, status,
-                       idx_out=idx[j:j + 1], w_out=wt[j:j + 1])
+class Timer:
+    """Timed blocks of exactly K steps, each between a barrier and a synchronize, with
+    per-step CUDA events on the launching stream and nvidia-smi sampling throughout."""
 
-    for s in range(args.warmup):
-        flush.fill_(s & 255)
-        step(s)
-    torch.cuda.synchronize()
+    def __init__(self, ctx, tag):
+        self.ctx, self.tag = ctx, tag
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    clocks = Clocks("/tmp/k3moe_bench_clocks_%d_%d.csv" % (os.getpid(), rank))
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with clocks:
-        t_wall = time.perf_counter()
-        for s in range(args.steps):
-            flush.fill_((s + 7) & 255)
-            ev[s][0].record(stream)
-            step(args.warmup + s)
-            ev[s][1].record(stream)
+    def run(self, step, K, W, flush=None):
+        import torch
+        c = self.ctx
+        for s in range(W):
+            if flush:
+                flush(s)
+            step(s)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
-    if dist:
-        dist.barrier()
-    assert status.item() == 0, k3.status_str(status.item())
-    ms = [a.elapsed_time(b) for a, b in ev]
-    t_dev = reduce_max(dist, sum(ms) / 1e3, dev)
+        clocks = Clocks("/tmp/k3moe_bench_clocks_%s_%d_%d.csv" % (self.tag, os.getpid(), c.rank))
+        per_step, blocks, nb = [], 0, 1
+        with clocks:
+            t_wall = time.perf_counter()
+            while blocks < nb:
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(K)]
+                if c.dist:
+                    c.dist.barrier()
+                torch.cuda.synchronize()
+                tb = time.perf_counter()
+                for s in range(K):
+                    i = W + blocks * K + s
+                    if flush:
+                        flush(i)
+                    ev[s][0].record(c.stream)
+                    step(i)
+                    ev[s][1].record(c.stream)
+                torch.cuda.synchronize()
+                if c.dist:
+                    c.dist.barrier()
+                per_step += [a.elapsed_time(b) for a, b in ev]
+                if blocks == 0:  # every rank runs the slowest rank's number of blocks
+                    nb = int(reduce_max(c.dist, blocks_needed(time.perf_counter() - tb), c.dev))
+                blocks += 1
+            t_wall = time.perf_counter() - t_wall
+        self.blocks, self.wall = blocks, t_wall
+        self.clocks = clocks.summary(c.local)
+        self.ms = per_step
+        # the job's device time: the slowest rank's sum of step times
+        self.t_dev = reduce_max(c.dist, sum(per_step) / 1e3, c.dev)
+        return self
 
-    # per-kernel device time: the same steps again with the library's event tracing on
-    # (tracing brackets every launch with events, so it also turns off the programmatic
-    # overlap of consecutive kernels; the step time above is taken without it)
+
+class Ctx:
+    """Device, process group, the resident expert pool and the layer's small weights."""
+
+    def __init__(self, args):
+        import torch
+        self.rank, self.world, self.local = dist_env()
+        torch.cuda.set_device(self.local)
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+            self.dist = dist
+        import synth
+        import synth.device as sd
+        import mxfp4_routed_expert_02_gb300 as k3
+        self.k3, self.synth, self.sd = k3, synth, sd
+        self.dev = torch.device("cuda", self.local)
+        self.stream = torch.cuda.current_stream()
+        self.seed = 0
+        cfg = synth.config("decode1")
+        if args.experts != cfg.n_experts:   # smaller expert pool: profiling captures only
+            cfg = synth.config("decode1", n_experts=args.experts)
+        self.cfg = cfg
+        self.stride = (cfg.record_bytes + 4095) // 4096 * 4096
+        self.experts = torch.empty(cfg.n_experts * self.stride, dtype=torch.uint8, device=self.dev)
+        sd.fill_experts(self.experts, cfg, self.seed, 0, stride=self.stride)
+        self.w = synth.layer_weights(cfg, self.seed)
+        t = self.t
+        self.wr, self.bias = t(self.w["wr"].view(np.int16)), t(self.w["bias"])
+        self.sg, self.su, self.sdn = (t(self.w[k].view(np.int16))
+                                      for k in ("sh_gate", "sh_up", "sh_down"))
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev)
+        self.flush_words = self.flush_buf.view(torch.int32)
+        self.flush_mode = args.flush
+
+    def t(self, a):
+        import torch
+        return torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def flush(self, s):
+        """Evict L2 between timed steps (outside the step's events): a 256 MB write, or a
+        256 MB read that leaves no dirty lines behind."""
+        if self.flush_mode == "write":
+            self.flush_buf.fill_(s & 255)
+        else:
+            self.flush_words.sum()
+
+    def flush_note(self):
+        return ("flushed between timed steps (256 MB %s, outside the step events)" %
+                self.flush_mode)
+
+
+def traced(ctx, step, n, first, flush=None):
+    """Per-kernel device times: n steps again with the library's event tracing on (it
+    brackets every launch with events and turns off programmatic overlap)."""
+    import torch
+    k3 = ctx.k3
     k3.k3moe_trace_enable(True)
-    for s in range(args.steps):
-        flush.fill_((s + 7) & 255)
-        step(args.warmup + s)
+    for s in range(n):
+        if flush:
+            flush(first + s)
+        step(first + s)
     torch.cuda.synchronize()
     trace = k3.k3moe_trace_read()
     k3.k3moe_trace_enable(False)
+    return {k: v for k, v in trace.items() if v[1]}
+
+
+def bench_decode1(ctx, args, K):
+    """The headline: one decode token per step."""
+    import torch
+    k3, synth, cfg = ctx.k3, ctx.synth, ctx.cfg
+    H, I, E, Kt = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
+    dims = k3.LayerDims(H, I, E, Kt, cfg.shared_inter)
+    NX = 256
+    xs_host = synth.activations(cfg, ctx.seed + 1 + ctx.rank, NX)
+    xs = ctx.t(xs_host.view(np.int16))
+    y = torch.empty((1, H), dtype=torch.float32, device=ctx.dev)
+    idx = torch.empty((NX, Kt), dtype=torch.int32, device=ctx.dev)
+    wt = torch.empty((NX, Kt), dtype=torch.float32, device=ctx.dev)
+    ws = k3.new_workspace(dims, 1, ctx.dev)
+    status = k3.new_status(ctx.dev)
+
+    def step(s):
+        j = s % NX
+        k3.k3moe_layer(dims, xs[j:j + 1], ctx.wr, ctx.bias, ctx.experts, ctx.stride, ctx.sg,
+                       ctx.su, ctx.sdn, y, ws, status, idx_out=idx[j:j + 1], w_out=wt[j:j + 1])
+
+    tm = Timer(ctx, "decode1").run(step, K, args.warmup, ctx.flush)
+    assert status.item() == 0, k3.status_str(status.item())
+    nsteps = tm.blocks * K
+    trace = traced(ctx, step, nsteps, args.warmup, ctx.flush)
 
     # distinct experts actually used per step (for the algorithmic bytes)
     steps_idx = idx.cpu().numpy()
-    used = [len(set(steps_idx[(args.warmup + s) % NX].tolist())) for s in range(args.steps)]
+    used = [len(set(steps_idx[(args.warmup + s) % NX].tolist())) for s in range(nsteps)]
     U = statistics.mean(used)
     nb = step_bytes(cfg, U)
     bytes_step = nb["k_decode_fused"]
     launches = sum(v[1] for v in trace.values())
-    kernels = {k: {"ms_avg": v[0] / v[1], "launches": v[1]} for k, v in trace.items() if v[1]}
+    kernels = {k: {"ms_avg": v[0] / v[1], "launches": v[1]} for k, v in trace.items()}
     # the dominant kernel: most device time among the kernels that stream the weights
     dom = max((k for k in kernels if k in nb),
               key=lambda k: kernels[k]["ms_avg"] * kernels[k]["launches"])
     pk = peaks()
     peak_hbm = pk["hbm_gbs"] if pk else 6800.0
-    dom_ms = kernels[dom]["ms_avg"]
-    achieved = nb[dom] / (dom_ms * 1e-3) / 1e9
+    achieved = nb[dom] / (kernels[dom]["ms_avg"] * 1e-3) / 1e9
     for k in kernels:
         if k in nb:
             kernels[k]["gbs"] = nb[k] / (kernels[k]["ms_avg"] * 1e-3) / 1e9
@@ -318,58 +410,40 @@ def run_ours(args):
     # y back to pinned host memory, every step
     xh = torch.from_numpy(xs_host.view(np.int16).copy()).pin_memory()
     yh = torch.empty((1, H), dtype=torch.float32).pin_memory()
-    xd = torch.empty((1, H), dtype=torch.int16, device=dev)
+    xd = torch.empty((1, H), dtype=torch.int16, device=ctx.dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for s in range(args.steps):
+    e0.record(ctx.stream)
+    for s in range(K):
         j = s % NX
         xd.copy_(xh[j:j + 1], non_blocking=True)
-        k3.k3moe_layer(dims, xd, wr, bias, experts, stride, sg, su, sdn, y, ws, status)
+        k3.k3moe_layer(dims, xd, ctx.wr, ctx.bias, ctx.experts, ctx.stride, ctx.sg, ctx.su,
+                       ctx.sdn, y, ws, status)
         yh.copy_(y, non_blocking=True)
-    e1.record(stream)
+    e1.record(ctx.stream)
     torch.cuda.synchronize()
-    t_e2e = reduce_max(dist, e0.elapsed_time(e1) / 1e3, dev)
+    t_e2e = reduce_max(ctx.dist, e0.elapsed_time(e1) / 1e3, ctx.dev)
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cfg, seed, 2)
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": job_rate(args.steps, world, t_dev), "unit": "tokens/s",
-            "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_dev / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "seed": seed,
-                       "l2": "flushed between timed steps (256 MB write, outside the step "
-                             "events)", "distinct_experts_per_step": U,
-                       "parallelism": "replicas" if world > 1 else "single"},
-            "hbm_gbs_step": bytes_step / (t_dev / args.steps) / 1e9,
-            "algorithmic_bytes_per_step": bytes_step,
-            "roofline": roofline,
-            "kernels": kernels,
-            "gpu_launches": launches,
-            "clocks": clocks.summary(local),
-            "e2e": {"value": job_rate(args.steps, world, t_e2e), "unit": "tokens/s",
-                    "h2d_bytes_per_step": H * 2,
-                    "d2h_bytes_per_step": H * 4},
-            "cpu_baseline": cpu,
-            "wall_s": t_wall,
-        }
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
-
-
-BATCH_WORKLOADS = {
-    "decode64_zipf": "decode64_zipf: 64 tokens/step through one full-shape MoE layer, expert "
-                     "popularity Zipf(1.1) through the correction bias",
-    "prefill4096": "prefill4096: 4096 tokens/step through one full-shape MoE layer, uniform "
-                   "routing (grouped MXFP4 GEMM on tcgen05)",
-    "stacked8": "stacked8: 1 token/step through 8 stacked full-shape MoE layers (126 GB of "
-                "MXFP4 resident) with RMSNorm and the residual stream between them",
-}
+    return {
+        "metric": METRIC, "value": job_rate(nsteps, ctx.world, tm.t_dev), "unit": "tokens/s",
+        "n_gpus": ctx.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tm.t_dev / nsteps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS["decode1"], "tokens_per_step": 1, "seed": ctx.seed,
+                   "l2": ctx.flush_note(), "distinct_experts_per_step": U,
+                   "timed_blocks": tm.blocks,
+                   "parallelism": "replicas" if ctx.world > 1 else "single"},
+        "hbm_gbs_step": bytes_step / (tm.t_dev / nsteps) / 1e9,
+        "algorithmic_bytes_per_step": bytes_step,
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": tm.clocks,
+        "e2e": {"value": job_rate(K, ctx.world, t_e2e), "unit": "tokens/s",
+                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4},
+        "wall_s": tm.wall,
+    }
 
 
 def useful_flops(cfg, P, T):
@@ -378,53 +452,40 @@ def useful_flops(cfg, P, T):
     return 2.0 * P * 3 * H * I + 2.0 * T * 3 * H * SI
 
 
-def run_batch(args):
-    """The multi-token and stacked workloads (one JSON line each, same contract)."""
+def bench_batch(ctx, name, args, K, tokens=0):
+    """decode64_zipf / prefill4096 (one layer, many tokens) or stacked8 (eight layers, one
+    token), on the resident pool (the pool is layer 0 of the stack)."""
     import torch
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    import synth
-    import synth.device as sd
-    import mxfp4_routed_expert_02_gb300 as k3
-
-    name = args.workload
-    cfg = synth.config("decode1" if name == "stacked8" else name)
-    if args.experts != cfg.n_experts:   # smaller expert pool: profiling captures only
-        cfg = synth.config(cfg.name, n_experts=args.experts)
+    k3, synth, sd = ctx.k3, ctx.synth, ctx.sd
+    cfg = synth.config("decode1" if name == "stacked8" else name,
+                       n_experts=ctx.cfg.n_experts)
     L = 8 if name == "stacked8" else 1
-    T = 1 if name == "stacked8" else (args.tokens or cfg.tokens)
-    seed = 0
-    dev = torch.device("cuda", local)
-    H, I, E, K = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
-    dims = k3.LayerDims(H, I, E, K, cfg.shared_inter)
-    stride = (cfg.record_bytes + 4095) // 4096 * 4096
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    layers = []
-    for l in range(L):
-        ex = torch.empty(E * stride, dtype=torch.uint8, device=dev)
-        sd.fill_experts(ex, cfg, seed, l, stride=stride)
-        w = synth.layer_weights(cfg, seed, l)
-        layers.append(dict(wr=t(w["wr"].view(np.int16)), bias=t(w["bias"]), experts=ex,
-                           stride=stride, sh_gate=t(w["sh_gate"].view(np.int16)),
-                           sh_up=t(w["sh_up"].view(np.int16)),
-                           sh_down=t(w["sh_down"].view(np.int16))))
-    ws = k3.new_workspace(dims, T, dev)
-    status = k3.new_status(dev)
+    T = 1 if name == "stacked8" else (tokens or cfg.tokens)
+    H, I, E, Kt = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk
+    dims = k3.LayerDims(H, I, E, Kt, cfg.shared_inter)
+    stride = ctx.stride
+    layers = [dict(wr=ctx.wr, bias=ctx.bias, experts=ctx.experts, stride=stride, sh_gate=ctx.sg,
+                   sh_up=ctx.su, sh_down=ctx.sdn)]
+    if name == "decode64_zipf":   # same weights, the bias that steers popularity
+        layers[0]["bias"] = ctx.t(synth.layer_weights(cfg, ctx.seed)["bias"])
+    for l in range(1, L):
+        ex = torch.empty(E * stride, dtype=torch.uint8, device=ctx.dev)
+        sd.fill_experts(ex, cfg, ctx.seed, l, stride=stride)
+        w = synth.layer_weights(cfg, ctx.seed, l)
+        layers.append(dict(wr=ctx.t(w["wr"].view(np.int16)), bias=ctx.t(w["bias"]), experts=ex,
+                           stride=stride, sh_gate=ctx.t(w["sh_gate"].view(np.int16)),
+                           sh_up=ctx.t(w["sh_up"].view(np.int16)),
+                           sh_down=ctx.t(w["sh_down"].view(np.int16))))
+    ws = k3.new_workspace(dims, T, ctx.dev)
+    status = k3.new_status(ctx.dev)
     NX = 4
-    xs_host = [synth.activations(cfg, seed + 1 + rank * NX + j, T) for j in range(NX)]
-    xs = [t(a.view(np.int16)) for a in xs_host]
-    y = torch.empty((T, H), dtype=torch.float32, device=dev)
-    idx = torch.empty((L, T, K), dtype=torch.int32, device=dev)
-    wts = torch.empty((L, T, K), dtype=torch.float32, device=dev)
-    h = torch.empty((T, H), dtype=torch.float32, device=dev)
-    h.copy_(torch.from_numpy((xs_host[0].astype(np.uint32) << 16).view(np.float32)).to(dev))
-    xsc = torch.empty((T, H), dtype=torch.int16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    xs_host = [synth.activations(cfg, ctx.seed + 1 + ctx.rank * NX + j, T) for j in range(NX)]
+    xs = [ctx.t(a.view(np.int16)) for a in xs_host]
+    y = torch.empty((T, H), dtype=torch.float32, device=ctx.dev)
+    idx = torch.empty((L, T, Kt), dtype=torch.int32, device=ctx.dev)
+    wts = torch.empty((L, T, Kt), dtype=torch.float32, device=ctx.dev)
+    h = ctx.t((xs_host[0].astype(np.uint32) << 16).view(np.float32))
+    xsc = torch.empty((T, H), dtype=torch.int16, device=ctx.dev)
     lw = layers[0]
 
     def step(s):
@@ -436,41 +497,15 @@ def run_batch(args):
                            lw["sh_gate"], lw["sh_up"], lw["sh_down"], y, ws, status,
                            idx_out=idx[0], w_out=wts[0])
 
-    for s in range(args.warmup):
-        if name != "stacked8":
-            flush.fill_(s & 255)
-        step(s)
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    clocks = Clocks("/tmp/k3moe_bench_clocks_%d_%d.csv" % (os.getpid(), rank))
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with clocks:
-        for s in range(args.steps):
-            if name != "stacked8":
-                flush.fill_((s + 7) & 255)
-            ev[s][0].record(stream)
-            step(args.warmup + s)
-            ev[s][1].record(stream)
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+    flush = None if name == "stacked8" else ctx.flush
+    tm = Timer(ctx, name).run(step, K, args.warmup, flush)
     assert status.item() == 0, k3.status_str(status.item())
-    ms = [a.elapsed_time(b) for a, b in ev]
-    t_dev = reduce_max(dist, sum(ms) / 1e3, torch.device("cuda", local))
-    # per-kernel device time from a traced pass
-    k3.k3moe_trace_enable(True)
-    for s in range(min(args.steps, 3)):
-        step(args.warmup + s)
-    torch.cuda.synchronize()
-    trace = k3.k3moe_trace_read()
-    k3.k3moe_trace_enable(False)
-    nsteps_tr = min(args.steps, 3)
-    kernels = {k: {"ms_avg": v[0] / v[1], "launches_per_step": v[1] / nsteps_tr}
-               for k, v in trace.items() if v[1]}
-    launches = int(sum(v[1] for v in trace.values()) / nsteps_tr * args.steps)
+    nsteps = tm.blocks * K
+    ntr = min(nsteps, 3)
+    trace = traced(ctx, step, ntr, args.warmup, flush)
+    kernels = {k: {"ms_avg": v[0] / v[1], "launches_per_step": v[1] / ntr}
+               for k, v in trace.items()}
+    launches = int(sum(v[1] for v in trace.values()) / ntr * nsteps)
     # distinct experts of the last step, per layer
     ids = idx.cpu().numpy()
     U = [len(set(ids[l].ravel().tolist())) for l in range(L)]
@@ -480,10 +515,10 @@ def run_batch(args):
     pk = peaks()
     peak_hbm = pk["hbm_gbs"] if pk else 6800.0
     peak_bf16 = pk["bf16_tflops"] if pk else 1900.0
-    sec = t_dev / args.steps
+    sec = tm.t_dev / nsteps
+    extra = {}
     if name == "prefill4096":
-        P = T * K
-        fl = useful_flops(cfg, P, T)
+        P = T * Kt
         gk = kernels.get("k_tc_gemm_gateup", {}).get("ms_avg")
         dk = kernels.get("k_tc_gemm_down", {}).get("ms_avg")
         gfl = 2.0 * P * 2 * H * I
@@ -495,7 +530,7 @@ def run_batch(args):
                     "useful_flops": gfl,
                     "issued_mma_flops": gfl * k3.k3moe.TC_TERMS_X,
                     "hbm_frac_step": step_bytes_v / sec / 1e9 / peak_hbm}
-        extra = {"useful_tflops_step": fl / sec / 1e12,
+        extra = {"useful_tflops_step": useful_flops(cfg, P, T) / sec / 1e12,
                  "down_kernel_tflops": 2.0 * P * H * I / (dk * 1e-3) / 1e12 if dk else None}
     else:
         if name == "decode64_zipf":
@@ -511,41 +546,68 @@ def run_batch(args):
                     "traffic": None, "algorithmic_bytes": db,
                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else
                                    "fallback 6.8 TB/s (of fallback)"}
-        extra = {}
-    lat = sorted(ms)
+    lat = sorted(tm.ms)
     line = {
-        "metric": METRIC, "value": job_rate(T * args.steps, world, t_dev), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": METRIC, "value": job_rate(T * nsteps, ctx.world, tm.t_dev),
+        "unit": "tokens/s", "n_gpus": ctx.world, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": BATCH_WORKLOADS[name], "tokens_per_step": T, "layers": L,
-                   "seed": seed, "distinct_experts_per_layer": U,
+        "config": {"workload": WORKLOADS[name], "tokens_per_step": T, "layers": L,
+                   "seed": ctx.seed, "distinct_experts_per_layer": U, "timed_blocks": tm.blocks,
                    "l2": ("inputs larger than L2 (2.9 GB of weights per step)" if L > 1 else
-                          "flushed between timed steps (256 MB write)")},
+                          ctx.flush_note())},
         "hbm_gbs_step": step_bytes_v / sec / 1e9,
         "algorithmic_bytes_per_step": step_bytes_v,
-        "latency_ms": {"p50": lat[len(lat) // 2], "p99": lat[min(len(lat) - 1, int(len(lat) * 0.99))]},
+        "latency_ms": {"p50": lat[len(lat) // 2],
+                       "p99": lat[min(len(lat) - 1, int(len(lat) * 0.99))]},
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
-        "clocks": clocks.summary(local), "cpu_baseline": None,
+        "clocks": tm.clocks,
     }
     line.update(extra)
-    if rank == 0:
+    del layers, ws
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_ours(args):
+    import torch
+    ctx = Ctx(args)
+    steps = lambda name: args.steps or DEFAULT_STEPS[name]
+    if args.workload in ("all", "decode1"):
+        line = bench_decode1(ctx, args, steps("decode1"))
+        if args.workload == "all":
+            line["workloads"] = {}
+            for name in ("decode64_zipf", "prefill4096", "stacked8"):
+                sub = bench_batch(ctx, name, args, steps(name))
+                for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline",
+                          "data", "dtype", "warmup"):
+                    sub.pop(k, None)
+                line["workloads"][name] = sub
+            line["gpu_launches"] += sum(v["gpu_launches"] for v in line["workloads"].values())
+        line["cpu_baseline"] = None
+        if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(ctx.cfg, ctx.seed, 2)
+    else:
+        line = bench_batch(ctx, args.workload, args, steps(args.workload), args.tokens)
+        line["cpu_baseline"] = None
+    if ctx.rank == 0:
         print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    if ctx.dist:
+        ctx.dist.destroy_process_group()
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0,
-                    help="timed steps (0 = the workload's default: long enough for the "
-                         "200 ms clock sampler to see the timed region)")
+                    help="timed steps per block (0 = each workload's default)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="decode1",
-                    choices=["decode1", "decode64_zipf", "prefill4096", "stacked8"])
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "decode1", "decode64_zipf", "prefill4096", "stacked8"])
+    ap.add_argument("--flush", default="write", choices=["write", "read"],
+                    help="how L2 is evicted between timed steps")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step of a batch workload (0 = the workload's own; "
                          "other values only for small profiler captures)")
@@ -553,15 +615,12 @@ def main():
                     help="routed experts resident (896 = the workload; fewer only to keep "
                          "profiler captures small)")
     args = ap.parse_args()
-    if args.steps <= 0:
-        args.steps = {"decode1": 3000, "decode64_zipf": 200, "prefill4096": 40,
-                      "stacked8": 256}[args.workload]
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
+        if args.steps <= 0:
+            args.steps = 3
         run_reference(args)
-    elif args.workload != "decode1":
-        run_batch(args)
     else:
         run_ours(args)
 

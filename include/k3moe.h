@@ -170,9 +170,10 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
  *     looks up the device address of the array (which may load the library's device
  *     code) and sets kernel attributes.  Make that first call before any stream capture
  *     starts on the device.  K3MOE_ERR_CUDA if the lookup fails.
- *   - The array is zero when the library loads, and every call leaves the counter words
- *     at its start zero again (see Workspace above); the rest is written before it is
- *     read.
+ *   - Each call first clears the counter words at the array's start (the 256 bytes that
+ *     Workspace above describes) with one cudaMemsetAsync on `stream`, which allocates
+ *     nothing; so a call starts clean even after earlier calls raced on the array.  The
+ *     rest of the array is written before it is read.
  *   - Every call on a device shares the one array.  Calls ordered on one stream are
  *     safe; two calls whose work can overlap on the device (different streams without
  *     an ordering between them, or concurrent host threads) race on the array and

@@ -948,7 +948,8 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
 }
 
 // k3moe_layer with the static array as its workspace: size check first (nothing is
-// launched when the request does not fit), then the per-device address lookup.
+// launched when the request does not fit), then the per-device address lookup and the
+// argument checks, then the counter words cleared on the caller's stream.
 k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *x_bf16,
                                         int32_t T, const uint16_t *wr_bf16, const float *bias,
                                         const k3moe_experts *experts, const uint16_t *sh_gate,
@@ -964,6 +965,15 @@ k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *
     return K3MOE_ERR_SCRATCH_LIMIT;
   void *scratch = static_scratch();
   if (!scratch) return K3MOE_ERR_CUDA;
+  const k3moe_status a = check_layer_args(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate,
+                                          sh_up, sh_down, idx_out, w_out, y, ydt, scratch,
+                                          K3MOE_STATIC_SCRATCH_BYTES, status_dev);
+  if (a != K3MOE_OK) return a;
+  // the counter words at the array's start must be zero when the kernels start; clearing
+  // them on the call's stream also undoes what calls that raced on the array left there
+  if (cudaMemsetAsync(scratch, 0, kWsHeader, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return K3MOE_ERR_CUDA;
   return k3moe_layer(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up, sh_down, idx_out,
                      w_out, y, ydt, accumulate, scratch, K3MOE_STATIC_SCRATCH_BYTES, status_dev,
                      stream);

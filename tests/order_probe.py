@@ -10,8 +10,8 @@ associative, so the order shows in the result when the terms are chosen for it:
   * output row i names three router positions (p, q, r).  Expert p's down row i is a
     random MXFP4 row at a large scale, expert q's is the same row with every code's sign
     flipped (E2M1 code ^ 8), so w_p d_p[i] = -w_q d_q[i] exactly when w_p = w_q; expert
-    r's is a random row about 2^60 smaller; every other expert's row i has scale byte 255
-    and contributes exactly zero;
+    r's is a random row about 2^60 smaller; every other expert's row i has zero codes and
+    scale byte 255 and contributes exactly zero;
   * summed left to right, S + b rounds to S while b is below half an ulp of S, so the
     row's sum is exactly 0 unless position r comes after both p and q, in which case it
     is exactly fl(w_r d_r[i]) (the big pair cancels first).
@@ -55,8 +55,10 @@ def records(H, I, K, seed):
     tr = triples(K)
     pattern = np.array([tr[i % len(tr)] for i in range(H)], dtype=np.int64)
     rowb, rows_s = I // 2, I // 32
-    down = rng.integers(0, 256, (K, H, rowb), dtype=np.uint8)   # background codes
-    down_s = np.full((K, H, rows_s), 255, np.uint8)             # background: contributes 0
+    # background rows: code 0 with scale byte 255, exactly zero on every path (a path
+    # that reads byte 255 as 2^-127 still multiplies it by zero codes)
+    down = np.zeros((K, H, rowb), np.uint8)
+    down_s = np.full((K, H, rows_s), 255, np.uint8)
     base = rng.integers(0, 256, (H, rowb), dtype=np.uint8)
     small = rng.integers(0, 256, (H, rowb), dtype=np.uint8)
     for i, (p, q, r) in enumerate(pattern):

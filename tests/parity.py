@@ -42,6 +42,7 @@ class Layer:
     def __init__(self, cfg: synth.Config, seed: int = 0, layer: int = 0, device_fill=None,
                  tokens=None):
         self.cfg, self.seed, self.layer = cfg, seed, layer
+        self.overrides = {}
         self.dims = dims_of(cfg)
         w = synth.layer_weights(cfg, seed, layer)
         self.host = w
@@ -75,9 +76,27 @@ class Layer:
             self.d_sg = self.d_su = self.d_sd = None
 
     def expert_record(self, e: int) -> np.ndarray:
+        if e in self.overrides:
+            return self.overrides[e]
         if self._host_experts is not None:
             return self._host_experts[e]
         return synth.expert_record(self.cfg, self.seed, self.layer, e)
+
+    def set_expert(self, e: int, rec: np.ndarray):
+        """Replace expert e's record on the device and for the oracle."""
+        rec = np.ascontiguousarray(rec, np.uint8)
+        self.experts.view(self.cfg.n_experts, self.stride)[e, :self.rec_bytes].copy_(
+            torch.from_numpy(rec))
+        self.overrides[int(e)] = rec
+
+    def set_router(self, wr=None, bias=None):
+        """Replace the router weights and/or the correction bias (device and oracle)."""
+        if wr is not None:
+            self.host["wr"] = wr
+            self.d_wr = torch.from_numpy(np.ascontiguousarray(wr).view(np.int16)).cuda()
+        if bias is not None:
+            self.host["bias"] = bias
+            self.d_bias = torch.from_numpy(np.ascontiguousarray(bias)).cuda()
 
     def run(self, x=None, ydt=torch.float32, accumulate=False, y=None):
         x = self.d_x if x is None else x

@@ -55,3 +55,14 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.reduce_max(None, 3.25, None) == 3.25
     assert bench.job_rate(7, 1, 2.0) == 3.5
+
+
+def test_timed_blocks_cover_a_second_of_load():
+    # the clock sampler reads every 200 ms: short timed regions are repeated (blocks of
+    # exactly K steps each) until the timed work lasts at least a second
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.blocks_needed(0.3) == 4
+    assert bench.blocks_needed(0.25) == 4
+    assert bench.blocks_needed(2.0) == 1
+    assert bench.blocks_needed(0.0) == 1

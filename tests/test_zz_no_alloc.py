@@ -11,7 +11,6 @@ import dataclasses
 import os
 import re
 
-import numpy as np
 import pytest
 import torch
 
@@ -67,6 +66,9 @@ CASES = [
     ("tiny_bf16", 256, 128, 16, 2, 1, 4, torch.bfloat16),
     ("two_passes", 256, 128, 16, 2, 1, 65, torch.float32),
     ("decode_width_t1", 7168, 1536, 40, 16, 1, 1, torch.float32),
+    # the largest request within the limit: the model's shape at nine tokens (tensor-core
+    # path), 8,157,952 of the array's 8,388,608 bytes
+    ("model_t9", 7168, 1536, 896, 16, 1, 9, torch.float32),
 ]
 
 
@@ -98,7 +100,9 @@ def _run(L, x, ydt, static):
 def test_static_scratch_matches_workspace_call_two_calls_in_a_row(name, H, I, E, K, NS, T, ydt):
     L = _layer_inputs(H, I, E, K, NS, T, seed=11 + T)
     xa = L.d_x
-    xb = torch.flip(L.d_x, dims=[0]).contiguous() if T > 1 else (L.d_x ^ 0x0001)
+    # a second input with other routes: the tokens in reverse order, and every sign
+    # flipped (which negates every router logit)
+    xb = torch.flip(L.d_x, dims=[0]).contiguous() ^ -32768
     # the workspace call first, then two static-scratch calls on different inputs in a
     # row: the second overwrites the scratch the first used
     ref_a = _run(L, xa, ydt, static=False)
@@ -106,16 +110,14 @@ def test_static_scratch_matches_workspace_call_two_calls_in_a_row(name, H, I, E,
     got_a = _run(L, xa, ydt, static=True)
     got_b = _run(L, xb, ydt, static=True)
     torch.cuda.synchronize()
+    # the two inputs route differently, so a read of the first call's scratch would show
+    assert not torch.equal(ref_a[1], ref_b[1])
+    # the kernels are deterministic: the same inputs give the same bits, whatever memory
+    # holds the scratch
     for ref, got in ((ref_a, got_a), (ref_b, got_b)):
         y_r, i_r, w_r, s_r = ref
         y_g, i_g, w_g, s_g = got
         assert int(s_r.item()) == 0 and int(s_g.item()) == 0
         assert torch.equal(i_g, i_r)
         assert torch.equal(w_g, w_r)
-        yr, yg = y_r.float().cpu().numpy(), y_g.float().cpu().numpy()
-        if ydt == torch.float32:
-            err = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
-            assert err <= 1e-6, err
-        else:
-            err = np.abs(yg - yr).max() / max(np.abs(yr).max(), 1e-30)
-            assert err <= 1e-2, err
+        assert torch.equal(y_g, y_r)
