@@ -54,6 +54,10 @@ def lib():
             "k3o_moe_token": (None, [c_int, c_int, c_int, c_int, u16p, ctypes.POINTER(u8p), f32p,
                                      u16p, u16p, u16p, c_float, c_float, f32p, c_int]),
             "k3o_combine": (None, [c_int, c_int, f32p, f32p, f32p, f32p]),
+            "k3o_latent_moe_token": (None, [c_int, c_int, c_int, c_int, c_int, u16p, u16p, u16p,
+                                            f32p, c_int, c_float, ctypes.POINTER(u8p), f32p,
+                                            u16p, u16p, u16p, c_float, c_float, f32p, f32p,
+                                            f32p, c_int]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -274,6 +278,67 @@ def moe_layer(x_bf16, wr_bf16, bias, get_expert, topk: int, H: int, I: int, sh_g
                 cache[e] = get_expert(e)
             recs.append(cache[e])
         y[n] = moe_token(x[t], recs, w[n], H, I, sh_gate, sh_up, sh_down, b1, b2, nthreads)
+        if len(cache) > 64:
+            cache.clear()
+    return idx, w, y
+
+
+def latent_moe_token(x_bf16, recs, w, H: int, L: int, I: int, w_down, w_up, norm_w=None,
+                     latent_norm: bool = True, eps: float = 1e-5, sh_gate=None, sh_up=None,
+                     sh_down=None, b1: float = 4.0, b2: float = 25.0, nthreads: int = 0,
+                     intermediates: bool = False):
+    """One routed token through the LatentMoE (kimi-k3-in-c, section 9, LatentMoE listing
+    steps 2-6): z = Wdn x; the float router-order sum of w_j expert_j(z) in the latent;
+    RMSNorm of that aggregate (weight norm_w, eps) when latent_norm; Wup times it; plus
+    the shared experts on the original x, unweighted.  Returns y [H], or (y, z, accL)
+    with intermediates=True."""
+    x = _c(x_bf16, np.uint16)
+    K = len(recs)
+    recs = [_c(r, np.uint8) for r in recs]
+    arr = (ctypes.POINTER(ctypes.c_uint8) * max(K, 1))(*[_p(r, ctypes.c_uint8) for r in recs])
+    w = _c(w, np.float32)
+    wdn = _c(w_down, np.uint16)
+    wup = _c(w_up, np.uint16)
+    assert wdn.shape == (L, H) and wup.shape == (H, L)
+    nw = _c(np.ones(L, np.float32) if norm_w is None else norm_w, np.float32)
+    SI = 0 if sh_gate is None else int(np.asarray(sh_gate).shape[0])
+    g = None if sh_gate is None else _c(sh_gate, np.uint16)
+    u = None if sh_up is None else _c(sh_up, np.uint16)
+    dn = None if sh_down is None else _c(sh_down, np.uint16)
+    y = np.empty(H, dtype=np.float32)
+    z = np.empty(L, dtype=np.float32)
+    acc = np.empty(L, dtype=np.float32)
+    lib().k3o_latent_moe_token(H, L, I, K, SI, _p(x, ctypes.c_uint16), _p(wdn, ctypes.c_uint16),
+                               _p(wup, ctypes.c_uint16), _p(nw, ctypes.c_float),
+                               int(bool(latent_norm)), float(eps), arr, _p(w, ctypes.c_float),
+                               _p(g, ctypes.c_uint16), _p(u, ctypes.c_uint16),
+                               _p(dn, ctypes.c_uint16), b1, b2, _p(y, ctypes.c_float),
+                               _p(z, ctypes.c_float), _p(acc, ctypes.c_float), nthreads)
+    return (y, z, acc) if intermediates else y
+
+
+def latent_moe_layer(x_bf16, wr_bf16, bias, get_expert, topk: int, H: int, L: int, I: int,
+                     w_down, w_up, norm_w=None, latent_norm: bool = True, eps: float = 1e-5,
+                     sh_gate=None, sh_up=None, sh_down=None, renorm: bool = True,
+                     routed_scale: float = 1.0, b1: float = 4.0, b2: float = 25.0,
+                     tokens=None, nthreads: int = 0):
+    """The LatentMoE layer for the listed tokens: step 1 routes on the FULL-width x
+    (``router``), steps 2-6 are ``latent_moe_token``.  ``get_expert(e)`` returns expert
+    e's record of the (L, I) layout.  Returns (idx, w, y [len(tokens)][H])."""
+    x = np.atleast_2d(np.asarray(x_bf16, dtype=np.uint16))
+    tokens = list(range(x.shape[0]) if tokens is None else tokens)
+    idx, w, _, _ = router(x[tokens], wr_bf16, bias, topk, renorm, routed_scale, nthreads)
+    y = np.empty((len(tokens), H), dtype=np.float32)
+    cache = {}
+    for n, t in enumerate(tokens):
+        recs = []
+        for e in idx[n]:
+            e = int(e)
+            if e not in cache:
+                cache[e] = get_expert(e)
+            recs.append(cache[e])
+        y[n] = latent_moe_token(x[t], recs, w[n], H, L, I, w_down, w_up, norm_w, latent_norm,
+                                eps, sh_gate, sh_up, sh_down, b1, b2, nthreads)
         if len(cache) > 64:
             cache.clear()
     return idx, w, y

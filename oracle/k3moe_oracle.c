@@ -23,6 +23,12 @@
  *   routed sum in router order, shared
  *   expert added unweighted ................. section 9 (LatentMoE listing, steps 3, 6);
  *                                              Kimi-K3.cpp "The consumer-memory idea" 7
+ *   the LatentMoE: down-projection, experts
+ *   in the latent, RMSNorm of the aggregate,
+ *   up-projection, shared experts on the
+ *   full-width input ........................ section 9 (LatentMoE listing, steps 1-6);
+ *                                              section 2 (K3Cfg: latent, n_shared,
+ *                                              latent_norm)
  *
  * Precision: every sum the page accumulates in double is accumulated in double here,
  * every sum the page accumulates in float (the routed sum in router order, the shared
@@ -320,4 +326,48 @@ void k3o_moe_token(int H, int I, int K, int SI, const uint16_t *x,
     free(xf);
     free(d);
     free(ds);
+}
+
+/* One token through the page's LatentMoE (section 9, LatentMoE listing), its route
+ * (step 1, the router on the FULL-width x) already known:
+ *   2. z = Wdn x              Wdn bf16 [L][H]; double accumulation, rounded to float
+ *   3. accL = the float router-order sum of w[j] * expert_j(z)   (k3o_combine); the
+ *                             experts run in the latent: input z (float), records of
+ *                             the (L, I) layout
+ *   4. if norm: accL = RMSNorm(accL) with weight nw [L] and eps -- on the AGGREGATE,
+ *                             after the sum, not on each expert's output
+ *   5. y = Wup accL           Wup bf16 [H][L]
+ *   6. y = y + shared(x)      the shared experts (bf16 gate/up [SI][H], down [H][SI]; the
+ *                             page's two experts of width I are one of width SI = 2 I)
+ *                             on the ORIGINAL x, added unweighted with one float add per
+ *                             element; skipped when sh_gate == NULL.
+ * z_out and accl_out ([L] each, optional) receive z and the latent sum after step 4. */
+void k3o_latent_moe_token(int H, int L, int I, int K, int SI, const uint16_t *x,
+                          const uint16_t *wdn, const uint16_t *wup, const float *nw, int norm,
+                          float eps, const uint8_t *const *recs, const float *w,
+                          const uint16_t *sh_gate, const uint16_t *sh_up,
+                          const uint16_t *sh_down, float b1, float b2, float *y, float *z_out,
+                          float *accl_out, int nthreads) {
+    float *xf = (float *)malloc(sizeof(float) * (size_t)H);
+    float *z = (float *)malloc(sizeof(float) * (size_t)L);
+    float *d = (float *)malloc(sizeof(float) * (size_t)L * (size_t)(K > 0 ? K : 1));
+    float *acc = (float *)malloc(sizeof(float) * (size_t)L);
+    for (int i = 0; i < H; i++) xf[i] = k3o_bf16_to_f32(x[i]);
+    k3o_bf16_gemv(L, H, wdn, xf, z, nthreads);
+    for (int j = 0; j < K; j++) k3o_expert(L, I, recs[j], z, b1, b2, d + (size_t)j * L, nthreads);
+    k3o_combine(L, K, w, d, NULL, acc);
+    if (norm) k3o_rmsnorm(L, acc, nw, eps, acc);
+    k3o_bf16_gemv(H, L, wup, acc, y, nthreads);
+    if (sh_gate) {
+        float *ds = (float *)malloc(sizeof(float) * (size_t)H);
+        k3o_shared_expert(H, SI, sh_gate, sh_up, sh_down, xf, b1, b2, ds, nthreads);
+        for (int i = 0; i < H; i++) y[i] = y[i] + ds[i];
+        free(ds);
+    }
+    if (z_out) memcpy(z_out, z, sizeof(float) * (size_t)L);
+    if (accl_out) memcpy(accl_out, acc, sizeof(float) * (size_t)L);
+    free(xf);
+    free(z);
+    free(d);
+    free(acc);
 }
