@@ -10,8 +10,10 @@ expert pool:
   prefill4096    4096 tokens per step, uniform routing, grouped GEMMs on tcgen05;
   stacked8       1 token per step through 8 stacked layers (126 GB of MXFP4 resident),
                  RMSNorm and the residual stream in between;
+  latent_decode1 1 token per step through the pages' LatentMoE layer (experts in a
+                 3584-wide latent, its own 15.7 GB pool, two shared experts);
 
-the last three as nested entries of the one JSON line (``workloads``).  ``--workload``
+the last four as nested entries of the one JSON line (``workloads``).  ``--workload``
 times one of them alone as the line's headline.  Timed regions: blocks of exactly K
 steps, each between a barrier and a synchronize, repeated until at least a second of
 load has passed so that the clock sampler sees the timed work; every step between CUDA
@@ -48,9 +50,13 @@ WORKLOADS = {
                    "routing (grouped MXFP4 GEMM on tcgen05)",
     "stacked8": "stacked8: 1 token/step through 8 stacked full-shape MoE layers (126 GB of "
                 "MXFP4 resident) with RMSNorm and the residual stream between them",
+    "latent_decode1": "latent_decode1: 1 token/step through the pages' LatentMoE layer (hidden "
+                      "7168, 896 MXFP4 experts top-16 in a 3584-wide latent with inter 3072, "
+                      "latent RMSNorm, 2 bf16 shared experts of 3072 on the full width)",
 }
 WORKLOAD = WORKLOADS["decode1"]
-DEFAULT_STEPS = {"decode1": 3000, "decode64_zipf": 200, "prefill4096": 40, "stacked8": 256}
+DEFAULT_STEPS = {"decode1": 3000, "decode64_zipf": 200, "prefill4096": 40, "stacked8": 256,
+                 "latent_decode1": 1000}
 MIN_TIMED_SECONDS = 1.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
@@ -569,6 +575,91 @@ def bench_batch(ctx, name, args, K, tokens=0):
     return line
 
 
+def latent_step_bytes(cfg, U):
+    """Algorithmic bytes of one LatentMoE decode step with U distinct routed experts, per
+    kernel: the router, the projections (down, up and the shared experts' down), the
+    shared gate/up, the experts' gate/up and down."""
+    H, L, I, E, SI = cfg.hidden, cfg.latent, cfg.inter, cfg.n_experts, cfg.shared_inter
+    op = I * L // 2 + I * L // 32
+    return {"k_router_t1": E * H * 2 + H * 2,
+            "k_proj": L * H * 2 * 2 + H * SI * 2 + H * 4,
+            "k_proj_shared_gateup": 2 * SI * H * 2,
+            "k_expert_gateup": U * 2 * op,
+            "k_down_tma": U * op}
+
+
+def bench_latent(ctx, args, K):
+    """The pages' LatentMoE layer, one decode token per step, on its own expert pool (records
+    of the latent layout)."""
+    import torch
+    k3, synth, sd = ctx.k3, ctx.synth, ctx.sd
+    cfg = synth.config("latent_decode1", n_experts=ctx.cfg.n_experts)
+    H, L, I, E, Kt, SI = cfg.hidden, cfg.latent, cfg.inter, cfg.n_experts, cfg.topk, cfg.shared_inter
+    dims = k3.LatentDims(H, L, I, E, Kt, SI)
+    stride = (cfg.record_bytes + 4095) // 4096 * 4096
+    ex = torch.empty(E * stride, dtype=torch.uint8, device=ctx.dev)
+    sd.fill_experts(ex, cfg, ctx.seed, 0, stride=stride)
+    w = synth.layer_weights(cfg, ctx.seed)
+    d = {k: ctx.t(w[k].view(np.int16)) for k in ("wr", "w_down", "w_up", "sh_gate", "sh_up",
+                                                 "sh_down")}
+    d["bias"], d["norm_w"] = ctx.t(w["bias"]), ctx.t(w["norm_w"])
+    NX = 64
+    xs = ctx.t(synth.activations(cfg, ctx.seed + 1 + ctx.rank, NX).view(np.int16))
+    y = torch.empty((1, H), dtype=torch.float32, device=ctx.dev)
+    idx = torch.empty((NX, Kt), dtype=torch.int32, device=ctx.dev)
+    wt = torch.empty((NX, Kt), dtype=torch.float32, device=ctx.dev)
+    ws = k3.new_latent_workspace(dims, 1, ctx.dev)
+    status = k3.new_status(ctx.dev)
+
+    def step(s):
+        j = s % NX
+        k3.k3moe_latent_layer(dims, xs[j:j + 1], d["wr"], d["bias"], d["w_down"], d["w_up"],
+                              d["norm_w"], ex, stride, d["sh_gate"], d["sh_up"], d["sh_down"], y,
+                              ws, status, idx_out=idx[j:j + 1], w_out=wt[j:j + 1])
+
+    tm = Timer(ctx, "latent_decode1").run(step, K, args.warmup, ctx.flush)
+    assert status.item() == 0, k3.status_str(status.item())
+    nsteps = tm.blocks * K
+    ntr = min(nsteps, 50)
+    trace = traced(ctx, step, ntr, args.warmup, ctx.flush)
+    ids = idx.cpu().numpy()
+    U = statistics.mean(len(set(ids[(args.warmup + s) % NX].tolist())) for s in range(ntr))
+    nb = latent_step_bytes(cfg, U)
+    kernels = {k: {"ms_avg": v[0] / v[1], "launches_per_step": v[1] / ntr} for k, v in trace.items()}
+    for k in kernels:
+        if k in nb:
+            per_launch = nb[k] / kernels[k]["launches_per_step"]
+            kernels[k]["gbs"] = per_launch / (kernels[k]["ms_avg"] * 1e-3) / 1e9
+    bytes_step = sum(nb.values())
+    sec = tm.t_dev / nsteps
+    pk = peaks()
+    peak_hbm = pk["hbm_gbs"] if pk else 6800.0
+    dom = max((k for k in kernels if k in nb),
+              key=lambda k: kernels[k]["ms_avg"] * kernels[k]["launches_per_step"])
+    dom_bytes = nb[dom] / kernels[dom]["launches_per_step"]
+    achieved = dom_bytes / (kernels[dom]["ms_avg"] * 1e-3) / 1e9
+    line = {
+        "value": job_rate(nsteps, ctx.world, tm.t_dev), "unit": "tokens/s", "steps": K,
+        "ms_per_step": 1e3 * sec,
+        "config": {"workload": WORKLOADS["latent_decode1"], "tokens_per_step": 1,
+                   "seed": ctx.seed, "distinct_experts_per_step": U, "timed_blocks": tm.blocks,
+                   "l2": ctx.flush_note()},
+        "hbm_gbs_step": bytes_step / sec / 1e9, "algorithmic_bytes_per_step": bytes_step,
+        "hbm_frac_step": bytes_step / sec / 1e9 / peak_hbm,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak_hbm,
+                     "unit": "GB/s", "frac": achieved / peak_hbm, "traffic": None,
+                     "algorithmic_bytes": dom_bytes,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else
+                                    "fallback 6.8 TB/s (of fallback)"},
+        "kernels": kernels,
+        "gpu_launches": int(sum(v[1] for v in trace.values()) / ntr * nsteps),
+        "clocks": tm.clocks,
+    }
+    del ex, ws
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ours(args):
     import torch
     ctx = Ctx(args)
@@ -577,8 +668,9 @@ def run_ours(args):
         line = bench_decode1(ctx, args, steps("decode1"))
         if args.workload == "all":
             line["workloads"] = {}
-            for name in ("decode64_zipf", "prefill4096", "stacked8"):
-                sub = bench_batch(ctx, name, args, steps(name))
+            for name in ("decode64_zipf", "prefill4096", "stacked8", "latent_decode1"):
+                sub = (bench_latent(ctx, args, steps(name)) if name == "latent_decode1" else
+                       bench_batch(ctx, name, args, steps(name)))
                 for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline",
                           "data", "dtype", "warmup"):
                     sub.pop(k, None)
@@ -587,6 +679,11 @@ def run_ours(args):
         line["cpu_baseline"] = None
         if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(ctx.cfg, ctx.seed, 2)
+    elif args.workload == "latent_decode1":
+        line = bench_latent(ctx, args, steps(args.workload))
+        line.update({"metric": METRIC, "n_gpus": ctx.world, "warmup": args.warmup,
+                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                     "dtype": "f32", "data": "synthetic", "cpu_baseline": None})
     else:
         line = bench_batch(ctx, args.workload, args, steps(args.workload), args.tokens)
         line["cpu_baseline"] = None
@@ -605,7 +702,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "decode1", "decode64_zipf", "prefill4096", "stacked8"])
+                    choices=["all", "decode1", "decode64_zipf", "prefill4096", "stacked8",
+                             "latent_decode1"])
     ap.add_argument("--flush", default="write", choices=["write", "read"],
                     help="how L2 is evicted between timed steps")
     ap.add_argument("--tokens", type=int, default=0,

@@ -186,6 +186,58 @@ k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *
                                         k3moe_dtype ydt, int32_t accumulate,
                                         int32_t *status_dev, k3moe_stream_t stream);
 
+/* The pages' LatentMoE layer (kimi-k3-in-c, section 9, LatentMoE listing steps 1-6; its
+ * config fields in section 2, K3Cfg: latent, moe_inter, n_shared, latent_norm, rms_eps).
+ *   hidden        H, the layer width (x and y are [T][H])
+ *   latent        L, the width the routed experts run in (3584 in the model); multiple of 32
+ *   inter         I, the routed experts' intermediate width (3072 in the model)
+ *   n_experts, topk, group, situ_b1, situ_b2, routed_scale, renorm: as in k3moe_dims
+ *   shared_inter  SI = I x n_shared (6144 in the model: two shared experts of width I,
+ *                 which together are one SiTU-GLU of width SI), or 0
+ *   rms_eps       epsilon of the latent RMSNorm (1e-5)
+ *   latent_norm   1: RMSNorm the aggregated latent sum (with latent_norm_w), 0: skip it  */
+typedef struct {
+    int32_t hidden, latent, inter, n_experts, topk, group, shared_inter;
+    float situ_b1, situ_b2, routed_scale, rms_eps;
+    int32_t renorm, latent_norm;
+} k3moe_latent_dims;
+
+/* Weights of one LatentMoE layer (device pointers).                                    */
+typedef struct {
+    const uint16_t *wr_bf16;        /* [E][H] router, applied to the FULL-width x          */
+    const float *bias;              /* [E] correction bias, or NULL                       */
+    const uint16_t *w_down;         /* [L][H] bf16, x -> latent                           */
+    const uint16_t *w_up;           /* [H][L] bf16, latent -> full width                  */
+    const float *latent_norm_w;     /* [L] float weight of the latent RMSNorm             */
+    k3moe_experts experts;          /* records of the (L, I) layout: w1/w3 [I][L/2],
+                                       w2 [L][I/2] (17,547,264 bytes at L 3584, I 3072)   */
+    const uint16_t *sh_gate, *sh_up; /* [SI][H] bf16 (NULL when SI == 0)                  */
+    const uint16_t *sh_down;        /* [H][SI] bf16                                        */
+} k3moe_latent_weights;
+
+/* Bytes of workspace k3moe_latent_layer needs for T tokens (0 for invalid dims).        */
+size_t k3moe_latent_workspace_size(const k3moe_latent_dims *dims, int32_t T);
+
+/* One LatentMoE layer step for T tokens x (bf16 [T][H]), per token:
+ *   1. route on the full-width x: idx, w as k3moe_route (same rules, ties, renorm);
+ *   2. z = Wdn x                                  (float; bf16 weights, fp32 sums)
+ *   3. accL = sum_{j=0}^{K-1} w[j] expert_idx[j](z)  (float, in router order; the experts
+ *                                                   take z in float)
+ *   4. accL = RMSNorm(accL) * latent_norm_w        (when latent_norm: on the AGGREGATE,
+ *                                                   sum of squares in double)
+ *   5. y = Wup accL
+ *   6. y = y + W2s SiTU(W1s x, W3s x)              (the shared experts on the ORIGINAL x,
+ *                                                   unweighted, one float add)
+ * y [T][H] of dtype ydt (=, or += when accumulate).  idx_out / w_out [T][K] receive the
+ * route when not NULL.  Errors as k3moe_layer (a NaN router score sets
+ * K3MOE_ERR_NONFINITE, a bad shape K3MOE_ERR_SHAPE, ...).  Needs
+ * k3moe_latent_workspace_size(dims, T) bytes of zero-filled workspace.                  */
+k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_latent_weights *w,
+                                const uint16_t *x_bf16, int32_t T, int32_t *idx_out,
+                                float *w_out, void *y, k3moe_dtype ydt, int32_t accumulate,
+                                void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                k3moe_stream_t stream);
+
 /* Weights of one layer of a stack (the arguments k3moe_layer takes for it). */
 typedef struct {
     const uint16_t *wr_bf16;  /* [E][H] */

@@ -140,13 +140,15 @@ enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KI
                 KID_DEQUANT, KID_GATEUP_T1, KID_DOWN_TMA, KID_ROUTE_HIST, KID_ROUTE_SCATTER,
                 KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
                 KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_NORMS, KID_TC_ROUTER,
-                KID_ROUTE_CAND, KID_DECODE_FUSED, KID_COUNT };
+                KID_ROUTE_CAND, KID_DECODE_FUSED, KID_PROJ, KID_SHARED_GATEUP, KID_RMSNORM_F32,
+                KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {
     "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
     "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
     "k_route_scatter", "k_quant_x", "k_tc_gemm_gateup", "k_quant_act", "k_tc_gemm_down",
     "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine",
-    "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused"};
+    "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused", "k_proj",
+    "k_proj_shared_gateup", "k_rmsnorm_f32w"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -317,11 +319,12 @@ k3moe_status run_down(const DeviceInfo *di, const k3moe_dims *d, int Tc, const E
   return launch_status();
 }
 
-// Dispatch + gate/up + down/combine for Tc tokens with a given route.
-k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+// Dispatch + gate/up + down/combine for Tc tokens with a given route; x is bf16 [Tc][H],
+// or float [Tc][H] when x_f32 (the LatentMoE's latent).
+k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const void *x, int Tc,
                      const k3moe_experts *ex, const int32_t *idx, const float *w,
                      const uint16_t *sh_down, Ws &ws, void *y, k3moe_dtype ydt, int accumulate,
-                     int32_t *status, cudaStream_t st) {
+                     int32_t *status, cudaStream_t st, bool x_f32 = false) {
   const int H = d->hidden, I = d->inter, K = d->topk, E = d->n_experts;
   const int P = Tc * K;
   int Pp = 1;
@@ -338,12 +341,12 @@ k3moe_status run_ffn(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *
   const int tiles = I / kTileRows;
   int grid = maxU * tiles;
   if (grid > 16 * di->sms) grid = 16 * di->sms;
-  const int mb = Tc == 1 ? 1 : 2;
+  const int mb = (Tc == 1 || x_f32) ? 1 : 2;
   int bd = pathB ? 256 : ((G + 31) / 32) * 32;
   if (bd < 32 * mb) bd = 32 * mb;
   {
     TraceScope ts(KID_GATEUP, st);
-    if (launch_expert_gateup(mb, grid, bd, st, x, H, I, K, ea, ws.disp, P, d->situ_b1,
+    if (launch_expert_gateup(mb, grid, bd, st, x, x_f32, H, I, K, ea, ws.disp, P, d->situ_b1,
                              d->situ_b2, ws.act_hi, ws.act_lo, ws.act_ex) != cudaSuccess)
       return K3MOE_ERR_CUDA;
   }
@@ -730,6 +733,52 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
 // The tensor-core path applies from two tokens on, for the shapes it takes.
 bool use_tc(const k3moe_dims *d, int T) { return T >= 2 && tc_shape_ok(d); }
 
+// ---- the LatentMoE layer ---------------------------------------------------------------
+// The router's dims (full width) and the experts' dims (in the latent, no shared expert)
+// of a LatentMoE layer.
+k3moe_status latent_dims(const k3moe_latent_dims *d, k3moe_dims *full, k3moe_dims *lat) {
+  if (!d) return K3MOE_ERR_ARG;
+  if (d->latent < 32 || d->latent > 8192 || d->latent % 32) return K3MOE_ERR_SHAPE;
+  if (d->latent_norm && !(d->rms_eps >= 0.f)) return K3MOE_ERR_ARG;
+  *full = k3moe_dims{d->hidden, d->inter, d->n_experts, d->topk, d->group, d->shared_inter,
+                     d->situ_b1, d->situ_b2, d->routed_scale, d->renorm};
+  *lat = k3moe_dims{d->latent, d->inter, d->n_experts, d->topk, d->group, 0,
+                    d->situ_b1, d->situ_b2, d->routed_scale, d->renorm};
+  k3moe_status s = check_dims(full);
+  return s != K3MOE_OK ? s : check_dims(lat);
+}
+
+// Workspace of one pass of up to kDecodeTokens tokens: the router's part, the experts'
+// part, then z [Tc][L], the latent sum [Tc][L], the up-projection [Tc][H] and the shared
+// activations [Tc][SI] (float).
+struct WsLatent {
+  Ws route, ffn;
+  float *z, *accl, *up, *act_s;
+  size_t total;
+};
+
+WsLatent ws_latent_layout(const k3moe_dims *full, const k3moe_dims *lat, int T, void *base) {
+  const int Tc = T < kDecodeTokens ? T : kDecodeTokens;
+  WsLatent w{};
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  w.route = ws_layout(full, Tc, base);
+  size_t o = w.route.total;
+  w.ffn = ws_layout(lat, Tc, reinterpret_cast<void *>(b + o));
+  o += w.ffn.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += up16(bytes);
+    return reinterpret_cast<float *>(b + at);
+  };
+  const size_t L = lat->hidden, H = full->hidden, SI = full->shared_inter;
+  w.z = take((size_t)Tc * L * 4);
+  w.accl = take((size_t)Tc * L * 4);
+  w.up = take((size_t)Tc * H * 4);
+  w.act_s = take((size_t)Tc * (SI > 0 ? SI : 1) * 4);
+  w.total = o;
+  return w;
+}
+
 }  // namespace
 
 // ---- scratch of k3moe_layer_static_scratch -------------------------------------------
@@ -977,6 +1026,103 @@ k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *
   return k3moe_layer(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up, sh_down, idx_out,
                      w_out, y, ydt, accumulate, scratch, K3MOE_STATIC_SCRATCH_BYTES, status_dev,
                      stream);
+}
+
+size_t k3moe_latent_workspace_size(const k3moe_latent_dims *dims, int32_t T) {
+  k3moe_dims full, lat;
+  if (latent_dims(dims, &full, &lat) != K3MOE_OK || T < 0) return 0;
+  if (T == 0) return 16;
+  return ws_latent_layout(&full, &lat, T, nullptr).total;
+}
+
+// The LatentMoE layer in passes of up to kDecodeTokens tokens: route on the full-width x,
+// project into the latent, the experts in the latent (float input) with their router-order
+// sum, RMSNorm of that sum, project back up, then the shared experts on x, whose down
+// projection adds the up-projection and writes y.
+k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_latent_weights *lw,
+                                const uint16_t *x_bf16, int32_t T, int32_t *idx_out,
+                                float *w_out, void *y, k3moe_dtype ydt, int32_t accumulate,
+                                void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                k3moe_stream_t stream) {
+  k3moe_dims full, lat;
+  k3moe_status s = latent_dims(dims, &full, &lat);
+  if (s != K3MOE_OK) return s;
+  if (T < 0 || (ydt != K3MOE_F32 && ydt != K3MOE_BF16)) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!lw || !x_bf16 || !lw->wr_bf16 || !lw->w_down || !lw->w_up || !lw->experts.experts ||
+      !y || !workspace || !status_dev)
+    return K3MOE_ERR_ARG;
+  if (dims->latent_norm && !lw->latent_norm_w) return K3MOE_ERR_ARG;
+  const bool shared = dims->shared_inter > 0;
+  if (shared && (!lw->sh_gate || !lw->sh_up || !lw->sh_down)) return K3MOE_ERR_ARG;
+  if ((idx_out == nullptr) != (w_out == nullptr)) return K3MOE_ERR_ARG;
+  int64_t off[7];
+  record_offsets(&lat, off);
+  if (lw->experts.expert_stride < off[6] || lw->experts.expert_stride % 16) return K3MOE_ERR_ALIGN;
+  if (!aligned16(x_bf16) || !aligned16(lw->wr_bf16) || !aligned16(lw->w_down) ||
+      !aligned16(lw->w_up) || !aligned16(lw->experts.experts) || !aligned16(y) ||
+      !aligned16(workspace) || (lw->bias && !aligned16(lw->bias)) ||
+      (lw->latent_norm_w && !aligned16(lw->latent_norm_w)) ||
+      (idx_out && (!aligned16(idx_out) || !aligned16(w_out))) ||
+      (shared && (!aligned16(lw->sh_gate) || !aligned16(lw->sh_up) || !aligned16(lw->sh_down))))
+    return K3MOE_ERR_ALIGN;
+  if (ws_bytes < k3moe_latent_workspace_size(dims, T)) return K3MOE_ERR_WORKSPACE;
+  const DeviceInfo *di = device_info();
+  if (!di) return K3MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  WsLatent ws = ws_latent_layout(&full, &lat, T, workspace);
+  const int H = dims->hidden, L = dims->latent, K = dims->topk, SI = dims->shared_inter;
+  const float b1 = dims->situ_b1, b2 = dims->situ_b2;
+  for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
+    const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
+    const uint16_t *xc = x_bf16 + (size_t)t0 * H;
+    int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : ws.route.idx;
+    float *w_c = w_out ? w_out + (size_t)t0 * K : ws.route.w;
+    void *yc = static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt);
+    // 1. route on the full-width x
+    s = run_route(di, &full, xc, Tc, lw->wr_bf16, lw->bias, nullptr, nullptr, ws.route, idx_c,
+                  w_c, status_dev, st, true);
+    if (s != K3MOE_OK) return s;
+    // 2. z = Wdn x
+    {
+      TraceScope ts(KID_PROJ, st);
+      if (launch_proj(st, di->sms, lw->w_down, nullptr, L, H, xc, false, Tc, ws.z, nullptr,
+                      nullptr, 0, 0, b1, b2) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+    // 3. the experts in the latent, summed in router order into accL
+    s = run_ffn(di, &lat, ws.z, Tc, &lw->experts, idx_c, w_c, nullptr, ws.ffn, ws.accl, K3MOE_F32,
+                0, status_dev, st, true);
+    if (s != K3MOE_OK) return s;
+    // 4. RMSNorm of the aggregate
+    if (dims->latent_norm) {
+      TraceScope ts(KID_RMSNORM_F32, st);
+      if (launch_rmsnorm_f32w(st, ws.accl, Tc, L, lw->latent_norm_w, dims->rms_eps, ws.accl) !=
+          cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+    // 5. up = Wup accL (straight into y when there is no shared expert)
+    {
+      TraceScope ts(KID_PROJ, st);
+      if (launch_proj(st, di->sms, lw->w_up, nullptr, H, L, ws.accl, true, Tc, ws.up, nullptr,
+                      shared ? nullptr : yc, (int)ydt, accumulate, b1, b2) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+    // 6. shared experts on the original x, added unweighted: y (=|+=) up + Wsd SiTU(..)
+    if (shared) {
+      {
+        TraceScope ts(KID_SHARED_GATEUP, st);
+        if (launch_proj(st, di->sms, lw->sh_gate, lw->sh_up, SI, H, xc, false, Tc, ws.act_s,
+                        nullptr, nullptr, 0, 0, b1, b2) != cudaSuccess)
+          return K3MOE_ERR_CUDA;
+      }
+      TraceScope ts(KID_PROJ, st);
+      if (launch_proj(st, di->sms, lw->sh_down, nullptr, H, SI, ws.act_s, true, Tc, nullptr,
+                      ws.up, yc, (int)ydt, accumulate, b1, b2) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+  }
+  return K3MOE_OK;
 }
 
 // The stacked decode loop: per layer, RMSNorm of the residual stream into bf16, then the

@@ -186,6 +186,22 @@ __device__ __forceinline__ int prescale_group_f16(const float (&v)[32], uint32_t
   return ex;
 }
 
+// The group prescaled as prescale_group_f16 does, as two f16 terms: hi = f16(x'), lo =
+// f16(x' - hi) (the residual is exact in float), about 22 significant bits for float
+// inputs.  Returns the exponent ex (x' = x 2^-ex).
+__device__ __forceinline__ int prescale_group_f16_hilo(const float (&v)[32], uint32_t (&hi)[16],
+                                                       uint32_t (&lo)[16]) {
+  const int ex = prescale_group_f16(v, hi);
+  const float s = pow2i(-ex);
+#pragma unroll
+  for (int p = 0; p < 16; p++) {
+    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hi[p]));
+    __half2 l = __floats2half2_rn(v[2 * p] * s - h.x, v[2 * p + 1] * s - h.y);
+    lo[p] = *reinterpret_cast<uint32_t *>(&l);
+  }
+  return ex;
+}
+
 // SiTU-GLU (kimi-k3-in-c, section 9): the sigmoid takes the uncapped gate.
 __device__ __forceinline__ float situ(float g, float u, float b1, float b2) {
   const float a = b1 * tanhf(g / b1) * (1.f / (1.f + expf(-g)));

@@ -136,9 +136,12 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t *__restrict__ i
 // f16 hi + f16 lo of act * 2^-ex with one exponent ex per 32 rows (= one group of the
 // down projection's input).
 // ------------------------------------------------------------------------------------
-template <int MB>
+// XF32: x is float [T][H] (the LatentMoE's latent input) instead of bf16; each group is
+// prescaled the same way into two f16 terms (hi + residual, about 22 significant bits)
+// and the products take both terms (group_dot2).
+template <int MB, bool XF32>
 __global__ void __launch_bounds__(256) k_expert_gateup(
-    const uint16_t *__restrict__ x, int H, int I, int K, ExpertArgs ex,
+    const void *__restrict__ xv, int H, int I, int K, ExpertArgs ex,
     const int32_t *__restrict__ disp, int P, float b1, float b2,
     uint16_t *__restrict__ act_hi, uint16_t *__restrict__ act_lo, int32_t *__restrict__ act_ex) {
   __shared__ float gu[MB][kTileRows][2];
@@ -169,28 +172,42 @@ __global__ void __launch_bounds__(256) k_expert_gateup(
       // ---- this thread's group column of x for each token of the chunk, as f16
       const int g = pathB ? (tid % G) : tid;
       const bool gact = g < G;
-      uint32_t xr[MB][16];
+      uint32_t xr[MB][16], xl[MB][16];
       int xe[MB];
 #pragma unroll
       for (int m = 0; m < MB; m++) {
         xe[m] = 0;
 #pragma unroll
-        for (int p = 0; p < 16; p++) xr[m][p] = 0u;
+        for (int p = 0; p < 16; p++) xr[m][p] = xl[m][p] = 0u;
         if (m < mcount && gact) {
           const int t = plist[pc + m] / K;
-          const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H + g * kGroup);
           float v[32];
+          if (XF32) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                static_cast<const float *>(xv) + (size_t)t * H + g * kGroup);
 #pragma unroll
-          for (int q = 0; q < 4; q++) {
-            const uint4 c = __ldg(src + q);
-            const uint32_t a[4] = {c.x, c.y, c.z, c.w};
+            for (int q = 0; q < 8; q++) {
+              const float4 c = __ldg(src + q);
+              v[4 * q] = c.x;
+              v[4 * q + 1] = c.y;
+              v[4 * q + 2] = c.z;
+              v[4 * q + 3] = c.w;
+            }
+          } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const uint16_t *>(xv) + (size_t)t * H + g * kGroup);
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-              v[8 * q + 2 * k] = bf16_lo(a[k]);
-              v[8 * q + 2 * k + 1] = bf16_hi(a[k]);
+            for (int q = 0; q < 4; q++) {
+              const uint4 c = __ldg(src + q);
+              const uint32_t a[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+              for (int k = 0; k < 4; k++) {
+                v[8 * q + 2 * k] = bf16_lo(a[k]);
+                v[8 * q + 2 * k + 1] = bf16_hi(a[k]);
+              }
             }
           }
-          xe[m] = prescale_group_f16(v, xr[m]);
+          xe[m] = XF32 ? prescale_group_f16_hilo(v, xr[m], xl[m]) : prescale_group_f16(v, xr[m]);
         }
       }
 
@@ -221,7 +238,7 @@ __global__ void __launch_bounds__(256) k_expert_gateup(
           for (int m = 0; m < MB; m++) {
 #pragma unroll
             for (int c = 0; c < 8; c++) {
-              const float part = group_dot(xr[m], wc[c]);
+              const float part = XF32 ? group_dot2(xr[m], xl[m], wc[c]) : group_dot(xr[m], wc[c]);
               vals[m * 8 + c] = (sc[c] == 255u) ? 0.f : part * group_factor(sc[c], xe[m]);
             }
           }
@@ -258,8 +275,10 @@ __global__ void __launch_bounds__(256) k_expert_gateup(
             const uint32_t su = __ldg(w3s + (size_t)r * G + g);
 #pragma unroll
             for (int m = 0; m < MB; m++) {
-              float a = (sg == 255u) ? 0.f : group_dot(xr[m], wg) * group_factor(sg, xe[m]);
-              float b = (su == 255u) ? 0.f : group_dot(xr[m], wu) * group_factor(su, xe[m]);
+              const float dg = XF32 ? group_dot2(xr[m], xl[m], wg) : group_dot(xr[m], wg);
+              const float du = XF32 ? group_dot2(xr[m], xl[m], wu) : group_dot(xr[m], wu);
+              float a = (sg == 255u) ? 0.f : dg * group_factor(sg, xe[m]);
+              float b = (su == 255u) ? 0.f : du * group_factor(su, xe[m]);
               for (int o = G >> 1; o > 0; o >>= 1) {
                 a += __shfl_xor_sync(0xffffffffu, a, o);
                 b += __shfl_xor_sync(0xffffffffu, b, o);
@@ -442,16 +461,21 @@ __global__ void __launch_bounds__(256) k_down_combine(
   }
 }
 
-cudaError_t launch_expert_gateup(int mb, int grid, int block, cudaStream_t st, const uint16_t *x,
-                                 int H, int I, int K, const ExpertArgs &ex, const int32_t *disp,
-                                 int P, float b1, float b2, uint16_t *act_hi, uint16_t *act_lo,
-                                 int32_t *act_ex) {
-  if (mb == 1)
-    k_expert_gateup<1><<<grid, block, 0, st>>>(x, H, I, K, ex, disp, P, b1, b2, act_hi, act_lo,
-                                               act_ex);
-  else
-    k_expert_gateup<2><<<grid, block, 0, st>>>(x, H, I, K, ex, disp, P, b1, b2, act_hi, act_lo,
-                                               act_ex);
+cudaError_t launch_expert_gateup(int mb, int grid, int block, cudaStream_t st, const void *x,
+                                 bool x_f32, int H, int I, int K, const ExpertArgs &ex,
+                                 const int32_t *disp, int P, float b1, float b2,
+                                 uint16_t *act_hi, uint16_t *act_lo, int32_t *act_ex) {
+  if (x_f32) {  // one token per register block: two f16 terms per input use the registers
+    k_expert_gateup<1, true><<<grid, block, 0, st>>>(x, H, I, K, ex, disp, P, b1, b2, act_hi,
+                                                     act_lo, act_ex);
+  } else {
+    if (mb == 1)
+      k_expert_gateup<1, false><<<grid, block, 0, st>>>(x, H, I, K, ex, disp, P, b1, b2, act_hi,
+                                                        act_lo, act_ex);
+    else
+      k_expert_gateup<2, false><<<grid, block, 0, st>>>(x, H, I, K, ex, disp, P, b1, b2, act_hi,
+                                                        act_lo, act_ex);
+  }
   return cudaGetLastError();
 }
 

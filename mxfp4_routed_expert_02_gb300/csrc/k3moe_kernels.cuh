@@ -44,11 +44,12 @@ struct ExpertArgs {
   long long off[6];  // w1p, w1s, w2p, w2s, w3p, w3s
 };
 
-// Launches k_expert_gateup<mb> (mb = tokens per register block: 1 or 2).
-cudaError_t launch_expert_gateup(int mb, int grid, int block, cudaStream_t st, const uint16_t *x,
-                                 int H, int I, int K, const ExpertArgs &ex, const int32_t *disp,
-                                 int P, float b1, float b2, uint16_t *act_hi, uint16_t *act_lo,
-                                 int32_t *act_ex);
+// Launches k_expert_gateup<mb> (mb = tokens per register block: 1 or 2); x is bf16
+// [T][H], or float [T][H] when x_f32.
+cudaError_t launch_expert_gateup(int mb, int grid, int block, cudaStream_t st, const void *x,
+                                 bool x_f32, int H, int I, int K, const ExpertArgs &ex,
+                                 const int32_t *disp, int P, float b1, float b2,
+                                 uint16_t *act_hi, uint16_t *act_lo, int32_t *act_ex);
 
 __global__ void k_down_combine(int T, int H, int I, int K, ExpertArgs ex,
                                const int32_t *__restrict__ idx, const float *__restrict__ w,
@@ -135,6 +136,17 @@ __global__ void k_dequant(const uint8_t *__restrict__ packed, const uint8_t *__r
 
 __global__ void k_rmsnorm_bf16(const float *__restrict__ h, int T, int n, float eps,
                                uint16_t *__restrict__ out);
+
+// ---- LatentMoE pieces (k3moe_latent.cu)
+// out = W in (bf16 W [R][C], T input rows of C, bf16 or float); with W2 the shared gate/up
+// pair, SiTU applied; with y the layer output y (=|+=) addend + value (ydt), else float out.
+cudaError_t launch_proj(cudaStream_t st, int sms, const uint16_t *W, const uint16_t *W2, int R,
+                        int C, const void *in, bool in_f32, int T, float *out,
+                        const float *addend, void *y, int ydt, int accumulate, float b1,
+                        float b2);
+// RMSNorm of T float rows of n with weight w (nullptr: 1), sum of squares in double.
+cudaError_t launch_rmsnorm_f32w(cudaStream_t st, const float *in, int T, int n, const float *w,
+                                float eps, float *out);
 constexpr int kRmsThreads = 256;  // threads per row of k_rmsnorm_bf16
 constexpr int kRmsVec = 8;        // float4 per thread held in registers (rows up to 8192)
 

@@ -30,6 +30,7 @@ EXPORTS = (
     "k3moe_record_layout", "k3moe_workspace_size", "k3moe_route", "k3moe_expert_ffn_mxfp4",
     "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_decode_stack", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4",
     "k3moe_test_expire_wait", "k3moe_trace_enable", "k3moe_trace_read", "k3moe_status_str",
+    "k3moe_latent_layer", "k3moe_latent_workspace_size",
 )
 
 
@@ -53,6 +54,24 @@ class Experts(ctypes.Structure):
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [("wr_bf16", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("experts", Experts),
+                ("sh_gate", ctypes.c_void_p), ("sh_up", ctypes.c_void_p),
+                ("sh_down", ctypes.c_void_p)]
+
+
+class LatentDimsC(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("latent", ctypes.c_int32),
+                ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("shared_inter", ctypes.c_int32), ("situ_b1", ctypes.c_float),
+                ("situ_b2", ctypes.c_float), ("routed_scale", ctypes.c_float),
+                ("rms_eps", ctypes.c_float), ("renorm", ctypes.c_int32),
+                ("latent_norm", ctypes.c_int32)]
+
+
+class LatentWeightsC(ctypes.Structure):
+    _fields_ = [("wr_bf16", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+                ("latent_norm_w", ctypes.c_void_p), ("experts", Experts),
                 ("sh_gate", ctypes.c_void_p), ("sh_up", ctypes.c_void_p),
                 ("sh_down", ctypes.c_void_p)]
 
@@ -106,6 +125,12 @@ def lib(build_if_missing: bool = True):
     L.k3moe_trace_read.restype = i32
     L.k3moe_trace_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p),
                                    ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+    L.k3moe_latent_workspace_size.restype = sz
+    L.k3moe_latent_workspace_size.argtypes = [ctypes.POINTER(LatentDimsC), i32]
+    L.k3moe_latent_layer.restype = i32
+    L.k3moe_latent_layer.argtypes = [ctypes.POINTER(LatentDimsC),
+                                     ctypes.POINTER(LatentWeightsC), vp, i32, vp, vp, vp, i32,
+                                     i32, vp, sz, vp, vp]
     L.k3moe_status_str.restype = ctypes.c_char_p
     L.k3moe_status_str.argtypes = [i32]
     _LIB = L
@@ -278,6 +303,63 @@ def k3moe_rmsnorm_bf16(h, out, eps: float = 1e-5, stream=None):
 def k3moe_dequant_mxfp4(packed, scales, rows: int, cols: int, out, stream=None):
     _check("k3moe_dequant_mxfp4", lib().k3moe_dequant_mxfp4(
         _ptr(packed), _ptr(scales), int(rows), int(cols), _ptr(out), _stream(stream)))
+
+
+@dataclass
+class LatentDims:
+    """Shapes of a LatentMoE layer (k3moe_latent_dims)."""
+    hidden: int
+    latent: int
+    inter: int
+    n_experts: int
+    topk: int
+    shared_inter: int = 0
+    situ_b1: float = 4.0
+    situ_b2: float = 25.0
+    routed_scale: float = 1.0
+    rms_eps: float = 1e-5
+    renorm: int = 1
+    latent_norm: int = 1
+    group: int = 32
+
+    def c(self) -> LatentDimsC:
+        return LatentDimsC(self.hidden, self.latent, self.inter, self.n_experts, self.topk,
+                           self.group, self.shared_inter, self.situ_b1, self.situ_b2,
+                           self.routed_scale, self.rms_eps, self.renorm, self.latent_norm)
+
+
+def latent_workspace_size(dims: LatentDims, T: int) -> int:
+    d = dims.c()
+    return int(lib().k3moe_latent_workspace_size(ctypes.byref(d), int(T)))
+
+
+def new_latent_workspace(dims: LatentDims, T: int, device=None) -> torch.Tensor:
+    n = latent_workspace_size(dims, T)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def k3moe_latent_layer(dims: LatentDims, x, wr, bias, w_down, w_up, norm_w, experts,
+                       expert_stride: int, sh_gate, sh_up, sh_down, y, workspace, status,
+                       idx_out=None, w_out=None, accumulate: bool = False, stream=None):
+    """The LatentMoE layer step (k3moe_latent_layer): tensors on the device, bf16 weights
+    and x as bf16 or their 16-bit patterns, norm_w float [L] (or None without the norm)."""
+    d = dims.c()
+    x, wr = _bits16(x, "x"), _bits16(wr, "wr")
+    w_down, w_up = _bits16(w_down, "w_down"), _bits16(w_up, "w_up")
+    if sh_gate is not None:
+        sh_gate, sh_up, sh_down = (_bits16(sh_gate, "sh_gate"), _bits16(sh_up, "sh_up"),
+                                   _bits16(sh_down, "sh_down"))
+    T = x.shape[0]
+    ydt = F32 if y.dtype == torch.float32 else BF16
+    if ydt == BF16:
+        y = _bits16(y, "y")
+    lw = LatentWeightsC(_ptr(wr), _ptr(bias), _ptr(w_down), _ptr(w_up), _ptr(norm_w),
+                        Experts(ctypes.c_void_p(experts.data_ptr()), int(expert_stride)),
+                        _ptr(sh_gate), _ptr(sh_up), _ptr(sh_down))
+    _check("k3moe_latent_layer", lib().k3moe_latent_layer(
+        ctypes.byref(d), ctypes.byref(lw), _ptr(x), T, _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
+        int(bool(accumulate)), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)))
 
 
 def status_str(code: int) -> str:

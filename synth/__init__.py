@@ -12,6 +12,11 @@ measured on):
   decode64_zipf   as decode1, 64 tokens, bias steering expert popularity to Zipf(1.1)
   prefill4096     as decode1, 4096 tokens, uniform routing
   stacked8        8 decode1 layers, batch 1, 256 steps, RMSNorm + residual in between
+  latent_decode1  the pages' LatentMoE: hidden 7168, experts in a 3584-wide latent with
+                  intermediate 3072, 896 experts, top-16, 2 shared experts of width 3072
+                  on the full-width input, 1 token
+  latent_tiny     the same structure at hidden 256, latent 128, inter 128, 16 experts,
+                  top-2, 2 shared experts, 4 tokens
 
 Value recipe (all configurations):
   * routed experts: E2M1 nibbles uniform over all 16 codes (so packed bytes uniform over
@@ -19,7 +24,9 @@ Value recipe (all configurations):
   * router weight and shared-expert weights: bf16 ~ N(0, 1/fan_in) (standard deviation
     1/sqrt(fan_in): hidden for router/gate/up, inter for down);
   * correction bias: float32 U(-0.1, 0.1);
-  * activations: bf16 N(0, 1).
+  * activations: bf16 N(0, 1);
+  * LatentMoE projections: bf16 ~ N(0, 1/fan_in) (hidden for the down-projection, latent
+    for the up-projection); latent RMSNorm weight float32 N(1, 0.1^2).
 
 Expert bytes come from a counter-based generator, SplitMix64 (Steele, Lea & Flood,
 "Fast splittable pseudorandom number generators", OOPSLA 2014): output i of the stream
@@ -41,6 +48,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 OP_W1P, OP_W1S, OP_W2P, OP_W2S, OP_W3P, OP_W3S = range(6)
 # tensor ids for the numpy-drawn tensors
 T_X, T_ROUTER, T_BIAS, T_SH_GATE, T_SH_UP, T_SH_DOWN, T_ZIPF_PERM, T_ZIPF_JIT = range(8)
+T_W_DOWN, T_W_UP, T_LATENT_NORM = 8, 9, 10
 
 
 @dataclass(frozen=True)
@@ -64,10 +72,16 @@ class Config:
     routed_scale: float = 1.0
     renorm: int = 1
     rms_eps: float = 1e-5
+    latent: int = 0                   # > 0: a LatentMoE layer, experts in this width
+
+    @property
+    def expert_in(self):
+        """Input width of the routed experts: the latent, or the hidden width."""
+        return self.latent if self.latent else self.hidden
 
     @property
     def record_offsets(self):
-        return record_offsets(self.hidden, self.inter)
+        return record_offsets(self.expert_in, self.inter)
 
     @property
     def record_bytes(self):
@@ -90,6 +104,9 @@ CONFIGS = {
                             zipf_beta=ZIPF_BETA_1P1),
     "prefill4096": Config("prefill4096", 7168, 1536, 896, 16, 4096),
     "stacked8": Config("stacked8", 7168, 1536, 896, 16, 1, layers=8, steps=256),
+    "latent_decode1": Config("latent_decode1", 7168, 3072, 896, 16, 1, n_shared=2,
+                             latent=3584),
+    "latent_tiny": Config("latent_tiny", 256, 128, 16, 2, 4, n_shared=2, latent=128),
 }
 
 
@@ -226,6 +243,12 @@ def layer_weights(cfg: Config, seed: int, layer: int = 0) -> dict:
         out["sh_gate"] = normal_bf16(seed, layer, T_SH_GATE, (SI, H), 1.0 / math.sqrt(H))
         out["sh_up"] = normal_bf16(seed, layer, T_SH_UP, (SI, H), 1.0 / math.sqrt(H))
         out["sh_down"] = normal_bf16(seed, layer, T_SH_DOWN, (H, SI), 1.0 / math.sqrt(SI))
+    if cfg.latent:
+        L = cfg.latent
+        out["w_down"] = normal_bf16(seed, layer, T_W_DOWN, (L, H), 1.0 / math.sqrt(H))
+        out["w_up"] = normal_bf16(seed, layer, T_W_UP, (H, L), 1.0 / math.sqrt(L))
+        out["norm_w"] = (1.0 + 0.1 * _rng(seed, layer, T_LATENT_NORM).standard_normal(
+            L, dtype=np.float32)).astype(np.float32)
     return out
 
 
