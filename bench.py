@@ -7,13 +7,16 @@ expert pool:
 
   decode1        1 token per step (the headline: value, e2e, roofline, cpu_baseline);
   decode64_zipf  64 tokens per step, expert popularity Zipf(1.1) through the bias;
+  decode64_uniform  64 tokens per step, uniform routing;
   prefill4096    4096 tokens per step, uniform routing, grouped GEMMs on tcgen05;
   stacked8       1 token per step through 8 stacked layers (126 GB of MXFP4 resident),
                  RMSNorm and the residual stream in between;
   latent_decode1 1 token per step through the pages' LatentMoE layer (experts in a
                  3584-wide latent, its own 15.7 GB pool, two shared experts);
+  streamed_decode1  1 token per step with the records in pinned host memory and 256
+                 device slots in front of them (the LRU expert cache);
 
-the last four as nested entries of the one JSON line (``workloads``).  ``--workload``
+the last six as nested entries of the one JSON line (``workloads``).  ``--workload``
 times one of them alone as the line's headline.  Timed regions: blocks of exactly K
 steps, each between a barrier and a synchronize, repeated until at least a second of
 load has passed so that the clock sampler sees the timed work; every step between CUDA
@@ -46,17 +49,23 @@ WORKLOADS = {
                "1536, 896 MXFP4 experts top-16, 1 bf16 shared expert 7168x1536)",
     "decode64_zipf": "decode64_zipf: 64 tokens/step through one full-shape MoE layer, expert "
                      "popularity Zipf(1.1) through the correction bias",
+    "decode64_uniform": "decode64_uniform: 64 tokens/step through one full-shape MoE layer, "
+                        "uniform routing",
     "prefill4096": "prefill4096: 4096 tokens/step through one full-shape MoE layer, uniform "
                    "routing (grouped MXFP4 GEMM on tcgen05)",
     "stacked8": "stacked8: 1 token/step through 8 stacked full-shape MoE layers (126 GB of "
                 "MXFP4 resident) with RMSNorm and the residual stream between them",
+    "streamed_decode1": "streamed_decode1: 1 token/step through one full-shape MoE layer whose "
+                        "896 MXFP4 expert records live in pinned host memory, read over the "
+                        "host link into 256 device slots by the LRU expert cache",
     "latent_decode1": "latent_decode1: 1 token/step through the pages' LatentMoE layer (hidden "
                       "7168, 896 MXFP4 experts top-16 in a 3584-wide latent with inter 3072, "
                       "latent RMSNorm, 2 bf16 shared experts of 3072 on the full width)",
 }
 WORKLOAD = WORKLOADS["decode1"]
-DEFAULT_STEPS = {"decode1": 3000, "decode64_zipf": 200, "prefill4096": 40, "stacked8": 256,
-                 "latent_decode1": 1000}
+DEFAULT_STEPS = {"decode1": 3000, "decode64_zipf": 200, "decode64_uniform": 200,
+                 "prefill4096": 40, "stacked8": 256,
+                 "latent_decode1": 1000, "streamed_decode1": 200}
 MIN_TIMED_SECONDS = 1.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
@@ -285,7 +294,8 @@ class Timer:
                     c.dist.barrier()
                 per_step += [a.elapsed_time(b) for a, b in ev]
                 if blocks == 0:  # every rank runs the slowest rank's number of blocks
-                    nb = int(reduce_max(c.dist, blocks_needed(time.perf_counter() - tb), c.dev))
+                    nb = int(reduce_max(c.dist, blocks_needed(time.perf_counter() - tb,
+                                                              c.min_seconds), c.dev))
                 blocks += 1
             t_wall = time.perf_counter() - t_wall
         self.blocks, self.wall = blocks, t_wall
@@ -330,6 +340,7 @@ class Ctx:
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=self.dev)
         self.flush_words = self.flush_buf.view(torch.int32)
         self.flush_mode = args.flush
+        self.min_seconds = args.min_seconds
 
     def t(self, a):
         import torch
@@ -539,7 +550,7 @@ def bench_batch(ctx, name, args, K, tokens=0):
         extra = {"useful_tflops_step": useful_flops(cfg, P, T) / sec / 1e12,
                  "down_kernel_tflops": 2.0 * P * H * I / (dk * 1e-3) / 1e12 if dk else None}
     else:
-        if name == "decode64_zipf":
+        if name.startswith("decode64"):
             dom = "k_tc_gemm_gateup"
             db = sum(u * 2 * op for u in U) / L        # gate/up bytes of the distinct experts
         else:
@@ -660,6 +671,82 @@ def bench_latent(ctx, args, K):
     return line
 
 
+def h2d_gbs(ctx, src_pinned, nbytes):
+    """Rate of one large copy from pinned host memory to the device (the link's roof for
+    the streamed workload), best of 5."""
+    import torch
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=ctx.dev)
+    best = 0.0
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(ctx.stream)
+        dst.copy_(src_pinned[:nbytes], non_blocking=True)
+        e1.record(ctx.stream)
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del dst
+    return best
+
+
+def bench_streamed(ctx, args, K, n_slots=256):
+    """One decode token per step with the layer's expert records in pinned host memory and
+    n_slots device slots in front of them (k3moe_layer_streamed)."""
+    import torch
+    k3, synth, cfg = ctx.k3, ctx.synth, ctx.cfg
+    H, E, Kt = cfg.hidden, cfg.n_experts, cfg.topk
+    dims = k3.LayerDims(H, cfg.inter, E, Kt, cfg.shared_inter)
+    host = torch.empty(E * ctx.stride, dtype=torch.uint8, pin_memory=True)
+    host.copy_(ctx.experts.view(-1)[:E * ctx.stride])        # the same records as decode1
+    n_slots = min(n_slots, E)
+    slots = torch.empty(n_slots * ctx.stride, dtype=torch.uint8, device=ctx.dev)
+    cache = k3.ExpertCache([host.data_ptr()], E, cfg.record_bytes, ctx.stride, slots.data_ptr(),
+                           n_slots, ctx.stride)
+    link = h2d_gbs(ctx, host, 1 << 30)
+    NX = 4096
+    xs = ctx.t(synth.activations(cfg, ctx.seed + 2 + ctx.rank, NX).view(np.int16))
+    y = torch.empty((1, H), dtype=torch.float32, device=ctx.dev)
+    ws = k3.new_streamed_workspace(dims, 1, ctx.dev)
+    status = k3.new_status(ctx.dev)
+
+    def step(s):
+        j = s % NX
+        k3.k3moe_layer_streamed(dims, cache, 0, xs[j:j + 1], ctx.wr, ctx.bias, ctx.sg, ctx.su,
+                                ctx.sdn, y, ws, status)
+
+    for s in range(4 * n_slots // Kt):      # fill the slots before the warm-up proper
+        step(s)
+    first = cache.stats()
+    tm = Timer(ctx, "streamed_decode1").run(step, K, args.warmup, ctx.flush)
+    assert status.item() == 0, k3.status_str(status.item())
+    nsteps = tm.blocks * K
+    last = cache.stats()
+    # the timed steps' hits and misses (the warm-up's are in between `first` and the region;
+    # the rate over all calls since `first` is used)
+    calls = nsteps + args.warmup
+    misses = (last["misses"] - first["misses"]) / calls
+    hits = (last["hits"] - first["hits"]) / calls
+    sec = tm.t_dev / nsteps
+    copy_bytes = misses * cfg.record_bytes
+    line = {
+        "value": job_rate(nsteps, ctx.world, tm.t_dev), "unit": "tokens/s", "steps": K,
+        "ms_per_step": 1e3 * sec,
+        "config": {"workload": WORKLOADS["streamed_decode1"], "tokens_per_step": 1,
+                   "seed": ctx.seed, "slots": n_slots, "slot_bytes": ctx.stride,
+                   "timed_blocks": tm.blocks, "l2": ctx.flush_note()},
+        "cache": {"hit_rate": hits / max(hits + misses, 1e-9), "misses_per_step": misses,
+                  "h2d_bytes_per_step": copy_bytes},
+        "roofline": {"bound": "host link", "achieved": copy_bytes / sec / 1e9, "peak": link,
+                     "unit": "GB/s", "frac": copy_bytes / sec / 1e9 / link, "traffic": None,
+                     "peak_source": "one 1 GiB copy from pinned host memory, measured here"},
+        "gpu_launches": None,
+        "clocks": tm.clocks,
+    }
+    cache.close()
+    del host, slots, ws
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ours(args):
     import torch
     ctx = Ctx(args)
@@ -668,19 +755,25 @@ def run_ours(args):
         line = bench_decode1(ctx, args, steps("decode1"))
         if args.workload == "all":
             line["workloads"] = {}
-            for name in ("decode64_zipf", "prefill4096", "stacked8", "latent_decode1"):
-                sub = (bench_latent(ctx, args, steps(name)) if name == "latent_decode1" else
-                       bench_batch(ctx, name, args, steps(name)))
+            for name in ("decode64_zipf", "decode64_uniform", "prefill4096", "stacked8",
+                         "latent_decode1", "streamed_decode1"):
+                if name == "latent_decode1":
+                    sub = bench_latent(ctx, args, steps(name))
+                elif name == "streamed_decode1":
+                    sub = bench_streamed(ctx, args, steps(name))
+                else:
+                    sub = bench_batch(ctx, name, args, steps(name))
                 for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline",
                           "data", "dtype", "warmup"):
                     sub.pop(k, None)
                 line["workloads"][name] = sub
-            line["gpu_launches"] += sum(v["gpu_launches"] for v in line["workloads"].values())
+            line["gpu_launches"] += sum(v["gpu_launches"] or 0 for v in line["workloads"].values())
         line["cpu_baseline"] = None
         if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(ctx.cfg, ctx.seed, 2)
-    elif args.workload == "latent_decode1":
-        line = bench_latent(ctx, args, steps(args.workload))
+    elif args.workload in ("latent_decode1", "streamed_decode1"):
+        line = (bench_latent if args.workload == "latent_decode1" else bench_streamed)(
+            ctx, args, steps(args.workload))
         line.update({"metric": METRIC, "n_gpus": ctx.world, "warmup": args.warmup,
                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                      "dtype": "f32", "data": "synthetic", "cpu_baseline": None})
@@ -702,8 +795,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "decode1", "decode64_zipf", "prefill4096", "stacked8",
-                             "latent_decode1"])
+                    choices=["all", "decode1", "decode64_zipf", "decode64_uniform",
+                             "prefill4096", "stacked8", "latent_decode1", "streamed_decode1"])
+    ap.add_argument("--min-seconds", type=float, default=MIN_TIMED_SECONDS,
+                    help="least timed work per workload, in blocks of --steps (0: one block, "
+                         "for profiler captures)")
     ap.add_argument("--flush", default="write", choices=["write", "read"],
                     help="how L2 is evicted between timed steps")
     ap.add_argument("--tokens", type=int, default=0,

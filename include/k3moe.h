@@ -55,7 +55,8 @@ typedef enum {
     K3MOE_ERR_TIMEOUT = 6,    /* a bounded device-side wait gave up */
     K3MOE_ERR_BAD_EXPERT = 7, /* an expert index outside [0, n_experts) */
     K3MOE_ERR_NONFINITE = 8,  /* a router score that is NaN or infinite */
-    K3MOE_ERR_SCRATCH_LIMIT = 9 /* the call needs more than K3MOE_STATIC_SCRATCH_BYTES */
+    K3MOE_ERR_SCRATCH_LIMIT = 9, /* the call needs more than K3MOE_STATIC_SCRATCH_BYTES */
+    K3MOE_ERR_CACHE_FULL = 10    /* one call's distinct experts exceed the cache's slots */
 } k3moe_status;
 
 typedef enum { K3MOE_F32 = 0, K3MOE_BF16 = 1 } k3moe_dtype;
@@ -237,6 +238,71 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
                                 float *w_out, void *y, k3moe_dtype ydt, int32_t accumulate,
                                 void *workspace, size_t ws_bytes, int32_t *status_dev,
                                 k3moe_stream_t stream);
+
+/* ---- Host-tier expert streaming --------------------------------------------------------
+ * For layers whose experts do not all fit in HBM: the records stay in host memory (on a
+ * GB300's Grace host, reached over NVLink-C2C) and a fixed pool of record-sized slots in
+ * device memory caches them, the GPU counterpart of the pages' expert cache
+ * (kimi-k3-in-c, section 12 "An LRU cache for the experts"; Kimi-K3.cpp, "The
+ * consumer-memory idea", items 3-7):
+ *   - a slot is empty, in flight (reserved, being read) or holds one expert of one layer;
+ *   - a call first pins every selected expert already resident (a hit) and marks it used,
+ *     then reserves a slot for each miss, serially, in router order: an empty slot if any
+ *     (the first one), else the least recently used slot that is neither pinned nor in
+ *     flight;
+ *   - every miss is then read as one batch, one host-to-device copy per record (in host
+ *     address order), on the call's stream, and the slots are published;
+ *   - the layer is computed on the slots, the routed sum still in router order.
+ * The cache is a host object; it allocates no device memory.  Host memory of the records
+ * should be pinned (cudaHostAlloc / cudaHostRegister) for the copies to run at the link's
+ * rate; pageable memory works, slower.  One cache may serve several layers (a key is
+ * (layer, expert)).  Calls on one cache must not run concurrently from several threads
+ * with overlapping streams (the slots they publish would race); the host state itself is
+ * locked. */
+typedef struct k3moe_expert_cache k3moe_expert_cache;
+
+/* Create a cache for n_layers layers of n_experts records of record_bytes each: layer l's
+ * expert e at host_experts[l] + e * host_stride (HOST pointers, owned by the caller, alive
+ * while the cache is); n_slots slots at slots + s * slot_stride (a DEVICE pointer, 16-byte
+ * aligned, slot_stride >= record_bytes and a multiple of 16).  Host only (no CUDA call). */
+k3moe_status k3moe_cache_create(int32_t n_layers, const uint8_t *const *host_experts,
+                                int32_t n_experts, int64_t record_bytes, int64_t host_stride,
+                                uint8_t *slots, int32_t n_slots, int64_t slot_stride,
+                                k3moe_expert_cache **cache);
+k3moe_status k3moe_cache_destroy(k3moe_expert_cache *cache);
+
+/* Host only: the cache's decision for one call of n experts (router order, duplicates
+ * allowed) of a layer, as k3moe_layer_streamed takes it -- slots[j] the slot of expert j,
+ * load[j] = 1 where it has to be read -- with the reads taken as done.  For callers that
+ * move the records themselves, and for tests of the policy.  K3MOE_ERR_CACHE_FULL (the
+ * cache unchanged) when the call's distinct experts do not fit. */
+k3moe_status k3moe_cache_lookup(k3moe_expert_cache *cache, int32_t layer,
+                                const int32_t *experts, int32_t n, int32_t *slots,
+                                int32_t *load);
+
+/* Hits and misses counted per distinct expert of a call, and bytes read into slots. */
+k3moe_status k3moe_cache_stats(k3moe_expert_cache *cache, int64_t *hits, int64_t *misses,
+                               int64_t *bytes_loaded);
+
+/* Bytes of workspace k3moe_layer_streamed needs for T tokens (0 for invalid dims). */
+size_t k3moe_streamed_workspace_size(const k3moe_dims *dims, int32_t T);
+
+/* k3moe_layer with the routed experts of layer `layer` taken from the cache, in passes of
+ * up to 64 tokens: route (on the device), copy the routes to the host and wait for them
+ * (the call synchronises `stream` once per pass), look up / reserve the slots, read the
+ * misses, then the expert FFN and the shared expert on the device, the routed sum in router
+ * order.  Same arguments, results and error codes as k3moe_layer, except that the expert
+ * records come from the cache; K3MOE_ERR_CACHE_FULL (nothing computed for that pass) when
+ * a pass's distinct experts exceed the slots; K3MOE_ERR_CUDA if a copy cannot be issued.
+ * Needs k3moe_streamed_workspace_size(dims, T) bytes of workspace.                      */
+k3moe_status k3moe_layer_streamed(const k3moe_dims *dims, k3moe_expert_cache *cache,
+                                  int32_t layer, const uint16_t *x_bf16, int32_t T,
+                                  const uint16_t *wr_bf16, const float *bias,
+                                  const uint16_t *sh_gate, const uint16_t *sh_up,
+                                  const uint16_t *sh_down, int32_t *idx_out, float *w_out,
+                                  void *y, k3moe_dtype ydt, int32_t accumulate,
+                                  void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                  k3moe_stream_t stream);
 
 /* Weights of one layer of a stack (the arguments k3moe_layer takes for it). */
 typedef struct {

@@ -13,4 +13,5 @@ from .k3moe import (  # noqa: F401
     k3moe_rmsnorm_bf16, k3moe_dequant_mxfp4, k3moe_test_expire_wait, k3moe_trace_enable, k3moe_trace_read,
     record_layout, workspace_size, new_workspace, new_status, status_str, lib, EXPORTS,
     LatentDims, k3moe_latent_layer, latent_workspace_size, new_latent_workspace,
+    ExpertCache, k3moe_layer_streamed, streamed_workspace_size, new_streamed_workspace,
 )

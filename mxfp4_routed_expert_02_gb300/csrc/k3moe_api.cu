@@ -5,10 +5,12 @@
 #include <cstdio>
 #include <cstring>
 #include <cmath>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
 
+#include "k3moe_cache.h"
 #include "k3moe_tc.cuh"
 
 using namespace k3;
@@ -824,6 +826,7 @@ const char *k3moe_status_str(k3moe_status s) {
     case K3MOE_ERR_NONFINITE: return "non-finite router score";
     case K3MOE_ERR_SCRATCH_LIMIT:
       return "call needs more scratch than the static array holds (K3MOE_STATIC_SCRATCH_BYTES)";
+    case K3MOE_ERR_CACHE_FULL: return "the call's distinct experts exceed the cache's slots";
   }
   return "unknown status";
 }
@@ -1121,6 +1124,108 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
                       ws.up, yc, (int)ydt, accumulate, b1, b2) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
+  }
+  return K3MOE_OK;
+}
+
+// ---- host-tier expert streaming ---------------------------------------------------------
+// Workspace: the decode path's (one pass of up to kDecodeTokens tokens) plus the pass's slot
+// indices [Tc][K].
+size_t k3moe_streamed_workspace_size(const k3moe_dims *dims, int32_t T) {
+  if (check_dims(dims) != K3MOE_OK || T < 0) return 0;
+  if (T == 0) return 16;
+  const int Tc = T < kDecodeTokens ? T : kDecodeTokens;
+  return ws_layout(dims, T, nullptr).total + up16((size_t)Tc * dims->topk * 4);
+}
+
+k3moe_status k3moe_layer_streamed(const k3moe_dims *dims, k3moe_expert_cache *cache,
+                                  int32_t layer, const uint16_t *x_bf16, int32_t T,
+                                  const uint16_t *wr_bf16, const float *bias,
+                                  const uint16_t *sh_gate, const uint16_t *sh_up,
+                                  const uint16_t *sh_down, int32_t *idx_out, float *w_out,
+                                  void *y, k3moe_dtype ydt, int32_t accumulate,
+                                  void *workspace, size_t ws_bytes, int32_t *status_dev,
+                                  k3moe_stream_t stream) {
+  k3moe_status s = check_dims(dims);
+  if (s != K3MOE_OK) return s;
+  if (!cache || layer < 0 || layer >= cache->n_layers) return K3MOE_ERR_ARG;
+  int64_t off[7];
+  record_offsets(dims, off);
+  if (cache->n_experts != dims->n_experts || cache->record_bytes != off[6]) return K3MOE_ERR_ARG;
+  if (dims->topk > cache->n_slots) return K3MOE_ERR_CACHE_FULL;
+  // the slots stand in for the expert pool in the argument checks; the workspace is this
+  // path's own (decode passes only), checked below
+  const k3moe_experts slots{cache->slots, cache->slot_stride};
+  s = check_layer_args(dims, x_bf16, T, wr_bf16, bias, &slots, sh_gate, sh_up, sh_down, idx_out,
+                       w_out, y, ydt, workspace, ~size_t(0), status_dev);
+  if (s != K3MOE_OK || T == 0) return s;
+  if (ws_bytes < k3moe_streamed_workspace_size(dims, T)) return K3MOE_ERR_WORKSPACE;
+  const DeviceInfo *di = device_info();
+  if (!di) return K3MOE_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Ws ws = ws_layout(dims, T, workspace);
+  int32_t *slot_dev = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + ws.total);
+  const bool shared = dims->shared_inter > 0;
+  const int H = dims->hidden, K = dims->topk;
+  // the FFN addresses the slots as its expert pool
+  k3moe_dims ds = *dims;
+  ds.n_experts = cache->n_slots;
+  for (int t0 = 0; t0 < T; t0 += kDecodeTokens) {
+    const int Tc = (T - t0) < kDecodeTokens ? (T - t0) : kDecodeTokens;
+    const int n = Tc * K;
+    int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : ws.idx;
+    float *w_c = w_out ? w_out + (size_t)t0 * K : ws.w;
+    const uint16_t *xc = x_bf16 + (size_t)t0 * H;
+    // route, with the shared expert's gate/up (its activations stay in the workspace)
+    s = run_route(di, dims, xc, Tc, wr_bf16, bias, shared ? sh_gate : nullptr,
+                  shared ? sh_up : nullptr, ws, idx_c, w_c, status_dev, st, true);
+    if (s != K3MOE_OK) return s;
+    std::lock_guard<std::mutex> lk(cache->mu);
+    cache->route_host.resize(n);
+    cache->slot_host.resize(n);
+    cache->load_host.resize(n);
+    if (cudaMemcpyAsync(cache->route_host.data(), idx_c, (size_t)n * 4, cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+    s = k3::cache_reserve(cache, layer, cache->route_host.data(), n, cache->slot_host.data(),
+                          cache->load_host.data());
+    if (s != K3MOE_OK) return s;
+    // the misses as one batch of copies, in host address order
+    std::vector<int> order;
+    for (int j = 0; j < n; j++)
+      if (cache->load_host[j]) order.push_back(j);
+    std::sort(order.begin(), order.end(), [&](int a, int b) {
+      return cache->route_host[a] < cache->route_host[b];
+    });
+    std::vector<int32_t> ok(n, 0);
+    bool copied = true;
+    for (int j : order) {
+      const uint8_t *src = cache->host[layer] + (int64_t)cache->route_host[j] * cache->host_stride;
+      uint8_t *dst = cache->slots + (int64_t)cache->slot_host[j] * cache->slot_stride;
+      if (cudaMemcpyAsync(dst, src, (size_t)cache->record_bytes, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess) {
+        copied = false;
+        break;
+      }
+      ok[j] = 1;
+    }
+    k3::cache_publish(cache, layer, cache->route_host.data(), n, cache->slot_host.data(),
+                      cache->load_host.data(), ok.data());
+    if (!copied) {
+      cudaGetLastError();
+      return K3MOE_ERR_CUDA;
+    }
+    // slot indices to the device (a route outside the pool keeps slot -1: that pair is
+    // dropped and reported by the FFN, after whatever the router reported)
+    if (cudaMemcpyAsync(slot_dev, cache->slot_host.data(), (size_t)n * 4, cudaMemcpyHostToDevice,
+                        st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+    s = run_ffn(di, &ds, xc, Tc, &slots, slot_dev, w_c, shared ? sh_down : nullptr, ws,
+                static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt, accumulate,
+                status_dev, st);
+    if (s != K3MOE_OK) return s;
   }
   return K3MOE_OK;
 }

@@ -17,7 +17,9 @@ K3MOE_OK = 0
 STATUS_NAMES = {
     0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_WORKSPACE", 5: "ERR_CUDA",
     6: "ERR_TIMEOUT", 7: "ERR_BAD_EXPERT", 8: "ERR_NONFINITE", 9: "ERR_SCRATCH_LIMIT",
+    10: "ERR_CACHE_FULL",
 }
+K3MOE_ERR_CACHE_FULL = 10
 K3MOE_ERR_SCRATCH_LIMIT = 9
 # MXFP4 terms of the activations in the multi-token path (x, SiTU output); informational.
 TC_TERMS_X, TC_TERMS_ACT = 4, 4
@@ -30,7 +32,9 @@ EXPORTS = (
     "k3moe_record_layout", "k3moe_workspace_size", "k3moe_route", "k3moe_expert_ffn_mxfp4",
     "k3moe_layer", "k3moe_layer_static_scratch", "k3moe_decode_stack", "k3moe_rmsnorm_bf16", "k3moe_dequant_mxfp4",
     "k3moe_test_expire_wait", "k3moe_trace_enable", "k3moe_trace_read", "k3moe_status_str",
-    "k3moe_latent_layer", "k3moe_latent_workspace_size",
+    "k3moe_latent_layer", "k3moe_latent_workspace_size", "k3moe_cache_create",
+    "k3moe_cache_destroy", "k3moe_cache_lookup", "k3moe_cache_stats",
+    "k3moe_streamed_workspace_size", "k3moe_layer_streamed",
 )
 
 
@@ -131,6 +135,22 @@ def lib(build_if_missing: bool = True):
     L.k3moe_latent_layer.argtypes = [ctypes.POINTER(LatentDimsC),
                                      ctypes.POINTER(LatentWeightsC), vp, i32, vp, vp, vp, i32,
                                      i32, vp, sz, vp, vp]
+    cp = ctypes.c_void_p
+    L.k3moe_cache_create.restype = i32
+    L.k3moe_cache_create.argtypes = [i32, ctypes.POINTER(ctypes.c_void_p), i32, i64, i64, vp,
+                                     i32, i64, ctypes.POINTER(cp)]
+    L.k3moe_cache_destroy.restype = i32
+    L.k3moe_cache_destroy.argtypes = [cp]
+    L.k3moe_cache_lookup.restype = i32
+    L.k3moe_cache_lookup.argtypes = [cp, i32, vp, i32, vp, vp]
+    L.k3moe_cache_stats.restype = i32
+    L.k3moe_cache_stats.argtypes = [cp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                    ctypes.POINTER(i64)]
+    L.k3moe_streamed_workspace_size.restype = sz
+    L.k3moe_streamed_workspace_size.argtypes = [dp, i32]
+    L.k3moe_layer_streamed.restype = i32
+    L.k3moe_layer_streamed.argtypes = [dp, cp, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       i32, i32, vp, sz, vp, vp]
     L.k3moe_status_str.restype = ctypes.c_char_p
     L.k3moe_status_str.argtypes = [i32]
     _LIB = L
@@ -358,6 +378,82 @@ def k3moe_latent_layer(dims: LatentDims, x, wr, bias, w_down, w_up, norm_w, expe
                         _ptr(sh_gate), _ptr(sh_up), _ptr(sh_down))
     _check("k3moe_latent_layer", lib().k3moe_latent_layer(
         ctypes.byref(d), ctypes.byref(lw), _ptr(x), T, _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
+        int(bool(accumulate)), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)))
+
+
+class ExpertCache:
+    """The library's host-side expert cache (k3moe_cache_create): the records of n_layers
+    layers in host memory (``host_ptrs``: one address per layer, records ``host_stride``
+    apart), ``n_slots`` record-sized slots at device address ``slots_ptr``."""
+
+    def __init__(self, host_ptrs, n_experts: int, record_bytes: int, host_stride: int,
+                 slots_ptr: int, n_slots: int, slot_stride: int):
+        arr = (ctypes.c_void_p * len(host_ptrs))(*[ctypes.c_void_p(int(p)) for p in host_ptrs])
+        self._keep = arr
+        h = ctypes.c_void_p()
+        _check("k3moe_cache_create", lib().k3moe_cache_create(
+            len(host_ptrs), arr, int(n_experts), int(record_bytes), int(host_stride),
+            ctypes.c_void_p(int(slots_ptr)), int(n_slots), int(slot_stride), ctypes.byref(h)))
+        self.handle = h
+        self.n_slots = n_slots
+
+    def lookup(self, layer: int, experts):
+        """(slots, load) for one call's experts (host only: the cache's decision, the reads
+        taken as done).  Raises K3MoeError (ERR_CACHE_FULL) when they do not fit."""
+        import numpy as np
+        e = np.ascontiguousarray(experts, dtype=np.int32)
+        slots = np.empty_like(e)
+        load = np.empty_like(e)
+        _check("k3moe_cache_lookup", lib().k3moe_cache_lookup(
+            self.handle, int(layer), e.ctypes.data_as(ctypes.c_void_p), e.size,
+            slots.ctypes.data_as(ctypes.c_void_p), load.ctypes.data_as(ctypes.c_void_p)))
+        return slots, load
+
+    def stats(self):
+        h, m, b = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check("k3moe_cache_stats", lib().k3moe_cache_stats(self.handle, ctypes.byref(h),
+                                                              ctypes.byref(m), ctypes.byref(b)))
+        return {"hits": h.value, "misses": m.value, "bytes_loaded": b.value}
+
+    def close(self):
+        if self.handle:
+            lib().k3moe_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def streamed_workspace_size(dims: LayerDims, T: int) -> int:
+    d = dims.c()
+    return int(lib().k3moe_streamed_workspace_size(ctypes.byref(d), int(T)))
+
+
+def new_streamed_workspace(dims: LayerDims, T: int, device=None) -> torch.Tensor:
+    n = streamed_workspace_size(dims, T)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def k3moe_layer_streamed(dims: LayerDims, cache: ExpertCache, layer: int, x, wr, bias, sh_gate,
+                         sh_up, sh_down, y, workspace, status, idx_out=None, w_out=None,
+                         accumulate: bool = False, stream=None):
+    """k3moe_layer with the routed experts read through the expert cache."""
+    d = dims.c()
+    x, wr = _bits16(x, "x"), _bits16(wr, "wr")
+    if sh_gate is not None:
+        sh_gate, sh_up, sh_down = (_bits16(sh_gate, "sh_gate"), _bits16(sh_up, "sh_up"),
+                                   _bits16(sh_down, "sh_down"))
+    T = x.shape[0]
+    ydt = F32 if y.dtype == torch.float32 else BF16
+    if ydt == BF16:
+        y = _bits16(y, "y")
+    _check("k3moe_layer_streamed", lib().k3moe_layer_streamed(
+        ctypes.byref(d), cache.handle, int(layer), _ptr(x), T, _ptr(wr), _ptr(bias),
+        _ptr(sh_gate), _ptr(sh_up), _ptr(sh_down), _ptr(idx_out), _ptr(w_out), _ptr(y), ydt,
         int(bool(accumulate)), _ptr(workspace), workspace.numel(), _ptr(status),
         _stream(stream)))
 

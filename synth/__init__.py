@@ -10,6 +10,8 @@ measured on):
   tiny            hidden 256,  inter 128,  16 experts, top-2,  1 shared, 4 tokens
   decode1         hidden 7168, inter 1536, 896 experts, top-16, 1 shared, 1 token
   decode64_zipf   as decode1, 64 tokens, bias steering expert popularity to Zipf(1.1)
+  decode64_uniform  as decode1, 64 tokens, uniform routing (the pages' Quantile
+                  Balancing flattens expert use, so this is the realistic batch)
   prefill4096     as decode1, 4096 tokens, uniform routing
   stacked8        8 decode1 layers, batch 1, 256 steps, RMSNorm + residual in between
   latent_decode1  the pages' LatentMoE: hidden 7168, experts in a 3584-wide latent with
@@ -102,6 +104,7 @@ CONFIGS = {
     "decode1": Config("decode1", 7168, 1536, 896, 16, 1),
     "decode64_zipf": Config("decode64_zipf", 7168, 1536, 896, 16, 64, routing="zipf",
                             zipf_beta=ZIPF_BETA_1P1),
+    "decode64_uniform": Config("decode64_uniform", 7168, 1536, 896, 16, 64),
     "prefill4096": Config("prefill4096", 7168, 1536, 896, 16, 4096),
     "stacked8": Config("stacked8", 7168, 1536, 896, 16, 1, layers=8, steps=256),
     "latent_decode1": Config("latent_decode1", 7168, 3072, 896, 16, 1, n_shared=2,

@@ -397,10 +397,19 @@ def test_decode1_full_layer():
 
 
 @pytest.mark.slow
-def test_decode64_zipf_sampled():
-    cfg = synth.config("decode64_zipf")
+@pytest.mark.parametrize("name", ["decode64_zipf", "decode64_uniform"])
+def test_decode64_sampled(name):
+    cfg = synth.config(name)
     L = Layer(cfg, seed=0)
-    check_layer(L, T_sample=[0, 17, 40, 63])
+    y, idx, w, st = L.run()
+    assert st == 0
+    # every token's route against the oracle router, outputs on a sample of tokens
+    oi, ow, _, _ = oracle.router(L.x, L.host["wr"], L.host["bias"], 16)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    assert np.allclose(w.cpu().numpy(), ow, rtol=2e-7, atol=0)
+    tokens = [0, 17, 40, 63]
+    _, _, oy = L.oracle(tokens=tokens)
+    assert rel_l2(y.cpu().numpy()[tokens], oy) <= REL_L2_F32
 
 
 @pytest.mark.slow
