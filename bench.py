@@ -554,8 +554,10 @@ def bench_batch(ctx, name, args, K, tokens=0):
             dom = "k_tc_gemm_gateup"
             db = sum(u * 2 * op for u in U) / L        # gate/up bytes of the distinct experts
         else:
-            dom = "k_decode_fused"                      # one kernel per layer: all its bytes
-            db = sum(layer_bytes) / L
+            # the fused kernel runs up to 16 stacked layers per launch: a launch's bytes are
+            # the step's bytes over the launches in a step
+            dom = "k_decode_fused"
+            db = sum(layer_bytes) / max(kernels.get(dom, {}).get("launches_per_step", L), 1)
         dk = kernels.get(dom, {}).get("ms_avg")
         roofline = {"bound": "hbm", "kernel": dom,
                     "achieved": db / (dk * 1e-3) / 1e9 if dk else None, "peak": peak_hbm,

@@ -373,21 +373,24 @@ bool fused_takes(const DeviceInfo *di, const k3moe_dims *d) {
 // bounded-wait path).
 std::atomic<int> g_expire_wait{0};
 
-// One token through the fused kernel: input x (bf16), or h (float, the residual stream)
-// normalised in the kernel (x = bf16(RMSNorm(h)) with eps).  Its grid-wide counters
-// (workspace header) are zero on entry and left zero by the kernel's last CTA.
+// One token through the fused kernel, for L layers (1 .. kFuMaxLayers) in one launch:
+// input x (bf16; one layer), or h (float, the residual stream) normalised in the kernel
+// before every layer (x = bf16(RMSNorm(h)) with eps).  Its grid-wide counters (workspace
+// header) are zero on entry and left zero by the kernel's last CTA.
 k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x,
-                       const float *h, float eps, const uint16_t *wr, const float *bias,
-                       const k3moe_experts *ex, const uint16_t *sh_gate, const uint16_t *sh_up,
-                       const uint16_t *sh_down, Ws &ws, int32_t *idx, float *w, void *y,
-                       k3moe_dtype ydt, int accumulate, int32_t *status, cudaStream_t st) {
-  FusedT1Args a;
+                       const float *h, float eps, const FusedLayer *layers, int L, Ws &ws,
+                       void *y, k3moe_dtype ydt, int accumulate, int32_t *status,
+                       cudaStream_t st) {
+  if (L < 1 || L > kFuMaxLayers || (L > 1 && !h)) return K3MOE_ERR_ARG;
+  FusedT1Args a{};
   a.x = x; a.h = h; a.eps = eps;
   a.H = d->hidden; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
   a.SI = d->shared_inter;
-  a.wr = wr; a.bias = bias;
-  a.sh_gate = sh_gate; a.sh_up = sh_up; a.sh_down = sh_down;
-  a.ex = expert_args(d, ex);
+  a.L = L;
+  for (int l = 0; l < L; l++) a.lay[l] = layers[l];
+  int64_t off[7];
+  record_offsets(d, off);
+  for (int i = 0; i < 6; i++) a.ex.off[i] = off[i];
   a.renorm = d->renorm; a.routed_scale = d->routed_scale;
   a.b1 = d->situ_b1; a.b2 = d->situ_b2;
   a.sc = ws.sc; a.ch = ws.ch; a.act_s = ws.act_s;
@@ -395,12 +398,22 @@ k3moe_status run_fused(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
   a.bar = ws.bar;
   // |SiTU| <= b1 b2: scale the activations so that the largest stays below 2^15
   a.act_exp = act_scale_exp(d->situ_b1, d->situ_b2);
-  a.idx_out = idx; a.w_out = w;
   a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate;
   a.status = status;
   a.expire_dep2 = g_expire_wait.load(std::memory_order_relaxed);
   TraceScope ts(KID_DECODE_FUSED, st);
   return launch_fused_t1(a, di->sms, st) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
+FusedLayer fused_layer_of(const uint16_t *wr, const float *bias, const k3moe_experts *ex,
+                          const uint16_t *sh_gate, const uint16_t *sh_up,
+                          const uint16_t *sh_down, int32_t *idx, float *w) {
+  FusedLayer f{};
+  f.wr = wr; f.bias = bias;
+  f.sh_gate = sh_gate; f.sh_up = sh_up; f.sh_down = sh_down;
+  f.experts = ex->experts; f.stride = ex->expert_stride;
+  f.idx_out = idx; f.w_out = w;
+  return f;
 }
 
 // The whole layer for Tc tokens.  One token with a supported width: router kernel, then
@@ -412,9 +425,10 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
                        const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
                        Ws &ws, int32_t *idx, float *w, void *y, k3moe_dtype ydt, int accumulate,
                        int32_t *status, cudaStream_t st) {
-  if (Tc == 1 && fused_takes(di, d))
-    return run_fused(di, d, x, nullptr, 0.f, wr, bias, ex, sh_gate, sh_up, sh_down, ws, idx, w,
-                     y, ydt, accumulate, status, st);
+  if (Tc == 1 && fused_takes(di, d)) {
+    const FusedLayer f = fused_layer_of(wr, bias, ex, sh_gate, sh_up, sh_down, idx, w);
+    return run_fused(di, d, x, nullptr, 0.f, &f, 1, ws, y, ydt, accumulate, status, st);
+  }
   const int rb = t1_row_block(d->hidden);
   if (Tc == 1 && rb > 0) {
     k3moe_status s = run_route(di, d, x, Tc, wr, bias, sh_gate, sh_up, ws, idx, w, status, st,
@@ -1247,22 +1261,29 @@ k3moe_status k3moe_decode_stack(const k3moe_dims *dims, int32_t L,
   const DeviceInfo *di = device_info();
   if (!di) return K3MOE_ERR_CUDA;
   if (T == 1 && fused_takes(di, dims) && eps >= 0.f) {
-    // one launch per layer: the fused kernel normalises h itself (RMSNorm in every CTA)
-    // and adds the layer's output to it; x_scratch is not used
+    // up to kFuMaxLayers layers per launch: the fused kernel normalises h itself before
+    // every layer (RMSNorm in every CTA), adds the layer's output to it, and streams the
+    // next layer's router and shared-expert weights while it waits for every CTA to finish
+    // the layer; x_scratch is not used
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Ws ws = ws_layout(dims, T, workspace);
-    for (int l = 0; l < L; l++) {
-      const k3moe_layer_weights &lw = layers[l];
-      const bool shared = dims->shared_inter > 0;
-      s = check_layer_args(dims, h, T, lw.wr_bf16, lw.bias, &lw.experts, lw.sh_gate, lw.sh_up,
-                           lw.sh_down, idx_out, w_out, h, K3MOE_F32, workspace, ws_bytes,
-                           status_dev);
-      if (s != K3MOE_OK) return s;
-      const size_t ro = (size_t)l * K;
-      s = run_fused(di, dims, nullptr, h, eps, lw.wr_bf16, lw.bias, &lw.experts,
-                    shared ? lw.sh_gate : nullptr, shared ? lw.sh_up : nullptr,
-                    shared ? lw.sh_down : nullptr, ws, idx_out ? idx_out + ro : ws.idx,
-                    w_out ? w_out + ro : ws.w, h, K3MOE_F32, 1, status_dev, st);
+    const bool shared = dims->shared_inter > 0;
+    FusedLayer f[kFuMaxLayers];
+    for (int l0 = 0; l0 < L; l0 += kFuMaxLayers) {
+      const int n = (L - l0) < kFuMaxLayers ? (L - l0) : kFuMaxLayers;
+      for (int i = 0; i < n; i++) {
+        const int l = l0 + i;
+        const k3moe_layer_weights &lw = layers[l];
+        s = check_layer_args(dims, h, T, lw.wr_bf16, lw.bias, &lw.experts, lw.sh_gate, lw.sh_up,
+                             lw.sh_down, idx_out, w_out, h, K3MOE_F32, workspace, ws_bytes,
+                             status_dev);
+        if (s != K3MOE_OK) return s;
+        const size_t ro = (size_t)l * K;
+        f[i] = fused_layer_of(lw.wr_bf16, lw.bias, &lw.experts, shared ? lw.sh_gate : nullptr,
+                              shared ? lw.sh_up : nullptr, shared ? lw.sh_down : nullptr,
+                              idx_out ? idx_out + ro : nullptr, w_out ? w_out + ro : nullptr);
+      }
+      s = run_fused(di, dims, nullptr, h, eps, f, n, ws, h, K3MOE_F32, 1, status_dev, st);
       if (s != K3MOE_OK) return s;
     }
     return K3MOE_OK;

@@ -209,8 +209,15 @@ __host__ __device__ inline uint32_t fused_ring_bytes(int H, int I, int SI) {
   return g > d ? g : d;
 }
 
-__global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// One layer of the step (layer `layer` of a stack): everything below runs once per layer, the
+// CTA's roles meeting at a __syncthreads between layers.  kMulti: several layers share the
+// launch, so no copy may outlive a layer (after an expiry the consumers stop waiting for
+// their stages): the producer then also waits for a slot's previous fill to land before it
+// refills the slot.
+template <bool kMulti>
+__device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int layer, uint8_t *smem) {
+  const FusedLayer &lw = a.lay[layer];
+  unsigned *const bar = a.bar + 4 * layer;  // this layer's grid counters
   const int H = a.H, I = a.I, K = a.K, E = a.E, SI = a.SI;
   const int G = H / kGroup, nwc = G / 32;  // consumer warps per row parity
   const int rowb = H / 2;                  // packed bytes of a gate/up row
@@ -263,6 +270,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
+    if (layer > 0) {  // the previous layer's barriers are idle: invalidate, then set up again
+      for (int b = 0; b < 16 + 2 * kFuNSD + 6; b++) mbar_inval(fullG + b);
+    }
     for (int s = 0; s < NSG; s++) {
       mbar_init(&fullG[s], 1);
       mbar_init(&emptyG[s], 2 * nwc);
@@ -307,14 +317,27 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
             __threadfence_block();  // the published selections before their use
           }
         }
-        if (!mbar_wait(&emptyG[lane], ((t / NSG) & 1) ^ 1)) {
+        // the slot's previous stage consumed and landed (after an expiry its consumers
+        // stop waiting for it): one fill per slot at a time, so no copy outlives the layer
+        if (!mbar_wait(&emptyG[lane], ((t / NSG) & 1) ^ 1) ||
+            (kMulti && t >= NSG && !mbar_wait(&fullG[lane], ((t / NSG) & 1) ^ 1))) {
           set_status(a.status, K3MOE_ERR_TIMEOUT);
           ab = true;
           break;
         }
         uint8_t *dst = slot_ptr(lane);
         if (t == 0) {
-          // the token's input: bf16 x, or the float residual stream to normalise
+          // the token's input: bf16 x, or the float residual stream to normalise -- in a
+          // stack, once every CTA has added its tiles of the previous layer to it (the
+          // other lanes meanwhile issue this layer's router and shared-expert stages)
+          if (layer > 0) {
+            if (!wait_count(a.bar + 4 * (layer - 1) + 2, (unsigned)nb)) {
+              set_status(a.status, K3MOE_ERR_TIMEOUT);
+              ab = true;
+              break;
+            }
+            fence_proxy_async_all();  // the other CTAs' stores before the async-proxy read
+          }
           const uint32_t xbytes = a.h ? (uint32_t)(H * 4) : (uint32_t)rowh;
           mbar_arrive_expect_tx(&fullG[lane], xbytes);
           bulk_g2s(dst, a.h ? static_cast<const void *>(a.h) : static_cast<const void *>(a.x),
@@ -324,19 +347,19 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
           const int nrow = cntR - k0 < 2 ? cntR - k0 : 2;
           mbar_arrive_expect_tx(&fullG[lane], (uint32_t)(nrow * rowh));
           for (int rr = 0; rr < nrow; rr++)
-            bulk_g2s(dst + rr * rowh, a.wr + (size_t)(bx + nb * (k0 + rr)) * H, rowh,
+            bulk_g2s(dst + rr * rowh, lw.wr + (size_t)(bx + nb * (k0 + rr)) * H, rowh,
                      &fullG[lane]);
         } else if (t < tG) {
           const int p = bx + nb * (t - tS);
           mbar_arrive_expect_tx(&fullG[lane], (uint32_t)(2 * rowh));
-          bulk_g2s(dst, a.sh_gate + (size_t)p * H, rowh, &fullG[lane]);
-          bulk_g2s(dst + rowh, a.sh_up + (size_t)p * H, rowh, &fullG[lane]);
+          bulk_g2s(dst, lw.sh_gate + (size_t)p * H, rowh, &fullG[lane]);
+          bulk_g2s(dst + rowh, lw.sh_up + (size_t)p * H, rowh, &fullG[lane]);
         } else {
           const int tg = t - tG;
           const int item = bx + nb * (tg >> 1);
           const int j = item / blocks, blk = item % blocks;
           const int r = blk * kFuItemRows + (tg & 1) * kFuRB;
-          const uint8_t *rec = a.ex.base + (long long)sel[j] * a.ex.stride;
+          const uint8_t *rec = lw.experts + (long long)sel[j] * lw.stride;
           mbar_arrive_expect_tx(&fullG[lane], gstage);
           bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, kFuRB * rowb, &fullG[lane]);
           bulk_g2s(dst + kFuRB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, kFuRB * rowb,
@@ -362,6 +385,8 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
         ab = true;
       }
+      // and landed, before D copies may overwrite the slot's bytes (bounded)
+      if (last_g >= 0 && (kMulti || ab)) mbar_wait(&fullG[lane], (last_g / NSG) & 1, 400000000LL);
       __threadfence_block();
       gdone[lane] = 1;
     }
@@ -389,7 +414,8 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
       bool dep2 = false;
       for (; !ab && iD < nD; iD += kFuNSD) {
         const int q = lane, u = iD / kFuNSD;
-        if (!mbar_wait(&emptyD[q], (u & 1) ^ 1)) {
+        if (!mbar_wait(&emptyD[q], (u & 1) ^ 1) ||
+            (kMulti && u > 0 && !mbar_wait(&fullD[q], (u & 1) ^ 1))) {
           set_status(a.status, K3MOE_ERR_TIMEOUT);
           ab = true;
           break;
@@ -403,7 +429,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         mbar_arrive_expect_tx(&fullD[q], wbytes + abytes);
         if (routed) {
           for (int e2 = 0; e2 < 2; e2++) {
-            const uint8_t *rec = a.ex.base + (long long)sel[2 * m + e2] * a.ex.stride;
+            const uint8_t *rec = lw.experts + (long long)sel[2 * m + e2] * lw.stride;
             bulk_g2s(dst + e2 * dexp, rec + a.ex.off[2] + (size_t)r0 * rowb2,
                      kFuDownRows * rowb2, &fullD[q]);
             bulk_g2s(dst + e2 * dexp + kFuDownRows * rowb2,
@@ -411,12 +437,12 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
           }
         } else {
           const int rs0 = r0 + (m - hk) * RS;
-          bulk_g2s(dst, a.sh_down + (size_t)rs0 * SI, wbytes, &fullD[q]);
+          bulk_g2s(dst, lw.sh_down + (size_t)rs0 * SI, wbytes, &fullD[q]);
         }
         if (!dep2) {
           // (the expiry test waits for one arrival more than there are CTAs, briefly)
           const unsigned need = (unsigned)nb + (a.expire_dep2 ? 1u : 0u);
-          if (!wait_count(a.bar + 1, need, a.expire_dep2 ? kExpireBudget : kWaitBudget)) {
+          if (!wait_count(bar + 1, need, a.expire_dep2 ? kExpireBudget : kWaitBudget)) {
             set_status(a.status, K3MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             __threadfence_block();  // before the copies whose landing the workers wait for
@@ -433,11 +459,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
         }
       }
     }
-    // bounded waits for this lane's copies still in flight: the last D stage always (a
-    // worker whose wait expired no longer waits for it, and the CTA must not exit before
-    // it lands), the last R/S/G stage after an expiry here
-    if (ab && lane < NSG && last_g >= 0)
-      mbar_wait(&fullG[lane], (last_g / NSG) & 1, 400000000LL);
+    // bounded wait for this lane's last D copy (a worker whose wait expired no longer
+    // waits for it, and neither the CTA's exit nor the next layer's barrier set-up may
+    // come before it lands); its R/S/G fills have all landed above
     if (lane < kFuNSD && iD - kFuNSD >= 0 && iD - kFuNSD < nD)
       mbar_wait(&fullD[lane], ((iD - kFuNSD) / kFuNSD) & 1, 400000000LL);
     return;
@@ -464,7 +488,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     float mylogit = 0.f;
     // this lane's router-row bias, fetched now: by the time it is added the stream of
     // weight stages keeps every memory queue long
-    const float mybias = (a.bias && lane < cntR) ? __ldg(a.bias + bx + nb * lane) : 0.f;
+    const float mybias = (lw.bias && lane < cntR) ? __ldg(lw.bias + bx + nb * lane) : 0.f;
     for (int s = 0; s < nR; s++, n++) {
       const float *rt = take(n);
       float hi = 0.f, lo = 0.f;
@@ -487,7 +511,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     __syncwarp();  // the lanes' score writes before lane 0's fence, which covers them all
     if (lane == 0) {  // dependency 1: this CTA's router rows are written
       __threadfence();
-      atomicAdd(a.bar, 1u);
+      atomicAdd(bar, 1u);
     }
     // S: shared pair p -> SiTU(gate, up)
     for (int s = 0; s < nS; s++, n++) {
@@ -751,7 +775,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     const bool bulk = chb <= (uint32_t)kFuSmallBytes;
     bool ok = true;
     if (lane == 0) {
-      if (!wait_count(a.bar, (unsigned)nb)) {
+      if (!wait_count(bar, (unsigned)nb)) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
         *abort_flag = 1;
       }
@@ -783,9 +807,9 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     }
     if (lane < K) {
       wsel[lane] = w_sel;
-      if (bx == 0 && a.idx_out) {
-        a.idx_out[lane] = e_sel;
-        a.w_out[lane] = w_sel;
+      if (bx == 0 && lw.idx_out) {
+        lw.idx_out[lane] = e_sel;
+        lw.w_out[lane] = w_sel;
       }
     }
     __syncwarp();
@@ -799,7 +823,7 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
   named_bar_sync(kBarDown, NDT);
   if (tid == 0) {
     __threadfence();
-    atomicAdd(a.bar + 1, 1u);
+    atomicAdd(bar + 1, 1u);
   }
 
   // ---------------- D: down rows, shared down rows, router-order combine ----------------
@@ -905,17 +929,29 @@ __global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
     }
     named_bar_sync(kBarDown, NDT);
   }
-  // exit: every use of the counters by this CTA is over (its producer read the second
-  // one before it copied the activations its D stages needed); the last CTA to get here
-  // leaves all three zero for the next call
+  // exit of the layer: its tiles of y (or of the residual stream) are written; the next
+  // layer's input stage waits for every CTA's exit.  After the last layer every use of the
+  // counters is over (a CTA reads them only before its own exit), so the last CTA to get
+  // here leaves all of them zero for the next call.
   if (tid == 0) {
     __threadfence();
-    if (atomicAdd(a.bar + 2, 1u) == (unsigned)nb - 1) {
-      a.bar[0] = 0u;
-      a.bar[1] = 0u;
-      a.bar[2] = 0u;
+    if (atomicAdd(bar + 2, 1u) == (unsigned)nb - 1 && layer == a.L - 1) {
+      for (int k = 0; k < 4 * a.L; k++) a.bar[k] = 0u;
       __threadfence();
     }
+  }
+}
+
+template <bool kMulti>
+__global__ void __launch_bounds__(kFuThreads, 1) k_decode_fused(FusedT1Args a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (!kMulti) {
+    fused_layer<false>(a, 0, smem);
+    return;
+  }
+  for (int l = 0; l < a.L; l++) {
+    if (l > 0) __syncthreads();  // every role of the CTA is done with layer l - 1
+    fused_layer<true>(a, l, smem);
   }
 }
 
@@ -933,7 +969,10 @@ size_t fused_t1_smem(int H, int I, int E, int K, int SI, int grid) {
 }
 
 cudaError_t set_fused_smem_limit() {
-  return cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k_decode_fused<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_decode_fused<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               227 * 1024);
 }
 
@@ -950,7 +989,8 @@ cudaError_t launch_fused_t1(const FusedT1Args &a, int grid, cudaStream_t st) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode_fused, a);
+  return a.L > 1 ? cudaLaunchKernelEx(&cfg, k_decode_fused<true>, a)
+                 : cudaLaunchKernelEx(&cfg, k_decode_fused<false>, a);
 }
 
 }  // namespace k3

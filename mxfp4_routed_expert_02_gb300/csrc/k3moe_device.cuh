@@ -263,6 +263,10 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");
 }
+// Invalidate an mbarrier no thread uses any more, before its memory is initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // Make barrier initialisation visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {

@@ -96,24 +96,35 @@ struct DownArgs {
 };
 
 // ---- the single-token layer step as one persistent kernel (k3moe_decode_fused.cu)
+// Weights and route outputs of one layer of the step (a stack of layers runs several in
+// one launch).
+struct FusedLayer {
+  const uint16_t *wr;                         // [E][H]
+  const float *bias;                          // [E] or null
+  const uint16_t *sh_gate, *sh_up, *sh_down;  // null when SI == 0
+  const uint8_t *experts;                     // expert e at experts + e * stride
+  long long stride;
+  int32_t *idx_out;                           // [K] or null
+  float *w_out;                               // [K] or null
+};
+// Layers per launch: each uses four grid counters of the 256-byte workspace header.
+constexpr int kFuMaxLayers = 16;
 struct FusedT1Args {
   const uint16_t *x;  // [H] bf16 (unused when h is set)
   const float *h;     // [H] residual stream: when set, x = bf16(RMSNorm(h)) in the kernel
   float eps;          // RMSNorm epsilon (with h)
   int H, I, E, K, SI;
-  const uint16_t *wr;  // [E][H]
-  const float *bias;   // [E] or null
-  const uint16_t *sh_gate, *sh_up, *sh_down;  // null when SI == 0
-  ExpertArgs ex;
+  int L;                        // layers, 1 .. kFuMaxLayers (more than one needs h)
+  FusedLayer lay[kFuMaxLayers];
+  ExpertArgs ex;                // record offsets (base and stride are per layer)
   int renorm;
   float routed_scale, b1, b2;
   float *sc, *ch;       // [E] workspace
   float *act_s;         // [SI] workspace
   uint16_t *act;              // [K][I] workspace
-  unsigned *bar;              // dependency 1, dependency 2, exit: zero on entry and on exit
+  unsigned *bar;              // per layer l, bar[4l ..]: dependency 1, dependency 2, exit;
+                              // zero on entry and on exit
   int act_exp;                // activations are stored as f16 of act * 2^-act_exp
-  int32_t *idx_out;
-  float *w_out;  // [K] or null
   void *y;
   int ydt, accumulate;
   int32_t *status;
