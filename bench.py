@@ -80,7 +80,7 @@ TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode_fused.cu",
 # k_decode_fused: captured with a 64-expert pool (351,598,080 B per launch), plus the
 # router rows the full 896-expert pool adds ((896 - 64) x 7168 x 2 B): every other byte
 # the kernel reads is the same at both pool sizes (16 selected experts, the shared expert).
-TRAFFIC_CAPTURED = {"sources": "dacd8f370a02f450",
+TRAFFIC_CAPTURED = {"sources": "f4f4b1248ad42362",
                     "bytes": {"k_decode_fused": 351598080 + (896 - 64) * 7168 * 2}}
 
 
