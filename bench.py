@@ -16,7 +16,8 @@ expert pool:
   streamed_decode1  1 token per step with the records in pinned host memory and 256
                  device slots in front of them (the LRU expert cache);
 
-the last six as nested entries of the one JSON line (``workloads``).  ``--workload``
+the last six as nested entries of the one JSON line (``workloads``; at one GPU only -- a
+multi-GPU run times the headline).  ``--workload``
 times one of them alone as the line's headline.  Timed regions: blocks of exactly K
 steps, each between a barrier and a synchronize, repeated until at least a second of
 load has passed so that the clock sampler sees the timed work; every step between CUDA
@@ -755,7 +756,9 @@ def run_ours(args):
     steps = lambda name: args.steps or DEFAULT_STEPS[name]
     if args.workload in ("all", "decode1"):
         line = bench_decode1(ctx, args, steps("decode1"))
-        if args.workload == "all":
+        # the other workloads ride along at one GPU only: a scaling run times the headline
+        # (and N ranks would each hold their own 126 GB stack and pinned host pool)
+        if args.workload == "all" and ctx.world == 1:
             line["workloads"] = {}
             for name in ("decode64_zipf", "decode64_uniform", "prefill4096", "stacked8",
                          "latent_decode1", "streamed_decode1"):
