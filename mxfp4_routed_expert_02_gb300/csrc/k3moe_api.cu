@@ -439,8 +439,8 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
     const size_t stage = (size_t)2 * rb * (H / 2 + G);
     int ns = (int)((227 * 1024 - gateup_t1_smem(H, d->n_experts, d->topk, rb, 0)) / stage);
     if (ns > 16) ns = 16;
-    GateUpT1Args a;
-    a.x = x; a.H = H; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
+    GateUpT1Args a{};
+    a.x = x; a.xf = nullptr; a.H = H; a.I = d->inter; a.E = d->n_experts; a.K = d->topk;
     a.ex = ea; a.sc = ws.sc; a.ch = ws.ch; a.renorm = d->renorm;
     a.routed_scale = d->routed_scale; a.idx_out = idx; a.w_out = w; a.disp = ws.disp;
     a.b1 = d->situ_b1; a.b2 = d->situ_b2;
@@ -1096,9 +1096,12 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
     int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : ws.route.idx;
     float *w_c = w_out ? w_out + (size_t)t0 * K : ws.route.w;
     void *yc = static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt);
+    // one token at a latent width the single-token gate/up kernel takes: it selects the
+    // top-k itself from the router's scores and streams the experts through its ring
+    const int rb = Tc == 1 ? t1_row_block(L) : 0;
     // 1. route on the full-width x
     s = run_route(di, &full, xc, Tc, lw->wr_bf16, lw->bias, nullptr, nullptr, ws.route, idx_c,
-                  w_c, status_dev, st, true);
+                  w_c, status_dev, st, rb == 0);
     if (s != K3MOE_OK) return s;
     // 2. z = Wdn x
     {
@@ -1108,8 +1111,31 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
         return K3MOE_ERR_CUDA;
     }
     // 3. the experts in the latent, summed in router order into accL
-    s = run_ffn(di, &lat, ws.z, Tc, &lw->experts, idx_c, w_c, nullptr, ws.ffn, ws.accl, K3MOE_F32,
-                0, status_dev, st, true);
+    if (rb > 0) {
+      const ExpertArgs ea = expert_args(&lat, &lw->experts);
+      const int G = L / kGroup;
+      const size_t stage = (size_t)2 * rb * (L / 2 + G);
+      int ns = (int)((227 * 1024 - gateup_t1_smem(L, dims->n_experts, K, rb, 0)) / stage);
+      if (ns > 16) ns = 16;
+      GateUpT1Args g{};
+      g.x = nullptr; g.xf = ws.z; g.H = L; g.I = dims->inter; g.E = dims->n_experts; g.K = K;
+      g.ex = ea; g.sc = ws.route.sc; g.ch = ws.route.ch; g.renorm = dims->renorm;
+      g.routed_scale = dims->routed_scale; g.idx_out = idx_c; g.w_out = w_c;
+      g.disp = ws.ffn.disp; g.b1 = b1; g.b2 = b2;
+      g.act_hi = ws.ffn.act_hi; g.act_lo = ws.ffn.act_lo; g.act_ex = ws.ffn.act_ex;
+      g.status = status_dev; g.RB = rb; g.NS = ns;
+      {
+        TraceScope ts(KID_GATEUP_T1, st);
+        int grid = K * (dims->inter / kTileRows);
+        if (grid > di->sms) grid = di->sms;
+        if (launch_gateup_t1(g, grid, st, !g_trace.on) != cudaSuccess) return K3MOE_ERR_CUDA;
+      }
+      s = run_down(di, &lat, 1, ea, idx_c, w_c, nullptr, ws.ffn, ws.accl, K3MOE_F32, 0,
+                   status_dev, st, !g_trace.on);
+    } else {
+      s = run_ffn(di, &lat, ws.z, Tc, &lw->experts, idx_c, w_c, nullptr, ws.ffn, ws.accl,
+                  K3MOE_F32, 0, status_dev, st, true);
+    }
     if (s != K3MOE_OK) return s;
     // 4. RMSNorm of the aggregate
     if (dims->latent_norm) {

@@ -38,7 +38,9 @@ __host__ __device__ inline int gu_ring_offset(int E, int K) {
 // buffers, by tile parity).  An epilogue warp adds the warps' parts of a 32-row tile in a
 // fixed order, applies SiTU and writes the activations; consumers hand tiles to it
 // through mbarriers and never wait for one another.
-template <int RB>
+// XF32: the input is a.xf (float, the LatentMoE's latent), prescaled into two f16 terms
+// per group (hi + residual) and multiplied with both (group_dot2).
+template <int RB, bool XF32>
 __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = a.H, I = a.I, K = a.K;
@@ -179,24 +181,37 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
   // ---------------- consumers: thread (h, g) ----------------
   const int h = tid / C, g = tid % C;
   const bool gact = g < G;
-  uint32_t xr[16];
+  uint32_t xr[16], xl[16];
   int xe = 0;
 #pragma unroll
-  for (int p = 0; p < 16; p++) xr[p] = 0u;
+  for (int p = 0; p < 16; p++) xr[p] = xl[p] = 0u;
   if (gact) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + g * kGroup);
     float v[32];
+    if (XF32) {
+      const float4 *src = reinterpret_cast<const float4 *>(a.xf + g * kGroup);
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-      const uint4 c = __ldg(src + q);
-      const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-      for (int k = 0; k < 4; k++) {
-        v[8 * q + 2 * k] = bf16_lo(w4[k]);
-        v[8 * q + 2 * k + 1] = bf16_hi(w4[k]);
+      for (int q = 0; q < 8; q++) {
+        const float4 c = __ldg(src + q);
+        v[4 * q] = c.x;
+        v[4 * q + 1] = c.y;
+        v[4 * q + 2] = c.z;
+        v[4 * q + 3] = c.w;
       }
+      xe = prescale_group_f16_hilo(v, xr, xl);
+    } else {
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.x + g * kGroup);
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const uint4 c = __ldg(src + q);
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          v[8 * q + 2 * k] = bf16_lo(w4[k]);
+          v[8 * q + 2 * k + 1] = bf16_hi(w4[k]);
+        }
+      }
+      xe = prescale_group_f16(v, xr);
     }
-    xe = prescale_group_f16(v, xr);
   }
 
   int it = 0, n = 0;
@@ -233,8 +248,12 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
             const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
             const uint4 wu = reinterpret_cast<const uint4 *>(st + (RB + q) * rowb)[g];
             const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
-            if (sg != 255u) vals[b2 * RB + 2 * k] = group_dot(xr, wg) * group_factor(sg, xe);
-            if (su != 255u) vals[b2 * RB + 2 * k + 1] = group_dot(xr, wu) * group_factor(su, xe);
+            if (sg != 255u)
+              vals[b2 * RB + 2 * k] =
+                  (XF32 ? group_dot2(xr, xl, wg) : group_dot(xr, wg)) * group_factor(sg, xe);
+            if (su != 255u)
+              vals[b2 * RB + 2 * k + 1] =
+                  (XF32 ? group_dot2(xr, xl, wu) : group_dot(xr, wu)) * group_factor(su, xe);
           }
         }
         __syncwarp();
@@ -270,9 +289,14 @@ cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, b
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.RB == 4) return cudaLaunchKernelEx(&cfg, k_gateup_t1<4>, a);
-  if (a.RB == 8) return cudaLaunchKernelEx(&cfg, k_gateup_t1<8>, a);
-  return cudaLaunchKernelEx(&cfg, k_gateup_t1<16>, a);
+  if (a.xf) {
+    if (a.RB == 4) return cudaLaunchKernelEx(&cfg, k_gateup_t1<4, true>, a);
+    if (a.RB == 8) return cudaLaunchKernelEx(&cfg, k_gateup_t1<8, true>, a);
+    return cudaLaunchKernelEx(&cfg, k_gateup_t1<16, true>, a);
+  }
+  if (a.RB == 4) return cudaLaunchKernelEx(&cfg, k_gateup_t1<4, false>, a);
+  if (a.RB == 8) return cudaLaunchKernelEx(&cfg, k_gateup_t1<8, false>, a);
+  return cudaLaunchKernelEx(&cfg, k_gateup_t1<16, false>, a);
 }
 
 // ------------------------------------------------------------------------------------
@@ -547,17 +571,19 @@ cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool p
 
 cudaError_t set_decode_smem_limits() {
   const int big = 227 * 1024;
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gateup_t1<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
-          cudaSuccess ||
-      (e = cudaFuncSetAttribute(k_gateup_t1<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
-          cudaSuccess ||
-      (e = cudaFuncSetAttribute(k_gateup_t1<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
-          cudaSuccess ||
-      (e = cudaFuncSetAttribute(k_down_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)) !=
-          cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(k_down_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+  const void *fns[] = {reinterpret_cast<const void *>(k_gateup_t1<4, false>),
+                       reinterpret_cast<const void *>(k_gateup_t1<8, false>),
+                       reinterpret_cast<const void *>(k_gateup_t1<16, false>),
+                       reinterpret_cast<const void *>(k_gateup_t1<4, true>),
+                       reinterpret_cast<const void *>(k_gateup_t1<8, true>),
+                       reinterpret_cast<const void *>(k_gateup_t1<16, true>),
+                       reinterpret_cast<const void *>(k_down_tma<true>),
+                       reinterpret_cast<const void *>(k_down_tma<false>)};
+  for (const void *f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace k3

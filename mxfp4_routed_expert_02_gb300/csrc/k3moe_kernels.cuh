@@ -64,6 +64,7 @@ __global__ void k_down_combine(int T, int H, int I, int K, ExpertArgs ex,
 // ---- decode kernels with bulk-copy rings (k3moe_decode.cu)
 struct GateUpT1Args {
   const uint16_t *x;
+  const float *xf;  // when set, the input is this float row instead of x (two f16 terms)
   int H, I, E, K;
   ExpertArgs ex;
   const float *sc, *ch;  // [E] router scores / selection scores
