@@ -591,14 +591,16 @@ def bench_batch(ctx, name, args, K, tokens=0):
 
 def latent_step_bytes(cfg, U):
     """Algorithmic bytes of one LatentMoE decode step with U distinct routed experts, per
-    kernel: the router, the projections (down, up and the shared experts' down), the
-    shared gate/up, the experts' gate/up and down."""
+    kernel (by trace name): the router, the projection into the latent, the experts'
+    gate/up and down, the projection back, the shared experts' gate/up and down."""
     H, L, I, E, SI = cfg.hidden, cfg.latent, cfg.inter, cfg.n_experts, cfg.shared_inter
     op = I * L // 2 + I * L // 32
-    return {"k_router_t1": E * H * 2 + H * 2,
-            "k_proj": L * H * 2 * 2 + H * SI * 2 + H * 4,
+    return {"k_router_shared": E * H * 2 + H * 2,
+            "k_proj_down": L * H * 2,
+            "k_proj_up": H * L * 2 + H * 4,
             "k_proj_shared_gateup": 2 * SI * H * 2,
-            "k_expert_gateup": U * 2 * op,
+            "k_proj_shared_down": H * SI * 2,
+            "k_gateup_t1": U * 2 * op,
             "k_down_tma": U * op}
 
 

@@ -143,14 +143,14 @@ enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KI
                 KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
                 KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_NORMS, KID_TC_ROUTER,
                 KID_ROUTE_CAND, KID_DECODE_FUSED, KID_PROJ, KID_SHARED_GATEUP, KID_RMSNORM_F32,
-                KID_COUNT };
+                KID_PROJ_UP, KID_PROJ_SHARED_DOWN, KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {
     "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
     "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
     "k_route_scatter", "k_quant_x", "k_tc_gemm_gateup", "k_quant_act", "k_tc_gemm_down",
     "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine",
-    "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused", "k_proj",
-    "k_proj_shared_gateup", "k_rmsnorm_f32w"};
+    "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused", "k_proj_down",
+    "k_proj_shared_gateup", "k_rmsnorm_f32w", "k_proj_up", "k_proj_shared_down"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -1107,7 +1107,7 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
     {
       TraceScope ts(KID_PROJ, st);
       if (launch_proj(st, di->sms, lw->w_down, nullptr, L, H, xc, false, Tc, ws.z, nullptr,
-                      nullptr, 0, 0, b1, b2) != cudaSuccess)
+                      nullptr, 0, 0, b1, b2, !g_trace.on) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
     // 3. the experts in the latent, summed in router order into accL
@@ -1137,18 +1137,21 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
                   K3MOE_F32, 0, status_dev, st, true);
     }
     if (s != K3MOE_OK) return s;
-    // 4. RMSNorm of the aggregate
-    if (dims->latent_norm) {
+    // 4. RMSNorm of the aggregate: its own kernel for a large pass, else done by every block
+    //    of the up-projection on the rows it reads
+    const bool fold_norm = dims->latent_norm && Tc <= kProjRows;
+    if (dims->latent_norm && !fold_norm) {
       TraceScope ts(KID_RMSNORM_F32, st);
-      if (launch_rmsnorm_f32w(st, ws.accl, Tc, L, lw->latent_norm_w, dims->rms_eps, ws.accl) !=
-          cudaSuccess)
+      if (launch_rmsnorm_f32w(st, ws.accl, Tc, L, lw->latent_norm_w, dims->rms_eps, ws.accl,
+                              !g_trace.on) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
     // 5. up = Wup accL (straight into y when there is no shared expert)
     {
-      TraceScope ts(KID_PROJ, st);
+      TraceScope ts(KID_PROJ_UP, st);
       if (launch_proj(st, di->sms, lw->w_up, nullptr, H, L, ws.accl, true, Tc, ws.up, nullptr,
-                      shared ? nullptr : yc, (int)ydt, accumulate, b1, b2) != cudaSuccess)
+                      shared ? nullptr : yc, (int)ydt, accumulate, b1, b2, !g_trace.on,
+                      fold_norm, lw->latent_norm_w, dims->rms_eps) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
     // 6. shared experts on the original x, added unweighted: y (=|+=) up + Wsd SiTU(..)
@@ -1156,12 +1159,12 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
       {
         TraceScope ts(KID_SHARED_GATEUP, st);
         if (launch_proj(st, di->sms, lw->sh_gate, lw->sh_up, SI, H, xc, false, Tc, ws.act_s,
-                        nullptr, nullptr, 0, 0, b1, b2) != cudaSuccess)
+                        nullptr, nullptr, 0, 0, b1, b2, !g_trace.on) != cudaSuccess)
           return K3MOE_ERR_CUDA;
       }
-      TraceScope ts(KID_PROJ, st);
+      TraceScope ts(KID_PROJ_SHARED_DOWN, st);
       if (launch_proj(st, di->sms, lw->sh_down, nullptr, H, SI, ws.act_s, true, Tc, nullptr,
-                      ws.up, yc, (int)ydt, accumulate, b1, b2) != cudaSuccess)
+                      ws.up, yc, (int)ydt, accumulate, b1, b2, !g_trace.on) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
   }

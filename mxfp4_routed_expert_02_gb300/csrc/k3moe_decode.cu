@@ -11,11 +11,11 @@
 namespace k3 {
 
 // ------------------------------------------------------------------------------------
-// Gate/up + SiTU for ONE token, TMA ring.  Block = C consumer threads (one per 32-column
-// group of the H inputs, C = ceil(G/32)*32) + 1 producer warp.  Work items = (selected
-// expert j, 32-row tile), statically strided over the grid.  A stage holds RB rows of
-// gate and up (packed) and their scale bytes; the consumer keeps the 32x2 partial sums
-// of its group column in registers and reduces them once per tile.
+// Gate/up + SiTU for ONE token, TMA ring.  Block = HP x C consumer threads (C =
+// ceil(G/32)*32, one per 32-column group of the H inputs in each of HP row phases) + a
+// producer warp + an epilogue warp.  Work items = (selected expert j, 32-row tile),
+// statically strided over the grid.  A stage holds RB rows of gate and up (packed) and
+// their scale bytes; a consumer keeps the partial sums of its group column in registers.
 // Each CTA recomputes the top-k from the router's scores (a few microseconds, no extra
 // launch); CTA 0 publishes the route (idx, w) and the dispatch lists.
 // ------------------------------------------------------------------------------------
@@ -32,27 +32,29 @@ __host__ __device__ inline int gu_ring_offset(int E, int K) {
   return (kGuScores + 8 * topk_scratch_keys(E, K) + 127) & ~127;
 }
 
-// Two consumer threads per group column: thread (h, g), h = 0/1, takes the rows of a stage
-// with row parity h.  Every two stages a thread's 2*RB partial sums (RB/2 rows x gate/up
-// x 2 stages) are transpose-reduced inside its warp and parked in shared memory (one of two
-// buffers, by tile parity).  An epilogue warp adds the warps' parts of a 32-row tile in a
+// HP consumer threads per group column (HP = 2, or 4 when the row is at most 128 groups
+// long, so that narrow inputs still keep 16 consumer warps streaming): thread (h, g),
+// h < HP, takes the rows q of a stage with q % HP == h.  Every two stages a thread's
+// 4*RB/HP partial sums (RB/HP rows x gate/up x 2 stages) are transpose-reduced inside its
+// warp and parked in shared memory (one of two buffers, by tile parity).  An epilogue warp adds the warps' parts of a 32-row tile in a
 // fixed order, applies SiTU and writes the activations; consumers hand tiles to it
 // through mbarriers and never wait for one another.
 // XF32: the input is a.xf (float, the LatentMoE's latent), prescaled into two f16 terms
 // per group (hi + residual) and multiplied with both (group_dot2).
-template <int RB, bool XF32>
-__global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
+template <int RB, bool XF32, int HP>
+__global__ void __launch_bounds__(HP == 4 ? 576 : 512, 1) k_gateup_t1(GateUpT1Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = a.H, I = a.I, K = a.K;
   const int G = H / kGroup;
-  const int C = ((G + 31) / 32) * 32;   // threads per row parity
-  const int nwc = C / 32;               // warps per row parity
+  const int C = ((G + 31) / 32) * 32;   // threads per row phase
+  const int nwc = C / 32;               // warps per row phase
   const int NS = a.NS;
   const int rowb = H / 2;
   const uint32_t stage_bytes = (uint32_t)(2 * RB * (rowb + G));
   const int tiles = I / kTileRows;
   constexpr int nblk = kTileRows / RB;  // stages per tile (even)
-  constexpr int V = RB * 2;             // values per two stages: RB/2 rows x 2 mats x 2
+  constexpr int RP = RB / HP;           // rows of a stage per consumer thread
+  constexpr int V = 4 * RP;             // values per two stages: RP rows x 2 mats x 2
 
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kGuBars);
   uint64_t *empty = full + 16;
@@ -69,10 +71,10 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
   if (tid == 0) {
     for (int s = 0; s < NS; s++) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2 * nwc);
+      mbar_init(&empty[s], HP * nwc);
     }
     for (int p = 0; p < 2; p++) {
-      mbar_init(&redbar[p], 2 * nwc);
+      mbar_init(&redbar[p], HP * nwc);
       mbar_init(&redfree[p], 1);
     }
     *abort_flag = 0;
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
   pdl_launch_dependents();
 
   const int nitems = K * tiles;
-  if (warp == 2 * nwc) {
+  if (warp == HP * nwc) {
     // ---------------- producer: lane p < NS owns ring slot p ----------------
     // A single thread issues only a few bulk copies per microsecond, so the stages are
     // spread over NS lanes; each slot's fills are issued by one lane, in phase order.
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
     return;
   }
 
-  if (warp == 2 * nwc + 1) {
+  if (warp == HP * nwc + 1) {
     // ---------------- epilogue: SiTU and activation output per tile ----------------
     int n = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, n++) {
@@ -148,8 +150,8 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
         set_status(a.status, K3MOE_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      // row `lane` of the tile was computed by the warps of row parity lane % 2
-      const int hp = lane & 1;
+      // row `lane` of the tile was computed by the warps of row phase lane % HP
+      const int hp = lane % HP;
       float gs = 0.f, us = 0.f;
       for (int w = hp * nwc; w < (hp + 1) * nwc; w++) {
         gs += rt[(w * 32 + lane) * 2];
@@ -243,27 +245,27 @@ __global__ void __launch_bounds__(512, 1) k_gateup_t1(GateUpT1Args a) {
           const uint8_t *sgs = st + 2 * RB * rowb;
           const uint8_t *sus = sgs + RB * G;
 #pragma unroll
-          for (int k = 0; k < RB / 2; k++) {
-            const int q = h + 2 * k;  // row within the stage
+          for (int k = 0; k < RP; k++) {
+            const int q = h + HP * k;  // row within the stage
             const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
             const uint4 wu = reinterpret_cast<const uint4 *>(st + (RB + q) * rowb)[g];
             const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
             if (sg != 255u)
-              vals[b2 * RB + 2 * k] =
+              vals[b2 * 2 * RP + 2 * k] =
                   (XF32 ? group_dot2(xr, xl, wg) : group_dot(xr, wg)) * group_factor(sg, xe);
             if (su != 255u)
-              vals[b2 * RB + 2 * k + 1] =
+              vals[b2 * 2 * RP + 2 * k + 1] =
                   (XF32 ? group_dot2(xr, xl, wu) : group_dot(xr, wu)) * group_factor(su, xe);
           }
         }
         __syncwarp();
         if (lane == 0 && !aborted) mbar_arrive(&empty[s]);
       }
-      // value v = b2*RB + 2k + m  ->  tile row b*RB + b2*RB + h + 2k, matrix m
+      // value v = b2*2*RP + 2k + m  ->  tile row (b + b2)*RB + h + HP*k, matrix m
       const float tot = warp_transpose_reduce<V>(vals);
       if (lane < V) {
-        const int b2 = lane / RB, k = (lane % RB) / 2, m = lane & 1;
-        rt[(warp * 32 + (b * RB + b2 * RB + h + 2 * k)) * 2 + m] = tot;
+        const int b2 = lane / (2 * RP), k = (lane % (2 * RP)) / 2, m = lane & 1;
+        rt[(warp * 32 + ((b + b2) * RB + h + HP * k)) * 2 + m] = tot;
       }
     }
     __syncwarp();
@@ -276,12 +278,15 @@ size_t gateup_t1_smem(int H, int E, int K, int RB, int NS) {
   return gu_ring_offset(E, K) + (size_t)NS * 2 * RB * (H / 2 + G);
 }
 
+int gateup_t1_phases(int H) { return H / kGroup <= 128 ? 4 : 2; }
+
 cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, bool pdl) {
   const int G = a.H / kGroup;
   const int C = ((G + 31) / 32) * 32;
+  const int HP = gateup_t1_phases(a.H);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(2 * C + 64);
+  cfg.blockDim = dim3(HP * C + 64);
   cfg.dynamicSmemBytes = gateup_t1_smem(a.H, a.E, a.K, a.RB, a.NS);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -289,14 +294,20 @@ cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, b
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.xf) {
-    if (a.RB == 4) return cudaLaunchKernelEx(&cfg, k_gateup_t1<4, true>, a);
-    if (a.RB == 8) return cudaLaunchKernelEx(&cfg, k_gateup_t1<8, true>, a);
-    return cudaLaunchKernelEx(&cfg, k_gateup_t1<16, true>, a);
+  if (a.RB != 8 && a.RB != 16) return cudaErrorInvalidValue;
+  const bool r8 = a.RB == 8;
+  if (HP == 4) {
+    if (a.xf)
+      return r8 ? cudaLaunchKernelEx(&cfg, k_gateup_t1<8, true, 4>, a)
+                : cudaLaunchKernelEx(&cfg, k_gateup_t1<16, true, 4>, a);
+    return r8 ? cudaLaunchKernelEx(&cfg, k_gateup_t1<8, false, 4>, a)
+              : cudaLaunchKernelEx(&cfg, k_gateup_t1<16, false, 4>, a);
   }
-  if (a.RB == 4) return cudaLaunchKernelEx(&cfg, k_gateup_t1<4, false>, a);
-  if (a.RB == 8) return cudaLaunchKernelEx(&cfg, k_gateup_t1<8, false>, a);
-  return cudaLaunchKernelEx(&cfg, k_gateup_t1<16, false>, a);
+  if (a.xf)
+    return r8 ? cudaLaunchKernelEx(&cfg, k_gateup_t1<8, true, 2>, a)
+              : cudaLaunchKernelEx(&cfg, k_gateup_t1<16, true, 2>, a);
+  return r8 ? cudaLaunchKernelEx(&cfg, k_gateup_t1<8, false, 2>, a)
+            : cudaLaunchKernelEx(&cfg, k_gateup_t1<16, false, 2>, a);
 }
 
 // ------------------------------------------------------------------------------------
@@ -571,12 +582,14 @@ cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool p
 
 cudaError_t set_decode_smem_limits() {
   const int big = 227 * 1024;
-  const void *fns[] = {reinterpret_cast<const void *>(k_gateup_t1<4, false>),
-                       reinterpret_cast<const void *>(k_gateup_t1<8, false>),
-                       reinterpret_cast<const void *>(k_gateup_t1<16, false>),
-                       reinterpret_cast<const void *>(k_gateup_t1<4, true>),
-                       reinterpret_cast<const void *>(k_gateup_t1<8, true>),
-                       reinterpret_cast<const void *>(k_gateup_t1<16, true>),
+  const void *fns[] = {reinterpret_cast<const void *>(k_gateup_t1<8, false, 2>),
+                       reinterpret_cast<const void *>(k_gateup_t1<16, false, 2>),
+                       reinterpret_cast<const void *>(k_gateup_t1<8, true, 2>),
+                       reinterpret_cast<const void *>(k_gateup_t1<16, true, 2>),
+                       reinterpret_cast<const void *>(k_gateup_t1<8, false, 4>),
+                       reinterpret_cast<const void *>(k_gateup_t1<16, false, 4>),
+                       reinterpret_cast<const void *>(k_gateup_t1<8, true, 4>),
+                       reinterpret_cast<const void *>(k_gateup_t1<16, true, 4>),
                        reinterpret_cast<const void *>(k_down_tma<true>),
                        reinterpret_cast<const void *>(k_down_tma<false>)};
   for (const void *f : fns) {

@@ -152,13 +152,18 @@ __global__ void k_rmsnorm_bf16(const float *__restrict__ h, int T, int n, float 
 // ---- LatentMoE pieces (k3moe_latent.cu)
 // out = W in (bf16 W [R][C], T input rows of C, bf16 or float); with W2 the shared gate/up
 // pair, SiTU applied; with y the layer output y (=|+=) addend + value (ydt), else float out.
+// norm (float input, no W2, T <= kProjRows): the input rows RMS-normalised with weight nw
+// on the fly, as launch_rmsnorm_f32w would write them.
+constexpr int kProjRows = 4;
 cudaError_t launch_proj(cudaStream_t st, int sms, const uint16_t *W, const uint16_t *W2, int R,
                         int C, const void *in, bool in_f32, int T, float *out,
                         const float *addend, void *y, int ydt, int accumulate, float b1,
-                        float b2);
-// RMSNorm of T float rows of n with weight w (nullptr: 1), sum of squares in double.
+                        float b2, bool pdl, bool norm = false, const float *nw = nullptr,
+                        float eps = 0.f);
+// RMSNorm of T float rows of n with weight w (nullptr: 1), sum of squares as a float-float
+// pair.
 cudaError_t launch_rmsnorm_f32w(cudaStream_t st, const float *in, int T, int n, const float *w,
-                                float eps, float *out);
+                                float eps, float *out, bool pdl);
 constexpr int kRmsThreads = 256;  // threads per row of k_rmsnorm_bf16
 constexpr int kRmsVec = 8;        // float4 per thread held in registers (rows up to 8192)
 

@@ -8,7 +8,11 @@
 //     gate and up rows together and applies SiTU.
 //   * k_rmsnorm_f32w: RMSNorm of the aggregated latent with its weight.
 // These are GEMVs for decode-sized batches: one warp streams one weight row with 16-byte
-// loads, several loads in flight per lane, so the kernels are bound by HBM.
+// loads, four in flight per lane and matrix (more in flight leaves the loads waiting on
+// the arithmetic: a standalone sweep of this row-per-warp pattern read 51 MB in 17.7 us at
+// four, 18.7 at eight and 22.8 at sixteen).  Launched as
+// programmatic dependents, each kernel asks for its first weight rows in L2 while the
+// kernel before it drains, and reads no activation before that kernel has completed.
 #include "k3moe_kernels.cuh"
 
 namespace k3 {
@@ -54,29 +58,118 @@ __device__ __forceinline__ float dot8_bf16(uint4 w, const float (&v)[8], float a
   return acc;
 }
 
+// Error-free sum of two floats: s + e == a + b exactly (Knuth's TwoSum, no contraction).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// 1 / sqrt(ss / n + eps) for the row x[0..n), ss its sum of squares (kimi-k3-in-c, section
+// 5, where the sum is accumulated in double).  Here the sum is a float-float pair: every
+// square is split exactly (product + its FMA residual), the thread's terms in index order,
+// then a butterfly per warp and the warps in order, so the result is the same on every run
+// and within a few float roundings of the double sum; the root is rounded once (__frsqrt_rn).
+// All threads of the block call it; the value is returned in thread 0.  red: 16 floats of
+// shared memory.
+__device__ float block_inv_rms(const float *x, int n, float eps, float *red) {
+  float hi = 0.f, lo = 0.f;
+  const int bd = blockDim.x;
+  for (int i0 = threadIdx.x; i0 < n; i0 += 8 * bd) {
+    float v[8];  // eight loads in flight; the missing tail adds exact zeros
+#pragma unroll
+    for (int k = 0; k < 8; k++) v[k] = i0 + k * bd < n ? x[i0 + k * bd] : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const float p = __fmul_rn(v[k], v[k]);
+      const float pe = fmaf(v[k], v[k], -p);
+      float s, e;
+      two_sum(hi, p, s, e);
+      hi = s;
+      lo = __fadd_rn(lo, __fadd_rn(e, pe));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // both partners add the same two pairs
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    float s, e;
+    two_sum(hi, oh, s, e);
+    hi = s;
+    lo = __fadd_rn(e, __fadd_rn(lo, ol));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[2 * (threadIdx.x >> 5)] = hi;
+    red[2 * (threadIdx.x >> 5) + 1] = lo;
+  }
+  __syncthreads();
+  float inv = 0.f;
+  if (threadIdx.x == 0) {
+    float th = 0.f, tl = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) {
+      float s, e;
+      two_sum(th, red[2 * w], s, e);
+      th = s;
+      tl = __fadd_rn(tl, __fadd_rn(e, red[2 * w + 1]));
+    }
+    const float ms = __fdiv_rn(__fadd_rn(th, tl), (float)n);
+    inv = __frsqrt_rn(__fadd_rn(ms, eps));
+  }
+  __syncthreads();  // red may be reused
+  return inv;
+}
+
 }  // namespace
 
-constexpr int kProjT = 4;   // token rows per pass over a weight row
-constexpr int kProjU = 4;   // 16-byte weight chunks in flight per lane
+constexpr int kProjT = kProjRows;  // token rows per pass over a weight row
+constexpr int kProjU = 4;  // 16-byte weight chunks in flight per lane and matrix
 
 // Rows r of W [R][C] (bf16, row-major) against T input rows in [T][C]:
 //   s[t][r] = sum_c W[r][c] in[t][c]           (fp32 products and sums; the lanes' parts
 //                                                reduced in a fixed butterfly, so results
 //                                                are the same on every run)
 // GU: W2 [R][C] is a second matrix and the output is SiTU(s, s2) (shared gate and up).
+// NORM (float input, T <= kProjT): the input rows are RMS-normalised first, in[t][c] ->
+// (in[t][c] * inv_t) * nw[c] (nw == nullptr: weight 1), inv_t computed by every block
+// from the whole row -- the same values k_rmsnorm_f32w writes.
 // Output: when y == nullptr, out[t][r] = value (float); else the final layer output
 // y[t][r] (=|+=) addend[t][r] + value, float or bf16 (round to nearest even).
-template <bool IN_F32, bool GU>
+template <bool IN_F32, bool GU, bool NORM>
 __global__ void __launch_bounds__(256) k_proj(const uint16_t *__restrict__ W,
                                               const uint16_t *__restrict__ W2, int R, int C,
                                               const void *__restrict__ in, int T,
                                               float *__restrict__ out,
                                               const float *__restrict__ addend, void *y, int ydt,
-                                              int accumulate, float b1, float b2) {
+                                              int accumulate, float b1, float b2,
+                                              const float *__restrict__ nw, float eps) {
+  __shared__ float s_red[16];
+  __shared__ float s_inv[kProjT];
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int nch = C >> 3;
-  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < R; r += gridDim.x * wpb) {
+  const int r_first = blockIdx.x * wpb + (threadIdx.x >> 5);
+  const int r_step = gridDim.x * wpb;
+  // each warp keeps its next row on its way to L2 while it reads the current one (weights
+  // only: nothing the previous kernel writes)
+  if (lane == 0 && r_first < R) {
+    bulk_prefetch_l2(W + (size_t)r_first * C, (uint32_t)C * 2);
+    if (GU) bulk_prefetch_l2(W2 + (size_t)r_first * C, (uint32_t)C * 2);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (NORM) {
+    for (int t = 0; t < T; t++) {
+      const float v = block_inv_rms(static_cast<const float *>(in) + (size_t)t * C, C, eps,
+                                    s_red);
+      if (threadIdx.x == 0) s_inv[t] = v;
+    }
+    __syncthreads();
+  }
+  for (int r = r_first; r < R; r += r_step) {
+    if (lane == 0 && r + r_step < R) {
+      bulk_prefetch_l2(W + (size_t)(r + r_step) * C, (uint32_t)C * 2);
+      if (GU) bulk_prefetch_l2(W2 + (size_t)(r + r_step) * C, (uint32_t)C * 2);
+    }
     const uint4 *w4 = reinterpret_cast<const uint4 *>(W + (size_t)r * C);
     const uint4 *u4 = GU ? reinterpret_cast<const uint4 *>(W2 + (size_t)r * C) : nullptr;
     for (int t0 = 0; t0 < T; t0 += kProjT) {
@@ -101,6 +194,16 @@ __global__ void __launch_bounds__(256) k_proj(const uint16_t *__restrict__ W,
             if (m < nt) {
               float v[8];
               load_in8<IN_F32>(in, C, t0 + m, c, v);
+              if (NORM) {
+                const float inv = s_inv[t0 + m];
+                float wn[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+                if (nw) load_in8<true>(nw, C, 0, c, wn);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                  const float q = __fmul_rn(v[j], inv);
+                  v[j] = nw ? __fmul_rn(q, wn[j]) : q;
+                }
+              }
               acc[m] = dot8_bf16(wv[k], v, acc[m]);
               if (GU) acc2[m] = dot8_bf16(uv[k], v, acc2[m]);
             }
@@ -144,30 +247,19 @@ __global__ void __launch_bounds__(256) k_proj(const uint16_t *__restrict__ W,
 }
 
 // out[t] = (in[t] * inv) * w (float, left to right; w == nullptr: weight 1) with
-// inv = (float)(1 / sqrt(ss / n + eps)), ss the row's sum of squares in double (kimi-k3-in-c,
-// section 5).  One block per row; the double partial sums are added in a fixed order.
-// in and out may be the same array.
+// inv = 1 / sqrt(ss / n + eps) from block_inv_rms (kimi-k3-in-c, section 5).  One block per
+// row; in and out may be the same array.
 __global__ void __launch_bounds__(256) k_rmsnorm_f32w(const float *in, int n,
                                                       const float *__restrict__ w, float eps,
                                                       float *out) {
-  __shared__ double red[8];
+  __shared__ float red[16];
   __shared__ float inv_s;
+  pdl_wait();
+  pdl_launch_dependents();
   const float *x = in + (size_t)blockIdx.x * n;
   float *o = out + (size_t)blockIdx.x * n;
-  double ss = 0.0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const double v = (double)x[i];
-    ss = fma(v, v, ss);
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double tot = 0.0;
-    for (int k = 0; k < (int)(blockDim.x >> 5); k++) tot += red[k];
-    inv_s = (float)(1.0 / sqrt(tot / (double)n + (double)eps));
-  }
+  const float v = block_inv_rms(x, n, eps, red);
+  if (threadIdx.x == 0) inv_s = v;
   __syncthreads();
   const float inv = inv_s;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -176,34 +268,50 @@ __global__ void __launch_bounds__(256) k_rmsnorm_f32w(const float *in, int n,
   }
 }
 
+namespace {
+
+cudaLaunchConfig_t proj_config(cudaStream_t st, int grid, int block, bool pdl,
+                               cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
 cudaError_t launch_proj(cudaStream_t st, int sms, const uint16_t *W, const uint16_t *W2, int R,
                         int C, const void *in, bool in_f32, int T, float *out,
                         const float *addend, void *y, int ydt, int accumulate, float b1,
-                        float b2) {
+                        float b2, bool pdl, bool norm, const float *nw, float eps) {
+  if (norm && (!in_f32 || W2 || T > kProjT)) return cudaErrorInvalidValue;
+  using Fn = void (*)(const uint16_t *, const uint16_t *, int, int, const void *, int, float *,
+                      const float *, void *, int, int, float, float, const float *, float);
+  const Fn fn = norm ? k_proj<true, false, true>
+                     : W2 ? (in_f32 ? k_proj<true, true, false> : k_proj<false, true, false>)
+                          : (in_f32 ? k_proj<true, false, false> : k_proj<false, false, false>);
+  // one wave of resident blocks, each warp taking every (grid x 8)-th row
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 256, 0) != cudaSuccess || occ < 1)
+    occ = 1;
   int grid = (R + 7) / 8;
-  if (grid > 16 * sms) grid = 16 * sms;
-  if (W2) {
-    if (in_f32)
-      k_proj<true, true><<<grid, 256, 0, st>>>(W, W2, R, C, in, T, out, addend, y, ydt,
-                                               accumulate, b1, b2);
-    else
-      k_proj<false, true><<<grid, 256, 0, st>>>(W, W2, R, C, in, T, out, addend, y, ydt,
-                                                accumulate, b1, b2);
-  } else {
-    if (in_f32)
-      k_proj<true, false><<<grid, 256, 0, st>>>(W, W2, R, C, in, T, out, addend, y, ydt,
-                                                accumulate, b1, b2);
-    else
-      k_proj<false, false><<<grid, 256, 0, st>>>(W, W2, R, C, in, T, out, addend, y, ydt,
-                                                 accumulate, b1, b2);
-  }
-  return cudaGetLastError();
+  if (grid > occ * sms) grid = occ * sms;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = proj_config(st, grid, 256, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, fn, W, W2, R, C, in, T, out, addend, y, ydt, accumulate, b1,
+                            b2, nw, eps);
 }
 
 cudaError_t launch_rmsnorm_f32w(cudaStream_t st, const float *in, int T, int n, const float *w,
-                                float eps, float *out) {
-  k_rmsnorm_f32w<<<T, 256, 0, st>>>(in, n, w, eps, out);
-  return cudaGetLastError();
+                                float eps, float *out, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = proj_config(st, T, 256, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_f32w, in, n, w, eps, out);
 }
 
 }  // namespace k3
