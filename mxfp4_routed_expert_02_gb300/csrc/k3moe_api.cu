@@ -535,8 +535,12 @@ WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
 
 // Token/pair tables of a tensor-core GEMM over K_bytes of K per row.
 void tc_k_split(long long k_bytes, TcGemmArgs &a) {
-  a.kchunks = (int)((k_bytes + 127) / 128);
-  a.ksteps_last = (int)((k_bytes - 128LL * (a.kchunks - 1) + 31) / 32);
+  a.kchunks = (int)((k_bytes + kTcChunk - 1) / kTcChunk);
+  a.ksteps_last = (int)((k_bytes - (long long)kTcChunk * (a.kchunks - 1) + 31) / 32);
+}
+// Bytes between terms of the quantised scales ([term][256-column group][row][8]).
+long long tc_sf_tstride(long long k_bytes, long long cstride) {
+  return (k_bytes + 127) / 128 * cstride;
 }
 
 // Expert FFN of Tc tokens on the tensor cores, given the route (idx, w [Tc][K]):
@@ -584,7 +588,7 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   const unsigned long long gu_strides[3] = {(unsigned long long)H / 2,
                                             (unsigned long long)(off[4] - off[0]),
                                             (unsigned long long)es};
-  const unsigned gu_box[4] = {128u, (unsigned)kTcRows, 2, 1};  // 128 bytes of K x 128 rows x both
+  const unsigned gu_box[4] = {(unsigned)kTcChunk, (unsigned)kTcRows, 2, 1};  // K chunk x 128 rows x both
   if (!tc_map(&mgu, rec + off[0], 4, gu_dims, gu_strides, gu_box) ||
       !tc_map3d(&md, rec + off[2], I / 2, H, E, I / 2, es, kTcRows) ||
       !tc_map3d(&mx, ws.xq, H / 2, P, kTcTermsX, H / 2, (unsigned long long)P * (H / 2), ntile,
@@ -612,7 +616,7 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     a.sf_rowb = H / kGroup;
     a.sfb = ws.xs;
     a.sfb_cstride = (long long)P * 8;
-    a.sfb_tstride = (long long)a.kchunks * a.sfb_cstride;
+    a.sfb_tstride = tc_sf_tstride(H / 2, a.sfb_cstride);
     a.out = ws.act;
     a.out_ld = I;
     a.a_pair = 1;
@@ -628,21 +632,36 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     k_quant_act<<<grid, 256, 0, st>>>(ws.act, P, I, ws.aq, ws.as);
   }
   {
+    // down: two consecutive 128-row tiles of W2 per item when H is a multiple of 256, so
+    // that they share one B stage (half the activation traffic per output row)
+    const bool pair = H % (2 * kTcRows) == 0;
     TcGemmArgs a = g;
-    a.mtiles = (H + kTcRows - 1) / kTcRows;
+    a.mtiles = pair ? H / (2 * kTcRows) : (H + kTcRows - 1) / kTcRows;
     a.M_rows = H;
     tc_k_split(I / 2, a);
     a.sfa[0] = rec + off[3];
-    a.sfa[1] = nullptr;
+    a.sfa[1] = pair ? rec + off[3] : nullptr;
     a.sfa_gstride = ex->expert_stride;
     a.sf_rowb = I / kGroup;
     a.sfb = ws.as;
     a.sfb_cstride = (long long)P * 8;
-    a.sfb_tstride = (long long)a.kchunks * a.sfb_cstride;
+    a.sfb_tstride = tc_sf_tstride(I / 2, a.sfb_cstride);
     a.out = ws.dpair;
     a.out_ld = H;
+    a.a_pair = pair ? 2 : 0;
+    CUtensorMap md2;
+    if (pair) {
+      const unsigned long long d_dims[4] = {(unsigned long long)I / 2, (unsigned long long)kTcRows,
+                                            (unsigned long long)H / kTcRows,
+                                            (unsigned long long)E};
+      const unsigned long long d_strides[3] = {(unsigned long long)I / 2,
+                                               (unsigned long long)kTcRows * (I / 2), es};
+      const unsigned d_box[4] = {(unsigned)kTcChunk, (unsigned)kTcRows, 2, 1};
+      if (!tc_map(&md2, rec + off[2], 4, d_dims, d_strides, d_box)) return K3MOE_ERR_CUDA;
+    }
     TraceScope ts(KID_TC_DOWN, st);
-    if (launch_tc_gemm(TcKind::kMxf4Down, a, md, md, ma, di->sms, st) != cudaSuccess)
+    if (launch_tc_gemm(pair ? TcKind::kMxf4DownPair : TcKind::kMxf4Down, a, pair ? md2 : md,
+                       pair ? md2 : md, ma, di->sms, st) != cudaSuccess)
       return K3MOE_ERR_CUDA;
   }
   if (SI > 0) {

@@ -16,13 +16,16 @@
 //         contribution") is written to tensor memory as 0, i.e. 2^-127.
 //   F16:  A and B bf16 (kind::f16, fp32 accumulate); B may be NT bf16 terms (hi + lo).
 // Epilogues: SITU (two A matrices, gate and up: act = SiTU(D_gate, D_up)) or STORE
-// (one A matrix: D as is); both write fp32 [B row][feature].
+// (D as is; with two A matrices they are two consecutive 128-row tiles of one matrix,
+// which then share every B stage); both write fp32 [B row][feature].
 //
-// Design: one CTA per SM (persistent), work item = (group, 128-row tile of A, tile of up
-// to 128 B rows).  Warp roles: 0-3 write the scale vectors of each stage into tensor
+// Design: one CTA per SM (persistent), work item = (group, 128- or 256-row tile of A, tile
+// of up to 128 B rows).  Warp roles: 0-3 write the scale vectors of each stage into tensor
 // memory (warp q owns TMEM lanes 32q..32q+31; A row m's scales sit in lane m, B's are
-// replicated in every lane quarter, column n / 32, lane n % 32), 4 issues TMA loads (128-byte swizzled
-// tiles of 128 rows x 128 bytes of K), 5 issues the MMAs (one thread), 6-13 drain the
+// replicated in every lane quarter, column n / 32, lane n % 32), 4 issues TMA loads
+// (swizzled tiles of 128 rows x kTcChunk bytes of K; 128-byte chunks: 64-byte ones would fit
+// twice as many stages but measured 1.6-1.7x slower, each row segment then being half a
+// 128-byte line), 5 issues the MMAs (one thread), 6-13 drain the
 // accumulator (two warps per lane quarter).  Shared-memory stages and the scale slots in
 // tensor memory are released together by tcgen05.commit on the stage's "empty" barrier.
 #include <cuda.h>
@@ -39,8 +42,11 @@ constexpr int kTcWarpTma = 4;
 constexpr int kTcWarpMma = 5;
 constexpr int kTcWarpEpi = 6;             // warps 6..13
 constexpr int kTcTile = kTcRows;          // A rows and B rows per tile
-constexpr int kTcChunkBytes = 128;        // K bytes per stage (one 128-byte swizzle atom)
-constexpr uint32_t kTcBox = kTcTile * kTcChunkBytes;  // bytes of one TMA box (16 KB)
+constexpr int kTcChunkBytes = kTcChunk;   // K bytes per stage (one swizzle atom)
+constexpr uint32_t kTcBox = kTcTile * kTcChunkBytes;  // bytes of one A box (16 KB)
+constexpr int kSfB = 2 * kTcSteps;        // scale bytes per row per stage (2 per K step)
+constexpr int kSfW = 4 * kTcSteps;        // TMEM columns of one operand's scales per stage
+static_assert(kTcChunkBytes == 64 || kTcChunkBytes == 128, "64- or 128-byte swizzle");
 constexpr int kTcTmemCols = 512;
 constexpr int kTcItemTable = 512;         // per-CTA work items kept in shared memory
 constexpr uint32_t kTcItemTableBytes = kTcItemTable * 16;
@@ -62,65 +68,15 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
-  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8 rows
-  d |= (uint64_t)1 << 46;            // descriptor version
-  d |= (uint64_t)2 << 61;            // 128-byte swizzle
-  return d;
-}
-
-__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
-      "[%5], p; }" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-      "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// The same, issued by one elected lane of a converged warp (the whole warp computes the
-// operands, so they stay warp-uniform).
-__device__ __forceinline__ void mma_mxf4_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %6, 0;\n"
-      "  @e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, "
-      "[%4], [%5], p; }" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_f16_el(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                           uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %4, 0;\n"
-      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// The MMAs below take a descriptor as its low word plus this constant high word (stride
-// 1024 bytes between 8-row groups, descriptor version 1, 128-byte swizzle); offsets within
-// shared memory change only the address field of the low word, which cannot carry out of it
-// below 256 KB.
-constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
-__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) {
+// Shared-memory matrix descriptors (K-major, swizzled: 8-row atoms of kTcChunkBytes-byte
+// rows).  The MMAs take a descriptor as its low word (start address >> 4; leading byte
+// offset 1, unused for swizzled K-major) plus this constant high word (stride byte offset
+// = one 8-row atom, descriptor version 1, swizzle mode 4 = 64 B or 2 = 128 B); offsets
+// within shared memory change only the address field of the low word, which cannot carry
+// out of it below 256 KB.  A K step inside the atom moves the start address by 32 bytes.
+constexpr uint32_t kDescHi = ((8u * kTcChunkBytes) >> 4) | (1u << 14) |
+                             ((kTcChunkBytes == 64 ? 4u : 2u) << 29);
+__device__ __forceinline__ uint32_t sw_desc_lo(uint32_t saddr) {
   return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
 }
 __device__ __forceinline__ void mma_mxf4_el_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t hi,
@@ -183,6 +139,20 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+// One operand's scale columns of a stage (x8 or x16 by the array's size).
+__device__ __forceinline__ void tmem_st_sf(uint32_t taddr, const uint32_t (&v)[8]) {
+  tmem_st_x8(taddr, v);
+}
+[[maybe_unused]] __device__ __forceinline__ void tmem_st_sf(uint32_t taddr,
+                                                            const uint32_t (&v)[16]) {
+  tmem_st_x16(taddr, v);
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -209,49 +179,28 @@ __device__ __forceinline__ void tmem_wait_ld2(uint32_t (&v)[16], uint32_t (&w)[1
                :
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&f)[16]) {
-  uint32_t v[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
-               :
-               : "memory");
+// The kSfB scale bytes of one row for K chunk c (groups kSfB*c ..), fewer at the row's end;
+// bytes past the row read 0.  Returned in .x (and .y for 8 bytes).
+__device__ __forceinline__ uint2 load_scales(const uint8_t *row, int G, int c) {
+  const int g0 = kSfB * c;
+  uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int j = 0; j < 16; j++) f[j] = __uint_as_float(v[j]);
+  for (int j = 0; j < kSfB; j++) {
+    const uint32_t b = (g0 + j < G) ? (uint32_t)__ldg(row + g0 + j) : 0u;
+    w[j >> 2] |= b << (8 * (j & 3));
+  }
+  return make_uint2(w[0], w[1]);
 }
-
-// Eight scale bytes of one row for K chunk c (groups 8c .. 8c+7), fewer at the row's end;
-// bytes past the row read 0.  Scale byte 255 becomes 0 when map255.
-__device__ __forceinline__ uint2 load_scales8(const uint8_t *row, int G, int c, bool map255) {
-  const int g0 = 8 * c;
-  uint32_t lo = 0, hi = 0;
-  if (g0 + 8 <= G && ((reinterpret_cast<uintptr_t>(row + g0) & 7) == 0)) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(row + g0));
-    lo = v.x;
-    hi = v.y;
-  } else {
-    for (int j = 0; j < 8; j++) {
-      const uint32_t b = (g0 + j < G) ? (uint32_t)__ldg(row + g0 + j) : 0u;
-      if (j < 4)
-        lo |= b << (8 * j);
-      else
-        hi |= b << (8 * (j - 4));
-    }
-  }
-  if (map255) {
-    lo &= ~__vcmpeq4(lo, 0xffffffffu);
-    hi &= ~__vcmpeq4(hi, 0xffffffffu);
-  }
-  return make_uint2(lo, hi);
+// kSfB staged scale bytes at p (kSfB-aligned) as a uint2 (.y = 0 for 4 bytes).
+__device__ __forceinline__ uint2 ld_staged_scales(const uint8_t *p) {
+  if (kSfB == 8) return *reinterpret_cast<const uint2 *>(p);
+  return make_uint2(*reinterpret_cast<const uint32_t *>(p), 0u);
+}
+__device__ __forceinline__ void st_staged_scales(uint8_t *p, uint2 v) {
+  if (kSfB == 8)
+    *reinterpret_cast<uint2 *>(p) = v;
+  else
+    *reinterpret_cast<uint32_t *>(p) = v.x;
 }
 // The two scale bytes of K step i (groups 2i, 2i+1 of the chunk), in bytes 0 and 1.
 __device__ __forceinline__ uint32_t step_scales(uint2 s, int i) {
@@ -298,9 +247,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
+// Copies kSfB bytes (both addresses kSfB-aligned).
+__device__ __forceinline__ void cp_async_sf(void *dst, const void *src) {
+  if (kSfB == 8)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
 }
 // Arrives on `bar` once every cp.async this thread issued so far has landed.
 __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
@@ -308,15 +262,15 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
                : "memory");
 }
 
-// Shared memory after the 1 KB header: NS data stages [A_0 .. A_{NA-1}: 128 rows x 128 B]
-// [B_0 .. B_{NT-1}: ntile rows x 128 B] (1 KB aligned), then NSF scale slots [A scales:
-// NA x 128 rows x 8 B][B scales: NT x ntile rows x 8 B].
+// Shared memory after the 1 KB header: NS data stages [A_0 .. A_{NA-1}: 128 rows x kTcChunk]
+// [B_0 .. B_{NT-1}: ntile rows x kTcChunk] (1 KB aligned), then NSF scale slots [A scales:
+// NA x 128 rows x kSfB][B scales: NT x ntile rows x kSfB].
 __host__ __device__ inline uint32_t tc_stage_bytes(int na, int nt, int ntile) {
   const uint32_t b = (uint32_t)na * kTcBox + (uint32_t)nt * ntile * kTcChunkBytes;
   return (b + 1023u) & ~1023u;
 }
 __host__ __device__ inline uint32_t tc_sf_bytes(int na, int nt, int ntile) {
-  return ((uint32_t)na * kTcTile * 8 + (uint32_t)nt * ntile * 8 + 15u) & ~15u;
+  return ((uint32_t)na * kTcTile * kSfB + (uint32_t)nt * ntile * kSfB + 15u) & ~15u;
 }
 
 // SiTU-GLU in the tensor-core epilogue: b1 tanh(g/b1) sigmoid(g) * b2 tanh(u/b2) with the
@@ -333,7 +287,7 @@ __device__ __forceinline__ float situ_fast(float g, float u, float b1, float ib1
 }
 
 // The MMAs of one stage, issued by a converged warp: NQ groups of B terms side by side, NA A
-// matrices, K steps 0 .. nk-1 of the stage's 128-byte chunk.  Everything but the stage's
+// matrices, K steps 0 .. nk-1 of the stage's chunk.  Everything but the stage's
 // descriptor low word, its scale-slot column, the accumulator columns and the first-chunk
 // flag is a compile-time offset, so the issuing warp spends few instructions per MMA (the
 // issue loop runs on the pipeline's critical path: commit, refill, landing, issue).
@@ -342,7 +296,7 @@ __device__ __forceinline__ void tc_issue_stage(uint32_t alo, uint32_t blo, uint3
                                                uint32_t slot, uint32_t dcol0, uint32_t dcol1,
                                                uint32_t idesc, bool first) {
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
+  for (int i = 0; i < kTcSteps; i++) {
     if (i < nk) {
 #pragma unroll
       for (int m = 0; m < NA; m++) {
@@ -353,8 +307,8 @@ __device__ __forceinline__ void tc_issue_stage(uint32_t alo, uint32_t blo, uint3
           const uint32_t b_lo = blo + (uint32_t)u * bstep + (uint32_t)(2 * i);
           const uint32_t acc = (i == 0 && u == 0 && first) ? 0u : 1u;
           if (KIND == 0)
-            mma_mxf4_el_lo(dcol, a_lo, b_lo, kDescHi, idesc, slot + 16 * (NQ + m) + 4 * i,
-                           slot + 16 * u + 4 * i, acc);
+            mma_mxf4_el_lo(dcol, a_lo, b_lo, kDescHi, idesc, slot + kSfW * (NQ + m) + 4 * i,
+                           slot + kSfW * u + 4 * i, acc);
           else
             mma_f16_el_lo(dcol, a_lo, b_lo, kDescHi, idesc, acc);
         }
@@ -391,13 +345,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int TG = a.tgroup, NQ = NT / TG;
   // TMEM columns per stage of scale vectors: B term groups first (16 columns each), then
   // the A matrices (16 each); multi-column accesses stay aligned to their width
-  const int kSfSlot = kScales ? 16 * (NQ + NA) : 0;
+  const int kSfSlot = kScales ? kSfW * (NQ + NA) : 0;
   const int NS = a.nstages, NSF = a.nsf, ntile = a.ntile;
   const int aw = TG * ntile;  // accumulator columns of one A matrix
   const uint32_t stage_bytes = tc_stage_bytes(NA, NT, ntile);
   const uint32_t tma_bytes = (uint32_t)NA * kTcBox + (uint32_t)NT * ntile * kTcChunkBytes;
   const uint32_t sf_bytes = tc_sf_bytes(NA, NT, ntile);
-  const uint32_t off_sfa = 0, off_sfb = (uint32_t)NA * kTcTile * 8;
+  const uint32_t off_sfa = 0, off_sfb = (uint32_t)NA * kTcTile * kSfB;
+  // output rows of an item: A matrices side by side (gate, up) share the item's 128 rows;
+  // in the row-pair mode matrix m holds rows 128 m .. of the item's 256
+  const int mrows = a.a_pair == 2 ? 2 * kTcTile : kTcTile;
+  const int moff = a.a_pair == 2 ? kTcTile : 0;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -464,7 +422,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // few large copies: a stage costs the TMA unit about the same whether it moves 4 KB
         // or 32 KB, so both A matrices come in one 4-D box where their layout allows, and
         // all NT terms of B in one box of depth NT
-        if (NA > 1 && a.a_pair) {
+        if (NA > 1 && a.a_pair == 2) {
+          tma_load4d(st, &tmA0, c * kTcChunkBytes, 0, 2 * ti.mt, ga, &full[s]);
+        } else if (NA > 1 && a.a_pair) {
           tma_load4d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, 0, ga, &full[s]);
         } else {
           tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
@@ -481,7 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the stage's TMEM slot is free.
     if (kScales) {
       const int q = warp;
-      const bool g8 = (G % 8) == 0;
+      const bool gal = (G % kSfB) == 0;  // a row's chunk bytes are kSfB-aligned
       const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
       int ld = 0, stn = 0;
       while (stn < total && !*abort_flag) {
@@ -494,27 +454,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int k = ld % NSF;
           uint8_t *sfs = sfring + (size_t)k * sf_bytes;
           const int r = 32 * q + lane;  // this thread's A row and B row in the tile
-          const int row = ti.mt * kTcTile + r;
 #pragma unroll
           for (int m = 0; m < NA; m++) {
-            uint8_t *dst = sfs + off_sfa + (m * kTcTile + r) * 8;
+            const int row = ti.mt * mrows + m * moff + r;
+            uint8_t *dst = sfs + off_sfa + (m * kTcTile + r) * kSfB;
             const uint8_t *src = a.sfa[m] + (long long)ga * a.sfa_gstride + (long long)row * G;
-            if (row < a.M_rows && g8 && 8 * c + 8 <= G) {
-              cp_async8(dst, src + 8 * c);
+            if (row < a.M_rows && gal && kSfB * c + kSfB <= G) {
+              cp_async_sf(dst, src + kSfB * c);
             } else {
-              const uint2 v = row < a.M_rows ? load_scales8(src, G, c, false) : make_uint2(0u, 0u);
-              *reinterpret_cast<uint2 *>(dst) = v;
+              const uint2 v = row < a.M_rows ? load_scales(src, G, c) : make_uint2(0u, 0u);
+              st_staged_scales(dst, v);
             }
           }
           if (r < ntile) {
+            // B scales are stored 8 per row per 256-column K group: this chunk's kSfB of them
+            const long long boff = (long long)(c / (8 / kSfB)) * a.sfb_cstride +
+                                   (long long)(ti.brow0 + r) * 8 + (c % (8 / kSfB)) * kSfB;
 #pragma unroll
             for (int t = 0; t < NT; t++) {
-              uint8_t *dst = sfs + off_sfb + (t * ntile + r) * 8;
+              uint8_t *dst = sfs + off_sfb + (t * ntile + r) * kSfB;
               if (r < ti.nvalid)
-                cp_async8(dst, a.sfb + (long long)t * a.sfb_tstride +
-                                   (long long)c * a.sfb_cstride + (long long)(ti.brow0 + r) * 8);
+                cp_async_sf(dst, a.sfb + (long long)t * a.sfb_tstride + boff);
               else
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
+                st_staged_scales(dst, make_uint2(0u, 0u));
             }
           }
           cp_async_arrive(&sfload[k]);
@@ -535,34 +497,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint8_t *sfs = sfring + (size_t)k * sf_bytes;
         const uint32_t slot = tmem + sf_col0 + (uint32_t)(sj * kSfSlot);
-        // A: K step i of matrix m reads column slot + 16(NQ + m) + 4i + (row / 32);
+        // A: K step i of matrix m reads column slot + kSfW(NQ + m) + 4i + (row / 32);
         // scale byte 255 (no contribution) becomes 0
 #pragma unroll
         for (int m = 0; m < NA; m++) {
-          uint2 v = *reinterpret_cast<const uint2 *>(sfs + off_sfa + (m * kTcTile + 32 * q + lane) * 8);
+          uint2 v = ld_staged_scales(sfs + off_sfa + (m * kTcTile + 32 * q + lane) * kSfB);
           v.x &= ~__vcmpeq4(v.x, 0xffffffffu);
           v.y &= ~__vcmpeq4(v.y, 0xffffffffu);
 #pragma unroll
-          for (int i = 0; i < 4; i++)
-            tmem_st_x1(slot + lane_sel + 16 * (NQ + m) + 4 * i + q, step_scales(v, i));
+          for (int i = 0; i < kTcSteps; i++)
+            tmem_st_x1(slot + lane_sel + kSfW * (NQ + m) + 4 * i + q, step_scales(v, i));
         }
-        // B: K step i of term group u reads column slot + 16u + 4i + n/32 at lane n % 32
+        // B: K step i of term group u reads column slot + kSfW u + 4i + n/32 at lane n % 32
         // of every lane quarter (each 32-row quarter of the MMA reads its own copy), for
         // the group's rows n = 0 .. aw-1 (term u*TG + n / ntile, row n % ntile; those are
         // consecutive in the staged scale bytes)
 #pragma unroll
         for (int u = 0; u < NT; u++) {
           if (u < NQ) {
-            uint32_t vb[16];
+            uint32_t vb[kSfW];
 #pragma unroll
             for (int jj = 0; jj < 4; jj++) {
               const int n = 32 * jj + lane;
-              const uint2 v = (n < aw) ? *reinterpret_cast<const uint2 *>(sfs + off_sfb + (u * aw + n) * 8)
+              const uint2 v = (n < aw) ? ld_staged_scales(sfs + off_sfb + (u * aw + n) * kSfB)
                                        : make_uint2(0u, 0u);
 #pragma unroll
-              for (int i = 0; i < 4; i++) vb[4 * i + jj] = step_scales(v, i);
+              for (int i = 0; i < kTcSteps; i++) vb[4 * i + jj] = step_scales(v, i);
             }
-            tmem_st_x16(slot + lane_sel + 16 * u, vb);
+            tmem_st_sf(slot + lane_sel + kSfW * u, vb);
           }
         }
         tmem_wait_st();
@@ -624,10 +586,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           {
-            const uint32_t alo = sw128_desc_lo(smem_u32(stages + (size_t)s * stage_bytes));
+            const uint32_t alo = sw_desc_lo(smem_u32(stages + (size_t)s * stage_bytes));
             const uint32_t blo = alo + ((uint32_t)(NA * kTcBox) >> 4);
             const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
-            const int nk = (c == a.kchunks - 1) ? a.ksteps_last : 4;
+            const int nk = (c == a.kchunks - 1) ? a.ksteps_last : kTcSteps;
             if (NQ == 1)
               tc_issue_stage<KIND, NA, 1>(alo, blo, bstep, nk, slot, dcol0, dcol1, idesc, c == 0);
             else if (NQ == 2)
@@ -663,7 +625,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *abort_flag = 1;
       }
       tc_fence_after();
-      const int row = ti.mt * kTcTile + 32 * q + lane;
+      const int row = ti.mt * mrows + 32 * q + lane;
       const uint32_t lane_sel = (uint32_t)(32 * q) << 16;
       if (got && !*abort_flag) {
         const uint32_t dbase = tmem + lane_sel + (uint32_t)(db * NA * aw);
@@ -695,6 +657,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 orow[(long long)j * a.out_ld] = v;
               }
             }
+          }
+          if (EPI == 1 && NA > 1 && row + moff < a.M_rows) {  // row-pair mode: second half
+            float *orow = a.out + (long long)(ti.brow0 + c0) * a.out_ld + row + moff;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+              if (c0 + j < ti.nvalid) orow[(long long)j * a.out_ld] = __uint_as_float(d1[j]);
           }
         }
       }
@@ -753,7 +721,8 @@ bool tc_map(CUtensorMap *m, const void *base, int rank, const unsigned long long
     }
   }
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void *>(base), d, st,
-            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            kTcChunkBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -773,25 +742,32 @@ bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
 static void tc_depths(int na, int nt, int ntile, int tg, bool scales, int *ns, int *nsf) {
   const size_t budget = 227 * 1024 - 2048 - kTcItemTableBytes;
   const size_t stage = tc_stage_bytes(na, nt, ntile), sfb = scales ? tc_sf_bytes(na, nt, ntile) : 0;
-  int f = scales ? 8 : 0;
-  int s = 0;
-  for (;; f = f > 2 ? f - 2 : 0) {
-    s = (int)((budget - f * sfb) / stage);
-    if (s >= 2 || f == 0) break;
-  }
+  int by_tmem = 8;
   if (scales) {
     const int free_cols = kTcTmemCols - ((na * tg * ntile + 15) & ~15);
-    const int by_tmem = free_cols / (16 * (na + nt / tg));
-    if (s > by_tmem) s = by_tmem;
+    by_tmem = free_cols / (kSfW * (na + nt / tg));
   }
-  *ns = s > 8 ? 8 : s;
-  *nsf = f;
+  // the most data stages (at most 8, and what TMEM holds), then the most scale slots
+  int best_s = -1, best_f = 0;
+  for (int f = scales ? 8 : 0; f >= (scales ? 2 : 0); f -= 2) {
+    if ((size_t)f * sfb >= budget) continue;
+    int s = (int)((budget - f * sfb) / stage);
+    if (s > 8) s = 8;
+    if (s > by_tmem) s = by_tmem;
+    if (s > best_s) {
+      best_s = s;
+      best_f = f;
+    }
+    if (!scales) break;
+  }
+  *ns = best_s < 0 ? 0 : best_s;
+  *nsf = best_f;
 }
 
 // Accumulator buffers: two (the epilogue of one item overlaps the next item's MMAs) when
 // they fit in TMEM next to the scale slots, else one.
 static int tc_nacc(int na, int nt, int ntile, int tg, bool scales, int ns) {
-  const int sf = scales ? ns * 16 * (na + nt / tg) : 0;
+  const int sf = scales ? ns * kSfW * (na + nt / tg) : 0;
   return (((2 * na * tg * ntile + 15) & ~15) + sf <= kTcTmemCols) ? 2 : 1;
 }
 
@@ -840,6 +816,7 @@ cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &
   switch (kind) {
     case TcKind::kMxf4GateUp: return launch_tc<0, 2, kTcTermsX, 0>(a, A0, A1, B, grid, st);
     case TcKind::kMxf4Down: return launch_tc<0, 1, kTcTermsAct, 1>(a, A0, A1, B, grid, st);
+    case TcKind::kMxf4DownPair: return launch_tc<0, 2, kTcTermsAct, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16GateUp: return launch_tc<1, 2, 1, 0>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Down: return launch_tc<1, 1, 2, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Store: return launch_tc<1, 1, 1, 1>(a, A0, A1, B, grid, st);

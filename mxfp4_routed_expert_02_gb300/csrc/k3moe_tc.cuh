@@ -8,6 +8,8 @@
 namespace k3 {
 
 constexpr int kTcRows = 128;     // A rows / B rows per tensor-core tile
+constexpr int kTcChunk = 128;    // K bytes per pipeline stage (one swizzle atom: 128 or 64)
+constexpr int kTcSteps = kTcChunk / 32;  // MMA K steps (32 bytes of K each) per stage
 constexpr int kTcTermsX = 4;     // MXFP4 terms of the layer input x (bf16)
 constexpr int kTcTermsAct = 4;   // MXFP4 terms of the SiTU activations (float)
 constexpr int kTcTokens = 4096;  // tokens per pass of the multi-token path
@@ -20,8 +22,8 @@ struct TcGemmArgs {
   int ngroups;
   int mtiles;        // ceil(M_rows / 128)
   int M_rows;        // rows of each A matrix (outputs)
-  int kchunks;       // 128-byte chunks of K
-  int ksteps_last;   // 32-byte MMA steps in the last chunk (1..4)
+  int kchunks;       // kTcChunk-byte chunks of K
+  int ksteps_last;   // 32-byte MMA steps in the last chunk (1..kTcSteps)
   int ntile;         // B rows per tile (multiple of 16, at most 128)
   int nstages;       // data stages, set by the launcher
   int nsf;           // scale-byte slots, set by the launcher
@@ -29,27 +31,30 @@ struct TcGemmArgs {
   int tgroup;        // B terms side by side in one MMA (divides the term count), set by
                      // the launcher
   int a_pair;        // 1: A matrices 0 and 1 are one 4-D map (third dimension = matrix),
-                     // fetched by one copy per stage
+                     // fetched by one copy per stage; 2: they are two consecutive 128-row
+                     // tiles of ONE matrix (4-D map: K bytes, 128 rows, tile, group), so an
+                     // item's M tile covers 256 output rows and both halves share the B
+                     // stage
   const uint8_t *sfa[2];   // MXF4: scale bytes of A matrix m for group 0, rows of sf_rowb
   long long sfa_gstride;   // bytes between consecutive groups' A scales
   int sf_rowb;             // scale bytes per row (K / 32)
-  const uint8_t *sfb;      // MXF4: B scale bytes [term][K chunk][B row][8]
+  const uint8_t *sfb;      // MXF4: B scale bytes [term][256-column K group][B row][8]
   long long sfb_tstride;   // bytes between terms
-  long long sfb_cstride;   // bytes between K chunks (B rows x 8)
+  long long sfb_cstride;   // bytes between 256-column K groups (B rows x 8)
   float *out;              // [B row][out_ld]
   long long out_ld;
   float b1, b2;            // SiTU caps (gate/up epilogue)
   int32_t *status;
 };
 
-enum class TcKind { kMxf4GateUp, kMxf4Down, kBf16GateUp, kBf16Down, kBf16Store };
+enum class TcKind { kMxf4GateUp, kMxf4Down, kMxf4DownPair, kBf16GateUp, kBf16Down, kBf16Store };
 
 // Tensor map of bytes of rank 3..5 (dims[0] = K bytes, innermost; strides in bytes of
-// dims 1..rank-1) with 128-byte swizzle and boxes of box[0] = 128 bytes x box[1..]; false if
-// the driver entry point is missing or the layout is refused.
+// dims 1..rank-1) with the kTcChunk-byte swizzle and boxes of box[0] = kTcChunk bytes x
+// box[1..]; false if the driver entry point is missing or the layout is refused.
 bool tc_map(CUtensorMap *m, const void *base, int rank, const unsigned long long *dims,
             const unsigned long long *strides, const unsigned *box);
-// The 3-D case (inner = K bytes, rows, depth) with boxes of 128 bytes x box_rows x
+// The 3-D case (inner = K bytes, rows, depth) with boxes of kTcChunk bytes x box_rows x
 // box_depth.
 bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
               unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
