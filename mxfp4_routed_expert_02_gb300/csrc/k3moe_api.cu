@@ -559,10 +559,10 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
   const uint8_t *rec = ex->experts;
   const unsigned long long es = (unsigned long long)ex->expert_stride;
   // B rows per tile: 1.25 x the mean number of pairs per expert, rounded up to 16, at
-  // least 32 and at most 128 (few experts then need a second tile)
+  // most 128 (few experts then need a second tile)
   const int used = P < E ? P : E;
   int ntile = ((((5 * P + 4 * used - 1) / (4 * used)) + 15) / 16) * 16;
-  ntile = ntile < 32 ? 32 : (ntile > kTcRows ? kTcRows : ntile);
+  ntile = ntile > kTcRows ? kTcRows : ntile;
   {
     TraceScope ts(KID_ROUTE_HIST, st);
     k_route_hist<<<1, 1024, (size_t)E * 4, st>>>(idx, P, E, ntile, ws.off, ws.tile_off, ws.inv,
