@@ -546,11 +546,12 @@ long long tc_sf_tstride(long long k_bytes, long long cstride) {
 // Expert FFN of Tc tokens on the tensor cores, given the route (idx, w [Tc][K]):
 // dispatch, x encoding, gate/up + SiTU, activation encoding, down, then (with the shared
 // expert when sh_gate != NULL) the router-order combine into y.
-k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x, int Tc,
                         const k3moe_experts *ex, const int32_t *idx, const float *w,
                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
                         WsTc &ws, void *y, k3moe_dtype ydt, int accumulate, int32_t *status,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool x_f32 = false) {
+  if (x_f32 && sh_gate) return K3MOE_ERR_ARG;  // the shared GEMMs take bf16 x
   const int H = d->hidden, I = d->inter, E = d->n_experts, K = d->topk;
   const int SI = sh_gate ? d->shared_inter : 0;
   const int P = Tc * K;
@@ -577,7 +578,8 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_
     const long long n = (long long)Tc * (H / kGroup);
     int grid = (int)((n + 255) / 256);
     if (grid > 16 * di->sms) grid = 16 * di->sms;
-    k_quant_x<<<grid, 256, 0, st>>>(x, Tc, H, K, ws.inv, P, ws.xq, ws.xs);
+    if (launch_quant_x(x_f32, grid, st, x, Tc, H, K, ws.inv, P, ws.xq, ws.xs) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
   }
   if (launch_status() != K3MOE_OK) return K3MOE_ERR_CUDA;
   // gate and up packed matrices of every expert as one 4-D map (K bytes, rows, matrix,
@@ -785,10 +787,15 @@ k3moe_status latent_dims(const k3moe_latent_dims *d, k3moe_dims *full, k3moe_dim
 
 // Workspace of one pass of up to kDecodeTokens tokens: the router's part, the experts'
 // part, then z [Tc][L], the latent sum [Tc][L], the up-projection [Tc][H] and the shared
-// activations [Tc][SI] (float).
+// activations [Tc][SI] (float); for passes of two tokens or more at a latent shape the
+// grouped GEMMs take, the tensor-core experts' part after them.
 struct WsLatent {
   Ws route, ffn;
   float *z, *accl, *up, *act_s;
+  bool has_tc;
+  WsTc tc;
+  uint16_t *hs;  // [2][Tc][max(L, SI)] bf16 hi / lo terms of a float GEMM input
+  float *ds;     // [Tc][H] shared experts' output
   size_t total;
 };
 
@@ -810,8 +817,49 @@ WsLatent ws_latent_layout(const k3moe_dims *full, const k3moe_dims *lat, int T, 
   w.accl = take((size_t)Tc * L * 4);
   w.up = take((size_t)Tc * H * 4);
   w.act_s = take((size_t)Tc * (SI > 0 ? SI : 1) * 4);
+  w.has_tc = use_tc(lat, Tc) && use_tc(full, Tc);
+  if (w.has_tc) {
+    w.tc = ws_tc_layout(lat, Tc, reinterpret_cast<void *>(b + o));
+    o += up16(w.tc.total);
+    const size_t C = L > SI ? L : SI;
+    w.hs = reinterpret_cast<uint16_t *>(take((size_t)2 * Tc * C * 2));
+    w.ds = take((size_t)Tc * H * 4);
+  }
   w.total = o;
   return w;
+}
+
+// out[t][r] (float, row length R) = sum_c A0[r][c] B[t][c] on the tensor cores for a bf16
+// matrix A0 [R][C] and B given as nb bf16 terms [nb][Tc][C] (their products summed); with A1
+// (the same shape) the output is SiTU(A0 B, A1 B).  g carries the one-group table of the Tc
+// rows (k_group1), the SiTU caps and the status word.
+k3moe_status tc_bf16_gemm(const DeviceInfo *di, TcKind kind, const uint16_t *A0,
+                          const uint16_t *A1, int R, int C, const uint16_t *B, int nb, int Tc,
+                          float *out, const TcGemmArgs &g, cudaStream_t st) {
+  CUtensorMap ma0, ma1, mb;
+  const unsigned long long rb = 2ull * C;
+  if (!tc_map3d(&ma0, A0, rb, R, 1, rb, rb * R, kTcRows) ||
+      (A1 && !tc_map3d(&ma1, A1, rb, R, 1, rb, rb * R, kTcRows)) ||
+      !tc_map3d(&mb, B, rb, Tc, nb, rb, rb * Tc, g.ntile, nb))
+    return K3MOE_ERR_CUDA;
+  TcGemmArgs a = g;
+  a.mtiles = (R + kTcRows - 1) / kTcRows;
+  a.M_rows = R;
+  tc_k_split((long long)rb, a);
+  a.out = out;
+  a.out_ld = R;
+  return launch_tc_gemm(kind, a, ma0, A1 ? ma1 : ma0, mb, di->sms, st) == cudaSuccess
+             ? K3MOE_OK
+             : K3MOE_ERR_CUDA;
+}
+
+k3moe_status launch_split(const DeviceInfo *di, const float *v, long long n, uint16_t *out,
+                          cudaStream_t st) {
+  TraceScope ts(KID_SPLIT, st);
+  int grid = (int)((n + 255) / 256);
+  if (grid > 16 * di->sms) grid = 16 * di->sms;
+  k_split_bf16<<<grid, 256, 0, st>>>(v, n, out);
+  return launch_status();
 }
 
 }  // namespace
@@ -1122,8 +1170,28 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
     s = run_route(di, &full, xc, Tc, lw->wr_bf16, lw->bias, nullptr, nullptr, ws.route, idx_c,
                   w_c, status_dev, st, rb == 0);
     if (s != K3MOE_OK) return s;
+    // more tokens than one pass of the GEMV kernels takes: the four bf16 projections as
+    // GEMMs on the tensor cores (one group of Tc rows)
+    const bool proj_tc = ws.has_tc && Tc > kProjRows;
+    TcGemmArgs g1{};
+    if (proj_tc) {
+      k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, ws.tc.off1, ws.tc.tile_off1);
+      g1.off = ws.tc.off1;
+      g1.tile_off = ws.tc.tile_off1;
+      g1.gid = nullptr;
+      g1.ngroups = 1;
+      g1.ntile = kTcRows;
+      g1.b1 = b1;
+      g1.b2 = b2;
+      g1.status = status_dev;
+    }
     // 2. z = Wdn x
-    {
+    if (proj_tc) {
+      TraceScope ts(KID_PROJ, st);
+      s = tc_bf16_gemm(di, TcKind::kBf16Store, lw->w_down, nullptr, L, H, xc, 1, Tc, ws.z, g1,
+                       st);
+      if (s != K3MOE_OK) return s;
+    } else {
       TraceScope ts(KID_PROJ, st);
       if (launch_proj(st, di->sms, lw->w_down, nullptr, L, H, xc, false, Tc, ws.z, nullptr,
                       nullptr, 0, 0, b1, b2, !g_trace.on) != cudaSuccess)
@@ -1151,6 +1219,11 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
       }
       s = run_down(di, &lat, 1, ea, idx_c, w_c, nullptr, ws.ffn, ws.accl, K3MOE_F32, 0,
                    status_dev, st, !g_trace.on);
+    } else if (ws.has_tc && Tc >= 2) {
+      // two tokens or more: the grouped GEMMs on the tensor cores, z encoded as four
+      // MXFP4 terms like the direct layer's x
+      s = run_ffn_tc(di, &lat, ws.z, Tc, &lw->experts, idx_c, w_c, nullptr, nullptr, nullptr,
+                     ws.tc, ws.accl, K3MOE_F32, 0, status_dev, st, true);
     } else {
       s = run_ffn(di, &lat, ws.z, Tc, &lw->experts, idx_c, w_c, nullptr, ws.ffn, ws.accl,
                   K3MOE_F32, 0, status_dev, st, true);
@@ -1164,6 +1237,37 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
       if (launch_rmsnorm_f32w(st, ws.accl, Tc, L, lw->latent_norm_w, dims->rms_eps, ws.accl,
                               !g_trace.on) != cudaSuccess)
         return K3MOE_ERR_CUDA;
+    }
+    if (proj_tc) {
+      // 5-6 on the tensor cores: up = Wup accL (accL as bf16 hi + lo), the shared experts'
+      // SiTU(Wg x, Wu x) and its down projection (hi + lo), then y (=|+=) up + shared
+      s = launch_split(di, ws.accl, (long long)Tc * L, ws.hs, st);
+      if (s != K3MOE_OK) return s;
+      {
+        TraceScope ts(KID_PROJ_UP, st);
+        s = tc_bf16_gemm(di, TcKind::kBf16Down, lw->w_up, nullptr, H, L, ws.hs, 2, Tc, ws.up,
+                         g1, st);
+        if (s != K3MOE_OK) return s;
+      }
+      if (shared) {
+        {
+          TraceScope ts(KID_SHARED_GATEUP, st);
+          s = tc_bf16_gemm(di, TcKind::kBf16GateUp, lw->sh_gate, lw->sh_up, SI, H, xc, 1, Tc,
+                           ws.act_s, g1, st);
+          if (s != K3MOE_OK) return s;
+        }
+        s = launch_split(di, ws.act_s, (long long)Tc * SI, ws.hs, st);
+        if (s != K3MOE_OK) return s;
+        TraceScope ts(KID_PROJ_SHARED_DOWN, st);
+        s = tc_bf16_gemm(di, TcKind::kBf16Down, lw->sh_down, nullptr, H, SI, ws.hs, 2, Tc,
+                         ws.ds, g1, st);
+        if (s != K3MOE_OK) return s;
+      }
+      TraceScope ts(KID_COMBINE, st);
+      if (launch_add_out(st, di->sms, ws.up, shared ? ws.ds : nullptr, yc, (int)ydt, accumulate,
+                         (long long)Tc * H) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+      continue;
     }
     // 5. up = Wup accL (straight into y when there is no shared expert)
     {

@@ -160,6 +160,9 @@ cudaError_t launch_proj(cudaStream_t st, int sms, const uint16_t *W, const uint1
                         const float *addend, void *y, int ydt, int accumulate, float b1,
                         float b2, bool pdl, bool norm = false, const float *nw = nullptr,
                         float eps = 0.f);
+// y (=|+=) up + ds elementwise over n values (ds may be nullptr), float or bf16 y.
+cudaError_t launch_add_out(cudaStream_t st, int sms, const float *up, const float *ds, void *y,
+                           int ydt, int accumulate, long long n);
 // RMSNorm of T float rows of n with weight w (nullptr: 1), sum of squares as a float-float
 // pair.
 cudaError_t launch_rmsnorm_f32w(cudaStream_t st, const float *in, int T, int n, const float *w,

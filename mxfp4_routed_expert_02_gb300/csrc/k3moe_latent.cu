@@ -268,6 +268,24 @@ __global__ void __launch_bounds__(256) k_rmsnorm_f32w(const float *in, int n,
   }
 }
 
+// y[i] (=|+=) up[i] + ds[i] (ds == nullptr: up[i]), float or bf16 (round to nearest even):
+// the layer output of a pass whose projections ran on the tensor cores.
+__global__ void __launch_bounds__(256) k_add_out(const float *__restrict__ up,
+                                                 const float *__restrict__ ds, void *y, int ydt,
+                                                 int accumulate, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float s = ds ? __fadd_rn(up[i], ds[i]) : up[i];
+    if (ydt == K3MOE_F32) {
+      float *yf = static_cast<float *>(y);
+      yf[i] = accumulate ? __fadd_rn(yf[i], s) : s;
+    } else {
+      uint16_t *yb = static_cast<uint16_t *>(y);
+      yb[i] = f32_to_bf16(accumulate ? __fadd_rn(bf16_lo(yb[i]), s) : s);
+    }
+  }
+}
+
 namespace {
 
 cudaLaunchConfig_t proj_config(cudaStream_t st, int grid, int block, bool pdl,
@@ -312,6 +330,14 @@ cudaError_t launch_rmsnorm_f32w(cudaStream_t st, const float *in, int T, int n, 
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = proj_config(st, T, 256, pdl, attr);
   return cudaLaunchKernelEx(&cfg, k_rmsnorm_f32w, in, n, w, eps, out);
+}
+
+cudaError_t launch_add_out(cudaStream_t st, int sms, const float *up, const float *ds, void *y,
+                           int ydt, int accumulate, long long n) {
+  long long g = (n + 255) / 256;
+  if (g > 8LL * sms) g = 8LL * sms;
+  k_add_out<<<(int)g, 256, 0, st>>>(up, ds, y, ydt, accumulate, n);
+  return cudaGetLastError();
 }
 
 }  // namespace k3

@@ -149,11 +149,12 @@ __device__ __forceinline__ void encode_terms(float (&r)[32], uint4 (&q)[NT], uin
   }
 }
 
-// x [T][H] bf16 -> the kTcTermsX-term encoding of every (token, slot) pair's row, written
-// at the pair's sorted position: xq [term][P][H/2] and the scale bytes xs [term][K chunk]
-// [P][8] (chunk = 8 groups, the block-scaled GEMM's stage).  One thread per (token,
+// x [T][H] bf16 (or float: XF32, the LatentMoE's latent) -> the kTcTermsX-term encoding of
+// every (token, slot) pair's row, written at the pair's sorted position: xq [term][P][H/2]
+// and the scale bytes xs [term][K chunk][P][8] (chunk = 8 groups).  One thread per (token,
 // group); the token's K slots receive the same bytes.
-__global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
+template <bool XF32>
+__global__ void k_quant_x(const void *__restrict__ xv, int T, int H, int K,
                           const int32_t *__restrict__ inv, int P, uint8_t *__restrict__ xq,
                           uint8_t *__restrict__ xs) {
   const int G = H / kGroup;
@@ -161,16 +162,30 @@ __global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(i / G), g = (int)(i % G);
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H + g * kGroup);
     float r[32];
+    if (XF32) {
+      const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(xv) +
+                                                           (size_t)t * H + g * kGroup);
 #pragma unroll
-    for (int c = 0; c < 4; c++) {
-      const uint4 v = __ldg(src + c);
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      for (int c = 0; c < 8; c++) {
+        const float4 v = __ldg(src + c);
+        r[4 * c] = v.x;
+        r[4 * c + 1] = v.y;
+        r[4 * c + 2] = v.z;
+        r[4 * c + 3] = v.w;
+      }
+    } else {
+      const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(xv) +
+                                                         (size_t)t * H + g * kGroup);
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        r[8 * c + 2 * k] = bf16_lo(w4[k]);
-        r[8 * c + 2 * k + 1] = bf16_hi(w4[k]);
+      for (int c = 0; c < 4; c++) {
+        const uint4 v = __ldg(src + c);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          r[8 * c + 2 * k] = bf16_lo(w4[k]);
+          r[8 * c + 2 * k + 1] = bf16_hi(w4[k]);
+        }
       }
     }
     uint4 q[kTcTermsX];
@@ -186,6 +201,15 @@ __global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
       }
     }
   }
+}
+
+cudaError_t launch_quant_x(bool x_f32, int grid, cudaStream_t st, const void *x, int T, int H,
+                           int K, const int32_t *inv, int P, uint8_t *xq, uint8_t *xs) {
+  if (x_f32)
+    k_quant_x<true><<<grid, 256, 0, st>>>(x, T, H, K, inv, P, xq, xs);
+  else
+    k_quant_x<false><<<grid, 256, 0, st>>>(x, T, H, K, inv, P, xq, xs);
+  return cudaGetLastError();
 }
 
 // act [P][I] float -> kTcTermsAct-term encoding: aq [term][P][I/2], scale bytes as

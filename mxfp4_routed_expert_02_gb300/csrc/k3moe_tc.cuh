@@ -67,9 +67,9 @@ __global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int 
                              int32_t *off, int32_t *tile_off, int32_t *inv, int32_t *status);
 __global__ void k_route_scatter(const int32_t *__restrict__ idx, int P,
                                 const int32_t *__restrict__ off, int32_t *perm, int32_t *inv);
-__global__ void k_quant_x(const uint16_t *__restrict__ x, int T, int H, int K,
-                          const int32_t *__restrict__ inv, int P, uint8_t *__restrict__ xq,
-                          uint8_t *__restrict__ xs);
+// k_quant_x on 256-thread blocks: x bf16, or float when x_f32.
+cudaError_t launch_quant_x(bool x_f32, int grid, cudaStream_t st, const void *x, int T, int H,
+                           int K, const int32_t *inv, int P, uint8_t *xq, uint8_t *xs);
 __global__ void k_quant_act(const float *__restrict__ act, int P, int I,
                             uint8_t *__restrict__ aq, uint8_t *__restrict__ as);
 __global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t *__restrict__ out);

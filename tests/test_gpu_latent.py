@@ -2,7 +2,9 @@
 oracle (README of FareedKhan-dev/kimi-k3-in-c, section 9, LatentMoE listing steps 1-6):
 routes bit-exact, the layer output within the layer step's tolerance (fp32 relative L2
 <= 1e-3, bf16 max-relative <= 2e-2), at small shapes with ragged passes and at the
-model's shape (hidden 7168, latent 3584, inter 3072, top-16, two shared experts)."""
+model's shape (hidden 7168, latent 3584, inter 3072, top-16, two shared experts): one token
+on the single-token kernels, 2-4 on the tensor-core experts with GEMV projections, more on
+tensor-core projections too."""
 import dataclasses
 
 import numpy as np
@@ -110,7 +112,9 @@ SHAPES = [
     (256, 128, 128, 16, 2, 0, 3),       # no shared expert: the up-projection writes y
     (256, 128, 128, 16, 2, 2, 65),      # two passes of the 64-token workspace
     (1024, 512, 512, 24, 6, 2, 3),
-    (768, 384, 256, 12, 5, 1, 7),       # odd top-k, one shared expert
+    (768, 384, 256, 12, 5, 1, 7),       # odd top-k, one shared expert; projections and
+                                        # experts on the tensor cores (more than 4 tokens)
+    (1024, 512, 512, 24, 6, 2, 67),     # a 64-token pass on the tensor cores, then 3 tokens
 ]
 
 
@@ -146,7 +150,7 @@ def test_latent_layer_nan_bias_sets_nonfinite_status():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("T", [1, 2])
+@pytest.mark.parametrize("T", [1, 2, 8])
 def test_latent_layer_at_the_model_shape(T):
     cfg = dataclasses.replace(synth.config("latent_decode1"), n_experts=64, tokens=T)
     L = LatentLayer(cfg, seed=50 + T, device_fill=True)
