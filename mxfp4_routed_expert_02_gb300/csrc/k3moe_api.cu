@@ -533,6 +533,18 @@ WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
   return w;
 }
 
+// K ranges per item for a GEMM of `items` work items over `kchunks` K chunks whose items
+// alone would leave most SMs idle (few output tiles, one B tile): the largest divisor of
+// kchunks up to `cap` with items x ranges <= sms.  The partial sums go to a buffer and are
+// added in range order by a small kernel.
+int tc_ksplit(int items, int kchunks, int sms, int cap) {
+  if (2 * items > sms) return 1;
+  int best = 1;
+  for (int k = 2; k <= cap && k <= kchunks; k++)
+    if (kchunks % k == 0 && items * k <= sms) best = k;
+  return best;
+}
+
 // Token/pair tables of a tensor-core GEMM over K_bytes of K per row.
 void tc_k_split(long long k_bytes, TcGemmArgs &a) {
   a.kchunks = (int)((k_bytes + kTcChunk - 1) / kTcChunk);
@@ -686,11 +698,27 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x
       a.mtiles = (SI + kTcRows - 1) / kTcRows;
       a.M_rows = SI;
       tc_k_split(2LL * H, a);
-      a.out = ws.act_s;
       a.out_ld = SI;
       TraceScope ts(KID_TC_SH_GATEUP, st);
-      if (launch_tc_gemm(TcKind::kBf16GateUp, a, msg, msu, mxs, di->sms, st) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
+      // few output tiles at a small batch: split K, the gate and up partials in the routed
+      // activations' buffer (free once they are encoded), P x I >= KS x 2 x Tc x SI floats
+      const int cap = std::min(16, (K * I) / (2 * SI));
+      const int KS = Tc <= nt1 ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
+      if (KS > 1) {
+        a.ksplit = KS;
+        a.out = ws.act;
+        a.out_mstride = (long long)Tc * SI;
+        a.out_kstride = 2LL * Tc * SI;
+        if (launch_tc_gemm(TcKind::kBf16Pair, a, msg, msu, mxs, di->sms, st) != cudaSuccess ||
+            launch_situ_parts(st, di->sms, ws.act, KS, 2LL * Tc * SI, (long long)Tc * SI,
+                              (long long)Tc * SI, d->situ_b1, d->situ_b2, ws.act_s) !=
+                cudaSuccess)
+          return K3MOE_ERR_CUDA;
+      } else {
+        a.out = ws.act_s;
+        if (launch_tc_gemm(TcKind::kBf16GateUp, a, msg, msu, mxs, di->sms, st) != cudaSuccess)
+          return K3MOE_ERR_CUDA;
+      }
     }
     {
       TraceScope ts(KID_SPLIT, st);
@@ -728,8 +756,7 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
   const int H = d->hidden, E = d->n_experts, K = d->topk;
   {
     TraceScope ts(KID_NORMS, st);
-    k_row_norms<<<(Tc + 3) / 4, 128, 0, st>>>(x, Tc, H, wt.xn);
-    k_row_norms<<<(E + 3) / 4, 128, 0, st>>>(wr, E, H, wt.wn);
+    k_row_norms<<<Tc + E, 128, 0, st>>>(x, Tc, wt.xn, wr, E, wt.wn, H);
   }
   k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, wt.off1, wt.tile_off1);
   CUtensorMap mw, mx;
@@ -748,8 +775,17 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
   a.status = status;
   {
     TraceScope ts(KID_TC_ROUTER, st);
-    a.out = wt.Lt;
+    // few output tiles at a small batch: split K, partials in the (still unused) per-pair
+    // down-output buffer, which holds P x H >= KS x Tc x E floats for KS <= K H / E
+    const int cap = std::min(16, (int)((long long)K * H / E));
+    const int KS = Tc <= kTcRows ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
+    a.ksplit = KS;
+    a.out_kstride = (long long)Tc * E;
+    a.out = KS > 1 ? wt.dpair : wt.Lt;
     if (launch_tc_gemm(TcKind::kBf16Store, a, mw, mw, mx, di->sms, st) != cudaSuccess)
+      return K3MOE_ERR_CUDA;
+    if (KS > 1 && launch_sum_parts(st, di->sms, wt.dpair, KS, (long long)Tc * E,
+                                   (long long)Tc * E, wt.Lt) != cudaSuccess)
       return K3MOE_ERR_CUDA;
   }
   {

@@ -10,7 +10,9 @@
 //    most H additions, each within 2^-23 of a partial sum bounded by
 //    S = sum_k |x_k Wr[e][k]| <= |x|_2 |Wr[e]|_2 (Cauchy-Schwarz):
 //    |L~ - logit| <= H * 2^-23 * |x|_2 |Wr[e]|_2.  The bound is taken with a factor 2 to
-//    spare; the norms come from k_row_norms.
+//    spare; the norms come from k_row_norms.  Under split K (small batches) L~ is the
+//    range-order sum of K-range partials: still at most H additions, every partial sum
+//    bounded by S, so the same bound holds.
 // 2. Per token, from those intervals, a lower and an upper bound of every expert's ch.
 //    With tau the K-th largest lower bound, at least K experts have ch >= tau, so an
 //    expert whose upper bound is below tau is not among the K largest.  The others (the
@@ -23,34 +25,54 @@
 
 namespace k3 {
 
-// Euclidean norm of each of R bf16 rows of width H (a multiple of 8), one warp per row,
-// rounded up by a relative 2^-10 so that it bounds the exact norm.  The squares of bf16
-// values are exact in float (8-bit significands); a lane adds n = 8 * ceil(H / 256) of them
-// in order and five shuffle levels follow, so the float sum S' has |S' - S| <= g S with
-// g = m u / (1 - m u), m = n + 4 additions on any path, u = 2^-24.  With the square root
-// and the final product rounded up, the result is >= sqrt(S) whenever g < 2^-9, that is for
-// H below 2^20 (hidden sizes are at most 8192 here).
-__global__ void __launch_bounds__(128) k_row_norms(const uint16_t *__restrict__ v, int R, int H,
-                                                   float *__restrict__ out) {
-  const int lane = threadIdx.x & 31;
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (warp >= R) return;
-  const uint4 *row = reinterpret_cast<const uint4 *>(v + (size_t)warp * H);
+// Euclidean norms of the R0 bf16 rows of v0 and the R1 rows of v1 (width H, a multiple of
+// 8), one 128-thread block per row, rounded up by a relative 2^-10 so that each bounds the
+// exact norm.  The squares of bf16 values are exact in float (8-bit significands); a thread
+// adds n = 8 * ceil(H / 1024) of them in order (all its loads issued first), then five
+// shuffle levels and the four warps' sums in order follow, so the float sum S' has
+// |S' - S| <= g S with g = m u / (1 - m u), m = n + 8 additions on any path, u = 2^-24.
+// With the square root and the final product rounded up, the result is >= sqrt(S) whenever
+// g < 2^-9, that is for H below 2^19 (hidden sizes are at most 8192 here).
+__global__ void __launch_bounds__(128) k_row_norms(const uint16_t *__restrict__ v0, int R0,
+                                                   float *__restrict__ out0,
+                                                   const uint16_t *__restrict__ v1, int R1,
+                                                   float *__restrict__ out1, int H) {
+  __shared__ float wsum[4];
+  const int b = blockIdx.x;
+  if (b >= R0 + R1) return;
+  const uint16_t *v = b < R0 ? v0 + (size_t)b * H : v1 + (size_t)(b - R0) * H;
+  const uint4 *row = reinterpret_cast<const uint4 *>(v);
+  const int nq = H / 8;
   float acc = 0.f;
-#pragma unroll 4
-  for (int q = lane; q < H / 8; q += 32) {
-    const uint4 w = __ldg(row + q);
-    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+  for (int q0 = threadIdx.x; q0 < nq; q0 += 128 * 8) {
+    uint4 w[8];  // eight loads in flight; past the row's end zeros, whose squares add nothing
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-      const float lo = bf16_lo(a[k]), hi = bf16_hi(a[k]);
-      acc = __fmaf_rn(lo, lo, acc);
-      acc = __fmaf_rn(hi, hi, acc);
+    for (int k = 0; k < 8; k++)
+      w[k] = q0 + 128 * k < nq ? __ldg(row + q0 + 128 * k) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const uint32_t a[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        const float lo = bf16_lo(a[e]), hi = bf16_hi(a[e]);
+        acc = __fmaf_rn(lo, lo, acc);
+        acc = __fmaf_rn(hi, hi, acc);
+      }
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-  if (lane == 0) out[warp] = __fmul_ru(__fsqrt_ru(acc), 1.0009765625f);  // 1 + 2^-10
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = wsum[0];
+    for (int k = 1; k < 4; k++) t = __fadd_rn(t, wsum[k]);
+    const float nv = __fmul_ru(__fsqrt_ru(t), 1.0009765625f);  // 1 + 2^-10
+    if (b < R0)
+      out0[b] = nv;
+    else
+      out1[b - R0] = nv;
+  }
 }
 
 // Logistic in float for the bounds (a few ulp from the exact value; the slack covers it).

@@ -385,14 +385,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sf_col0 = (uint32_t)((ND * NA * aw + 15) & ~15);
 
   pdl_wait();
-  const int nitems = a.tile_off[a.ngroups] * a.mtiles;
+  // split K: an item is (tile, M tile, K range ks of KS), its kc chunks from ks * kc on; its
+  // output goes to the ks-th partial buffer
+  const int KS = a.ksplit > 1 ? a.ksplit : 1;
+  const int kc = a.kchunks / KS;
+  const int nitems = a.tile_off[a.ngroups] * a.mtiles * KS;
   const int my_items = nitems > (int)blockIdx.x ? (nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-  const int total = my_items * a.kchunks;  // stages this CTA runs
+  const int total = my_items * kc;  // stages this CTA runs
   const int G = a.sf_rowb;                 // scale bytes per A row
   // this CTA's work items (the k-th is item blockIdx.x + k * gridDim.x), looked up once
   int4 *itab = reinterpret_cast<int4 *>(sfring + (size_t)NSF * sf_bytes);
   for (int k = tid; k < my_items && k < kTcItemTable; k += blockDim.x) {
-    const TcItem ti = tc_item(a, (int)blockIdx.x + k * (int)gridDim.x);
+    const TcItem ti = tc_item(a, ((int)blockIdx.x + k * (int)gridDim.x) / KS);
     itab[k] = make_int4(ti.g, ti.mt, ti.brow0, ti.nvalid);
   }
   __syncthreads();
@@ -401,15 +405,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int4 v = itab[k];
       return TcItem{v.x, v.y, v.z, v.w};
     }
-    return tc_item(a, (int)blockIdx.x + k * (int)gridDim.x);
+    return tc_item(a, ((int)blockIdx.x + k * (int)gridDim.x) / KS);
   };
+  // the K range of the CTA's k-th item
+  auto ks_at = [&](int k) -> int { return ((int)blockIdx.x + k * (int)gridDim.x) % KS; };
 
   if (warp == kTcWarpTma) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       for (int it = 0; it < total && !*abort_flag; it++) {
-        const int c = it % a.kchunks;
-        const TcItem ti = item_at(it / a.kchunks);
+        const int c = ks_at(it / kc) * kc + it % kc;
+        const TcItem ti = item_at(it / kc);
         const int ga = a.gid ? a.gid[ti.g] : ti.g;
         const int s = it % NS;
         if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1)) {
@@ -448,8 +454,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         while (ld < total && ld < stn + NSF &&
                (ld == stn ? mbar_wait(&sffree[ld % NSF], ((ld / NSF) & 1) ^ 1)
                           : mbar_test(&sffree[ld % NSF], ((ld / NSF) & 1) ^ 1))) {
-          const int c = ld % a.kchunks;
-          const TcItem ti = item_at(ld / a.kchunks);
+          const int c = ks_at(ld / kc) * kc + ld % kc;
+          const TcItem ti = item_at(ld / kc);
           const int ga = a.gid ? a.gid[ti.g] : ti.g;
           const int k = ld % NSF;
           uint8_t *sfs = sfring + (size_t)k * sf_bytes;
@@ -572,7 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int c = 0; c < a.kchunks; c++, it++) {
+        const int c0k = ks_at(n) * kc;
+        for (int c = 0; c < kc; c++, it++) {
           const int s = it % NS;
           const uint32_t par = (it / NS) & 1;
           const bool got = mbar_wait(&full[s], par) && (!kScales || mbar_wait(&sfull[s], par));
@@ -589,7 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t alo = sw_desc_lo(smem_u32(stages + (size_t)s * stage_bytes));
             const uint32_t blo = alo + ((uint32_t)(NA * kTcBox) >> 4);
             const uint32_t slot = tmem + sf_col0 + (uint32_t)(s * kSfSlot);
-            const int nk = (c == a.kchunks - 1) ? a.ksteps_last : kTcSteps;
+            const int nk = (c0k + c == a.kchunks - 1) ? a.ksteps_last : kTcSteps;
             if (NQ == 1)
               tc_issue_stage<KIND, NA, 1>(alo, blo, bstep, nk, slot, dcol0, dcol1, idesc, c == 0);
             else if (NQ == 2)
@@ -646,8 +653,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (NA > 1) d1[j] = __float_as_uint(__uint_as_float(d1[j]) + __uint_as_float(e1[j]));
             }
           }
+          float *obase = a.out + (long long)ks_at(n) * a.out_kstride;
           if (row < a.M_rows) {
-            float *orow = a.out + (long long)(ti.brow0 + c0) * a.out_ld + row;
+            float *orow = obase + (long long)(ti.brow0 + c0) * a.out_ld + row;
 #pragma unroll
             for (int j = 0; j < 16; j++) {
               if (c0 + j < ti.nvalid) {
@@ -659,7 +667,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           if (EPI == 1 && NA > 1 && row + moff < a.M_rows) {  // row-pair mode: second half
-            float *orow = a.out + (long long)(ti.brow0 + c0) * a.out_ld + row + moff;
+            float *orow = obase + (long long)(ti.brow0 + c0) * a.out_ld + row + moff;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+              if (c0 + j < ti.nvalid) orow[(long long)j * a.out_ld] = __uint_as_float(d1[j]);
+          }
+          if (EPI == 2 && row < a.M_rows) {  // both matrices stored: the second at + mstride
+            float *orow = obase + a.out_mstride + (long long)(ti.brow0 + c0) * a.out_ld + row;
 #pragma unroll
             for (int j = 0; j < 16; j++)
               if (c0 + j < ti.nvalid) orow[(long long)j * a.out_ld] = __uint_as_float(d1[j]);
@@ -818,10 +832,57 @@ cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &
     case TcKind::kMxf4Down: return launch_tc<0, 1, kTcTermsAct, 1>(a, A0, A1, B, grid, st);
     case TcKind::kMxf4DownPair: return launch_tc<0, 2, kTcTermsAct, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16GateUp: return launch_tc<1, 2, 1, 0>(a, A0, A1, B, grid, st);
+    case TcKind::kBf16Pair: return launch_tc<1, 2, 1, 2>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Down: return launch_tc<1, 1, 2, 1>(a, A0, A1, B, grid, st);
     case TcKind::kBf16Store: return launch_tc<1, 1, 1, 1>(a, A0, A1, B, grid, st);
   }
   return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------------------
+// Split-K partial sums, added in partial order k = 0 .. KS-1 (the same on every run).
+// out[i] = sum_k part[k * kstride + i]
+__global__ void k_sum_parts(const float *__restrict__ part, int KS, long long kstride,
+                            long long n, float *__restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float v = part[i];
+    for (int k = 1; k < KS; k++) v = __fadd_rn(v, part[k * kstride + i]);
+    out[i] = v;
+  }
+}
+// act[i] = SiTU(sum_k part[k * kstride + i], sum_k part[k * kstride + mstride + i]), the
+// gate/up epilogue's SiTU.
+__global__ void k_situ_parts(const float *__restrict__ part, int KS, long long kstride,
+                             long long mstride, long long n, float b1, float b2,
+                             float *__restrict__ act) {
+  const float ib1 = 1.f / b1, ib2 = 1.f / b2;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float g = part[i], u = part[mstride + i];
+    for (int k = 1; k < KS; k++) {
+      g = __fadd_rn(g, part[k * kstride + i]);
+      u = __fadd_rn(u, part[k * kstride + mstride + i]);
+    }
+    act[i] = situ_fast(g, u, b1, ib1, b2, ib2);
+  }
+}
+
+cudaError_t launch_sum_parts(cudaStream_t st, int sms, const float *part, int KS,
+                             long long kstride, long long n, float *out) {
+  long long g = (n + 255) / 256;
+  if (g > 8LL * sms) g = 8LL * sms;
+  k_sum_parts<<<(int)g, 256, 0, st>>>(part, KS, kstride, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_situ_parts(cudaStream_t st, int sms, const float *part, int KS,
+                              long long kstride, long long mstride, long long n, float b1,
+                              float b2, float *act) {
+  long long g = (n + 255) / 256;
+  if (g > 8LL * sms) g = 8LL * sms;
+  k_situ_parts<<<(int)g, 256, 0, st>>>(part, KS, kstride, mstride, n, b1, b2, act);
+  return cudaGetLastError();
 }
 
 }  // namespace k3

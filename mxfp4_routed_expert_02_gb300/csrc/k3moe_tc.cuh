@@ -43,11 +43,18 @@ struct TcGemmArgs {
   long long sfb_cstride;   // bytes between 256-column K groups (B rows x 8)
   float *out;              // [B row][out_ld]
   long long out_ld;
+  int ksplit;              // K ranges per item (0 or 1: none); kchunks must divide by it.
+                           // The partial sum of range ks goes to out + ks * out_kstride
+  long long out_kstride;
+  long long out_mstride;   // kBf16Pair: the second matrix's output at out + out_mstride
   float b1, b2;            // SiTU caps (gate/up epilogue)
   int32_t *status;
 };
 
-enum class TcKind { kMxf4GateUp, kMxf4Down, kMxf4DownPair, kBf16GateUp, kBf16Down, kBf16Store };
+// kBf16Pair: two bf16 matrices on one B, both products stored (the gate/up pair's partial
+// sums under split K; k_situ_parts then adds them up and applies SiTU).
+enum class TcKind { kMxf4GateUp, kMxf4Down, kMxf4DownPair, kBf16GateUp, kBf16Pair, kBf16Down,
+                    kBf16Store };
 
 // Tensor map of bytes of rank 3..5 (dims[0] = K bytes, innermost; strides in bytes of
 // dims 1..rank-1) with the kTcChunk-byte swizzle and boxes of box[0] = kTcChunk bytes x
@@ -59,6 +66,12 @@ bool tc_map(CUtensorMap *m, const void *base, int rank, const unsigned long long
 bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
               unsigned long long rows, unsigned long long depth, unsigned long long row_stride,
               unsigned long long depth_stride, int box_rows, int box_depth = 1);
+// Split-K partials added in range order: out = sum_k part_k; act = SiTU(gate, up) sums.
+cudaError_t launch_sum_parts(cudaStream_t st, int sms, const float *part, int KS,
+                             long long kstride, long long n, float *out);
+cudaError_t launch_situ_parts(cudaStream_t st, int sms, const float *part, int KS,
+                              long long kstride, long long mstride, long long n, float b1,
+                              float b2, float *act);
 cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &A0,
                            const CUtensorMap &A1, const CUtensorMap &B, int grid,
                            cudaStream_t st);
@@ -74,7 +87,9 @@ __global__ void k_quant_act(const float *__restrict__ act, int P, int I,
                             uint8_t *__restrict__ aq, uint8_t *__restrict__ as);
 __global__ void k_split_bf16(const float *__restrict__ v, long long n, uint16_t *__restrict__ out);
 __global__ void k_group1(int n, int ntile, int32_t *off, int32_t *tile_off);
-__global__ void k_row_norms(const uint16_t *__restrict__ v, int R, int H, float *__restrict__ out);
+__global__ void k_row_norms(const uint16_t *__restrict__ v0, int R0, float *__restrict__ out0,
+                            const uint16_t *__restrict__ v1, int R1, float *__restrict__ out1,
+                            int H);
 __global__ void k_route_candidates(const float *__restrict__ Lt, const float *__restrict__ xn,
                                    const float *__restrict__ wn,
                                    const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
