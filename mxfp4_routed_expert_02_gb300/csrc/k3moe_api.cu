@@ -482,6 +482,8 @@ struct WsTc {
   int32_t *idx;
   float *w;
   int32_t *off, *tile_off, *inv, *perm, *off1, *tile_off1;
+  int32_t *rcount;                // [ceil(P / kRouteChunk)][E] pairs per chunk and expert,
+                                  // then each chunk's first position per expert
   uint8_t *xq, *xs;               // [kTcTermsX][P][H/2], [kTcTermsX][P][H/32]
   float *act;                     // [P][I]
   uint8_t *aq, *as;               // [kTcTermsAct][P][I/2], [kTcTermsAct][P][I/32]
@@ -516,6 +518,8 @@ WsTc ws_tc_layout(const k3moe_dims *d, int T, void *base) {
   w.tile_off = reinterpret_cast<int32_t *>(take((E + 1) * 4));
   w.inv = reinterpret_cast<int32_t *>(take(P * 4));
   w.perm = reinterpret_cast<int32_t *>(take(P * 4));
+  w.rcount = reinterpret_cast<int32_t *>(
+      take((P + route_chunk((int)P) - 1) / route_chunk((int)P) * E * 4));
   w.off1 = reinterpret_cast<int32_t *>(take(8));
   w.tile_off1 = reinterpret_cast<int32_t *>(take(8));
   w.xq = take((size_t)kTcTermsX * P * (H / 2));
@@ -576,14 +580,16 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x
   const int used = P < E ? P : E;
   int ntile = ((((5 * P + 4 * used - 1) / (4 * used)) + 15) / 16) * 16;
   ntile = ntile > kTcRows ? kTcRows : ntile;
+  const int chunk = route_chunk(P), nch = (P + chunk - 1) / chunk;
   {
     TraceScope ts(KID_ROUTE_HIST, st);
-    k_route_hist<<<1, 1024, (size_t)E * 4, st>>>(idx, P, E, ntile, ws.off, ws.tile_off, ws.inv,
-                                                 status);
+    k_route_count<<<nch, 256, (size_t)E * 4, st>>>(idx, P, E, chunk, ws.rcount, ws.inv, status);
+    k_route_hist<<<1, 1024, (size_t)E * 4, st>>>(ws.rcount, nch, E, ntile, ws.off, ws.tile_off);
   }
   {
     TraceScope ts(KID_ROUTE_SCATTER, st);
-    k_route_scatter<<<E, 256, 0, st>>>(idx, P, ws.off, ws.perm, ws.inv);
+    k_route_scatter<<<nch, 256, (size_t)(E + chunk) * 4, st>>>(idx, P, E, chunk, ws.rcount,
+                                                               ws.perm, ws.inv);
   }
   {
     TraceScope ts(KID_QUANT_X, st);
@@ -764,6 +770,7 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
       !tc_map3d(&mx, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, kTcRows))
     return K3MOE_ERR_CUDA;
   TcGemmArgs a{};
+  int nadd = H;
   a.off = wt.off1;
   a.tile_off = wt.tile_off1;
   a.ngroups = 1;
@@ -779,6 +786,7 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
     // down-output buffer, which holds P x H >= KS x Tc x E floats for KS <= K H / E
     const int cap = std::min(16, (int)((long long)K * H / E));
     const int KS = Tc <= kTcRows ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
+    nadd = KS > 1 ? H / KS + KS : H;  // the longest chain of additions behind a logit
     a.ksplit = KS;
     a.out_kstride = (long long)Tc * E;
     a.out = KS > 1 ? wt.dpair : wt.Lt;
@@ -793,7 +801,7 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
     // enough blocks per token to cover the SMs twice, at most 8
     const int split = std::max(1, std::min(8, (2 * di->sms + Tc - 1) / Tc));
     k_route_candidates<<<dim3(Tc, split), 256, route_candidates_smem(H, E, K), st>>>(
-        wt.Lt, wt.xn, wt.wn, x, wr, bias, H, E, K, wt.sc, wt.ch, wt.ncand, status);
+        wt.Lt, wt.xn, wt.wn, x, wr, bias, H, E, K, nadd, wt.sc, wt.ch, wt.ncand, status);
   }
   {
     TraceScope ts(KID_TOPK, st);

@@ -11,15 +11,20 @@
 namespace k3 {
 
 // ------------------------------------------------------------------------------ dispatch
-// One block: per-expert pair counts, their exclusive prefix off[E+1], and the prefix of
-// ntile-row tiles tile_off[E+1].  Pairs whose expert index is outside [0, E) are counted
-// nowhere, get inv = -1 (the combine skips them) and set K3MOE_ERR_BAD_EXPERT.
-__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int ntile,
-                             int32_t *off, int32_t *tile_off, int32_t *inv, int32_t *status) {
+// A stable counting sort of the (token, slot) pairs by expert, in chunks of `chunk`
+// pairs (route_chunk): per-chunk counts, per-expert totals and their prefix sums, then every chunk places
+// its pairs after those of the earlier chunks, in pair order.
+
+// counts[c][e]: pairs of chunk c routed to expert e.  Pairs whose expert index is outside
+// [0, E) are counted nowhere, get inv = -1 (the combine skips them) and set
+// K3MOE_ERR_BAD_EXPERT.
+__global__ void k_route_count(const int32_t *__restrict__ idx, int P, int E, int chunk,
+                              int32_t *__restrict__ counts, int32_t *inv, int32_t *status) {
   extern __shared__ int32_t cnt[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+  const int p0 = blockIdx.x * chunk, p1 = min(P, p0 + chunk);
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
     const int e = idx[p];
     if (e >= 0 && e < E) {
       atomicAdd(&cnt[e], 1);
@@ -27,6 +32,22 @@ __global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int 
       inv[p] = -1;
       set_status(status, K3MOE_ERR_BAD_EXPERT);
     }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    counts[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// One block: per-expert totals over the nch chunks, their exclusive prefix off[E+1], the
+// prefix of ntile-row tiles tile_off[E+1], and counts[c][e] replaced by the first position
+// of expert e's pairs of chunk c: off[e] + the pairs of e in chunks 0 .. c-1.
+__global__ void k_route_hist(int32_t *__restrict__ counts, int nch, int E, int ntile,
+                             int32_t *off, int32_t *tile_off) {
+  extern __shared__ int32_t cnt[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int n = 0;
+    for (int c = 0; c < nch; c++) n += counts[(size_t)c * E + e];
+    cnt[e] = n;
   }
   __syncthreads();
   // exclusive scans of the counts and of the tile counts: thread i takes a run of
@@ -74,35 +95,47 @@ __global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int 
     off[E] = so;
     tile_off[E] = st;
   }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int pos = off[e];
+    for (int c = 0; c < nch; c++) {
+      const int n = counts[(size_t)c * E + e];
+      counts[(size_t)c * E + e] = pos;
+      pos += n;
+    }
+  }
 }
 
-// Block e lists expert e's pairs in pair order: perm[off[e] + r] = p and inv[p] =
-// off[e] + r for the r-th pair routed to e.  Stable, so the slot order is deterministic.
-__global__ void k_route_scatter(const int32_t *__restrict__ idx, int P,
-                                const int32_t *__restrict__ off, int32_t *perm, int32_t *inv) {
-  __shared__ int wsum[32];
-  const int e = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int base = off[e];
-  if (off[e + 1] == base) return;
-  for (int p0 = 0; p0 < P; p0 += blockDim.x) {
-    const int p = p0 + threadIdx.x;
-    const bool hit = p < P && idx[p] == e;
-    const unsigned b = __ballot_sync(0xffffffffu, hit);
-    if (lane == 0) wsum[warp] = __popc(b);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < nw; w++) {
-      before += (w < warp) ? wsum[w] : 0;
-      total += wsum[w];
+// Block c places the pairs of chunk c: the next position of expert e starts at first[c][e]
+// (k_route_hist); one warp walks the chunk (staged in shared memory) in pair order, 32 pairs
+// at a time (lanes with the same expert ranked by lane), so perm[off[e] + r] = p and
+// inv[p] = off[e] + r for the r-th pair routed to e overall.
+__global__ void k_route_scatter(const int32_t *__restrict__ idx, int P, int E, int chunk,
+                                const int32_t *__restrict__ first, int32_t *perm,
+                                int32_t *inv) {
+  extern __shared__ int32_t next[];  // [E], then the chunk's expert indices
+  int32_t *ci = next + E;
+  const int c = blockIdx.x;
+  const int p0 = c * chunk, p1 = min(P, p0 + chunk);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) next[e] = first[(size_t)c * E + e];
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) ci[p - p0] = idx[p];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const int e = p < p1 ? ci[p - p0] : -1;
+    const bool ok = e >= 0 && e < E;
+    const unsigned m = __match_any_sync(0xffffffffu, ok ? e : -1);
+    const int rank = __popc(m & ((1u << lane) - 1u));
+    const int base = ok ? next[e] : 0;
+    __syncwarp();
+    if (ok) {
+      perm[base + rank] = p;
+      inv[p] = base + rank;
+      if (rank == 0) next[e] = base + __popc(m);  // the lowest lane of the group advances it
     }
-    if (hit) {
-      const int pos = base + before + __popc(b & ((1u << lane) - 1u));
-      perm[pos] = p;
-      inv[p] = pos;
-    }
-    base += total;
-    __syncthreads();
+    __syncwarp();
   }
 }
 

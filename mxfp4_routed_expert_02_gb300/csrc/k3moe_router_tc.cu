@@ -11,8 +11,9 @@
 //    S = sum_k |x_k Wr[e][k]| <= |x|_2 |Wr[e]|_2 (Cauchy-Schwarz):
 //    |L~ - logit| <= H * 2^-23 * |x|_2 |Wr[e]|_2.  The bound is taken with a factor 2 to
 //    spare; the norms come from k_row_norms.  Under split K (small batches) L~ is the
-//    range-order sum of K-range partials: still at most H additions, every partial sum
-//    bounded by S, so the same bound holds.
+//    range-order sum of KS partials over H / KS inputs each: a chain of at most H / KS
+//    additions inside a partial and KS more between partials, every partial sum bounded
+//    by S, so H can be replaced by H / KS + KS in the bound.
 // 2. Per token, from those intervals, a lower and an upper bound of every expert's ch.
 //    With tau the K-th largest lower bound, at least K experts have ch >= tau, so an
 //    expert whose upper bound is below tau is not among the K largest.  The others (the
@@ -79,7 +80,8 @@ __global__ void __launch_bounds__(128) k_row_norms(const uint16_t *__restrict__ 
 __device__ __forceinline__ float logistic_f(float v) { return 1.f / (1.f + expf(-v)); }
 
 // gridDim.y blocks per token (blockIdx.x = token).  Lt [T][E] screening logits, xn [T] /
-// wn [E] row norms of x / Wr; x [T][H], wr [E][H] bf16.  Every block of a token computes
+// wn [E] row norms of x / Wr; x [T][H], wr [E][H] bf16; nadd bounds the additions on any
+// path of the screening sums (H, or H / KS + KS under split K).  Every block of a token computes
 // all E bounds and the threshold (cheap, and identical in every block); block y then owns
 // the experts e with e % gridDim.y == y: it computes the exact sc / ch of its candidates and
 // writes sc 0, ch -inf for its other experts, so no two blocks write the same entry.
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(256) k_route_candidates(
     const float *__restrict__ Lt, const float *__restrict__ xn, const float *__restrict__ wn,
     const uint16_t *__restrict__ x,
     const uint16_t *__restrict__ wr, const float *__restrict__ bias, int H, int E, int K,
-    float *__restrict__ sc, float *__restrict__ ch, int32_t *__restrict__ ncand,
+    int nadd, float *__restrict__ sc, float *__restrict__ ch, int32_t *__restrict__ ncand,
     int32_t *status) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(256) k_route_candidates(
   const float xnorm = xn[t];
   float *scr = sc + (size_t)t * E;
   float *chr = ch + (size_t)t * E;
-  const float nerr = (float)H * 2.384185791015625e-07f;  // H * 2^-22
+  const float nerr = (float)nadd * 2.384185791015625e-07f;  // nadd * 2^-22
   if (threadIdx.x == 0) {
     count = 0;
     total = 0;
@@ -164,20 +166,29 @@ __global__ void __launch_bounds__(256) k_route_candidates(
     const int e = clist[c];
     const uint4 *w4 = reinterpret_cast<const uint4 *>(wr + (size_t)e * H);
     float hi = 0.f, lo = 0.f;
-    for (int q = lane; q < nchunk; q += 32) {
-      const uint4 wv = __ldg(w4 + q), xv = xs4[q];
-      const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w}, xa[4] = {xv.x, xv.y, xv.z, xv.w};
+    for (int q0 = lane; q0 < nchunk; q0 += 32 * 8) {
+      uint4 wq[8];  // the row's loads eight at a time, then summed in the same order
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        float p = __fmul_rn(bf16_lo(wa[k]), bf16_lo(xa[k]));
-        float s, er;
-        two_sum(hi, p, s, er);
-        hi = s;
-        lo = __fadd_rn(lo, er);
-        p = __fmul_rn(bf16_hi(wa[k]), bf16_hi(xa[k]));
-        two_sum(hi, p, s, er);
-        hi = s;
-        lo = __fadd_rn(lo, er);
+      for (int b = 0; b < 8; b++)
+        wq[b] = q0 + 32 * b < nchunk ? __ldg(w4 + q0 + 32 * b) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int b = 0; b < 8; b++) {
+        const int q = q0 + 32 * b;
+        if (q >= nchunk) break;
+        const uint4 wv = wq[b], xv = xs4[q];
+        const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w}, xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          float p = __fmul_rn(bf16_lo(wa[k]), bf16_lo(xa[k]));
+          float s, er;
+          two_sum(hi, p, s, er);
+          hi = s;
+          lo = __fadd_rn(lo, er);
+          p = __fmul_rn(bf16_hi(wa[k]), bf16_hi(xa[k]));
+          two_sum(hi, p, s, er);
+          hi = s;
+          lo = __fadd_rn(lo, er);
+        }
       }
     }
     {

@@ -76,10 +76,16 @@ cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &
                            const CUtensorMap &A1, const CUtensorMap &B, int grid,
                            cudaStream_t st);
 
-__global__ void k_route_hist(const int32_t *__restrict__ idx, int P, int E, int ntile,
-                             int32_t *off, int32_t *tile_off, int32_t *inv, int32_t *status);
-__global__ void k_route_scatter(const int32_t *__restrict__ idx, int P,
-                                const int32_t *__restrict__ off, int32_t *perm, int32_t *inv);
+// Pairs per block of the dispatch's counting sort: small chunks spread a small batch over
+// several blocks, larger ones keep the per-chunk tables of a large batch short.
+inline int route_chunk(int P) { return P <= 16384 ? 256 : 1024; }
+__global__ void k_route_count(const int32_t *__restrict__ idx, int P, int E, int chunk,
+                              int32_t *__restrict__ counts, int32_t *inv, int32_t *status);
+__global__ void k_route_hist(int32_t *__restrict__ counts, int nch, int E, int ntile,
+                             int32_t *off, int32_t *tile_off);
+__global__ void k_route_scatter(const int32_t *__restrict__ idx, int P, int E, int chunk,
+                                const int32_t *__restrict__ first, int32_t *perm,
+                                int32_t *inv);
 // k_quant_x on 256-thread blocks: x bf16, or float when x_f32.
 cudaError_t launch_quant_x(bool x_f32, int grid, cudaStream_t st, const void *x, int T, int H,
                            int K, const int32_t *inv, int P, uint8_t *xq, uint8_t *xs);
@@ -94,7 +100,7 @@ __global__ void k_route_candidates(const float *__restrict__ Lt, const float *__
                                    const float *__restrict__ wn,
                                    const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
                                    const float *__restrict__ bias, int H, int E, int K,
-                                   float *__restrict__ sc, float *__restrict__ ch,
+                                   int nadd, float *__restrict__ sc, float *__restrict__ ch,
                                    int32_t *__restrict__ ncand, int32_t *status);
 size_t route_candidates_smem(int H, int E, int K);
 __global__ void k_combine(int T, int H, int K, const float *__restrict__ w,
