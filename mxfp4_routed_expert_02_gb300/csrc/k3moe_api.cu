@@ -782,10 +782,13 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
   a.status = status;
   {
     TraceScope ts(KID_TC_ROUTER, st);
-    // few output tiles at a small batch: split K, partials in the (still unused) per-pair
-    // down-output buffer, which holds P x H >= KS x Tc x E floats for KS <= K H / E
+    // split K, partials in the (still unused) per-pair down-output buffer, which holds
+    // P x H >= KS x Tc x E floats for KS <= K H / E: at a small batch because its few
+    // output tiles alone would leave most SMs idle; at a large one for the screening
+    // bound (H / KS + KS additions instead of H, so fewer candidates need exact logits)
     const int cap = std::min(16, (int)((long long)K * H / E));
-    const int KS = Tc <= kTcRows ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
+    int KS = Tc <= kTcRows ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
+    if (Tc > kTcRows && cap >= 8 && a.kchunks % 8 == 0) KS = 8;
     nadd = KS > 1 ? H / KS + KS : H;  // the longest chain of additions behind a logit
     a.ksplit = KS;
     a.out_kstride = (long long)Tc * E;
