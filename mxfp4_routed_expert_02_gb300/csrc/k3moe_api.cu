@@ -22,6 +22,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int sms = 0;
   bool attrs_set = false;
+  cudaStream_t side = nullptr;  // a second stream for work that overlaps the caller's
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -53,6 +54,18 @@ const DeviceInfo *device_info() {
     d.attrs_set = true;
   }
   return &d;
+}
+
+// This device's side stream (non-blocking, created once): independent parts of a call run
+// on it, forked from and joined back into the caller's stream by events.
+cudaStream_t side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.side && cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess)
+    d.side = nullptr;
+  return d.side;
 }
 
 // Lanes per pair in the down kernel: the largest power of two <= 32 dividing I/32 with
@@ -841,8 +854,9 @@ struct WsLatent {
   float *z, *accl, *up, *act_s;
   bool has_tc;
   WsTc tc;
-  uint16_t *hs;  // [2][Tc][max(L, SI)] bf16 hi / lo terms of a float GEMM input
-  float *ds;     // [Tc][H] shared experts' output
+  uint16_t *hs;    // [2][Tc][L] bf16 hi / lo terms of the latent sum (tensor-core passes)
+  uint16_t *hs_s;  // [2][Tc][SI] the same of the shared activations
+  float *ds;       // [Tc][H] shared experts' output
   size_t total;
 };
 
@@ -864,13 +878,13 @@ WsLatent ws_latent_layout(const k3moe_dims *full, const k3moe_dims *lat, int T, 
   w.accl = take((size_t)Tc * L * 4);
   w.up = take((size_t)Tc * H * 4);
   w.act_s = take((size_t)Tc * (SI > 0 ? SI : 1) * 4);
+  w.ds = take((size_t)Tc * H * 4);
   w.has_tc = use_tc(lat, Tc) && use_tc(full, Tc);
   if (w.has_tc) {
     w.tc = ws_tc_layout(lat, Tc, reinterpret_cast<void *>(b + o));
     o += up16(w.tc.total);
-    const size_t C = L > SI ? L : SI;
-    w.hs = reinterpret_cast<uint16_t *>(take((size_t)2 * Tc * C * 2));
-    w.ds = take((size_t)Tc * H * 4);
+    w.hs = reinterpret_cast<uint16_t *>(take((size_t)2 * Tc * L * 2));
+    w.hs_s = reinterpret_cast<uint16_t *>(take((size_t)2 * Tc * (SI > 0 ? SI : 1) * 2));
   }
   w.total = o;
   return w;
@@ -907,6 +921,57 @@ k3moe_status launch_split(const DeviceInfo *di, const float *v, long long n, uin
   if (grid > 16 * di->sms) grid = 16 * di->sms;
   k_split_bf16<<<grid, 256, 0, st>>>(v, n, out);
   return launch_status();
+}
+
+// The LatentMoE's shared experts of one pass, ds = Wsd SiTU(Wsg x, Wsu x) [Tc][H] float,
+// enqueued on the side stream after an event recorded on st (they read only x and write
+// only act_s / hs_s / ds); *join is recorded after them for st to wait on.
+k3moe_status run_latent_shared(const DeviceInfo *di, const k3moe_latent_weights *lw,
+                               const uint16_t *xc, int Tc, int H, int SI, bool proj_tc,
+                               const TcGemmArgs &g1, const WsLatent &ws, float b1, float b2,
+                               cudaStream_t st, cudaEvent_t *join) {
+  cudaStream_t ss = side_stream();
+  cudaEvent_t fork = nullptr;
+  if (!ss || cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess)
+    return K3MOE_ERR_CUDA;
+  if (cudaEventCreateWithFlags(join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    return K3MOE_ERR_CUDA;
+  }
+  const bool forked = cudaEventRecord(fork, st) == cudaSuccess &&
+                      cudaStreamWaitEvent(ss, fork, 0) == cudaSuccess;
+  cudaEventDestroy(fork);
+  if (!forked) return K3MOE_ERR_CUDA;
+  k3moe_status s = K3MOE_OK;
+  if (proj_tc) {
+    {
+      TraceScope ts(KID_SHARED_GATEUP, ss);
+      s = tc_bf16_gemm(di, TcKind::kBf16GateUp, lw->sh_gate, lw->sh_up, SI, H, xc, 1, Tc,
+                       ws.act_s, g1, ss);
+    }
+    if (s == K3MOE_OK) s = launch_split(di, ws.act_s, (long long)Tc * SI, ws.hs_s, ss);
+    if (s == K3MOE_OK) {
+      TraceScope ts(KID_PROJ_SHARED_DOWN, ss);
+      s = tc_bf16_gemm(di, TcKind::kBf16Down, lw->sh_down, nullptr, H, SI, ws.hs_s, 2, Tc,
+                       ws.ds, g1, ss);
+    }
+  } else {
+    {
+      TraceScope ts(KID_SHARED_GATEUP, ss);
+      if (launch_proj(ss, di->sms, lw->sh_gate, lw->sh_up, SI, H, xc, false, Tc, ws.act_s,
+                      nullptr, nullptr, 0, 0, b1, b2, false) != cudaSuccess)
+        s = K3MOE_ERR_CUDA;
+    }
+    if (s == K3MOE_OK) {
+      TraceScope ts(KID_PROJ_SHARED_DOWN, ss);
+      if (launch_proj(ss, di->sms, lw->sh_down, nullptr, H, SI, ws.act_s, true, Tc, ws.ds,
+                      nullptr, nullptr, 0, 0, b1, b2, false) != cudaSuccess)
+        s = K3MOE_ERR_CUDA;
+    }
+  }
+  // recorded whatever happened, so that st never waits on an event with nothing behind it
+  if (cudaEventRecord(*join, ss) != cudaSuccess) s = K3MOE_ERR_CUDA;
+  return s;
 }
 
 }  // namespace
@@ -1213,10 +1278,6 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
     // one token at a latent width the single-token gate/up kernel takes: it selects the
     // top-k itself from the router's scores and streams the experts through its ring
     const int rb = Tc == 1 ? t1_row_block(L) : 0;
-    // 1. route on the full-width x
-    s = run_route(di, &full, xc, Tc, lw->wr_bf16, lw->bias, nullptr, nullptr, ws.route, idx_c,
-                  w_c, status_dev, st, rb == 0);
-    if (s != K3MOE_OK) return s;
     // more tokens than one pass of the GEMV kernels takes: the four bf16 projections as
     // GEMMs on the tensor cores (one group of Tc rows)
     const bool proj_tc = ws.has_tc && Tc > kProjRows;
@@ -1232,6 +1293,23 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
       g1.b2 = b2;
       g1.status = status_dev;
     }
+    // 6 (first, on the side stream). The shared experts read only x: their SiTU(Wg x, Wu x)
+    // and down projection into ds run alongside the routed chain and join before the
+    // final add y (=|+=) up + ds.
+    struct EventGuard {  // destroys the join event on every way out of the pass
+      cudaEvent_t e = nullptr;
+      ~EventGuard() {
+        if (e) cudaEventDestroy(e);
+      }
+    } ev_join;
+    if (shared) {
+      s = run_latent_shared(di, lw, xc, Tc, H, SI, proj_tc, g1, ws, b1, b2, st, &ev_join.e);
+      if (s != K3MOE_OK) return s;
+    }
+    // 1. route on the full-width x
+    s = run_route(di, &full, xc, Tc, lw->wr_bf16, lw->bias, nullptr, nullptr, ws.route, idx_c,
+                  w_c, status_dev, st, rb == 0);
+    if (s != K3MOE_OK) return s;
     // 2. z = Wdn x
     if (proj_tc) {
       TraceScope ts(KID_PROJ, st);
@@ -1286,8 +1364,7 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
         return K3MOE_ERR_CUDA;
     }
     if (proj_tc) {
-      // 5-6 on the tensor cores: up = Wup accL (accL as bf16 hi + lo), the shared experts'
-      // SiTU(Wg x, Wu x) and its down projection (hi + lo), then y (=|+=) up + shared
+      // 5 on the tensor cores: up = Wup accL (accL as bf16 hi + lo)
       s = launch_split(di, ws.accl, (long long)Tc * L, ws.hs, st);
       if (s != K3MOE_OK) return s;
       {
@@ -1296,45 +1373,20 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
                          g1, st);
         if (s != K3MOE_OK) return s;
       }
-      if (shared) {
-        {
-          TraceScope ts(KID_SHARED_GATEUP, st);
-          s = tc_bf16_gemm(di, TcKind::kBf16GateUp, lw->sh_gate, lw->sh_up, SI, H, xc, 1, Tc,
-                           ws.act_s, g1, st);
-          if (s != K3MOE_OK) return s;
-        }
-        s = launch_split(di, ws.act_s, (long long)Tc * SI, ws.hs, st);
-        if (s != K3MOE_OK) return s;
-        TraceScope ts(KID_PROJ_SHARED_DOWN, st);
-        s = tc_bf16_gemm(di, TcKind::kBf16Down, lw->sh_down, nullptr, H, SI, ws.hs, 2, Tc,
-                         ws.ds, g1, st);
-        if (s != K3MOE_OK) return s;
-      }
-      TraceScope ts(KID_COMBINE, st);
-      if (launch_add_out(st, di->sms, ws.up, shared ? ws.ds : nullptr, yc, (int)ydt, accumulate,
-                         (long long)Tc * H) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
-      continue;
-    }
-    // 5. up = Wup accL (straight into y when there is no shared expert)
-    {
+    } else {
+      // 5. up = Wup accL (straight into y when there is no shared expert)
       TraceScope ts(KID_PROJ_UP, st);
       if (launch_proj(st, di->sms, lw->w_up, nullptr, H, L, ws.accl, true, Tc, ws.up, nullptr,
                       shared ? nullptr : yc, (int)ydt, accumulate, b1, b2, !g_trace.on,
                       fold_norm, lw->latent_norm_w, dims->rms_eps) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
-    // 6. shared experts on the original x, added unweighted: y (=|+=) up + Wsd SiTU(..)
-    if (shared) {
-      {
-        TraceScope ts(KID_SHARED_GATEUP, st);
-        if (launch_proj(st, di->sms, lw->sh_gate, lw->sh_up, SI, H, xc, false, Tc, ws.act_s,
-                        nullptr, nullptr, 0, 0, b1, b2, !g_trace.on) != cudaSuccess)
-          return K3MOE_ERR_CUDA;
-      }
-      TraceScope ts(KID_PROJ_SHARED_DOWN, st);
-      if (launch_proj(st, di->sms, lw->sh_down, nullptr, H, SI, ws.act_s, true, Tc, nullptr,
-                      ws.up, yc, (int)ydt, accumulate, b1, b2, !g_trace.on) != cudaSuccess)
+    if (shared || proj_tc) {
+      if (ev_join.e && cudaStreamWaitEvent(st, ev_join.e, 0) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+      TraceScope ts(KID_COMBINE, st);
+      if (launch_add_out(st, di->sms, ws.up, shared ? ws.ds : nullptr, yc, (int)ydt, accumulate,
+                         (long long)Tc * H) != cudaSuccess)
         return K3MOE_ERR_CUDA;
     }
   }
