@@ -572,14 +572,92 @@ long long tc_sf_tstride(long long k_bytes, long long cstride) {
   return (k_bytes + 127) / 128 * cstride;
 }
 
+// The shared expert of Tc tokens on the tensor cores: ds [Tc][H] = Wsd SiTU(Wsg x, Wsu x)
+// (bf16 weights; the activations as bf16 hi + lo for the down GEMM).  Under split K its
+// partial sums use ws.act, which the routed gate/up writes: callers run this either after
+// the routed down GEMM or before the routed gate/up.  group1_done: ws.off1 / tile_off1
+// already hold the one-group table of Tc rows.
+k3moe_status run_shared_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
+                           const uint16_t *sh_gate, const uint16_t *sh_up,
+                           const uint16_t *sh_down, WsTc &ws, int32_t *status, cudaStream_t st,
+                           bool group1_done) {
+  const int H = d->hidden, I = d->inter, K = d->topk, SI = d->shared_inter;
+  {
+    CUtensorMap msg, msu, msd, mxs, mhs;
+    const int nt1 = kTcRows;
+    if (!tc_map3d(&msg, sh_gate, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
+        !tc_map3d(&msu, sh_up, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
+        !tc_map3d(&msd, sh_down, 2ull * SI, H, 1, 2ull * SI, 2ull * SI * H, kTcRows) ||
+        !tc_map3d(&mxs, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, nt1) ||
+        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc, nt1, 2))
+      return K3MOE_ERR_CUDA;
+    if (!group1_done) k_group1<<<1, 32, 0, st>>>(Tc, nt1, ws.off1, ws.tile_off1);
+    TcGemmArgs s1{};
+    s1.b1 = d->situ_b1;
+    s1.b2 = d->situ_b2;
+    s1.status = status;
+    s1.off = ws.off1;
+    s1.tile_off = ws.tile_off1;
+    s1.ngroups = 1;
+    s1.ntile = nt1;
+    {
+      TcGemmArgs a = s1;
+      a.mtiles = (SI + kTcRows - 1) / kTcRows;
+      a.M_rows = SI;
+      tc_k_split(2LL * H, a);
+      a.out_ld = SI;
+      TraceScope ts(KID_TC_SH_GATEUP, st);
+      // few output tiles at a small batch: split K, the gate and up partials in the routed
+      // activations' buffer (free once they are encoded), P x I >= KS x 2 x Tc x SI floats
+      const int cap = std::min(16, (K * I) / (2 * SI));
+      const int KS = Tc <= nt1 ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
+      if (KS > 1) {
+        a.ksplit = KS;
+        a.out = ws.act;
+        a.out_mstride = (long long)Tc * SI;
+        a.out_kstride = 2LL * Tc * SI;
+        if (launch_tc_gemm(TcKind::kBf16Pair, a, msg, msu, mxs, di->sms, st) != cudaSuccess ||
+            launch_situ_parts(st, di->sms, ws.act, KS, 2LL * Tc * SI, (long long)Tc * SI,
+                              (long long)Tc * SI, d->situ_b1, d->situ_b2, ws.act_s) !=
+                cudaSuccess)
+          return K3MOE_ERR_CUDA;
+      } else {
+        a.out = ws.act_s;
+        if (launch_tc_gemm(TcKind::kBf16GateUp, a, msg, msu, mxs, di->sms, st) != cudaSuccess)
+          return K3MOE_ERR_CUDA;
+      }
+    }
+    {
+      TraceScope ts(KID_SPLIT, st);
+      const long long n = (long long)Tc * SI;
+      int grid = (int)((n + 255) / 256);
+      if (grid > 16 * di->sms) grid = 16 * di->sms;
+      k_split_bf16<<<grid, 256, 0, st>>>(ws.act_s, n, ws.hs);
+    }
+    {
+      TcGemmArgs a = s1;
+      a.mtiles = (H + kTcRows - 1) / kTcRows;
+      a.M_rows = H;
+      tc_k_split(2LL * SI, a);
+      a.out = ws.ds;
+      a.out_ld = H;
+      TraceScope ts(KID_TC_SH_DOWN, st);
+      if (launch_tc_gemm(TcKind::kBf16Down, a, msd, msd, mhs, di->sms, st) != cudaSuccess)
+        return K3MOE_ERR_CUDA;
+    }
+  }
+  return launch_status();
+}
+
 // Expert FFN of Tc tokens on the tensor cores, given the route (idx, w [Tc][K]):
 // dispatch, x encoding, gate/up + SiTU, activation encoding, down, then (with the shared
-// expert when sh_gate != NULL) the router-order combine into y.
+// expert when sh_gate != NULL) the router-order combine into y.  shared_done: ws.ds
+// already holds the shared expert's output (run_shared_tc, run before).
 k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x, int Tc,
                         const k3moe_experts *ex, const int32_t *idx, const float *w,
                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
                         WsTc &ws, void *y, k3moe_dtype ydt, int accumulate, int32_t *status,
-                        cudaStream_t st, bool x_f32 = false) {
+                        cudaStream_t st, bool x_f32 = false, bool shared_done = false) {
   if (x_f32 && sh_gate) return K3MOE_ERR_ARG;  // the shared GEMMs take bf16 x
   const int H = d->hidden, I = d->inter, E = d->n_experts, K = d->topk;
   const int SI = sh_gate ? d->shared_inter : 0;
@@ -697,66 +775,10 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x
                        pair ? md2 : md, ma, di->sms, st) != cudaSuccess)
       return K3MOE_ERR_CUDA;
   }
-  if (SI > 0) {
-    CUtensorMap msg, msu, msd, mxs, mhs;
-    const int nt1 = kTcRows;
-    if (!tc_map3d(&msg, sh_gate, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
-        !tc_map3d(&msu, sh_up, 2ull * H, SI, 1, 2ull * H, 2ull * H * SI, kTcRows) ||
-        !tc_map3d(&msd, sh_down, 2ull * SI, H, 1, 2ull * SI, 2ull * SI * H, kTcRows) ||
-        !tc_map3d(&mxs, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, nt1) ||
-        !tc_map3d(&mhs, ws.hs, 2ull * SI, Tc, 2, 2ull * SI, 2ull * SI * Tc, nt1, 2))
-      return K3MOE_ERR_CUDA;
-    k_group1<<<1, 32, 0, st>>>(Tc, nt1, ws.off1, ws.tile_off1);
-    TcGemmArgs s1 = g;
-    s1.off = ws.off1;
-    s1.tile_off = ws.tile_off1;
-    s1.ngroups = 1;
-    s1.ntile = nt1;
-    {
-      TcGemmArgs a = s1;
-      a.mtiles = (SI + kTcRows - 1) / kTcRows;
-      a.M_rows = SI;
-      tc_k_split(2LL * H, a);
-      a.out_ld = SI;
-      TraceScope ts(KID_TC_SH_GATEUP, st);
-      // few output tiles at a small batch: split K, the gate and up partials in the routed
-      // activations' buffer (free once they are encoded), P x I >= KS x 2 x Tc x SI floats
-      const int cap = std::min(16, (K * I) / (2 * SI));
-      const int KS = Tc <= nt1 ? tc_ksplit(a.mtiles, a.kchunks, di->sms, cap) : 1;
-      if (KS > 1) {
-        a.ksplit = KS;
-        a.out = ws.act;
-        a.out_mstride = (long long)Tc * SI;
-        a.out_kstride = 2LL * Tc * SI;
-        if (launch_tc_gemm(TcKind::kBf16Pair, a, msg, msu, mxs, di->sms, st) != cudaSuccess ||
-            launch_situ_parts(st, di->sms, ws.act, KS, 2LL * Tc * SI, (long long)Tc * SI,
-                              (long long)Tc * SI, d->situ_b1, d->situ_b2, ws.act_s) !=
-                cudaSuccess)
-          return K3MOE_ERR_CUDA;
-      } else {
-        a.out = ws.act_s;
-        if (launch_tc_gemm(TcKind::kBf16GateUp, a, msg, msu, mxs, di->sms, st) != cudaSuccess)
-          return K3MOE_ERR_CUDA;
-      }
-    }
-    {
-      TraceScope ts(KID_SPLIT, st);
-      const long long n = (long long)Tc * SI;
-      int grid = (int)((n + 255) / 256);
-      if (grid > 16 * di->sms) grid = 16 * di->sms;
-      k_split_bf16<<<grid, 256, 0, st>>>(ws.act_s, n, ws.hs);
-    }
-    {
-      TcGemmArgs a = s1;
-      a.mtiles = (H + kTcRows - 1) / kTcRows;
-      a.M_rows = H;
-      tc_k_split(2LL * SI, a);
-      a.out = ws.ds;
-      a.out_ld = H;
-      TraceScope ts(KID_TC_SH_DOWN, st);
-      if (launch_tc_gemm(TcKind::kBf16Down, a, msd, msd, mhs, di->sms, st) != cudaSuccess)
-        return K3MOE_ERR_CUDA;
-    }
+  if (SI > 0 && !shared_done) {
+    const k3moe_status r = run_shared_tc(di, d, static_cast<const uint16_t *>(x), Tc, sh_gate,
+                                         sh_up, sh_down, ws, status, st, false);
+    if (r != K3MOE_OK) return r;
   }
   {
     TraceScope ts(KID_COMBINE, st);
@@ -771,13 +793,14 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x
 // their error bounds on the tensor cores, exact scores for the candidates, then top-k.
 k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint16_t *x, int Tc,
                           const uint16_t *wr, const float *bias, WsTc &wt, int32_t *idx,
-                          float *w, int32_t *status, cudaStream_t st) {
+                          float *w, int32_t *status, cudaStream_t st,
+                          bool group1_done = false) {
   const int H = d->hidden, E = d->n_experts, K = d->topk;
   {
     TraceScope ts(KID_NORMS, st);
     k_row_norms<<<Tc + E, 128, 0, st>>>(x, Tc, wt.xn, wr, E, wt.wn, H);
   }
-  k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, wt.off1, wt.tile_off1);
+  if (!group1_done) k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, wt.off1, wt.tile_off1);
   CUtensorMap mw, mx;
   if (!tc_map3d(&mw, wr, 2ull * H, E, 1, 2ull * H, 2ull * H * E, kTcRows) ||
       !tc_map3d(&mx, x, 2ull * H, Tc, 1, 2ull * H, 2ull * H * Tc, kTcRows))
@@ -1145,12 +1168,17 @@ static k3moe_status check_layer_args(const k3moe_dims *dims, const void *x, int3
   return K3MOE_OK;
 }
 
-k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
-                         const uint16_t *wr_bf16, const float *bias, const k3moe_experts *experts,
-                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
-                         int32_t *idx_out, float *w_out, void *y, k3moe_dtype ydt,
-                         int32_t accumulate, void *workspace, size_t ws_bytes,
-                         int32_t *status_dev, k3moe_stream_t stream) {
+namespace {
+
+// The layer step.  overlap: on the tensor-core path the shared expert (it reads only x)
+// runs on the side stream while the tokens are routed, joined before the routed GEMMs
+// (off for the static-scratch entry, which creates nothing).
+k3moe_status layer_impl(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                        const uint16_t *wr_bf16, const float *bias, const k3moe_experts *experts,
+                        const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
+                        int32_t *idx_out, float *w_out, void *y, k3moe_dtype ydt,
+                        int32_t accumulate, void *workspace, size_t ws_bytes,
+                        int32_t *status_dev, k3moe_stream_t stream, bool overlap) {
   k3moe_status s = check_layer_args(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up,
                                     sh_down, idx_out, w_out, y, ydt, workspace, ws_bytes,
                                     status_dev);
@@ -1167,12 +1195,31 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
       int32_t *idx_c = idx_out ? idx_out + (size_t)t0 * K : wt.idx;
       float *w_c = w_out ? w_out + (size_t)t0 * K : wt.w;
       const uint16_t *xc = x_bf16 + (size_t)t0 * H;
-      s = run_route_tc(di, dims, xc, Tc, wr_bf16, bias, wt, idx_c, w_c, status_dev, st);
+      struct EventGuard {
+        cudaEvent_t e = nullptr;
+        ~EventGuard() {
+          if (e) cudaEventDestroy(e);
+        }
+      } fork, join;
+      cudaStream_t ss = overlap && shared ? side_stream() : nullptr;
+      if (ss) {
+        k_group1<<<1, 32, 0, st>>>(Tc, kTcRows, wt.off1, wt.tile_off1);
+        if (cudaEventCreateWithFlags(&fork.e, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&join.e, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventRecord(fork.e, st) != cudaSuccess ||
+            cudaStreamWaitEvent(ss, fork.e, 0) != cudaSuccess)
+          return K3MOE_ERR_CUDA;
+        s = run_shared_tc(di, dims, xc, Tc, sh_gate, sh_up, sh_down, wt, status_dev, ss, true);
+        if (cudaEventRecord(join.e, ss) != cudaSuccess && s == K3MOE_OK) s = K3MOE_ERR_CUDA;
+        if (s != K3MOE_OK) return s;
+      }
+      s = run_route_tc(di, dims, xc, Tc, wr_bf16, bias, wt, idx_c, w_c, status_dev, st, ss);
       if (s != K3MOE_OK) return s;
+      if (ss && cudaStreamWaitEvent(st, join.e, 0) != cudaSuccess) return K3MOE_ERR_CUDA;
       s = run_ffn_tc(di, dims, xc, Tc, experts, idx_c, w_c, shared ? sh_gate : nullptr,
                      shared ? sh_up : nullptr, shared ? sh_down : nullptr, wt,
                      static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt,
-                     accumulate, status_dev, st);
+                     accumulate, status_dev, st, false, ss != nullptr);
       if (s != K3MOE_OK) return s;
     }
     return K3MOE_OK;
@@ -1190,6 +1237,18 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
     if (s != K3MOE_OK) return s;
   }
   return K3MOE_OK;
+}
+
+}  // namespace
+
+k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t T,
+                         const uint16_t *wr_bf16, const float *bias, const k3moe_experts *experts,
+                         const uint16_t *sh_gate, const uint16_t *sh_up, const uint16_t *sh_down,
+                         int32_t *idx_out, float *w_out, void *y, k3moe_dtype ydt,
+                         int32_t accumulate, void *workspace, size_t ws_bytes,
+                         int32_t *status_dev, k3moe_stream_t stream) {
+  return layer_impl(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up, sh_down, idx_out,
+                    w_out, y, ydt, accumulate, workspace, ws_bytes, status_dev, stream, true);
 }
 
 // k3moe_layer with the static array as its workspace: size check first (nothing is
@@ -1219,9 +1278,9 @@ k3moe_status k3moe_layer_static_scratch(const k3moe_dims *dims, const uint16_t *
   if (cudaMemsetAsync(scratch, 0, kWsHeader, reinterpret_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return K3MOE_ERR_CUDA;
-  return k3moe_layer(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up, sh_down, idx_out,
-                     w_out, y, ydt, accumulate, scratch, K3MOE_STATIC_SCRATCH_BYTES, status_dev,
-                     stream);
+  return layer_impl(dims, x_bf16, T, wr_bf16, bias, experts, sh_gate, sh_up, sh_down, idx_out,
+                    w_out, y, ydt, accumulate, scratch, K3MOE_STATIC_SCRATCH_BYTES, status_dev,
+                    stream, false);
 }
 
 size_t k3moe_latent_workspace_size(const k3moe_latent_dims *dims, int32_t T) {
