@@ -253,9 +253,10 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
  *   - every miss is then read as one batch, one host-to-device copy per record (in host
  *     address order), on the call's stream, and the slots are published;
  *   - the layer is computed on the slots, the routed sum still in router order.
- * The cache is a host object; it allocates no device memory.  Host memory of the records
- * should be pinned (cudaHostAlloc / cudaHostRegister) for the copies to run at the link's
- * rate; pageable memory works, slower.  One cache may serve several layers (a key is
+ * The cache is a host object; it allocates no device memory (it keeps a few KB of pinned
+ * host memory for each pass's slot indices, freed by k3moe_cache_destroy).  Host memory of
+ * the records should be pinned (cudaHostAlloc / cudaHostRegister) for the copies to run at
+ * the link's rate; pageable memory works, slower.  One cache may serve several layers (a key is
  * (layer, expert)).  Calls on one cache must not run concurrently from several threads
  * with overlapping streams (the slots they publish would race); the host state itself is
  * locked. */

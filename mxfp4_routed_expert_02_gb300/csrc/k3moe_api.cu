@@ -1541,10 +1541,21 @@ k3moe_status k3moe_layer_streamed(const k3moe_dims *dims, k3moe_expert_cache *ca
       return K3MOE_ERR_CUDA;
     }
     // slot indices to the device (a route outside the pool keeps slot -1: that pair is
-    // dropped and reported by the FFN, after whatever the router reported)
-    if (cudaMemcpyAsync(slot_dev, cache->slot_host.data(), (size_t)n * 4, cudaMemcpyHostToDevice,
-                        st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
+    // dropped and reported by the FFN, after whatever the router reported), from pinned
+    // memory and without waiting: the FFN follows the copies on the same stream
+    if ((size_t)n > cache->slot_pin_n) {
+      if (cache->slot_pin) cudaFreeHost(cache->slot_pin);
+      cache->slot_pin = nullptr;
+      cache->slot_pin_n = 0;
+      if (cudaHostAlloc(&cache->slot_pin, (size_t)n * 4, cudaHostAllocDefault) != cudaSuccess) {
+        cache->slot_pin = nullptr;
+        return K3MOE_ERR_CUDA;
+      }
+      cache->slot_pin_n = (size_t)n;
+    }
+    std::copy(cache->slot_host.begin(), cache->slot_host.begin() + n, cache->slot_pin);
+    if (cudaMemcpyAsync(slot_dev, cache->slot_pin, (size_t)n * 4, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
       return K3MOE_ERR_CUDA;
     s = run_ffn(di, &ds, xc, Tc, &slots, slot_dev, w_c, shared ? sh_down : nullptr, ws,
                 static_cast<uint8_t *>(y) + (size_t)t0 * H * dtype_size(ydt), ydt, accumulate,

@@ -11,6 +11,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "k3moe.h"
 
 struct k3moe_expert_cache {
@@ -27,6 +29,13 @@ struct k3moe_expert_cache {
   std::mutex mu;
   // host scratch of one call (routes in, slots out)
   std::vector<int32_t> route_host, slot_host, load_host;
+  // pinned copy of a pass's slot indices, read by a copy on the call's stream; the next
+  // pass rewrites it only after its own route read-back has synchronised that stream
+  int32_t *slot_pin = nullptr;
+  size_t slot_pin_n = 0;
+  ~k3moe_expert_cache() {
+    if (slot_pin) cudaFreeHost(slot_pin);
+  }
 };
 
 namespace k3 {
