@@ -650,10 +650,10 @@ def bench_latent(ctx, args, K):
     sec = tm.t_dev / nsteps
     pk = peaks()
     peak_hbm = pk["hbm_gbs"] if pk else 6800.0
-    dom = max((k for k in kernels if k in nb),
-              key=lambda k: kernels[k]["ms_avg"] * kernels[k]["launches_per_step"])
-    dom_bytes = nb[dom] / kernels[dom]["launches_per_step"]
-    achieved = dom_bytes / (kernels[dom]["ms_avg"] * 1e-3) / 1e9
+    # the step's kernels run on two streams (the shared experts beside the routed chain),
+    # so a traced kernel's time includes its neighbours' share of the GPU: the roofline is
+    # taken over the whole step (its algorithmic bytes over the timed step)
+    achieved = bytes_step / sec / 1e9
     line = {
         "value": job_rate(nsteps, ctx.world, tm.t_dev), "unit": "tokens/s", "steps": K,
         "ms_per_step": 1e3 * sec,
@@ -662,9 +662,10 @@ def bench_latent(ctx, args, K):
                    "l2": ctx.flush_note()},
         "hbm_gbs_step": bytes_step / sec / 1e9, "algorithmic_bytes_per_step": bytes_step,
         "hbm_frac_step": bytes_step / sec / 1e9 / peak_hbm,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak_hbm,
+        "roofline": {"bound": "hbm", "kernel": "the whole step (seven launches on two streams)",
+                     "achieved": achieved, "peak": peak_hbm,
                      "unit": "GB/s", "frac": achieved / peak_hbm, "traffic": None,
-                     "algorithmic_bytes": dom_bytes,
+                     "algorithmic_bytes": bytes_step,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else
                                     "fallback 6.8 TB/s (of fallback)"},
         "kernels": kernels,
