@@ -313,6 +313,19 @@ k3moe_status run_down(const DeviceInfo *di, const k3moe_dims *d, int Tc, const E
   bool act_smem = false;
   int dgrid = H / kDownRows;
   if (dgrid > di->sms) dgrid = di->sms;
+  const int ns1 = (Tc == 1 && sh_down == nullptr) ? down_t1_slots(H, I, K, di->sms) : 0;
+  if (ns1 >= 3) {
+    // one token, no shared expert: whole-expert stages carrying their activations
+    TraceScope ts(KID_DOWN_TMA, st);
+    DownArgs a{};
+    a.T = 1; a.H = H; a.I = I; a.K = K; a.P = P;
+    a.ex = ea;
+    a.idx = idx; a.w = w; a.disp = ws.disp;
+    a.act_hi = ws.act_hi; a.act_lo = ws.act_lo; a.act_ex = ws.act_ex;
+    a.y = y; a.ydt = (int)ydt; a.accumulate = accumulate; a.NS = ns1;
+    a.status = status;
+    return launch_down_t1(a, di->sms, st, pdl) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+  }
   const int ns = down_slots(I, Tc, K, (H / kDownRows + dgrid - 1) / dgrid, &act_smem);
   TraceScope ts(ns >= 1 ? KID_DOWN_TMA : KID_DOWN, st);
   if (ns >= 1) {

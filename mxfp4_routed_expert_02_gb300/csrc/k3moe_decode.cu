@@ -563,6 +563,205 @@ size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem, int ntl) {
   return b + NS * stage;
 }
 
+// ------------------------------------------------------------------------------------
+// Down projection + router-order sum for ONE token without a shared expert (the
+// LatentMoE's experts), bulk-copy ring of whole-expert stages.  CTA b owns output rows
+// [b R, b R + R) (R a multiple of 8 chosen so that the rows spread evenly over the SMs: no
+// SM has a second tile to do while others are idle).  A stage holds one distinct expert's
+// R rows of W2 (packed + scales) AND that expert's activations (both f16 terms and the
+// group exponents), so no activation is read from global memory in the dot products.
+// Stage u goes to worker group u % 2 (eight warps); warp wg takes rows wg, wg + 8, .. of
+// the stage, its 32 lanes the input groups l, l + 32, .. (each group's activations loaded
+// once for all the warp's rows).  Then y[row] = sum_j w[j] d_j[row] in router order
+// (float), as in the other down kernels.
+// ------------------------------------------------------------------------------------
+constexpr int kD1Workers = 16;  // worker warps (two groups of eight)
+constexpr int kD1MaxSlots = 8;
+constexpr int kD1MaxRows = 48;  // rows per CTA at most
+
+__host__ __device__ inline uint32_t down_t1_stage_bytes(int I, int R) {
+  const uint32_t w = (uint32_t)R * (I / 2 + I / kGroup);  // rows: packed + scales
+  const uint32_t act = (uint32_t)I * 2 * 2 + (uint32_t)(I / kGroup) * 4;
+  return (w + act + 127u) & ~127u;
+}
+__host__ __device__ inline uint32_t down_t1_head_bytes(int K, int R) {  // bars, dbuf, w
+  return (uint32_t)((1024 + (K * R + K) * 4 + 127) & ~127);
+}
+
+__global__ void __launch_bounds__(kD1Workers * 32 + 32, 1) k_down_t1(DownArgs a, int R) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = a.H, I = a.I, K = a.K;
+  const int G2 = I / kGroup, NGL = G2 / 32, NS = a.NS;
+  const int rowb = I / 2;
+  const int r0 = (int)blockIdx.x * R;
+  const int nr = H - r0 < R ? H - r0 : R;  // rows of this CTA (the last may have fewer)
+  const uint32_t wbytes = (uint32_t)nr * rowb, sbytes = (uint32_t)nr * G2;
+  const uint32_t wcap = (uint32_t)R * rowb, scap = (uint32_t)R * G2;  // stage layout
+  const uint32_t abytes = (uint32_t)I * 2, ebytes = (uint32_t)G2 * 4;
+  const uint32_t stage_bytes = down_t1_stage_bytes(I, R);
+  const uint32_t tx = wbytes + sbytes + 2 * abytes + ebytes;
+  constexpr int NW = kD1Workers * 32;
+
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [NS]
+  uint64_t *empty = full + kD1MaxSlots;                  // [NS]
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 512);
+  float *dbuf = reinterpret_cast<float *>(smem + 1024);  // [K][R]
+  float *wsm = dbuf + K * R;                             // [K]
+  uint8_t *ring = smem + down_t1_head_bytes(K, R);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int q = 0; q < NS; q++) {
+      mbar_init(&full[q], 1);
+      mbar_init(&empty[q], 8);  // the eight warps of the group that consumes the stage
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int U = r0 < H ? a.disp[0] : 0;  // distinct experts (one pair each: one token)
+  const int *uexp = a.disp + 4;
+  const int *uoff = uexp + a.P;
+  const int *plist = uoff + a.P + 1;
+
+  if (warp == kD1Workers) {
+    // producer: lane p < NS fills ring slot p with the stages u = p, p + NS, ...
+    if (lane < NS) {
+      int u = lane;
+      bool ok = true;
+      for (; u < U; u += NS) {
+        const int pi = plist[uoff[u]];  // the pair of expert u
+        if (!mbar_wait(&empty[lane], ((u / NS) & 1) ^ 1)) {
+          set_status(a.status, K3MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const uint8_t *rec = a.ex.base + (long long)uexp[u] * a.ex.stride;
+        uint8_t *dst = ring + (size_t)lane * stage_bytes;
+        mbar_arrive_expect_tx(&full[lane], tx);
+        bulk_g2s(dst, rec + a.ex.off[2] + (size_t)r0 * rowb, wbytes, &full[lane]);
+        bulk_g2s(dst + wcap, rec + a.ex.off[3] + (size_t)r0 * G2, sbytes, &full[lane]);
+        bulk_g2s(dst + wcap + scap, a.act_hi + (size_t)pi * I, abytes, &full[lane]);
+        bulk_g2s(dst + wcap + scap + abytes, a.act_lo + (size_t)pi * I, abytes, &full[lane]);
+        bulk_g2s(dst + wcap + scap + 2 * abytes, a.act_ex + (size_t)pi * G2, ebytes,
+                 &full[lane]);
+      }
+      if (!ok && u - NS >= 0)  // bounded wait for this slot's last issued fill
+        mbar_wait(&full[lane], ((u - NS) / NS) & 1, 400000000LL);
+    }
+    return;
+  }
+
+  const int gd = warp >> 3, wg = warp & 7;
+  bool aborted = false;
+  for (int i = tid; i < K; i += NW) wsm[i] = a.w[i];
+  for (int i = tid; i < K * R; i += NW) dbuf[i] = 0.f;
+  asm volatile("bar.sync 1, %0;" ::"r"(NW) : "memory");
+  for (int u = gd; u < U; u += 2) {
+    const int q = u % NS;
+    if (!aborted && !mbar_wait(&full[q], (u / NS) & 1)) {
+      set_status(a.status, K3MOE_ERR_TIMEOUT);
+      aborted = true;
+      *abort_flag = 1;
+    }
+    if (!aborted) {
+      const uint8_t *st = ring + (size_t)q * stage_bytes;
+      const uint8_t *ss = st + wcap;
+      const uint16_t *s_hi = reinterpret_cast<const uint16_t *>(st + wcap + scap);
+      const uint16_t *s_lo = s_hi + I;
+      const int32_t *s_ex = reinterpret_cast<const int32_t *>(st + wcap + scap + 2 * abytes);
+      const int pi = plist[uoff[u]];
+      float acc[kD1MaxRows / 8];
+#pragma unroll
+      for (int k = 0; k < kD1MaxRows / 8; k++) acc[k] = 0.f;
+      for (int g = 0; g < NGL; g++) {
+        const int gg = g * 32 + lane;
+        uint32_t xh[16], xl[16];
+        const uint4 *ph = reinterpret_cast<const uint4 *>(s_hi + act_index(0, I, gg, 0));
+        const uint4 *pl = reinterpret_cast<const uint4 *>(s_lo + act_index(0, I, gg, 0));
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          const uint4 x0 = ph[c * G2], x1 = pl[c * G2];
+          xh[4 * c] = x0.x; xh[4 * c + 1] = x0.y; xh[4 * c + 2] = x0.z; xh[4 * c + 3] = x0.w;
+          xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
+        }
+        const int ex = s_ex[gg];
+#pragma unroll
+        for (int k = 0; k < kD1MaxRows / 8; k++) {
+          const int row = wg + 8 * k;
+          if (row < nr) {
+            const uint4 wv = reinterpret_cast<const uint4 *>(st + row * rowb)[gg];
+            const uint32_t sv = ss[row * G2 + gg];
+            if (sv != 255u) acc[k] += group_dot2(xh, xl, wv) * group_factor(sv, ex);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kD1MaxRows / 8; k++) {
+        if (wg + 8 * k < nr) {
+          float v = acc[k];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) dbuf[pi * R + wg + 8 * k] = v;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[q]);  // also when aborted: the producer never hangs
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NW) : "memory");
+  if (tid < nr) {
+    float sum = 0.f;
+    for (int j = 0; j < K; j++) sum = __fadd_rn(sum, __fmul_rn(wsm[j], dbuf[j * R + tid]));
+    if (*abort_flag) sum = 0.f;
+    const size_t o = (size_t)r0 + tid;
+    if (a.ydt == K3MOE_F32) {
+      float *yf = reinterpret_cast<float *>(a.y);
+      yf[o] = a.accumulate ? __fadd_rn(yf[o], sum) : sum;
+    } else {
+      uint16_t *yb = reinterpret_cast<uint16_t *>(a.y);
+      yb[o] = f32_to_bf16(a.accumulate ? __fadd_rn(bf16_lo(yb[o]), sum) : sum);
+    }
+  }
+}
+
+// Rows per CTA of k_down_t1 for H outputs on `sms` SMs (a multiple of 8, even spread).
+int down_t1_rows(int H, int sms) {
+  int R = (H + sms - 1) / sms;
+  R = (R + 7) / 8 * 8;
+  return R < 8 ? 8 : R;
+}
+
+// Ring slots of k_down_t1 for (H, I, K) on `sms` SMs (0: the kernel does not apply).
+int down_t1_slots(int H, int I, int K, int sms) {
+  if (I % 1024 != 0 || K > 32 || H % 8 != 0) return 0;  // 32 group lanes x NGL groups
+  const int R = down_t1_rows(H, sms);
+  if (R > kD1MaxRows) return 0;
+  const size_t avail = 227 * 1024 - down_t1_head_bytes(K, R);
+  int ns = (int)(avail / down_t1_stage_bytes(I, R));
+  if (ns > kD1MaxSlots) ns = kD1MaxSlots;
+  return ns >= 3 ? ns : 0;
+}
+
+cudaError_t launch_down_t1(const DownArgs &a, int sms, cudaStream_t st, bool pdl) {
+  const int R = down_t1_rows(a.H, sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.H + R - 1) / R);
+  cfg.blockDim = dim3(kD1Workers * 32 + 32);
+  cfg.dynamicSmemBytes = down_t1_head_bytes(a.K, R) + (size_t)a.NS * down_t1_stage_bytes(a.I, R);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_down_t1, a, R);
+}
+
 cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool pdl,
                             bool act_smem) {
   cudaLaunchConfig_t cfg = {};
@@ -591,7 +790,8 @@ cudaError_t set_decode_smem_limits() {
                        reinterpret_cast<const void *>(k_gateup_t1<8, true, 4>),
                        reinterpret_cast<const void *>(k_gateup_t1<16, true, 4>),
                        reinterpret_cast<const void *>(k_down_tma<true>),
-                       reinterpret_cast<const void *>(k_down_tma<false>)};
+                       reinterpret_cast<const void *>(k_down_tma<false>),
+                       reinterpret_cast<const void *>(k_down_t1)};
   for (const void *f : fns) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     if (e != cudaSuccess) return e;

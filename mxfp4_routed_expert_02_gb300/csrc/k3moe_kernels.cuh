@@ -141,6 +141,10 @@ cudaError_t launch_gateup_t1(const GateUpT1Args &a, int grid, cudaStream_t st, b
 size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem, int ntl);
 cudaError_t launch_down_tma(const DownArgs &a, int grid, cudaStream_t st, bool pdl,
                             bool act_smem);
+// The single-token down without a shared expert, whole-expert stages with their
+// activations (k_down_t1): ring slots for (I, K), 0 when it does not apply.
+int down_t1_slots(int H, int I, int K, int sms);
+cudaError_t launch_down_t1(const DownArgs &a, int sms, cudaStream_t st, bool pdl);
 cudaError_t set_decode_smem_limits();
 
 __global__ void k_dequant(const uint8_t *__restrict__ packed, const uint8_t *__restrict__ scales,

@@ -115,6 +115,8 @@ SHAPES = [
     (768, 384, 256, 12, 5, 1, 7),       # odd top-k, one shared expert; projections and
                                         # experts on the tensor cores (more than 4 tokens)
     (1024, 512, 512, 24, 6, 2, 67),     # a 64-token pass on the tensor cores, then 3 tokens
+    (2048, 1024, 512, 24, 6, 2, 1),     # one token on the single-token kernels (ring gate/up,
+    (2048, 1024, 1024, 24, 5, 0, 1),    # whole-expert down stages), odd top-k, no shared
 ]
 
 
