@@ -613,6 +613,7 @@ k3moe_status run_shared_tc(const DeviceInfo *di, const k3moe_dims *d, const uint
     s1.tile_off = ws.tile_off1;
     s1.ngroups = 1;
     s1.ntile = nt1;
+    s1.a_once = Tc <= nt1;
     {
       TcGemmArgs a = s1;
       a.mtiles = (SI + kTcRows - 1) / kTcRows;
@@ -726,6 +727,7 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x
   g.gid = nullptr;
   g.ngroups = E;
   g.ntile = ntile;
+  g.a_once = Tc <= ntile;  // a token picks an expert once: at most Tc rows per group
   g.b1 = d->situ_b1;
   g.b2 = d->situ_b2;
   g.status = status;
@@ -824,6 +826,7 @@ k3moe_status run_route_tc(const DeviceInfo *di, const k3moe_dims *d, const uint1
   a.tile_off = wt.tile_off1;
   a.ngroups = 1;
   a.ntile = kTcRows;
+  a.a_once = Tc <= kTcRows;
   a.mtiles = (E + kTcRows - 1) / kTcRows;
   a.M_rows = E;
   tc_k_split(2LL * H, a);
@@ -1361,6 +1364,7 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
       g1.gid = nullptr;
       g1.ngroups = 1;
       g1.ntile = kTcRows;
+      g1.a_once = Tc <= kTcRows;
       g1.b1 = b1;
       g1.b2 = b2;
       g1.status = status_dev;

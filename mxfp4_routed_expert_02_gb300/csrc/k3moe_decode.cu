@@ -127,11 +127,15 @@ __global__ void __launch_bounds__(HP == 4 ? 576 : 512, 1) k_gateup_t1(GateUpT1Ar
         const int r = tile * kTileRows + b * RB;
         uint8_t *dst = ring + (size_t)p * stage_bytes;
         mbar_arrive_expect_tx(&full[p], stage_bytes);
-        bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, RB * rowb, &full[p]);
-        bulk_g2s(dst + RB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, RB * rowb, &full[p]);
-        bulk_g2s(dst + 2 * RB * rowb, rec + a.ex.off[1] + (size_t)r * G, RB * G, &full[p]);
-        bulk_g2s(dst + 2 * RB * rowb + RB * G, rec + a.ex.off[5] + (size_t)r * G, RB * G,
-                 &full[p]);
+        // weights are read once: first out of L2
+        const uint64_t pol = l2_evict_first();
+        bulk_g2s_pol(dst, rec + a.ex.off[0] + (size_t)r * rowb, RB * rowb, &full[p], pol);
+        bulk_g2s_pol(dst + RB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, RB * rowb, &full[p],
+                     pol);
+        bulk_g2s_pol(dst + 2 * RB * rowb, rec + a.ex.off[1] + (size_t)r * G, RB * G, &full[p],
+                     pol);
+        bulk_g2s_pol(dst + 2 * RB * rowb + RB * G, rec + a.ex.off[5] + (size_t)r * G, RB * G,
+                     &full[p], pol);
       }
       if (!ok && it - NS >= 0)  // bounded wait for this slot's last issued fill
         mbar_wait(&full[p], ((it - NS) / NS) & 1, 400000000LL);
@@ -416,9 +420,11 @@ __global__ void __launch_bounds__(544, 1) k_down_tma(DownArgs a) {
         const uint8_t *rec = a.ex.base + (long long)uexp[u] * a.ex.stride;
         uint8_t *dst = ring + (size_t)p * stage_bytes;
         mbar_arrive_expect_tx(&full[p], stage_bytes);
-        bulk_g2s(dst, rec + a.ex.off[2] + (size_t)rs * rowb, kDnStageRows * rowb, &full[p]);
-        bulk_g2s(dst + kDnStageRows * rowb, rec + a.ex.off[3] + (size_t)rs * G2,
-                 kDnStageRows * G2, &full[p]);
+        const uint64_t pol = l2_evict_first();  // weights are read once: first out of L2
+        bulk_g2s_pol(dst, rec + a.ex.off[2] + (size_t)rs * rowb, kDnStageRows * rowb, &full[p],
+                     pol);
+        bulk_g2s_pol(dst + kDnStageRows * rowb, rec + a.ex.off[3] + (size_t)rs * G2,
+                     kDnStageRows * G2, &full[p], pol);
       }
       if (!ok && it - NS >= 0) mbar_wait(&full[p], ((it - NS) / NS) & 1, 400000000LL);
     }
@@ -643,8 +649,9 @@ __global__ void __launch_bounds__(kD1Workers * 32 + 32, 1) k_down_t1(DownArgs a,
         const uint8_t *rec = a.ex.base + (long long)uexp[u] * a.ex.stride;
         uint8_t *dst = ring + (size_t)lane * stage_bytes;
         mbar_arrive_expect_tx(&full[lane], tx);
-        bulk_g2s(dst, rec + a.ex.off[2] + (size_t)r0 * rowb, wbytes, &full[lane]);
-        bulk_g2s(dst + wcap, rec + a.ex.off[3] + (size_t)r0 * G2, sbytes, &full[lane]);
+        const uint64_t pol = l2_evict_first();  // weights are read once: first out of L2
+        bulk_g2s_pol(dst, rec + a.ex.off[2] + (size_t)r0 * rowb, wbytes, &full[lane], pol);
+        bulk_g2s_pol(dst + wcap, rec + a.ex.off[3] + (size_t)r0 * G2, sbytes, &full[lane], pol);
         bulk_g2s(dst + wcap + scap, a.act_hi + (size_t)pi * I, abytes, &full[lane]);
         bulk_g2s(dst + wcap + scap + abytes, a.act_lo + (size_t)pi * I, abytes, &full[lane]);
         bulk_g2s(dst + wcap + scap + 2 * abytes, a.act_ex + (size_t)pi * G2, ebytes,

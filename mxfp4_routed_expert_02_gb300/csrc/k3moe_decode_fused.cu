@@ -298,6 +298,9 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
     // ---------------- producer: lane p < NSG owns ring slot p ----------------
     bool ab = false;
     int last_g = -1;  // this lane's last R/S/G stage
+    // every weight byte is read once per step: its lines are the first L2 evicts (the
+    // lines the step finds in L2 stay, so dirty ones are not written back during it)
+    const uint64_t pol_first = l2_evict_first();
     if (lane < NSG) {
       int ready = 0;  // selections this lane has seen published
       for (int t = lane; t < nRSG; t += NSG) {
@@ -347,13 +350,13 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
           const int nrow = cntR - k0 < 2 ? cntR - k0 : 2;
           mbar_arrive_expect_tx(&fullG[lane], (uint32_t)(nrow * rowh));
           for (int rr = 0; rr < nrow; rr++)
-            bulk_g2s(dst + rr * rowh, lw.wr + (size_t)(bx + nb * (k0 + rr)) * H, rowh,
-                     &fullG[lane]);
+            bulk_g2s_pol(dst + rr * rowh, lw.wr + (size_t)(bx + nb * (k0 + rr)) * H, rowh,
+                         &fullG[lane], pol_first);
         } else if (t < tG) {
           const int p = bx + nb * (t - tS);
           mbar_arrive_expect_tx(&fullG[lane], (uint32_t)(2 * rowh));
-          bulk_g2s(dst, lw.sh_gate + (size_t)p * H, rowh, &fullG[lane]);
-          bulk_g2s(dst + rowh, lw.sh_up + (size_t)p * H, rowh, &fullG[lane]);
+          bulk_g2s_pol(dst, lw.sh_gate + (size_t)p * H, rowh, &fullG[lane], pol_first);
+          bulk_g2s_pol(dst + rowh, lw.sh_up + (size_t)p * H, rowh, &fullG[lane], pol_first);
         } else {
           const int tg = t - tG;
           const int item = bx + nb * (tg >> 1);
@@ -361,13 +364,14 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
           const int r = blk * kFuItemRows + (tg & 1) * kFuRB;
           const uint8_t *rec = lw.experts + (long long)sel[j] * lw.stride;
           mbar_arrive_expect_tx(&fullG[lane], gstage);
-          bulk_g2s(dst, rec + a.ex.off[0] + (size_t)r * rowb, kFuRB * rowb, &fullG[lane]);
-          bulk_g2s(dst + kFuRB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, kFuRB * rowb,
-                   &fullG[lane]);
-          bulk_g2s(dst + 2 * kFuRB * rowb, rec + a.ex.off[1] + (size_t)r * G, kFuRB * G,
-                   &fullG[lane]);
-          bulk_g2s(dst + 2 * kFuRB * rowb + kFuRB * G, rec + a.ex.off[5] + (size_t)r * G,
-                   kFuRB * G, &fullG[lane]);
+          bulk_g2s_pol(dst, rec + a.ex.off[0] + (size_t)r * rowb, kFuRB * rowb, &fullG[lane],
+                       pol_first);
+          bulk_g2s_pol(dst + kFuRB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, kFuRB * rowb,
+                       &fullG[lane], pol_first);
+          bulk_g2s_pol(dst + 2 * kFuRB * rowb, rec + a.ex.off[1] + (size_t)r * G, kFuRB * G,
+                       &fullG[lane], pol_first);
+          bulk_g2s_pol(dst + 2 * kFuRB * rowb + kFuRB * G, rec + a.ex.off[5] + (size_t)r * G,
+                       kFuRB * G, &fullG[lane], pol_first);
         }
         last_g = t;
       }
@@ -430,14 +434,15 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
         if (routed) {
           for (int e2 = 0; e2 < 2; e2++) {
             const uint8_t *rec = lw.experts + (long long)sel[2 * m + e2] * lw.stride;
-            bulk_g2s(dst + e2 * dexp, rec + a.ex.off[2] + (size_t)r0 * rowb2,
-                     kFuDownRows * rowb2, &fullD[q]);
-            bulk_g2s(dst + e2 * dexp + kFuDownRows * rowb2,
-                     rec + a.ex.off[3] + (size_t)r0 * G2, kFuDownRows * G2, &fullD[q]);
+            bulk_g2s_pol(dst + e2 * dexp, rec + a.ex.off[2] + (size_t)r0 * rowb2,
+                         kFuDownRows * rowb2, &fullD[q], pol_first);
+            bulk_g2s_pol(dst + e2 * dexp + kFuDownRows * rowb2,
+                         rec + a.ex.off[3] + (size_t)r0 * G2, kFuDownRows * G2, &fullD[q],
+                         pol_first);
           }
         } else {
           const int rs0 = r0 + (m - hk) * RS;
-          bulk_g2s(dst, lw.sh_down + (size_t)rs0 * SI, wbytes, &fullD[q]);
+          bulk_g2s_pol(dst, lw.sh_down + (size_t)rs0 * SI, wbytes, &fullD[q], pol_first);
         }
         if (!dep2) {
           // (the expiry test waits for one arrival more than there are CTAs, briefly)

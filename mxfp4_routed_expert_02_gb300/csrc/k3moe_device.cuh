@@ -322,6 +322,29 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// L2 eviction policy "evict first" (for every access that carries it): bytes read once.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// bulk_prefetch_l2 with an L2 eviction policy.
+__device__ __forceinline__ void bulk_prefetch_l2_pol(const void *src, uint32_t bytes,
+                                                     uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+               "r"(bytes), "l"(pol)
+               : "memory");
+}
+// bulk_g2s with an L2 eviction policy.
+__device__ __forceinline__ void bulk_g2s_pol(void *dst, const void *src, uint32_t bytes,
+                                             uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // Programmatic dependent launch: wait for the previous kernel's writes / let the next
 // kernel start its prologue.  Both are no-ops when the launch is not programmatic.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

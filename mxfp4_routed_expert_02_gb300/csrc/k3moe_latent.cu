@@ -19,11 +19,12 @@ namespace k3 {
 
 namespace {
 
-__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+// A weight chunk read once: no L1 allocation, first out of L2 (policy from l2_evict_first).
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p, uint64_t pol) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return v;
 }
 
@@ -152,8 +153,8 @@ __global__ void __launch_bounds__(256) k_proj(const uint16_t *__restrict__ W,
   // each warp keeps its next row on its way to L2 while it reads the current one (weights
   // only: nothing the previous kernel writes)
   if (lane == 0 && r_first < R) {
-    bulk_prefetch_l2(W + (size_t)r_first * C, (uint32_t)C * 2);
-    if (GU) bulk_prefetch_l2(W2 + (size_t)r_first * C, (uint32_t)C * 2);
+    bulk_prefetch_l2_pol(W + (size_t)r_first * C, (uint32_t)C * 2, l2_evict_first());
+    if (GU) bulk_prefetch_l2_pol(W2 + (size_t)r_first * C, (uint32_t)C * 2, l2_evict_first());
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -165,10 +166,11 @@ __global__ void __launch_bounds__(256) k_proj(const uint16_t *__restrict__ W,
     }
     __syncthreads();
   }
+  const uint64_t pol = l2_evict_first();  // the weights are read once
   for (int r = r_first; r < R; r += r_step) {
     if (lane == 0 && r + r_step < R) {
-      bulk_prefetch_l2(W + (size_t)(r + r_step) * C, (uint32_t)C * 2);
-      if (GU) bulk_prefetch_l2(W2 + (size_t)(r + r_step) * C, (uint32_t)C * 2);
+      bulk_prefetch_l2_pol(W + (size_t)(r + r_step) * C, (uint32_t)C * 2, pol);
+      if (GU) bulk_prefetch_l2_pol(W2 + (size_t)(r + r_step) * C, (uint32_t)C * 2, pol);
     }
     const uint4 *w4 = reinterpret_cast<const uint4 *>(W + (size_t)r * C);
     const uint4 *u4 = GU ? reinterpret_cast<const uint4 *>(W2 + (size_t)r * C) : nullptr;
@@ -182,8 +184,8 @@ __global__ void __launch_bounds__(256) k_proj(const uint16_t *__restrict__ W,
 #pragma unroll
         for (int k = 0; k < kProjU; k++) {
           const int c = c0 + 32 * k;
-          wv[k] = c < nch ? ld_stream16(w4 + c) : make_uint4(0u, 0u, 0u, 0u);
-          if (GU) uv[k] = c < nch ? ld_stream16(u4 + c) : make_uint4(0u, 0u, 0u, 0u);
+          wv[k] = c < nch ? ld_stream16(w4 + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+          if (GU) uv[k] = c < nch ? ld_stream16(u4 + c, pol) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int k = 0; k < kProjU; k++) {

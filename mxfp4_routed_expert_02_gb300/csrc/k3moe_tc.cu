@@ -118,6 +118,24 @@ __device__ __forceinline__ void tma_load3d(void *dst, const CUtensorMap *map, in
       : "memory");
 }
 
+// The same with an L2 eviction policy.
+__device__ __forceinline__ void tma_load3d_pol(void *dst, const CUtensorMap *map, int x, int y,
+                                               int z, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load4d_pol(void *dst, const CUtensorMap *map, int x, int y,
+                                               int z, int w, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+      "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load4d(void *dst, const CUtensorMap *map, int x, int y, int z,
                                            int w, uint64_t *bar) {
   asm volatile(
@@ -413,6 +431,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kTcWarpTma) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      uint64_t apol;
+      if (a.a_once)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(apol));
+      else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(apol));
       for (int it = 0; it < total && !*abort_flag; it++) {
         const int c = ks_at(it / kc) * kc + it % kc;
         const TcItem ti = item_at(it / kc);
@@ -428,13 +451,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // few large copies: a stage costs the TMA unit about the same whether it moves 4 KB
         // or 32 KB, so both A matrices come in one 4-D box where their layout allows, and
         // all NT terms of B in one box of depth NT
+        // A tiles read by this item only go first out of L2 (evict first; else normal)
         if (NA > 1 && a.a_pair == 2) {
-          tma_load4d(st, &tmA0, c * kTcChunkBytes, 0, 2 * ti.mt, ga, &full[s]);
+          tma_load4d_pol(st, &tmA0, c * kTcChunkBytes, 0, 2 * ti.mt, ga, &full[s], apol);
         } else if (NA > 1 && a.a_pair) {
-          tma_load4d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, 0, ga, &full[s]);
+          tma_load4d_pol(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, 0, ga, &full[s], apol);
         } else {
-          tma_load3d(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
-          if (NA > 1) tma_load3d(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s]);
+          tma_load3d_pol(st, &tmA0, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s], apol);
+          if (NA > 1)
+            tma_load3d_pol(st + kTcBox, &tmA1, c * kTcChunkBytes, ti.mt * kTcTile, ga, &full[s],
+                           apol);
         }
         tma_load3d(st + NA * kTcBox, &tmB, c * kTcChunkBytes, ti.brow0, 0, &full[s]);
       }

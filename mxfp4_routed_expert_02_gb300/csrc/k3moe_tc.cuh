@@ -49,6 +49,8 @@ struct TcGemmArgs {
   long long out_mstride;   // kBf16Pair: the second matrix's output at out + out_mstride
   float b1, b2;            // SiTU caps (gate/up epilogue)
   int32_t *status;
+  int a_once;              // every A tile is read by one item only (each group's B rows fit
+                           // one tile): its loads are marked first out of L2
 };
 
 // kBf16Pair: two bf16 matrices on one B, both products stored (the gate/up pair's partial
