@@ -78,11 +78,12 @@ TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode_fused.cu",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_device.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_topk.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_kernels.cuh"]
-# k_decode_fused: captured with a 64-expert pool (351,598,080 B per launch), plus the
-# router rows the full 896-expert pool adds ((896 - 64) x 7168 x 2 B): every other byte
-# the kernel reads is the same at both pool sizes (16 selected experts, the shared expert).
-TRAFFIC_CAPTURED = {"sources": "f4f4b1248ad42362",
-                    "bytes": {"k_decode_fused": 351598080 + (896 - 64) * 7168 * 2}}
+# k_decode_fused: captured with a 64-expert pool (347,882,240 B read + 3,195,136 B written
+# per launch), plus the router rows the full 896-expert pool adds ((896 - 64) x 7168 x 2 B):
+# every other byte the kernel reads is the same at both pool sizes (16 selected experts,
+# the shared expert).
+TRAFFIC_CAPTURED = {"sources": "822c78ca301b237b",
+                    "bytes": {"k_decode_fused": 347882240 + 3195136 + (896 - 64) * 7168 * 2}}
 
 
 def traffic_of(kernel):
