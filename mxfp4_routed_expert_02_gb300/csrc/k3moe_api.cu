@@ -680,11 +680,14 @@ k3moe_status run_ffn_tc(const DeviceInfo *di, const k3moe_dims *d, const void *x
   record_offsets(d, off);
   const uint8_t *rec = ex->experts;
   const unsigned long long es = (unsigned long long)ex->expert_stride;
-  // B rows per tile: 1.25 x the mean number of pairs per expert, rounded up to 16, at
-  // most 128 (few experts then need a second tile)
+  // B rows per tile: 1.25 x the mean number of pairs per expert, rounded up to a power of
+  // two from 16 to 128 (few experts then need a second tile; measured, heights of 48 and
+  // 96 rows run slower than the powers of two beside them: 4096 tokens 7.40 ms at 96 rows,
+  // 6.85 ms at 128)
   const int used = P < E ? P : E;
-  int ntile = ((((5 * P + 4 * used - 1) / (4 * used)) + 15) / 16) * 16;
-  ntile = ntile > kTcRows ? kTcRows : ntile;
+  const int want = (5 * P + 4 * used - 1) / (4 * used);
+  int ntile = 16;
+  while (ntile < want && ntile < kTcRows) ntile *= 2;
   const int chunk = route_chunk(P), nch = (P + chunk - 1) / chunk;
   {
     TraceScope ts(KID_ROUTE_HIST, st);
