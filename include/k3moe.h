@@ -28,7 +28,7 @@
  *   - Thread safety: calls are independent; two calls may run concurrently only if
  *     they use different workspaces.
  *   - Workspace: zero-fill it once before its first use (e.g. one cudaMemsetAsync).  Its
- *     first 256 bytes hold counters of the single-token kernel that must be zero when a
+ *     first 4096 bytes hold counters of the single-token kernels that must be zero when a
  *     call starts; every call leaves them zero, so a workspace can be reused across calls,
  *     entry points, shapes and token counts without clearing it again.  Do not write to
  *     a workspace between calls.  The rest is scratch.
@@ -171,7 +171,7 @@ k3moe_status k3moe_layer(const k3moe_dims *dims, const uint16_t *x_bf16, int32_t
  *     looks up the device address of the array (which may load the library's device
  *     code) and sets kernel attributes.  Make that first call before any stream capture
  *     starts on the device.  K3MOE_ERR_CUDA if the lookup fails.
- *   - Each call first clears the counter words at the array's start (the 256 bytes that
+ *   - Each call first clears the counter words at the array's start (the 4096 bytes that
  *     Workspace above describes) with one cudaMemsetAsync on `stream`, which allocates
  *     nothing; so a call starts clean even after earlier calls raced on the array.  The
  *     rest of the array is written before it is read.

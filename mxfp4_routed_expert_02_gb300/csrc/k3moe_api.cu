@@ -49,7 +49,8 @@ const DeviceInfo *device_info() {
             cudaSuccess ||
         cudaFuncSetAttribute(k_route_candidates, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              128 * 1024) != cudaSuccess ||
-        set_decode_smem_limits() != cudaSuccess || set_fused_smem_limit() != cudaSuccess)
+        set_decode_smem_limits() != cudaSuccess || set_fused_smem_limit() != cudaSuccess ||
+        set_gateup_tc1_smem_limit() != cudaSuccess)
       return nullptr;
     d.attrs_set = true;
   }
@@ -112,14 +113,17 @@ struct Ws {
   uint16_t *act_hi, *act_lo;
   int32_t *act_ex;
   float *act_s;
-  unsigned *bar;  // grid-barrier counters of the single-token fused kernel
+  unsigned *bar;  // grid-barrier counters of the single-token kernels (the header)
+  float *gpart;   // one token: partial gate/up sums of row tiles split between CTAs
   size_t total;
 };
 
-// The first kWsHeader bytes of every workspace hold the single-token kernel's grid-wide
+// The first kWsHeader bytes of every workspace hold the single-token kernels' grid-wide
 // counters, which must be zero before a call and are zero again after it; no layout
-// places anything else there.
-constexpr size_t kWsHeader = 256;
+// places anything else there: words [0, 4 kFuMaxLayers) the fused kernel's (4 per layer),
+// then those of the tensor-core gate/up (an exit counter and one per row tile).
+constexpr size_t kWsHeader = 4096;
+static_assert(4 * kFuMaxLayers + 1 + kTc1MaxTiles <= kWsHeader / 4, "counters overflow");
 
 Ws ws_layout(const k3moe_dims *d, int T, void *base) {
   const int Tc = T < kDecodeTokens ? T : kDecodeTokens;
@@ -141,6 +145,11 @@ Ws ws_layout(const k3moe_dims *d, int T, void *base) {
   w.act_lo = reinterpret_cast<uint16_t *>(take(P * d->inter * 2));
   w.act_ex = reinterpret_cast<int32_t *>(take(P * (d->inter / kGroup) * 4));
   w.act_s = reinterpret_cast<float *>(take((size_t)Tc * (d->shared_inter > 0 ? d->shared_inter : 1) * 4));
+  if (Tc == 1) {  // the tensor-core gate/up's split tiles: kTc1Pieces x 256 floats each
+    const int tiles = d->topk * ((d->inter + 127) / 128);
+    if (tiles <= kTc1MaxTiles)
+      w.gpart = reinterpret_cast<float *>(take((size_t)tiles * kTc1Pieces * 256 * 4));
+  }
   w.bar = reinterpret_cast<unsigned *>(b);  // the header
   w.total = o;
   return w;
@@ -156,14 +165,15 @@ enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KI
                 KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
                 KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_NORMS, KID_TC_ROUTER,
                 KID_ROUTE_CAND, KID_DECODE_FUSED, KID_PROJ, KID_SHARED_GATEUP, KID_RMSNORM_F32,
-                KID_PROJ_UP, KID_PROJ_SHARED_DOWN, KID_COUNT };
+                KID_PROJ_UP, KID_PROJ_SHARED_DOWN, KID_GATEUP_TC1, KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {
     "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
     "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
     "k_route_scatter", "k_quant_x", "k_tc_gemm_gateup", "k_quant_act", "k_tc_gemm_down",
     "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine",
     "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused", "k_proj_down",
-    "k_proj_shared_gateup", "k_rmsnorm_f32w", "k_proj_up", "k_proj_shared_down"};
+    "k_proj_shared_gateup", "k_rmsnorm_f32w", "k_proj_up", "k_proj_shared_down",
+    "k_gateup_tc1"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -442,6 +452,44 @@ FusedLayer fused_layer_of(const uint16_t *wr, const float *bias, const k3moe_exp
   return f;
 }
 
+// The single-token gate/up + SiTU (with the top-k and the dispatch lists): on the tensor
+// cores (k_gateup_tc1, one CTA per SM) where the shape, the grid and the workspace allow
+// it and the tensor maps of the expert pool encode, else k_gateup_t1 on grid_t1 CTAs.
+k3moe_status run_gateup1(const DeviceInfo *di, const k3moe_dims *d, const k3moe_experts *ex,
+                         const GateUpT1Args &a, Ws &ws, int grid_t1, cudaStream_t st, bool pdl) {
+  int ns = 0;
+  if (ws.gpart &&
+      gateup_tc1_smem(d->hidden, d->inter, d->n_experts, d->topk, di->sms, &ns) > 0) {
+    int64_t off[7];
+    record_offsets(d, off);
+    const unsigned long long H = (unsigned long long)d->hidden, I = (unsigned long long)d->inter;
+    const unsigned long long E = (unsigned long long)d->n_experts;
+    const unsigned long long es = (unsigned long long)ex->expert_stride;
+    // gate and up as one 4-D map: K bytes, rows, {gate, up}, expert; boxes of 128 rows x
+    // 128 bytes of both.  Their scales: 8-byte words (8 groups), rows, {gate, up}, expert.
+    const unsigned long long dw[4] = {H / 2, I, 2, E};
+    const unsigned long long sw[3] = {H / 2, (unsigned long long)(off[4] - off[0]), es};
+    const unsigned bw[4] = {(unsigned)kTcChunk, (unsigned)kTcRows, 2, 1};
+    const unsigned long long ds[4] = {H / 256, I, 2, E};
+    const unsigned long long ss[3] = {H / kGroup, (unsigned long long)(off[5] - off[1]), es};
+    const unsigned bs[4] = {2, (unsigned)kTcRows, 2, 1};
+    CUtensorMap mw, ms;
+    if (off[4] > off[0] && off[5] > off[1] && tc_map(&mw, ex->experts + off[0], 4, dw, sw, bw) &&
+        tc_map_words(&ms, ex->experts + off[1], 4, ds, ss, bs)) {
+      GateUpTc1Args t{};
+      t.g = a;
+      t.gpart = ws.gpart;
+      t.cnt = ws.bar + 4 * kFuMaxLayers;
+      t.NS = ns;
+      TraceScope ts(KID_GATEUP_TC1, st);
+      return launch_gateup_tc1(t, mw, ms, di->sms, st, pdl) == cudaSuccess ? K3MOE_OK
+                                                                            : K3MOE_ERR_CUDA;
+    }
+  }
+  TraceScope ts(KID_GATEUP_T1, st);
+  return launch_gateup_t1(a, grid_t1, st, pdl) == cudaSuccess ? K3MOE_OK : K3MOE_ERR_CUDA;
+}
+
 // The whole layer for Tc tokens.  One token with a supported width: router kernel, then
 // the single-token gate/up kernel (top-k and dispatch fused), then the down kernel, the
 // last two launched as programmatic dependents so their prologues overlap the previous
@@ -474,10 +522,10 @@ k3moe_status run_layer(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
     a.status = status; a.RB = rb; a.NS = ns;
     const bool pdl = !g_trace.on;
     {
-      TraceScope ts(KID_GATEUP_T1, st);
       int grid = d->topk * (d->inter / kTileRows);
       if (grid > di->sms) grid = di->sms;
-      if (launch_gateup_t1(a, grid, st, pdl) != cudaSuccess) return K3MOE_ERR_CUDA;
+      s = run_gateup1(di, d, ex, a, ws, grid, st, pdl);
+      if (s != K3MOE_OK) return s;
     }
     return run_down(di, d, Tc, ea, idx, w, sh_down, ws, y, ydt, accumulate, status, st, pdl);
   }
@@ -1416,10 +1464,10 @@ k3moe_status k3moe_latent_layer(const k3moe_latent_dims *dims, const k3moe_laten
       g.act_hi = ws.ffn.act_hi; g.act_lo = ws.ffn.act_lo; g.act_ex = ws.ffn.act_ex;
       g.status = status_dev; g.RB = rb; g.NS = ns;
       {
-        TraceScope ts(KID_GATEUP_T1, st);
         int grid = K * (dims->inter / kTileRows);
         if (grid > di->sms) grid = di->sms;
-        if (launch_gateup_t1(g, grid, st, !g_trace.on) != cudaSuccess) return K3MOE_ERR_CUDA;
+        s = run_gateup1(di, &lat, &lw->experts, g, ws.ffn, grid, st, !g_trace.on);
+        if (s != K3MOE_OK) return s;
       }
       s = run_down(di, &lat, 1, ea, idx_c, w_c, nullptr, ws.ffn, ws.accl, K3MOE_F32, 0,
                    status_dev, st, !g_trace.on);

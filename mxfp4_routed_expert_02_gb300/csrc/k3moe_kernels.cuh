@@ -110,6 +110,10 @@ struct FusedLayer {
 };
 // Layers per launch: each uses four grid counters of the 256-byte workspace header.
 constexpr int kFuMaxLayers = 16;
+// The tensor-core single-token gate/up (k_gateup_tc1): row tiles (expert slots x 128 rows)
+// at most, and the parts one tile may be split into between CTAs.
+constexpr int kTc1MaxTiles = 768;
+constexpr int kTc1Pieces = 2;
 struct FusedT1Args {
   const uint16_t *x;  // [H] bf16 (unused when h is set)
   const float *h;     // [H] residual stream: when set, x = bf16(RMSNorm(h)) in the kernel

@@ -6,7 +6,7 @@
 // LatentMoE listing, steps 3 and 6): y_t = sum_j w[t,j] d_j in slot order j, in float,
 // then the shared expert added unweighted; README of Maknee/Kimi-K3.cpp, "The
 // consumer-memory idea" item 7, fixes the router order of that sum.
-#include "k3moe_tc.cuh"
+#include "k3moe_tcgen05.cuh"
 
 namespace k3 {
 
@@ -139,48 +139,6 @@ __global__ void k_route_scatter(const int32_t *__restrict__ idx, int P, int E, i
   }
 }
 
-// One group of 32 values -> NT MXFP4 terms: term i takes the residual left by terms
-// 0..i-1, with the E8M0 scale 2^e chosen so that max|r| <= 6 * 2^e and each value rounded
-// to the nearest E2M1 code (hardware conversion, round to nearest even); residuals are
-// exact in float.  Codes packed two per byte, the even element in the low nibble.
-template <int NT>
-__device__ __forceinline__ void encode_terms(float (&r)[32], uint4 (&q)[NT], uint8_t (&sb)[NT]) {
-#pragma unroll
-  for (int t = 0; t < NT; t++) {
-    float m = 0.f;
-#pragma unroll
-    for (int k = 0; k < 32; k++) m = fmaxf(m, fabsf(r[k]));
-    int e = -127;
-    if (m > 0.f) {
-      e = exponent_of(m) - 2;
-      if (m > 6.f * pow2i(e)) e++;
-      e = e < -127 ? -127 : (e > 127 ? 127 : e);
-    }
-    sb[t] = (uint8_t)(e + 127);
-    const float inv_s = pow2i(-e), s = pow2i(e);
-    uint32_t w[4];
-#pragma unroll
-    for (int wq = 0; wq < 4; wq++) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int bb = 0; bb < 4; bb++) {
-        const int k = 8 * wq + 2 * bb;
-        uint32_t byte;
-        asm("{ .reg .b8 t8; cvt.rn.satfinite.e2m1x2.f32 t8, %1, %2; cvt.u32.u8 %0, t8; }"
-            : "=r"(byte)
-            : "f"(r[k + 1] * inv_s), "f"(r[k] * inv_s));
-        word |= byte << (8 * bb);
-        // residual: subtract the decoded value (exact)
-        const uint32_t h2 = e2m1x2_to_f16x2(byte);
-        const __half2 hv = *reinterpret_cast<const __half2 *>(&h2);
-        r[k] = __fsub_rn(r[k], __low2float(hv) * s);
-        r[k + 1] = __fsub_rn(r[k + 1], __high2float(hv) * s);
-      }
-      w[wq] = word;
-    }
-    q[t] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 // x [T][H] bf16 (or float: XF32, the LatentMoE's latent) -> the kTcTermsX-term encoding of
 // every (token, slot) pair's row, written at the pair's sorted position: xq [term][P][H/2]

@@ -63,6 +63,9 @@ enum class TcKind { kMxf4GateUp, kMxf4Down, kMxf4DownPair, kBf16GateUp, kBf16Pai
 // box[1..]; false if the driver entry point is missing or the layout is refused.
 bool tc_map(CUtensorMap *m, const void *base, int rank, const unsigned long long *dims,
             const unsigned long long *strides, const unsigned *box);
+// The same for 8-byte words without swizzle (dims[0] in words).
+bool tc_map_words(CUtensorMap *m, const void *base, int rank, const unsigned long long *dims,
+                  const unsigned long long *strides, const unsigned *box);
 // The 3-D case (inner = K bytes, rows, depth) with boxes of kTcChunk bytes x box_rows x
 // box_depth.
 bool tc_map3d(CUtensorMap *m, const void *base, unsigned long long inner_bytes,
@@ -77,6 +80,24 @@ cudaError_t launch_situ_parts(cudaStream_t st, int sms, const float *part, int K
 cudaError_t launch_tc_gemm(TcKind kind, const TcGemmArgs &a, const CUtensorMap &A0,
                            const CUtensorMap &A1, const CUtensorMap &B, int grid,
                            cudaStream_t st);
+
+// Gate/up + SiTU of one token on the tensor cores (k3moe_gateup_tc.cu): the arguments of
+// k_gateup_t1, the split tiles' partial sums [tile][kTc1Pieces][2][128], and the counters
+// (cnt[0] exit, cnt[1 + tile]; zero on entry, left zero).  tmw: the experts' gate and up
+// operands (K bytes, rows, {gate, up}, expert; 128-row x 128-byte boxes of both); tms:
+// their scale bytes as 8-byte words (words, rows, {gate, up}, expert; boxes of 2 x 128 x 2).
+struct GateUpTc1Args {
+  GateUpT1Args g;
+  float *gpart;
+  unsigned *cnt;
+  int NS;  // ring slots, set from gateup_tc1_smem
+};
+// Shared memory of the kernel for this shape and grid (0: it does not apply), ring slots
+// in *ns_out.
+size_t gateup_tc1_smem(int H, int I, int E, int K, int grid, int *ns_out);
+cudaError_t set_gateup_tc1_smem_limit();
+cudaError_t launch_gateup_tc1(const GateUpTc1Args &a, const CUtensorMap &tmw,
+                              const CUtensorMap &tms, int grid, cudaStream_t st, bool pdl);
 
 // Pairs per block of the dispatch's counting sort: small chunks spread a small batch over
 // several blocks, larger ones keep the per-chunk tables of a large batch short.

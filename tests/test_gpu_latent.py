@@ -156,5 +156,10 @@ def test_latent_layer_nan_bias_sets_nonfinite_status():
 def test_latent_layer_at_the_model_shape(T):
     cfg = dataclasses.replace(synth.config("latent_decode1"), n_experts=64, tokens=T)
     L = LatentLayer(cfg, seed=50 + T, device_fill=True)
+    k3.k3moe_trace_enable(True)
     _, err = check(L)
+    trace = k3.k3moe_trace_read()
+    k3.k3moe_trace_enable(False)
     print("latent layer at the model shape, T=%d: relative L2 error %.3e" % (T, err))
+    if T == 1:  # one token: the experts' gate/up on the tensor cores
+        assert trace.get("k_gateup_tc1", (0, 0))[1] >= 1

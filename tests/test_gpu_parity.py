@@ -396,6 +396,30 @@ def test_decode1_full_layer():
         assert err <= REL_L2_F32
 
 
+def test_single_token_tensor_core_gate_up_at_model_width():
+    """Top-15 (the fused kernel takes an even top-k only), one token at a time: the router
+    kernel, the single-token gate/up on the tensor cores (k_gateup_tc1, the route taken
+    in-kernel) and the down kernel, against the oracle."""
+    cfg = synth.config("decode1", topk=15)
+    L = Layer(cfg, seed=1, tokens=2)
+    for t in range(2):
+        k3.k3moe_trace_enable(True)
+        y, idx, w, st = L.run(x=L.d_x[t:t + 1])
+        trace = k3.k3moe_trace_read()
+        k3.k3moe_trace_enable(False)
+        assert st == 0
+        assert trace.get("k_gateup_tc1", (0, 0))[1] >= 1
+        assert trace.get("k_gateup_t1", (0, 0))[1] == 0
+        oi, ow, oy = oracle.moe_layer(L.x[t:t + 1], L.host["wr"], L.host["bias"],
+                                      L.expert_record, 15, 7168, 1536, L.host["sh_gate"],
+                                      L.host["sh_up"], L.host["sh_down"])
+        assert np.array_equal(idx.cpu().numpy(), oi)
+        assert np.allclose(w.cpu().numpy(), ow, rtol=2e-7, atol=0)
+        err = rel_l2(y.cpu().numpy(), oy)
+        print("top-15 token %d through the tensor-core gate/up: relative L2 error %.3e" % (t, err))
+        assert err <= REL_L2_F32
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["decode64_zipf", "decode64_uniform"])
 def test_decode64_sampled(name):
