@@ -113,7 +113,7 @@ def step_bytes(cfg, U):
     return {
         "k_router_shared": router, "k_router_t1": router,
         "k_expert_gateup": gate_up, "k_gateup_t1": gate_up,
-        "k_down_combine": down, "k_down_tma": down,
+        "k_down_combine": down, "k_down_tma": down, "k_down_t1": down,
         "k_decode_fused": router + gate_up + down,  # the whole step in one kernel
     }
 
@@ -639,14 +639,14 @@ def latent_step_bytes(cfg, U):
     gate/up and down, the projection back, the shared experts' gate/up and down."""
     H, L, I, E, SI = cfg.hidden, cfg.latent, cfg.inter, cfg.n_experts, cfg.shared_inter
     op = I * L // 2 + I * L // 32
-    return {"k_router_shared": E * H * 2 + H * 2,
+    return {"k_router_t1": E * H * 2 + H * 2,
             "k_proj_down": L * H * 2,
             "k_proj_up": H * L * 2 + H * 4,
             "k_proj_shared_gateup": 2 * SI * H * 2,
             "k_proj_shared_down": H * SI * 2,
             "k_gateup_t1": U * 2 * op,  # the experts' gate/up: one of the two kernels runs
             "k_gateup_tc1": U * 2 * op,
-            "k_down_tma": U * op}
+            "k_down_t1": U * op}
 
 
 def bench_latent(ctx, args, K):

@@ -165,7 +165,8 @@ enum KernelId { KID_ROUTER = 0, KID_TOPK, KID_DISPATCH, KID_GATEUP, KID_DOWN, KI
                 KID_QUANT_X, KID_TC_GATEUP, KID_QUANT_ACT, KID_TC_DOWN, KID_TC_SH_GATEUP,
                 KID_SPLIT, KID_TC_SH_DOWN, KID_COMBINE, KID_NORMS, KID_TC_ROUTER,
                 KID_ROUTE_CAND, KID_DECODE_FUSED, KID_PROJ, KID_SHARED_GATEUP, KID_RMSNORM_F32,
-                KID_PROJ_UP, KID_PROJ_SHARED_DOWN, KID_GATEUP_TC1, KID_COUNT };
+                KID_PROJ_UP, KID_PROJ_SHARED_DOWN, KID_GATEUP_TC1, KID_ROUTER_T1, KID_DOWN_T1,
+                KID_COUNT };
 const char *const kKernelNames[KID_COUNT] = {
     "k_router_shared", "k_topk", "k_dispatch", "k_expert_gateup", "k_down_combine",
     "k_rmsnorm_bf16", "k_dequant", "k_gateup_t1", "k_down_tma", "k_route_hist",
@@ -173,7 +174,7 @@ const char *const kKernelNames[KID_COUNT] = {
     "k_tc_gemm_shared_gateup", "k_split_bf16", "k_tc_gemm_shared_down", "k_combine",
     "k_row_norms", "k_tc_gemm_router", "k_route_candidates", "k_decode_fused", "k_proj_down",
     "k_proj_shared_gateup", "k_rmsnorm_f32w", "k_proj_up", "k_proj_shared_down",
-    "k_gateup_tc1"};
+    "k_gateup_tc1", "k_router_t1", "k_down_t1"};
 struct TraceRec {
   int kid;
   cudaEvent_t a, b;
@@ -251,7 +252,7 @@ k3moe_status run_route(const DeviceInfo *di, const k3moe_dims *d, const uint16_t
   int grid = (rows + 7) / 8;
   if (grid > 8 * di->sms) grid = 8 * di->sms;
   {
-    TraceScope ts(KID_ROUTER, st);
+    TraceScope ts(Tc == 1 ? KID_ROUTER_T1 : KID_ROUTER, st);
     const cudaError_t e =
         (Tc == 1) ? launch_router_t1(st, x, H, wr, E, bias, sh_gate, sh_up, SI, d->situ_b1,
                                      d->situ_b2, ws.sc, ws.ch, ws.act_s, status, !g_trace.on)
@@ -326,7 +327,7 @@ k3moe_status run_down(const DeviceInfo *di, const k3moe_dims *d, int Tc, const E
   const int ns1 = (Tc == 1 && sh_down == nullptr) ? down_t1_slots(H, I, K, di->sms) : 0;
   if (ns1 >= 3) {
     // one token, no shared expert: whole-expert stages carrying their activations
-    TraceScope ts(KID_DOWN_TMA, st);
+    TraceScope ts(KID_DOWN_T1, st);
     DownArgs a{};
     a.T = 1; a.H = H; a.I = I; a.K = K; a.P = P;
     a.ex = ea;
