@@ -78,12 +78,12 @@ TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode_fused.cu",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_device.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_topk.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_kernels.cuh"]
-# k_decode_fused: captured with a 64-expert pool (347,874,816 B read + 2,814,976 B written
+# k_decode_fused: captured with a 64-expert pool (347,873,280 B read + 2,811,392 B written
 # per launch), plus the router rows the full 896-expert pool adds ((896 - 64) x 7168 x 2 B):
 # every other byte the kernel reads is the same at both pool sizes (16 selected experts,
 # the shared expert).
-TRAFFIC_CAPTURED = {"sources": "20fddec2e041a1cd",
-                    "bytes": {"k_decode_fused": 347874816 + 2814976 + (896 - 64) * 7168 * 2}}
+TRAFFIC_CAPTURED = {"sources": "84198b209f90a141",
+                    "bytes": {"k_decode_fused": 347873280 + 2811392 + (896 - 64) * 7168 * 2}}
 
 
 def traffic_of(kernel):

@@ -43,8 +43,8 @@ constexpr int kFuEpi = 14;       // warp index of the reduction epilogue
 constexpr int kFuTopk = 15;      // warp index of the top-k (a worker only in D)
 constexpr int kFuProducer = 16;  // warp index of the bulk-copy producer
 constexpr int kFuThreads = 32 * (kFuWorkers + 1);
-constexpr int kFuRB = 4;         // gate/up rows per G stage
-constexpr int kFuItemRows = 8;   // gate/up rows per reduction item (two G stages)
+constexpr int kFuItemRows = 8;   // gate/up rows per reduction item (two G stages: the gate
+                                 // rows, then the up rows)
 constexpr int kFuNSD = 6;        // D ring slots: three per group of eight worker warps
 constexpr int kFuMaxNS = 8;      // R/S/G ring slots at most
 constexpr int kFuDownRows = 16;  // output rows per down tile
@@ -181,12 +181,12 @@ __device__ void topk_warp(const float *sc, const float *ch, const float *ch_s, i
 
 // ---- layout of the fused kernel, shared by the host and the device ----------------------
 // [small arrays | ring | partial sums].  The ring holds NSG X/R/S/G slots (the largest of
-// a G stage -- kFuRB rows of gate and of up, packed + scales -- and an R/S stage of two
-// bf16 rows of H); in phase D the same bytes hold kFuNSD D slots: the larger of a routed
+// a G stage -- the 8 rows of one item of the gate or the up matrix, packed + scales -- and
+// an R/S stage of two bf16 rows of H); in phase D the same bytes hold kFuNSD D slots: the larger of a routed
 // stage (16 rows of two experts, packed + scales, and those experts' activations) and a
 // shared stage (8 bf16 rows of the shared down matrix and its activations).
 __host__ __device__ inline uint32_t fused_gslot_bytes(int H) {
-  const uint32_t g = (uint32_t)(2 * kFuRB * (H / 2 + H / kGroup));
+  const uint32_t g = (uint32_t)(kFuItemRows * (H / 2 + H / kGroup));
   const uint32_t r = (uint32_t)(2 * H * 2);
   return ((g > r ? g : r) + 127u) & ~127u;
 }
@@ -222,7 +222,7 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
   const int G = H / kGroup, nwc = G / 32;  // consumer warps per row parity
   const int rowb = H / 2;                  // packed bytes of a gate/up row
   const int rowh = H * 2;                  // bytes of a bf16 row of H
-  const uint32_t gstage = (uint32_t)(2 * kFuRB * (rowb + G));
+  const uint32_t gstage = (uint32_t)(kFuItemRows * (rowb + G));
   const int G2 = I / kGroup, rowb2 = I / 2;
   const uint32_t dexp = fused_dexp_bytes(I);    // one expert's 16 down rows
   const uint32_t gslot = fused_gslot_bytes(H);
@@ -358,20 +358,19 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
           bulk_g2s_pol(dst, lw.sh_gate + (size_t)p * H, rowh, &fullG[lane], pol_first);
           bulk_g2s_pol(dst + rowh, lw.sh_up + (size_t)p * H, rowh, &fullG[lane], pol_first);
         } else {
+          // the item's 8 rows of one matrix per stage (gate, then up): two copies, each
+          // one contiguous run of the record
           const int tg = t - tG;
           const int item = bx + nb * (tg >> 1);
           const int j = item / blocks, blk = item % blocks;
-          const int r = blk * kFuItemRows + (tg & 1) * kFuRB;
+          const int r = blk * kFuItemRows;
+          const bool up = tg & 1;
           const uint8_t *rec = lw.experts + (long long)sel[j] * lw.stride;
           mbar_arrive_expect_tx(&fullG[lane], gstage);
-          bulk_g2s_pol(dst, rec + a.ex.off[0] + (size_t)r * rowb, kFuRB * rowb, &fullG[lane],
-                       pol_first);
-          bulk_g2s_pol(dst + kFuRB * rowb, rec + a.ex.off[4] + (size_t)r * rowb, kFuRB * rowb,
+          bulk_g2s_pol(dst, rec + a.ex.off[up ? 4 : 0] + (size_t)r * rowb, kFuItemRows * rowb,
                        &fullG[lane], pol_first);
-          bulk_g2s_pol(dst + 2 * kFuRB * rowb, rec + a.ex.off[1] + (size_t)r * G, kFuRB * G,
-                       &fullG[lane], pol_first);
-          bulk_g2s_pol(dst + 2 * kFuRB * rowb + kFuRB * G, rec + a.ex.off[5] + (size_t)r * G,
-                       kFuRB * G, &fullG[lane], pol_first);
+          bulk_g2s_pol(dst + kFuItemRows * rowb, rec + a.ex.off[up ? 5 : 1] + (size_t)r * G,
+                       kFuItemRows * G, &fullG[lane], pol_first);
         }
         last_g = t;
       }
@@ -731,9 +730,10 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
       if (lane == 0) rt[warp * 64] = acc;
       end_item(n);
     }
-    // G: an 8-row block = two stages of kFuRB gate and up rows; thread (h, g) takes the
-    // rows of parity h in input group g
-    constexpr int V = 2 * kFuRB;  // (2 rows x 2 matrices) x 2 stages
+    // G: an 8-row block = two stages, its gate rows and then its up rows; thread (h, g)
+    // takes the rows of parity h in input group g
+    constexpr int RH = kFuItemRows / 2;  // rows of one parity in an item
+    constexpr int V = 2 * RH;            // (4 rows) x (2 matrices)
     const float pxe = pow2i(xe);  // this thread's inputs are stored times 2^-xe
     for (int s = 0; s < nI; s++, n++) {
       float *rt = begin_item(n);
@@ -744,30 +744,26 @@ __device__ __forceinline__ void fused_layer(const FusedT1Args &a, const int laye
       const uint8_t *stA = stage_in(t);
       const uint8_t *stB = stage_in(t + 1);
 #pragma unroll
-      for (int b2 = 0; b2 < 2; b2++) {
-        const uint8_t *st = b2 ? stB : stA;
+      for (int m = 0; m < 2; m++) {  // m: the stage's matrix, 0 gate, 1 up
+        const uint8_t *st = m ? stB : stA;
         if (!aborted) {
-          const uint8_t *sgs = st + 2 * kFuRB * rowb;
-          const uint8_t *sus = sgs + kFuRB * G;
+          const uint8_t *ss = st + kFuItemRows * rowb;  // the rows' scale bytes
 #pragma unroll
-          for (int k = 0; k < kFuRB / 2; k++) {
-            const int q = h + 2 * k;  // row within the stage
-            const uint4 wg = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
-            const uint4 wu = reinterpret_cast<const uint4 *>(st + (kFuRB + q) * rowb)[g];
-            const uint32_t sg = sgs[q * G + g], su = sus[q * G + g];
-            vals[b2 * kFuRB + 2 * k] = group_dot(xr, wg) * group_scale(sg, pxe);
-            vals[b2 * kFuRB + 2 * k + 1] = group_dot(xr, wu) * group_scale(su, pxe);
+          for (int k = 0; k < RH; k++) {
+            const int q = h + 2 * k;  // row within the block
+            const uint4 w = reinterpret_cast<const uint4 *>(st + q * rowb)[g];
+            vals[m * RH + k] = group_dot(xr, w) * group_scale(ss[q * G + g], pxe);
           }
         }
       }
       stage_out(t);
       stage_out(t + 1);
       t += 2;
-      // value v = b2*RB + 2k + m  ->  block row b2*RB + h + 2k, matrix m
+      // value v = m * RH + k  ->  block row h + 2k, matrix m
       const float tot = warp_transpose_reduce<V>(vals);
       if (lane < V) {
-        const int b2 = lane / kFuRB, k = (lane % kFuRB) / 2, m = lane & 1;
-        rt[(warp * 32 + b2 * kFuRB + h + 2 * k) * 2 + m] = tot;
+        const int m = lane / RH, k = lane % RH;
+        rt[(warp * 32 + h + 2 * k) * 2 + m] = tot;
       }
       end_item(n);
     }
