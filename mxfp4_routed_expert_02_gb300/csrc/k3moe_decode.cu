@@ -574,8 +574,11 @@ size_t down_tma_smem(int I, int T, int P, int NS, bool act_smem, int ntl) {
 // LatentMoE's experts), bulk-copy ring of whole-expert stages.  CTA b owns output rows
 // [b R, b R + R) (R a multiple of 8 chosen so that the rows spread evenly over the SMs: no
 // SM has a second tile to do while others are idle).  A stage holds one distinct expert's
-// R rows of W2 (packed + scales) AND that expert's activations (both f16 terms and the
-// group exponents), so no activation is read from global memory in the dot products.
+// R rows of W2 (packed + scales) AND that expert's activations (the f16 term scaled by
+// its group's exponent, and the exponents), so no activation is read from global memory
+// in the dot products.  The f16 term alone carries 11 significant bits of every
+// activation (relative rounding at most 2^-12, as the single-token fused kernel hands its
+// activations over); the residual term the gate/up kernels also write is not read here.
 // Stage u goes to worker group u % 2 (eight warps); warp wg takes rows wg, wg + 8, .. of
 // the stage, its 32 lanes the input groups l, l + 32, .. (each group's activations loaded
 // once for all the warp's rows).  Then y[row] = sum_j w[j] d_j[row] in router order
@@ -587,7 +590,7 @@ constexpr int kD1MaxRows = 48;  // rows per CTA at most
 
 __host__ __device__ inline uint32_t down_t1_stage_bytes(int I, int R) {
   const uint32_t w = (uint32_t)R * (I / 2 + I / kGroup);  // rows: packed + scales
-  const uint32_t act = (uint32_t)I * 2 * 2 + (uint32_t)(I / kGroup) * 4;
+  const uint32_t act = (uint32_t)I * 2 + (uint32_t)(I / kGroup) * 4;
   return (w + act + 127u) & ~127u;
 }
 __host__ __device__ inline uint32_t down_t1_head_bytes(int K, int R) {  // bars, dbuf, w
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(kD1Workers * 32 + 32, 1) k_down_t1(DownArgs a,
   const uint32_t wcap = (uint32_t)R * rowb, scap = (uint32_t)R * G2;  // stage layout
   const uint32_t abytes = (uint32_t)I * 2, ebytes = (uint32_t)G2 * 4;
   const uint32_t stage_bytes = down_t1_stage_bytes(I, R);
-  const uint32_t tx = wbytes + sbytes + 2 * abytes + ebytes;
+  const uint32_t tx = wbytes + sbytes + abytes + ebytes;
   constexpr int NW = kD1Workers * 32;
 
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [NS]
@@ -653,9 +656,7 @@ __global__ void __launch_bounds__(kD1Workers * 32 + 32, 1) k_down_t1(DownArgs a,
         bulk_g2s_pol(dst, rec + a.ex.off[2] + (size_t)r0 * rowb, wbytes, &full[lane], pol);
         bulk_g2s_pol(dst + wcap, rec + a.ex.off[3] + (size_t)r0 * G2, sbytes, &full[lane], pol);
         bulk_g2s(dst + wcap + scap, a.act_hi + (size_t)pi * I, abytes, &full[lane]);
-        bulk_g2s(dst + wcap + scap + abytes, a.act_lo + (size_t)pi * I, abytes, &full[lane]);
-        bulk_g2s(dst + wcap + scap + 2 * abytes, a.act_ex + (size_t)pi * G2, ebytes,
-                 &full[lane]);
+        bulk_g2s(dst + wcap + scap + abytes, a.act_ex + (size_t)pi * G2, ebytes, &full[lane]);
       }
       if (!ok && u - NS >= 0)  // bounded wait for this slot's last issued fill
         mbar_wait(&full[lane], ((u - NS) / NS) & 1, 400000000LL);
@@ -679,22 +680,19 @@ __global__ void __launch_bounds__(kD1Workers * 32 + 32, 1) k_down_t1(DownArgs a,
       const uint8_t *st = ring + (size_t)q * stage_bytes;
       const uint8_t *ss = st + wcap;
       const uint16_t *s_hi = reinterpret_cast<const uint16_t *>(st + wcap + scap);
-      const uint16_t *s_lo = s_hi + I;
-      const int32_t *s_ex = reinterpret_cast<const int32_t *>(st + wcap + scap + 2 * abytes);
+      const int32_t *s_ex = reinterpret_cast<const int32_t *>(st + wcap + scap + abytes);
       const int pi = plist[uoff[u]];
       float acc[kD1MaxRows / 8];
 #pragma unroll
       for (int k = 0; k < kD1MaxRows / 8; k++) acc[k] = 0.f;
       for (int g = 0; g < NGL; g++) {
         const int gg = g * 32 + lane;
-        uint32_t xh[16], xl[16];
+        uint32_t xh[16];
         const uint4 *ph = reinterpret_cast<const uint4 *>(s_hi + act_index(0, I, gg, 0));
-        const uint4 *pl = reinterpret_cast<const uint4 *>(s_lo + act_index(0, I, gg, 0));
 #pragma unroll
         for (int c = 0; c < 4; c++) {
-          const uint4 x0 = ph[c * G2], x1 = pl[c * G2];
+          const uint4 x0 = ph[c * G2];
           xh[4 * c] = x0.x; xh[4 * c + 1] = x0.y; xh[4 * c + 2] = x0.z; xh[4 * c + 3] = x0.w;
-          xl[4 * c] = x1.x; xl[4 * c + 1] = x1.y; xl[4 * c + 2] = x1.z; xl[4 * c + 3] = x1.w;
         }
         const int ex = s_ex[gg];
 #pragma unroll
@@ -703,7 +701,7 @@ __global__ void __launch_bounds__(kD1Workers * 32 + 32, 1) k_down_t1(DownArgs a,
           if (row < nr) {
             const uint4 wv = reinterpret_cast<const uint4 *>(st + row * rowb)[gg];
             const uint32_t sv = ss[row * G2 + gg];
-            if (sv != 255u) acc[k] += group_dot2(xh, xl, wv) * group_factor(sv, ex);
+            if (sv != 255u) acc[k] += group_dot(xh, wv) * group_factor(sv, ex);
           }
         }
       }
