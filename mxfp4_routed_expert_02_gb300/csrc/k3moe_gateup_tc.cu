@@ -8,7 +8,8 @@
 // "Picking 16 experts of 896" for the top-k and the LatentMoE listing step 3 for the expert
 // FFN, section 4 for MXFP4, the activation listing for SiTU), with the same outputs: the
 // route and the dispatch lists (CTA 0), and the activations of the K (token, slot) pairs
-// as f16 hi + lo terms with one exponent per 32 rows, which the down kernels read.  The
+// as f16 hi + lo terms with one exponent per 32 rows (k_down_tma reads both terms,
+// k_down_t1 the hi term alone).  The
 // input enters as four MXFP4 terms per 32 values (the multi-token path's encoding), so
 // the products differ from k_gateup_t1's f16 ones by a relative ~4e-5.
 //
