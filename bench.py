@@ -70,19 +70,19 @@ DEFAULT_STEPS = {"decode1": 3000, "decode64_zipf": 200, "decode64_uniform": 200,
 MIN_TIMED_SECONDS = 1.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of each decode kernel, keyed to a hash of the sources the kernels are built
-# from: a changed kernel reports null until it is captured again.
+# capture of the decode kernel, keyed to a hash of the sources it is compiled from (its
+# translation unit and the headers that unit includes): a changed kernel reports null
+# until it is captured again.
 TRAFFIC_SOURCES = ["mxfp4_routed_expert_02_gb300/csrc/k3moe_decode_fused.cu",
-                   "mxfp4_routed_expert_02_gb300/csrc/k3moe_decode.cu",
-                   "mxfp4_routed_expert_02_gb300/csrc/k3moe_router.cu",
+                   "mxfp4_routed_expert_02_gb300/csrc/k3moe_kernels.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_device.cuh",
                    "mxfp4_routed_expert_02_gb300/csrc/k3moe_topk.cuh",
-                   "mxfp4_routed_expert_02_gb300/csrc/k3moe_kernels.cuh"]
+                   "include/k3moe.h"]
 # k_decode_fused: captured with a 64-expert pool (347,873,280 B read + 2,811,392 B written
 # per launch), plus the router rows the full 896-expert pool adds ((896 - 64) x 7168 x 2 B):
 # every other byte the kernel reads is the same at both pool sizes (16 selected experts,
 # the shared expert).
-TRAFFIC_CAPTURED = {"sources": "84198b209f90a141",
+TRAFFIC_CAPTURED = {"sources": "8f9947976e789b9b",
                     "bytes": {"k_decode_fused": 347873280 + 2811392 + (896 - 64) * 7168 * 2}}
 
 
