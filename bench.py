@@ -468,7 +468,9 @@ def bench_decode1(ctx, args, K):
         if k in nb:
             kernels[k]["gbs"] = nb[k] / (kernels[k]["ms_avg"] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
-                "frac": achieved / peak_hbm, "traffic": traffic_of(dom), "kernel": dom,
+                "frac": achieved / peak_hbm,
+                # the captured bytes are those of the full 896-expert pool
+                "traffic": traffic_of(dom) if cfg.n_experts == 896 else None, "kernel": dom,
                 "algorithmic_bytes": nb[dom],
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else
                                "fallback 6.8 TB/s (of fallback)"}
